@@ -1,0 +1,16 @@
+"""CPU oracle of the W4A16 fused MoE feed-forward -- test infrastructure only.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may use it.
+"""
+from .moe_oracle import (  # noqa: F401
+    GROUP_SIZE,
+    bf16_to_f64,
+    dequantize,
+    expert_dense,
+    expert_ffn,
+    moe_align,
+    moe_forward,
+    roofline_bytes_per_expert,
+    silu,
+    unpack_codes,
+)
