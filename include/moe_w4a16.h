@@ -1,0 +1,155 @@
+/*
+ * moe_w4a16 -- INT4 weight-only (W4A16) fused Mixture-of-Experts feed-forward
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (the MoE layer benchmarked on "The Commit That Captured a
+ * Plateau", commit text, and "The Pivot to Real Hardware ...", Step 1 and Input
+ * Knowledge items 1-2): every token t is routed to k experts e = topk_ids[t, j]
+ * with weights w = topk_weights[t, j], and
+ *
+ *     out[t] = sum_j w * W2[e] . ( SiLU(W1g[e] . x_t) * (W1u[e] . x_t) ),
+ *     SiLU(z) = z / (1 + exp(-z)),
+ *
+ * where W1 = [W1g; W1u] (gate rows [0, N), up rows [N, 2N)) is [2N, K] and W2 is
+ * [K, N]. Weights are symmetric INT4 with one bf16 scale per group of 32 values
+ * along each GEMM's reduction dimension: value = (u - 8) * scale for a stored
+ * nibble u in 0..15. Activations (x, out) are bf16.
+ *
+ * Conventions shared by every call:
+ *  - Every function returns MOE_W4A16_OK (0) or a negative code; the message of
+ *    the last failure on the calling thread is moe_w4a16_last_error().
+ *  - Pointers documented as "device" must be device (or managed) memory of the
+ *    handle's device; "host" pointers are ordinary host memory (pinned is faster).
+ *  - A `stream` argument is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls are stream-ordered and do not synchronise the host, except
+ *    where stated.
+ *  - The caller owns every buffer it passes; the library never frees them.
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_W4A16_OK = 0,
+  MOE_W4A16_INVALID_ARG = -1,         /* null pointer, negative size, bad handle */
+  MOE_W4A16_UNSUPPORTED_SHAPE = -2,   /* K % 128, N % 64, group_size != 32, E or topk out of range */
+  MOE_W4A16_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < moe_w4a16_workspace_size(h, M) */
+  MOE_W4A16_CUDA_ERROR = -4,          /* a CUDA runtime call failed (message has the CUDA error) */
+  MOE_W4A16_NOT_PACKED = -5           /* forward before moe_w4a16_pack */
+};
+
+/* Device status bits (see moe_w4a16_status). */
+enum {
+  MOE_W4A16_STATUS_BAD_EXPERT_ID = 1, /* a topk_ids entry was outside [0, E); that slot was skipped */
+  MOE_W4A16_STATUS_TIMEOUT = 2        /* a pipeline wait in a GEMM kernel gave up; output is invalid */
+};
+
+typedef struct moe_w4a16_ctx* moe_w4a16_t;
+
+/* Create a handle for E experts, hidden size K, intermediate size N, top-k
+ * routing and INT4 group size (must be 32). Binds to the current CUDA device and
+ * allocates the packed weight storage there (cudaMalloc, same byte count as the
+ * GPTQ-style inputs: E*(3*N*K/2 + 2*(2N*K/32 + K*N/32)) bytes).
+ * Requirements: K % 128 == 0, N % 64 == 0, 1 <= E <= 1024, 1 <= topk <= E.
+ * Host-synchronous. */
+int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t* out);
+
+/* Free the packed weights and the handle. Synchronises the device first. */
+int moe_w4a16_destroy(moe_w4a16_t h);
+
+/* Repack GPTQ-style weights into the library's device layout ("The Pivot to
+ * Real Hardware ...", Step 2: GPTQ int32 in, hardware-friendly tiles out, no
+ * act-order permutation). All four inputs are device pointers, C-contiguous:
+ *   w1_q int32 [E, K/8, 2N]   code i of a word = element 8*row+i (bits 4i..4i+3)
+ *   w1_s bf16  [E, K/32, 2N]
+ *   w2_q int32 [E, N/8, K]
+ *   w2_s bf16  [E, N/32, K]
+ * The inputs may be freed once the stream has passed this call. */
+int moe_w4a16_pack(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s,
+                   const int32_t* w2_q, const uint16_t* w2_s, void* stream);
+
+/* Bytes of device workspace that moe_w4a16_forward needs for M tokens (and any
+ * smaller M). Holds the per-call routing tables, the expert-sorted activations,
+ * the intermediate activations, split-K partial tiles and the fp32 output
+ * accumulator. No state persists in it between calls. */
+size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M);
+
+/* The fused forward. Device pointers:
+ *   hidden       bf16  [M, K]
+ *   topk_ids     int32 [M, topk]   expert ids; entries outside [0, E) are skipped
+ *                                  and set MOE_W4A16_STATUS_BAD_EXPERT_ID
+ *   topk_weights fp32  [M, topk]
+ *   out          bf16  [M, K]      written completely (rounded to nearest even)
+ *   workspace    >= moe_w4a16_workspace_size(h, M) bytes, 256-byte aligned
+ * M == 0 is a no-op. Launches 5 kernels on `stream`, allocates nothing. */
+int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                      const float* topk_weights, uint16_t* out, int M,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* End-to-end variant with HOST buffers (same shapes as moe_w4a16_forward):
+ * copies the inputs host->device into the workspace, runs the forward, copies
+ * `out` back and synchronises the stream before returning. The workspace must
+ * hold moe_w4a16_workspace_size(h, M) + moe_w4a16_host_staging_size(h, M) bytes. */
+size_t moe_w4a16_host_staging_size(moe_w4a16_t h, int M);
+int moe_w4a16_forward_host(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                           const float* topk_weights, uint16_t* out, int M,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Read the device status word of the last forward that used `workspace`
+ * (bits MOE_W4A16_STATUS_*; 0 = clean). Synchronises `stream`. */
+int moe_w4a16_status(moe_w4a16_t h, const void* workspace, int32_t* status, void* stream);
+
+/* Thread-local text of the last error (never NULL). */
+const char* moe_w4a16_last_error(void);
+
+/* Tuning and measurement knobs.
+ *   MOE_W4A16_OPT_NUM_CTAS   persistent GEMM grid size (default: SM count; 1..256)
+ *   MOE_W4A16_OPT_PROFILE    1 = record CUDA events between the forward's kernels
+ *                            (read with moe_w4a16_kernel_times; perturbs overlap)
+ *   MOE_W4A16_OPT_PDL        1 = launch dependent kernels with programmatic
+ *                            dependent launch (default 1) */
+enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3 };
+int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
+
+/* Milliseconds of each kernel of the last profiled forward, in launch order
+ * (align, gather, gemm1, gemm2, finalize). Synchronises on the recorded events.
+ * `n` is the capacity of `ms`; returns the number written or a negative code. */
+int moe_w4a16_kernel_times(moe_w4a16_t h, float* ms, int n);
+
+/* Total packed weight bytes held by the handle (weights + scales). */
+size_t moe_w4a16_packed_bytes(moe_w4a16_t h);
+
+/* ---- test-only exports ------------------------------------------------- */
+
+/* Token->expert align on its own, for bit-exact checks. Device pointers:
+ * topk_ids int32 [M, topk]; sorted_ids int32 [capacity]; expert_offsets int32
+ * [E+1]; num_padded int32 [1]. For every expert in id order: the flat slot ids
+ * t*topk+j routed to it in ascending order, then the sentinel M*topk up to a
+ * multiple of `block`. capacity must be >= M*topk + min(E, M*topk)*(block-1). */
+int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int block,
+                          int32_t* sorted_ids, int32_t* expert_offsets, int32_t* num_padded,
+                          int capacity, void* stream);
+
+/* Invert the repack: write the handle's packed weights back in the GPTQ-style
+ * layout of moe_w4a16_pack (device pointers, same shapes). */
+int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s,
+                           int32_t* w2_q, uint16_t* w2_s, void* stream);
+
+/* Copy the intermediate activations SiLU(gate)*up (bf16) of the last forward
+ * that used `workspace` into h_rows [M*topk, N] (device), row = flat slot id
+ * t*topk+j; rows of skipped slots are left untouched. */
+int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M,
+                                uint16_t* h_rows, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4A16_H */

@@ -1,0 +1,234 @@
+// Token->expert align, expert-sorted gather of the hidden states, output
+// finalisation and the intermediate-activation readback used by tests.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+// Exclusive prefix sum over the 1024 threads of the block; *total gets the sum.
+__device__ int block_exclusive_scan(int v, int* warp_tmp, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tmp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nwarps ? warp_tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tmp[lane] = t;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  const int before = (w > 0 ? warp_tmp[w - 1] : 0) + x - v;
+  *total = warp_tmp[nwarps - 1];
+  __syncthreads();
+  return before;
+}
+
+// One CTA of 1024 threads. Every warp owns a contiguous chunk of the flat slot
+// list, histograms it privately, and then scatters its chunk in order, so the
+// result is the stable counting sort: for each expert in id order, the flat slot
+// ids routed to it in ascending order, padded with the sentinel MK to a
+// multiple of `block`.
+__global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
+  extern __shared__ int sm[];
+  const int E = a.E;
+  int* hist = sm;  // [32][E]: per-warp counts, then per-warp start offsets
+  __shared__ int warp_tmp[32];
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0 && a.hdr) a.hdr[kHdrStatus] = 0;
+  for (int i = tid; i < 32 * E; i += blockDim.x) hist[i] = 0;
+  if (a.tickets)
+    for (int i = tid; i < a.n_tickets; i += blockDim.x) a.tickets[i] = 0;
+  __syncthreads();
+
+  const int chunk = (a.MK + 31) / 32;
+  const int lo = min(a.MK, w * chunk), hi = min(a.MK, lo + chunk);
+  int bad = 0;
+  for (int i = lo + lane; i < hi; i += 32) {
+    const int e = a.topk_ids[i];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[w * E + e], 1);
+    else
+      bad = 1;
+  }
+  if (bad && a.hdr) atomicOr(&a.hdr[kHdrStatus], 1);
+  __syncthreads();
+
+  int my_cnt = 0, my_pad = 0, my_tiles = 0;
+  if (tid < E) {
+    int run = 0;
+    for (int ww = 0; ww < 32; ++ww) {
+      const int c = hist[ww * E + tid];
+      hist[ww * E + tid] = run;
+      run += c;
+    }
+    my_cnt = run;
+    my_pad = (run + a.block - 1) / a.block * a.block;
+    my_tiles = a.bn_max > 0 ? (my_pad + a.bn_max - 1) / a.bn_max : 0;
+  }
+  int tot_pad = 0, tot_tiles = 0;
+  const int seg = block_exclusive_scan(my_pad, warp_tmp, &tot_pad);
+  const int tstart = block_exclusive_scan(my_tiles, warp_tmp, &tot_tiles);
+  int* seg_sm = hist + 32 * E;  // [E]
+  if (tid < E) seg_sm[tid] = seg;
+  __syncthreads();
+
+  for (int base = lo; base < hi; base += 32) {
+    const int i = base + lane;
+    int e = -1;
+    if (i < hi) {
+      const int v = a.topk_ids[i];
+      if (v >= 0 && v < E) e = v;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      a.sorted_ids[seg_sm[e] + hist[w * E + e] + rank] = i;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) hist[w * E + e] += __popc(peers);
+    __syncwarp();
+  }
+
+  if (tid < E) {
+    for (int p = seg + my_cnt; p < seg + my_pad; ++p) a.sorted_ids[p] = a.MK;
+    if (a.expert_offsets) {
+      a.expert_offsets[tid] = seg;
+      if (tid == E - 1) a.expert_offsets[E] = tot_pad;
+    }
+    if (a.bn_max > 0) {
+      for (int t = 0; t < my_tiles; ++t) {
+        TokenTile tt;
+        tt.expert = tid;
+        tt.g0 = (seg + t * a.bn_max) / kRowGroup;
+        tt.ngroups = min(a.bn_max, my_pad - t * a.bn_max) / kRowGroup;
+        tt.first = tstart;
+        a.tiles[tstart + t] = tt;
+      }
+      a.expert_tiles[tid] = my_tiles;
+    }
+  }
+  if (tid == 0) {
+    if (a.hdr) {
+      a.hdr[kHdrNumPadded] = tot_pad;
+      a.hdr[kHdrNumTiles] = tot_tiles;
+    }
+    if (a.num_padded_out) *a.num_padded_out = tot_pad;
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl) {
+  const size_t smem = (33 * static_cast<size_t>(a.E)) * sizeof(int);
+  cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  return launch_k(align_kernel, dim3(1), dim3(1024), smem, stream, pdl, a);
+}
+
+// Copy every expert-sorted row's hidden state into the blocked B-operand layout
+// (padding rows become zeros) and zero the fp32 output accumulator.
+__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+  pdl_wait();
+  const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  float4* acc4 = reinterpret_cast<float4*>(a.acc);
+  for (long long i = gt; i < a.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int groups = a.hdr[kHdrNumPadded] / kRowGroup;
+  const int cpr = a.K / 8;  // 16-byte chunks per row
+  for (int g = blockIdx.x; g < groups; g += gridDim.x) {
+    for (int idx = threadIdx.x; idx < kRowGroup * cpr; idx += blockDim.x) {
+      const int r = idx / cpr, ch = idx - r * cpr;
+      const int sid = a.sorted_ids[g * kRowGroup + r];
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (sid < a.MK)
+        v = *reinterpret_cast<const uint4*>(a.x + static_cast<long long>(sid / a.topk) * a.K +
+                                            ch * 8);
+      uint8_t* dst = a.xs + (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
+                     r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = v;
+    }
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
+                          bool pdl) {
+  const long long zero_blocks = (a.acc_elems / 4 + 255) / 256;
+  long long grid = max_groups > zero_blocks ? max_groups : zero_blocks;
+  const long long cap = 4LL * num_sms;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  return launch_k(gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream, pdl, a);
+}
+
+// out = bf16(acc), round to nearest even; eight elements per thread step.
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc,
+                                                       uint16_t* __restrict__ out, long long n) {
+  pdl_wait();
+  const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const float4* a4 = reinterpret_cast<const float4*>(acc);
+  uint4* o4 = reinterpret_cast<uint4*>(out);
+  for (long long i = gt; i < n / 8; i += nthr) {
+    const float4 x = a4[2 * i], y = a4[2 * i + 1];
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(x.x, x.y);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(x.z, x.w);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(y.x, y.y);
+    __nv_bfloat162 p3 = __floats2bfloat162_rn(y.z, y.w);
+    uint4 o;
+    o.x = *reinterpret_cast<uint32_t*>(&p0);
+    o.y = *reinterpret_cast<uint32_t*>(&p1);
+    o.z = *reinterpret_cast<uint32_t*>(&p2);
+    o.w = *reinterpret_cast<uint32_t*>(&p3);
+    o4[i] = o;
+  }
+}
+
+cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
+                            cudaStream_t stream, bool pdl) {
+  long long blocks = (n / 8 + 255) / 256;
+  const long long cap = 8LL * num_sms;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_k(finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, pdl,
+                  acc, out, n);
+}
+
+__global__ void read_intermediate_kernel(const uint8_t* __restrict__ hbuf,
+                                         const int32_t* __restrict__ sorted_ids,
+                                         const int32_t* __restrict__ hdr, int MK, int N, int Gcap,
+                                         uint16_t* __restrict__ h_rows) {
+  const int num_padded = hdr[kHdrNumPadded];
+  for (int p = blockIdx.x; p < num_padded; p += gridDim.x) {
+    const int sid = sorted_ids[p];
+    if (sid >= MK) continue;
+    const int g = p / kRowGroup, r = p % kRowGroup;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      const int kb = n >> 6, k = n & 63;
+      h_rows[static_cast<long long>(sid) * N + n] = *reinterpret_cast<const uint16_t*>(
+          hbuf + (static_cast<long long>(kb) * Gcap + g) * kRowGroupBytes + blocked_offset(r, k));
+    }
+  }
+}
+
+cudaError_t launch_read_intermediate(const uint8_t* hbuf, const int32_t* sorted_ids,
+                                     const int32_t* hdr, int MK, int N, int Gcap, int max_rows,
+                                     uint16_t* h_rows, cudaStream_t stream) {
+  int grid = max_rows < 1024 ? (max_rows > 0 ? max_rows : 1) : 1024;
+  read_intermediate_kernel<<<grid, 256, 0, stream>>>(hbuf, sorted_ids, hdr, MK, N, Gcap, h_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

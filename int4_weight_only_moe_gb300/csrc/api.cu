@@ -1,0 +1,403 @@
+// C-ABI of the W4A16 fused MoE library: handle, argument checks, workspace
+// layout and the launch sequence of the forward
+//   align -> gather -> gate/up GEMM -> down GEMM -> finalize.
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/moe_w4a16.h"
+#include "kernels.cuh"
+
+using namespace moe;
+
+struct moe_w4a16_ctx {
+  int E, K, N, topk, group;
+  int device;
+  int num_sms;
+  int num_ctas;
+  bool pdl;
+  bool profile;
+  uint8_t* w1p;
+  uint8_t* w2p;
+  size_t w1p_bytes, w2p_bytes;
+  bool packed;
+  cudaEvent_t ev[6];
+  bool ev_valid;
+};
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+#define MOE_CUDA_TRY(expr)                                                                   \
+  do {                                                                                       \
+    cudaError_t e_ = (expr);                                                                 \
+    if (e_ != cudaSuccess)                                                                   \
+      return fail(MOE_W4A16_CUDA_ERROR, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t hdr, tickets, sorted, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
+  int Pcap, Gcap;
+};
+
+// Workspace carve-up for M tokens. Pcap bounds the padded routed-row count:
+// M*k rows plus at most 15 padding rows for each expert that receives any.
+WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
+  WsLayout L{};
+  const long long MK = static_cast<long long>(M) * h->topk;
+  const long long active = MK < h->E ? MK : h->E;
+  long long pcap = align_up(static_cast<size_t>(MK + active * (kRowGroup - 1)), kRowGroup);
+  if (pcap < kRowGroup) pcap = kRowGroup;
+  L.Pcap = static_cast<int>(pcap);
+  L.Gcap = L.Pcap / kRowGroup;
+  size_t off = 0;
+  L.hdr = off;
+  off += kHdrWords * sizeof(int32_t);
+  off = align_up(off, 256);
+  L.tickets = off;
+  off = align_up(off + kMaxCtas * sizeof(int32_t), 256);
+  L.sorted = off;
+  off = align_up(off + static_cast<size_t>(L.Pcap) * sizeof(int32_t), 256);
+  L.tiles = off;
+  off = align_up(off + static_cast<size_t>(L.Gcap) * sizeof(TokenTile), 256);
+  L.expert_tiles = off;
+  off = align_up(off + static_cast<size_t>(h->E) * sizeof(int32_t), 1024);
+  L.xs = off;
+  off = align_up(off + static_cast<size_t>(L.Pcap) * h->K * 2, 1024);
+  L.hbuf = off;
+  off = align_up(off + static_cast<size_t>(L.Pcap) * h->N * 2, 1024);
+  L.scratch = off;
+  off = align_up(off + static_cast<size_t>(kMaxCtas) * 2 * kBNMax * kBM * sizeof(float), 1024);
+  L.acc = off;
+  off = align_up(off + static_cast<size_t>(M) * h->K * sizeof(float), 1024);
+  L.total = off;
+  return L;
+}
+
+size_t staging_bytes(const moe_w4a16_ctx* h, int M) {
+  const size_t mk = static_cast<size_t>(M) * h->topk;
+  return align_up(static_cast<size_t>(M) * h->K * 2, 256) * 2 + align_up(mk * 4, 256) * 2;
+}
+
+int check_handle(const moe_w4a16_ctx* h) {
+  if (!h) return fail(MOE_W4A16_INVALID_ARG, "null handle");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device)
+    return fail(MOE_W4A16_INVALID_ARG, "current CUDA device differs from the handle's device");
+  return MOE_W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_w4a16_last_error(void) { return g_last_error.c_str(); }
+
+int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t* out) {
+  if (!out) return fail(MOE_W4A16_INVALID_ARG, "out is null");
+  *out = nullptr;
+  if (group_size != kGroup) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "group_size must be 32");
+  if (E < 1 || E > kMaxExperts) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "E must be in [1, 1024]");
+  if (topk < 1 || topk > E) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "topk must be in [1, E]");
+  if (K <= 0 || K % 128 != 0) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "K must be a positive multiple of 128");
+  if (N <= 0 || N % 64 != 0) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "N must be a positive multiple of 64");
+  auto* h = new moe_w4a16_ctx();
+  std::memset(h, 0, sizeof(*h));
+  h->E = E;
+  h->K = K;
+  h->N = N;
+  h->topk = topk;
+  h->group = group_size;
+  h->pdl = true;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e == cudaSuccess) e = gemm_set_attributes();
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(MOE_W4A16_CUDA_ERROR, std::string("device setup: ") + cudaGetErrorString(e));
+  }
+  h->num_ctas = h->num_sms < kMaxCtas ? h->num_sms : kMaxCtas;
+  // w1: 2N rows x K, w2: K rows x N; half a byte per code plus 2 bytes per 32 codes
+  h->w1p_bytes = static_cast<size_t>(E) * (2 * N / kBM) * (K / kBK) * kWBlockBytes;
+  h->w2p_bytes = static_cast<size_t>(E) * (K / kBM) * (N / kBK) * kWBlockBytes;
+  e = cudaMalloc(&h->w1p, h->w1p_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->w2p, h->w2p_bytes);
+  if (e != cudaSuccess) {
+    cudaFree(h->w1p);
+    delete h;
+    return fail(MOE_W4A16_CUDA_ERROR, std::string("cudaMalloc packed weights: ") + cudaGetErrorString(e));
+  }
+  *out = h;
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_destroy(moe_w4a16_t h) {
+  if (!h) return fail(MOE_W4A16_INVALID_ARG, "null handle");
+  cudaDeviceSynchronize();
+  cudaFree(h->w1p);
+  cudaFree(h->w2p);
+  if (h->ev_valid)
+    for (auto& ev : h->ev) cudaEventDestroy(ev);
+  delete h;
+  return MOE_W4A16_OK;
+}
+
+size_t moe_w4a16_packed_bytes(moe_w4a16_t h) { return h ? h->w1p_bytes + h->w2p_bytes : 0; }
+
+int moe_w4a16_pack(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s, const int32_t* w2_q,
+                   const uint16_t* w2_s, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (!w1_q || !w1_s || !w2_q || !w2_s) return fail(MOE_W4A16_INVALID_ARG, "null weight pointer");
+  auto s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA_TRY(launch_repack(reinterpret_cast<const uint32_t*>(w1_q), w1_s, h->w1p, h->E, h->K,
+                             2 * h->N, 2 * h->N / kBM, h->K / kBK, 1, s));
+  MOE_CUDA_TRY(launch_repack(reinterpret_cast<const uint32_t*>(w2_q), w2_s, h->w2p, h->E, h->N,
+                             h->K, h->K / kBM, h->N / kBK, 0, s));
+  h->packed = true;
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s, int32_t* w2_q,
+                           uint16_t* w2_s, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (!w1_q || !w1_s || !w2_q || !w2_s) return fail(MOE_W4A16_INVALID_ARG, "null weight pointer");
+  if (!h->packed) return fail(MOE_W4A16_NOT_PACKED, "weights not packed");
+  auto s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA_TRY(launch_unpack(h->w1p, reinterpret_cast<uint32_t*>(w1_q), w1_s, h->E, h->K, 2 * h->N,
+                             2 * h->N / kBM, h->K / kBK, 1, s));
+  MOE_CUDA_TRY(launch_unpack(h->w2p, reinterpret_cast<uint32_t*>(w2_q), w2_s, h->E, h->N, h->K,
+                             h->K / kBM, h->N / kBK, 0, s));
+  return MOE_W4A16_OK;
+}
+
+size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M) {
+  if (!h || M < 0) return 0;
+  return ws_layout(h, M).total;
+}
+
+size_t moe_w4a16_host_staging_size(moe_w4a16_t h, int M) {
+  if (!h || M < 0) return 0;
+  return staging_bytes(h, M);
+}
+
+int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
+  if (!h) return fail(MOE_W4A16_INVALID_ARG, "null handle");
+  switch (option) {
+    case MOE_W4A16_OPT_NUM_CTAS:
+      if (value < 1 || value > kMaxCtas) return fail(MOE_W4A16_INVALID_ARG, "num_ctas must be in [1, 256]");
+      h->num_ctas = value;
+      return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_PROFILE:
+      if (value && !h->ev_valid) {
+        for (auto& ev : h->ev) MOE_CUDA_TRY(cudaEventCreate(&ev));
+        h->ev_valid = true;
+      }
+      h->profile = value != 0;
+      return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_PDL:
+      h->pdl = value != 0;
+      return MOE_W4A16_OK;
+    default:
+      return fail(MOE_W4A16_INVALID_ARG, "unknown option");
+  }
+}
+
+int moe_w4a16_kernel_times(moe_w4a16_t h, float* ms, int n) {
+  if (!h || !ms) return fail(MOE_W4A16_INVALID_ARG, "null argument");
+  if (!h->ev_valid) return fail(MOE_W4A16_INVALID_ARG, "profiling was never enabled");
+  MOE_CUDA_TRY(cudaEventSynchronize(h->ev[5]));
+  int w = 0;
+  for (int i = 0; i < 5 && w < n; ++i, ++w) MOE_CUDA_TRY(cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]));
+  return w;
+}
+
+int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                      const float* topk_weights, uint16_t* out, int M, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (M < 0) return fail(MOE_W4A16_INVALID_ARG, "M must be >= 0");
+  if (M == 0) return MOE_W4A16_OK;
+  if (!hidden || !topk_ids || !topk_weights || !out || !workspace)
+    return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  if (!h->packed) return fail(MOE_W4A16_NOT_PACKED, "moe_w4a16_pack has not been called");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(MOE_W4A16_INVALID_ARG, "workspace must be 256-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return fail(MOE_W4A16_INVALID_ARG, "hidden and out must be 16-byte aligned");
+  const long long MK = static_cast<long long>(M) * h->topk;
+  if (MK > (1LL << 26)) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "M * topk too large");
+  const WsLayout L = ws_layout(h, M);
+  if (workspace_bytes < L.total)
+    return fail(MOE_W4A16_WORKSPACE_TOO_SMALL,
+                "workspace too small: need " + std::to_string(L.total) + " bytes");
+  auto s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  int32_t* tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  TokenTile* tiles = reinterpret_cast<TokenTile*>(ws + L.tiles);
+  int32_t* expert_tiles = reinterpret_cast<int32_t*>(ws + L.expert_tiles);
+  uint8_t* xs = ws + L.xs;
+  uint8_t* hbuf = ws + L.hbuf;
+  float* scratch = reinterpret_cast<float*>(ws + L.scratch);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  const bool prof = h->profile && h->ev_valid;
+  const bool pdl = h->pdl && !prof;
+
+  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[0], s));
+  AlignArgs aa{};
+  aa.topk_ids = topk_ids;
+  aa.MK = static_cast<int>(MK);
+  aa.E = h->E;
+  aa.block = kRowGroup;
+  aa.bn_max = kBNMax;
+  aa.sorted_ids = sorted;
+  aa.tiles = tiles;
+  aa.expert_tiles = expert_tiles;
+  aa.hdr = hdr;
+  aa.tickets = tickets;
+  aa.n_tickets = kMaxCtas;
+  MOE_CUDA_TRY(launch_align(aa, s, false));
+  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
+
+  GatherArgs ga{};
+  ga.x = hidden;
+  ga.sorted_ids = sorted;
+  ga.hdr = hdr;
+  ga.MK = static_cast<int>(MK);
+  ga.topk = h->topk;
+  ga.K = h->K;
+  ga.Gcap = L.Gcap;
+  ga.xs = xs;
+  ga.acc = acc;
+  ga.acc_elems = static_cast<long long>(M) * h->K;
+  MOE_CUDA_TRY(launch_gather(ga, L.Gcap, h->num_sms, s, pdl));
+  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[2], s));
+
+  GemmArgs g1{};
+  g1.wpack = h->w1p;
+  g1.bsrc = xs;
+  g1.hdr = hdr;
+  g1.tiles = tiles;
+  g1.expert_tiles = expert_tiles;
+  g1.R = 2 * h->N / kBM;
+  g1.KBn = h->K / kBK;
+  g1.Gcap = L.Gcap;
+  g1.hout = hbuf;
+  g1.scratch = scratch;
+  g1.tickets = tickets;
+  g1.MK = static_cast<int>(MK);
+  g1.topk = h->topk;
+  g1.status = hdr + kHdrStatus;
+  MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
+  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
+
+  GemmArgs g2{};
+  g2.wpack = h->w2p;
+  g2.bsrc = hbuf;
+  g2.hdr = hdr;
+  g2.tiles = tiles;
+  g2.expert_tiles = expert_tiles;
+  g2.R = h->K / kBM;
+  g2.KBn = h->N / kBK;
+  g2.Gcap = L.Gcap;
+  g2.sorted_ids = sorted;
+  g2.topk_weights = topk_weights;
+  g2.acc = acc;
+  g2.Kout = h->K;
+  g2.MK = static_cast<int>(MK);
+  g2.topk = h->topk;
+  g2.status = hdr + kHdrStatus;
+  MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
+  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
+
+  MOE_CUDA_TRY(launch_finalize(acc, out, static_cast<long long>(M) * h->K, h->num_sms, s, pdl));
+  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[5], s));
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_forward_host(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                           const float* topk_weights, uint16_t* out, int M, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (M < 0) return fail(MOE_W4A16_INVALID_ARG, "M must be >= 0");
+  if (M == 0) return MOE_W4A16_OK;
+  if (!hidden || !topk_ids || !topk_weights || !out || !workspace)
+    return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  const size_t need = ws_layout(h, M).total;
+  const size_t stage = staging_bytes(h, M);
+  if (workspace_bytes < need + stage)
+    return fail(MOE_W4A16_WORKSPACE_TOO_SMALL,
+                "workspace too small: need " + std::to_string(need + stage) + " bytes");
+  auto s = static_cast<cudaStream_t>(stream);
+  uint8_t* st = static_cast<uint8_t*>(workspace) + need;
+  const size_t xb = static_cast<size_t>(M) * h->K * 2, rb = static_cast<size_t>(M) * h->topk * 4;
+  uint16_t* d_x = reinterpret_cast<uint16_t*>(st);
+  uint16_t* d_out = reinterpret_cast<uint16_t*>(st + align_up(xb, 256));
+  int32_t* d_ids = reinterpret_cast<int32_t*>(st + 2 * align_up(xb, 256));
+  float* d_w = reinterpret_cast<float*>(st + 2 * align_up(xb, 256) + align_up(rb, 256));
+  MOE_CUDA_TRY(cudaMemcpyAsync(d_x, hidden, xb, cudaMemcpyHostToDevice, s));
+  MOE_CUDA_TRY(cudaMemcpyAsync(d_ids, topk_ids, rb, cudaMemcpyHostToDevice, s));
+  MOE_CUDA_TRY(cudaMemcpyAsync(d_w, topk_weights, rb, cudaMemcpyHostToDevice, s));
+  if (int rc = moe_w4a16_forward(h, d_x, d_ids, d_w, d_out, M, workspace, need, stream)) return rc;
+  MOE_CUDA_TRY(cudaMemcpyAsync(out, d_out, xb, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaStreamSynchronize(s));
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_status(moe_w4a16_t h, const void* workspace, int32_t* status, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (!workspace || !status) return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  auto s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA_TRY(cudaMemcpyAsync(status, static_cast<const uint8_t*>(workspace), sizeof(int32_t),
+                               cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaStreamSynchronize(s));
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M, uint16_t* h_rows,
+                                void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (!workspace || !h_rows || M <= 0) return fail(MOE_W4A16_INVALID_ARG, "bad argument");
+  const WsLayout L = ws_layout(h, M);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  MOE_CUDA_TRY(launch_read_intermediate(ws + L.hbuf, reinterpret_cast<const int32_t*>(ws + L.sorted),
+                                        reinterpret_cast<const int32_t*>(ws + L.hdr), M * h->topk,
+                                        h->N, L.Gcap, L.Pcap, h_rows,
+                                        static_cast<cudaStream_t>(stream)));
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int block,
+                          int32_t* sorted_ids, int32_t* expert_offsets, int32_t* num_padded,
+                          int capacity, void* stream) {
+  if (M < 0 || topk < 1 || E < 1 || E > kMaxExperts || block < 1)
+    return fail(MOE_W4A16_INVALID_ARG, "bad shape");
+  if ((M > 0 && !topk_ids) || !sorted_ids || !expert_offsets || !num_padded)
+    return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  const long long MK = static_cast<long long>(M) * topk;
+  const long long active = MK < E ? MK : E;
+  if (capacity < MK + active * (block - 1))
+    return fail(MOE_W4A16_INVALID_ARG, "capacity too small");
+  AlignArgs aa{};
+  aa.topk_ids = topk_ids;
+  aa.MK = static_cast<int>(MK);
+  aa.E = E;
+  aa.block = block;
+  aa.bn_max = 0;
+  aa.sorted_ids = sorted_ids;
+  aa.expert_offsets = expert_offsets;
+  aa.num_padded_out = num_padded;
+  MOE_CUDA_TRY(launch_align(aa, static_cast<cudaStream_t>(stream), false));
+  return MOE_W4A16_OK;
+}
+
+}  // extern "C"

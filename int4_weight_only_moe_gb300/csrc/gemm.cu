@@ -1,0 +1,548 @@
+// The two expert GEMMs of the W4A16 fused MoE feed-forward on the 5th-generation
+// tensor cores (tcgen05), one persistent warp-specialised kernel template:
+//
+//   gate/up:  [g; u] = W1[e] . x_t   (W1 rows interleaved gate/up), epilogue
+//             h = SiLU(g) * u -> bf16 intermediate (blocked layout)
+//   down:     y = W2[e] . h_r,  epilogue acc[t] += topk_weight * y  (fp32 red.add)
+//
+// "Swap-AB" orientation: the 128 weight rows of a tile are the MMA M dimension
+// and the routed tokens of one expert (16..128, a multiple of 16) are MMA N, so a
+// single token (decode) costs one N=16 tile instead of a 128-row tile.
+//
+// Per CTA (one per SM), 16 warps:
+//   warp 0       bulk-copies packed INT4 weight blocks (4.5 KB) into a 16-deep ring
+//   warp 1       bulk-copies the activation tile (B operand) into a 6-deep ring
+//   warp 2       allocates tensor memory; one thread issues tcgen05.mma
+//   warps 4..11  dequantise INT4 -> bf16 in registers and store the A operand
+//                straight into tensor memory (tcgen05.st), 4-deep ring
+//   warps 12..15 epilogue: tcgen05.ld of the fp32 accumulator (double-buffered)
+//
+// The dequantisation writes the weight tile into tensor memory rather than
+// shared memory, so shared-memory bandwidth carries only the packed codes and the
+// activations; the MMA reads A from tensor memory and B from shared memory.
+//
+// Work split (stream-K): the units (expert, 128-row weight tile, token tile) each
+// have KBn k-blocks of 64 reduction elements; all units' k-blocks are laid end to
+// end and every CTA takes an equal contiguous share. Every SM therefore streams the
+// same number of weight bytes whatever the routing. A unit cut between CTAs is
+// finished by its last contributor: down-GEMM partials are simply added into the
+// fp32 accumulator; gate/up partials go to a per-CTA scratch slot, and the CTA
+// whose atomic ticket completes the unit's k-block count sums the slots in CTA
+// order (deterministic), applies SiLU*up and writes the tile. No CTA ever waits
+// for another.
+//
+// Every mbarrier wait is bounded in time (see mbar_wait); a wait that gives up
+// raises a CTA-wide abort flag, records MOE_W4A16_STATUS_TIMEOUT, and all roles
+// fall through to the teardown, which still waits for in-flight copies and MMAs
+// and frees tensor memory.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kNW = 16;                  // weight ring depth (shared memory)
+constexpr int kNB = 6;                   // activation ring depth (shared memory)
+constexpr int kNA = 4;                   // A-operand ring depth (tensor memory)
+constexpr int kBStage = kBNMax * 128;    // 16 KB
+constexpr int kTmemCols = 512;
+constexpr int kACols = 32;               // one k-block of bf16 A: 128 lanes x 32 columns
+constexpr int kAccCol0 = kNA * kACols;   // accumulators follow the A ring
+constexpr int kStatusTimeout = 2;
+
+constexpr int kSmB = 0;
+constexpr int kSmW = kSmB + kNB * kBStage;
+constexpr int kSmStage = ((kSmW + kNW * kWBlockBytes + 1023) / 1024) * 1024;
+constexpr int kSmBar = kSmStage + kBNMax * 128;
+// barrier indices
+constexpr int kBarWFull = 0;
+constexpr int kBarWEmpty = kBarWFull + kNW;
+constexpr int kBarBFull = kBarWEmpty + kNW;
+constexpr int kBarBEmpty = kBarBFull + kNB;
+constexpr int kBarAFull = kBarBEmpty + kNB;
+constexpr int kBarAEmpty = kBarAFull + kNA;
+constexpr int kBarAccFull = kBarAEmpty + kNA;
+constexpr int kBarAccEmpty = kBarAccFull + 2;
+constexpr int kBarDrain = kBarAccEmpty + 2;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kSmMisc = kSmBar + kNumBars * 8;
+constexpr int kSmBytes = kSmMisc + 64;
+constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
+static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
+static_assert(kAccCol0 + 2 * kBNMax <= kTmemCols, "tensor memory budget");
+
+constexpr int kWarpW = 0, kWarpB = 1, kWarpMma = 2, kWarpDeq0 = 4, kWarpEpi0 = 12;
+constexpr int kDeqThreads = 256, kEpiThreads = 128;
+constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
+
+// Bounded wait that ignores the abort flag: used at teardown to let copies and
+// MMAs already in flight land before shared and tensor memory are released.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;
+  }
+}
+
+struct Sched {
+  long long W;  // total k-blocks
+  int G;        // CTAs
+  __device__ __forceinline__ long long start(int c) const {
+    return static_cast<long long>(c) * W / G;
+  }
+  // CTA whose share contains k-block g.
+  __device__ int cta_of(long long g) const {
+    int c = static_cast<int>((g * G) / (W > 0 ? W : 1));
+    if (c > G - 1) c = G - 1;
+    while (c + 1 < G && start(c + 1) <= g) ++c;
+    while (c > 0 && start(c) > g) --c;
+    return c;
+  }
+};
+
+struct SegIter {
+  long long g, gend;
+  int KBn;
+  // Next (unit, k-block range) of this CTA's share.
+  __device__ __forceinline__ bool next(long long& u, int& kb0, int& kb1) {
+    if (g >= gend) return false;
+    u = g / KBn;
+    kb0 = static_cast<int>(g - u * KBn);
+    const long long lim = gend - u * KBn;
+    kb1 = static_cast<int>(lim < KBn ? lim : KBn);
+    g = u * KBn + kb1;
+    return true;
+  }
+};
+
+struct Unit {
+  int e, rt, g0, ng;
+};
+
+// Units are ordered [expert][row tile][token tile of that expert], so the token
+// tiles sharing one weight tile run back to back (the re-read hits L2).
+__device__ __forceinline__ Unit decode_unit(long long u, int R, const TokenTile* tiles,
+                                            const int32_t* expert_tiles) {
+  const TokenTile a = tiles[u / R];
+  const int te = expert_tiles[a.expert];
+  const long long up = u - static_cast<long long>(R) * a.first;
+  Unit r;
+  r.e = a.expert;
+  r.rt = static_cast<int>(up / te);
+  const TokenTile b = tiles[a.first + static_cast<int>(up % te)];
+  r.g0 = b.g0;
+  r.ng = b.ngroups;
+  return r;
+}
+
+// 32 INT4 codes (one scale group) -> 16 bf16x2 words, columns of the A operand.
+// (128 + u) is built exactly by OR-ing the code into the mantissa of bf16 128;
+// subtracting 136 gives u - 8 exactly, and one rounding multiply by the scale
+// gives bf16((u - 8) * s).
+__device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t sc, uint32_t (&out)[16]) {
+  const uint32_t s2 = sc | (sc << 16);
+  const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t v = ((w[j] >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+      out[4 * j + p] = bf16x2_mul(bf16x2_sub(v, 0x43084308u), s2);
+    }
+  }
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// SiLU(gate) * up for one 16-column chunk of the accumulator and store into the
+// staging tile (blocked, swizzled). Lanes (2i, 2i+1) hold the gate and up rows of
+// feature i; the even lane writes tokens 0..7 of the chunk, the odd lane 8..15.
+__device__ __forceinline__ void swiglu_chunk(const float (&v)[16], int chunk, int quad, int lane,
+                                             uint32_t s_stage) {
+  float p[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = __shfl_xor_sync(0xffffffffu, v[i], 1);
+  const bool is_gate = (lane & 1) == 0;
+  const int f = quad * 16 + (lane >> 1);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if ((i < 8) == is_gate) {
+      const float g = is_gate ? v[i] : p[i];
+      const float u = is_gate ? p[i] : v[i];
+      const float hv = g / (1.0f + __expf(-g)) * u;
+      const int row = chunk * 16 + i;
+      st_shared_u16(s_stage + blocked_offset(row, f), bf16_bits(hv));
+    }
+  }
+}
+
+template <int kMode>  // 1: gate/up + SwiGLU, 2: down + weighted scatter-add
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sB = base + kSmB, sW = base + kSmW, sStage = base + kSmStage;
+  const uint32_t sBar = base + kSmBar;
+  auto bar = [sBar](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kSmMisc);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + kSmMisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(gbase + kSmMisc + 8);
+  volatile int* epi_ok = reinterpret_cast<volatile int*>(gbase + kSmMisc + 16);  // [2][4]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNW; ++i) {
+      mbar_init(bar(kBarWFull + i), 1);
+      mbar_init(bar(kBarWEmpty + i), kDeqThreads);
+    }
+    for (int i = 0; i < kNB; ++i) {
+      mbar_init(bar(kBarBFull + i), 1);
+      mbar_init(bar(kBarBEmpty + i), 1);
+    }
+    for (int i = 0; i < kNA; ++i) {
+      mbar_init(bar(kBarAFull + i), kDeqThreads);
+      mbar_init(bar(kBarAEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarAccFull + i), 1);
+      mbar_init(bar(kBarAccEmpty + i), kEpiThreads);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  pdl_wait();  // the align/gather (or gate/up) kernel's outputs are read below
+  const int num_tiles = a.hdr[kHdrNumTiles];
+  const Sched sc{static_cast<long long>(num_tiles) * a.R * a.KBn, static_cast<int>(gridDim.x)};
+  const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
+  int* status = a.status;
+  pdl_launch_dependents();
+
+  if (warp == kWarpW) {
+    // ------------------------------------------------ packed-weight producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      SegIter si{my_begin, my_end, a.KBn};
+      long long u;
+      int kb0, kb1;
+      bool ok = true;
+      while (ok && si.next(u, kb0, kb1)) {
+        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        const uint8_t* src =
+            a.wpack + ((static_cast<long long>(un.e) * a.R + un.rt) * a.KBn + kb0) * kWBlockBytes;
+        for (int kb = kb0; kb < kb1; ++kb, ++it, src += kWBlockBytes) {
+          const int s = it % kNW;
+          if (!mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
+                         kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
+          bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
+        }
+      }
+      for (uint32_t j = 0; j < kNW && j < it; ++j) {
+        const uint32_t idx = it - 1 - j;
+        mbar_wait_drain(bar(kBarWFull + idx % kNW), (idx / kNW) & 1);
+      }
+    }
+  } else if (warp == kWarpB) {
+    // ------------------------------------------------ activation (B operand) producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      SegIter si{my_begin, my_end, a.KBn};
+      long long u;
+      int kb0, kb1;
+      bool ok = true;
+      while (ok && si.next(u, kb0, kb1)) {
+        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        const uint32_t bytes = static_cast<uint32_t>(un.ng) * kRowGroupBytes;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % kNB;
+          if (!mbar_wait(bar(kBarBEmpty + s), ((it / kNB) & 1) ^ 1, abort_flag, status,
+                         kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src =
+              a.bsrc + (static_cast<long long>(kb) * a.Gcap + un.g0) * kRowGroupBytes;
+          mbar_arrive_expect_tx(bar(kBarBFull + s), bytes);
+          bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarBFull + s));
+        }
+      }
+      for (uint32_t j = 0; j < kNB && j < it; ++j) {
+        const uint32_t idx = it - 1 - j;
+        mbar_wait_drain(bar(kBarBFull + idx % kNB), (idx / kNB) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      SegIter si{my_begin, my_end, a.KBn};
+      long long u;
+      int kb0, kb1;
+      bool ok = true;
+      while (ok && si.next(u, kb0, kb1)) {
+        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        const uint32_t idesc = idesc_bf16_f32(kBM, un.ng * kRowGroup);
+        const int ab = acc_it & 1;
+        if (!mbar_wait(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
+                       kStatusTimeout)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int sa = it % kNA, sb = it % kNB;
+          if (!mbar_wait(bar(kBarAFull + sa), (it / kNA) & 1, abort_flag, status,
+                         kStatusTimeout) ||
+              !mbar_wait(bar(kBarBFull + sb), (it / kNB) & 1, abort_flag, status,
+                         kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + sa * kACols;
+          const uint32_t b_addr = sB + sb * kBStage;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_mma_ts(d_tmem, a_tmem + kk * 8, sw128_kmajor_desc(b_addr + kk * 32), idesc,
+                      (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(kBarAEmpty + sa));
+          tc_commit(bar(kBarBEmpty + sb));
+        }
+        if (!ok) break;
+        tc_commit(bar(kBarAccFull + ab));
+        ++acc_it;
+      }
+      tc_commit(bar(kBarDrain));
+      mbar_wait_drain(bar(kBarDrain), 0);
+    }
+  } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
+    // ------------------------------------------------ dequantisation into tensor memory
+    const int quad = warp & 3;
+    const int half = (warp - kWarpDeq0) >> 2;  // scale group within the k-block
+    const int r = quad * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t it = 0;
+    SegIter si{my_begin, my_end, a.KBn};
+    long long u;
+    int kb0, kb1;
+    bool ok = true;
+    while (ok && si.next(u, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int ws = it % kNW, sa = it % kNA;
+        bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
+                              kStatusTimeout);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        const uint32_t wb = sW + ws * kWBlockBytes;
+        const uint4 qv = ld_shared_v4(wb + half * 2048 + r * 16);
+        const uint32_t scl = ld_shared_u16(wb + kWCodeBytes + half * 256 + r * 2);
+        uint32_t out[16];
+        dequant_group(qv, scl, out);
+        mbar_arrive(bar(kBarWEmpty + ws));
+        w_ok = mbar_wait(bar(kBarAEmpty + sa), ((it / kNA) & 1) ^ 1, abort_flag, status,
+                         kStatusTimeout);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(tmem + t_lane + sa * kACols + half * 16, out);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarAFull + sa));
+      }
+    }
+  } else if (warp >= kWarpEpi0) {
+    // ------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int epi_tid = threadIdx.x - kWarpEpi0 * 32;
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t acc_it = 0;
+    SegIter si{my_begin, my_end, a.KBn};
+    long long u;
+    int kb0, kb1;
+    while (si.next(u, kb0, kb1)) {
+      const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      const int nch = un.ng;  // 16-column chunks
+      const int ab = acc_it & 1;
+
+      // routing of the tile's token rows (down GEMM), fetched before the wait
+      int sid_r[4] = {0, 0, 0, 0}, tok_r[4] = {0, 0, 0, 0};
+      float w_r[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (kMode == 2) {
+        const int pbase = un.g0 * kRowGroup;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int row = 32 * j + lane;
+          const int sid = row < nch * 16 ? a.sorted_ids[pbase + row] : a.MK;
+          sid_r[j] = sid;
+          if (sid < a.MK) {
+            w_r[j] = a.topk_weights[sid];
+            tok_r[j] = sid / a.topk;
+          }
+        }
+      }
+
+      bool w_ok = mbar_wait(bar(kBarAccFull + ab), (acc_it >> 1) & 1, abort_flag, status,
+                            kStatusTimeout);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (lane == 0) epi_ok[(acc_it & 1) * 4 + quad] = w_ok ? 1 : 0;
+      named_bar_sync(kEpiBar, kEpiThreads);
+      const bool all_ok = epi_ok[(acc_it & 1) * 4 + 0] && epi_ok[(acc_it & 1) * 4 + 1] &&
+                          epi_ok[(acc_it & 1) * 4 + 2] && epi_ok[(acc_it & 1) * 4 + 3];
+      if (!all_ok) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem + t_lane + kAccCol0 + ab * kBNMax;
+
+      if constexpr (kMode == 1) {
+        const bool full = (kb0 == 0 && kb1 == a.KBn);
+        bool write_tile = full;
+        if (full) {
+          for (int c = 0; c < nch; ++c) {
+            uint32_t raw_v[16];
+            tmem_ld16(tacc + c * 16, raw_v);
+            tmem_ld_wait();
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(raw_v[i]);
+            swiglu_chunk(v, c, quad, lane, sStage);
+          }
+          tc_fence_before();
+          mbar_arrive(bar(kBarAccEmpty + ab));
+        } else {
+          // split unit: park this CTA's partial sums, take a ticket
+          const long long ustart = u * a.KBn;
+          const int part = (sc.start(blockIdx.x) < ustart) ? 1 : 0;
+          float* slot = a.scratch + (static_cast<long long>(blockIdx.x) * 2 + part) * kBNMax * kBM;
+          for (int c = 0; c < nch; ++c) {
+            uint32_t raw_v[16];
+            tmem_ld16(tacc + c * 16, raw_v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              __stcg(slot + (c * 16 + i) * kBM + r, __uint_as_float(raw_v[i]));
+          }
+          tc_fence_before();
+          mbar_arrive(bar(kBarAccEmpty + ab));
+          __threadfence();
+          named_bar_sync(kEpiBar, kEpiThreads);
+          const int c0 = sc.cta_of(ustart), c1 = sc.cta_of(ustart + a.KBn - 1);
+          if (epi_tid == 0) {
+            const int add = kb1 - kb0;
+            const int old = atomicAdd(a.tickets + c0, add);
+            *last_flag = (old + add == a.KBn) ? 1 : 0;
+          }
+          named_bar_sync(kEpiBar, kEpiThreads);
+          write_tile = *last_flag != 0;
+          if (write_tile) {
+            __threadfence();
+            for (int c = 0; c < nch; ++c) {
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = 0.f;
+              for (int cc = c0; cc <= c1; ++cc) {
+                const int pc = (sc.start(cc) < ustart) ? 1 : 0;
+                const float* sl =
+                    a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
+              }
+              swiglu_chunk(v, c, quad, lane, sStage);
+            }
+          }
+        }
+        if (write_tile) {
+          fence_proxy_async_smem();
+          named_bar_sync(kEpiBar, kEpiThreads);
+          if (epi_tid == 0) {
+            bulk_s2g(a.hout + (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes,
+                     sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          named_bar_sync(kEpiBar, kEpiThreads);
+        }
+      } else {
+        float* acc_col = a.acc + static_cast<long long>(un.rt) * kBM + r;
+#pragma unroll
+        for (int c = 0; c < kBNMax / 16; ++c) {
+          if (c < nch) {
+            uint32_t raw_v[16];
+            tmem_ld16(tacc + c * 16, raw_v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int row = c * 16 + i;
+              const int sid = __shfl_sync(0xffffffffu, sid_r[row >> 5], row & 31);
+              if (sid < a.MK) {
+                const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
+                const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
+                atomicAdd(acc_col + static_cast<long long>(tok) * a.Kout,
+                          wt * __uint_as_float(raw_v[i]));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(kBarAccEmpty + ab));
+      }
+      ++acc_it;
+    }
+    if (epi_tid == 0) bulk_wait_all();
+  }
+
+  // ------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t gemm_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmAlloc);
+}
+
+cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
+  return launch_k(gemm_kernel<1>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a);
+}
+
+cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
+  return launch_k(gemm_kernel<2>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a);
+}
+
+}  // namespace moe

@@ -1,0 +1,97 @@
+// Launchers of the forward's kernels (each defined in its own translation unit).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <utility>
+
+#include "layout.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+cudaError_t launch_repack(const uint32_t* q, const uint16_t* s, uint8_t* out, int E, int Kred,
+                          int Nout, int R, int KBn, int interleave, cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t* in, uint32_t* q, uint16_t* s, int E, int Kred, int Nout,
+                          int R, int KBn, int interleave, cudaStream_t stream);
+
+// Token->expert align (counting sort + padding + token-tile list). With bn_max == 0
+// no tile list is written (the debug entry point); expert_offsets may be null.
+struct AlignArgs {
+  const int32_t* topk_ids;
+  int MK;             // M * topk (flat slot count; also the padding sentinel)
+  int E;
+  int block;          // per-expert padding granularity
+  int bn_max;         // token-tile size (multiple of 16) or 0
+  int32_t* sorted_ids;
+  int32_t* expert_offsets;  // [E + 1] or null
+  TokenTile* tiles;         // or null
+  int32_t* expert_tiles;    // [E] token tiles per expert, or null
+  int32_t* hdr;             // workspace header (status, num_padded, num_tiles)
+  int32_t* tickets;         // zeroed, or null
+  int n_tickets;
+  int32_t* num_padded_out;  // optional extra copy of num_padded
+};
+cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl);
+
+// Expert-sorted, blocked copy of the hidden states; also zeroes the fp32 accumulator.
+struct GatherArgs {
+  const uint16_t* x;  // [M, K] bf16
+  const int32_t* sorted_ids;
+  const int32_t* hdr;
+  int MK, topk, K, Gcap;
+  uint8_t* xs;        // blocked [K/64][Gcap][16 x 128 B]
+  float* acc;         // [M, K] fp32, zeroed
+  long long acc_elems;
+};
+cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
+                          bool pdl);
+
+struct GemmArgs {
+  const uint8_t* wpack;    // packed weights of this GEMM
+  const uint8_t* bsrc;     // blocked activations (B operand)
+  const int32_t* hdr;
+  const TokenTile* tiles;
+  const int32_t* expert_tiles;
+  int R;                   // row tiles per expert
+  int KBn;                 // k-blocks per unit
+  int Gcap;                // row groups per k-block plane of bsrc / hout
+  // gate/up GEMM
+  uint8_t* hout;           // blocked intermediate activations [N/64][Gcap][...]
+  float* scratch;          // split-K partial tiles [kMaxCtas][2][kBNMax][128]
+  int32_t* tickets;        // [kMaxCtas]
+  // down GEMM
+  const int32_t* sorted_ids;
+  const float* topk_weights;
+  float* acc;              // [M, Kout] fp32
+  int Kout, MK, topk;
+  int32_t* status;
+};
+cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
+cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
+cudaError_t gemm_set_attributes();
+
+cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
+                            cudaStream_t stream, bool pdl);
+
+cudaError_t launch_read_intermediate(const uint8_t* hbuf, const int32_t* sorted_ids,
+                                     const int32_t* hdr, int MK, int N, int Gcap, int max_rows,
+                                     uint16_t* h_rows, cudaStream_t stream);
+
+// Launch helper: optional programmatic dependent launch attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace moe

@@ -1,0 +1,60 @@
+// Data layouts in device memory shared by the kernels and the host launcher.
+//
+// Packed weights (written once by the repack kernel). A GEMM operand W of shape
+// [rows, Kred] (rows = output features) is cut into tiles of 128 rows and
+// k-blocks of 64 reduction elements. Each (expert, row tile, k-block) is one
+// contiguous 4608-byte block, so one bulk copy moves it into shared memory:
+//
+//   bytes [0, 4096):    codes, [half h (0..1)][row r (0..127)][4 words]; word j of
+//                       (h, r) holds reduction elements 32h + 8j .. 32h + 8j + 7
+//   bytes [4096, 4608): bf16 scales, [half h][row r]; half h is the scale group
+//
+// Inside a word the eight 4-bit codes are interleaved so that one shift and one
+// mask put elements (2p, 2p+1) into the two bf16 halves of a 32-bit register:
+// element 2p sits at bits 4p..4p+3 and element 2p+1 at bits 16+4p..16+4p+3.
+//
+// Blocks are ordered [expert][row tile][k-block]; a whole row tile is contiguous.
+// The gate/up GEMM interleaves its rows: row 2i of tile rt is gate feature
+// 64*rt + i and row 2i+1 is up feature 64*rt + i, so one tile holds matching
+// gate and up rows for 64 intermediate features.
+//
+// Activations feeding the tensor core as the B operand (expert-sorted hidden
+// states and the intermediate activations) are "blocked": [k-block][row group of
+// 16 rows][16 rows x 128 bytes], each 128-byte row holding 64 bf16 reduction
+// elements with the 16-byte chunks XOR-swizzled by (row % 8). A contiguous run of
+// row groups of one k-block is exactly the shared-memory image the tensor core
+// reads with a 128-byte-swizzle K-major descriptor.
+#pragma once
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kGroup = 32;          // INT4 scale group along the reduction dimension
+constexpr int kBM = 128;            // weight rows per tile (MMA M)
+constexpr int kBK = 64;             // reduction elements per k-block
+constexpr int kWBlockBytes = 4608;  // one packed (row tile, k-block) block
+constexpr int kWCodeBytes = 4096;
+constexpr int kBNMax = 128;         // largest token tile (MMA N)
+constexpr int kRowGroup = 16;       // token rows per blocked row group
+constexpr int kRowGroupBytes = kRowGroup * 128;
+constexpr int kMaxCtas = 256;       // persistent grid limit (tickets / scratch slots)
+constexpr int kMaxExperts = 1024;
+
+// Byte offset of bf16 element (row, k) inside one 16-row group of a k-block
+// (row in [0, 16), k in [0, 64)).
+__host__ __device__ __forceinline__ uint32_t blocked_offset(int row, int k) {
+  return static_cast<uint32_t>(row * 128 + ((((k >> 3) ^ (row & 7)) & 7) << 4) + ((k & 7) << 1));
+}
+
+// One entry of the token-tile list built by the align kernel.
+struct TokenTile {
+  int expert;   // expert id
+  int g0;       // first row group (16 rows) in the expert-sorted order
+  int ngroups;  // row groups in the tile (MMA N = 16 * ngroups)
+  int first;    // index of this expert's first token tile
+};
+
+// Header words at the start of the workspace.
+enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrWords = 64 };
+
+}  // namespace moe

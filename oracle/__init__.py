@@ -8,6 +8,7 @@ from .moe_oracle import (  # noqa: F401
     dequantize,
     expert_dense,
     expert_ffn,
+    expert_hidden,
     moe_align,
     moe_forward,
     roofline_bytes_per_expert,

@@ -78,16 +78,23 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
+def expert_hidden(x: np.ndarray, w1: np.ndarray) -> np.ndarray:
+    """Intermediate activations ``h = SiLU(x W1[:N]^T) * (x W1[N:]^T)``, ``[T, N]``.
+
+    ``w1 [2N, K]`` holds the gate rows first and the up rows second.
+    """
+    n = w1.shape[0] // 2
+    gate = x @ w1[:n].T
+    up = x @ w1[n:].T
+    return silu(gate) * up
+
+
 def expert_ffn(x: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> np.ndarray:
     """SwiGLU expert MLP on rows ``x [T, K]`` with dense ``w1 [2N, K]``, ``w2 [K, N]``.
 
     ``gate = x W1[:N]^T``, ``up = x W1[N:]^T``, ``h = SiLU(gate) * up``, ``y = h W2^T``.
     """
-    n = w1.shape[0] // 2
-    gate = x @ w1[:n].T
-    up = x @ w1[n:].T
-    h = silu(gate) * up
-    return h @ w2.T
+    return expert_hidden(x, w1) @ w2.T
 
 
 def expert_dense(w1_q, w1_s, w2_q, w2_s, e: int, group_size: int = GROUP_SIZE):

@@ -1,0 +1,209 @@
+"""CUDA path vs the CPU oracle on seeded inputs, through the C-ABI (small and
+medium shapes that still span several tiles, ragged tails and split units).
+
+Bit-exact: the align (sorted ids, offsets, padded length) and the repack round
+trip. Floating point: relative L2 error <= 5e-3 and max |error| <= 2e-2 * rms of
+the reference, for the output and for the intermediate activations."""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_only_moe_gb300 as pkg
+import oracle
+from int4_weight_only_moe_gb300 import inputs
+from tests.gpu_helpers import Problem, assert_close, bf16_tensor_to_f64, bits16, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def zipf_ids(rng, M, E, k, s=1.1):
+    p = np.arange(1, E + 1, dtype=float) ** -s
+    p /= p.sum()
+    perm = rng.permutation(E)
+    return np.stack([perm[rng.choice(E, size=k, replace=False, p=p)] for _ in range(M)]).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------- align
+
+
+@pytest.mark.parametrize("M,k,E,block,dist", [
+    (0, 8, 16, 16, "uniform"), (1, 8, 384, 16, "uniform"), (4, 2, 8, 16, "uniform"),
+    (9, 8, 384, 16, "uniform"), (90, 8, 384, 16, "uniform"), (1024, 8, 384, 16, "uniform"),
+    (1024, 8, 384, 16, "zipf"), (333, 3, 1024, 64, "uniform"), (77, 5, 40, 1, "zipf"),
+    (500, 4, 7, 5, "dup"), (4096, 8, 384, 16, "zipf"),
+])
+def test_align_bit_exact(M, k, E, block, dist):
+    rng = np.random.default_rng(M * 31 + E)
+    if dist == "uniform":
+        ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(M)]).astype(np.int32) \
+            if M else np.zeros((0, k), np.int32)
+    elif dist == "zipf":
+        ids = zipf_ids(rng, M, E, k)
+    else:  # duplicates inside a token are still well defined
+        ids = rng.integers(0, E, size=(M, k)).astype(np.int32)
+    ref_sorted, ref_off, ref_n = oracle.moe_align(ids, E, block)
+    MK = M * k
+    cap = MK + min(E, MK) * (block - 1) + 1
+    d_ids = dev(ids) if M else torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_sorted = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    d_off = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    d_n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkg.moe_w4a16_align_debug(d_ids, M, k, E, block, d_sorted, d_off, d_n)
+    torch.cuda.synchronize()
+    n = int(d_n.item())
+    assert n == ref_n
+    np.testing.assert_array_equal(d_sorted.cpu().numpy()[:n], ref_sorted)
+    np.testing.assert_array_equal(d_off.cpu().numpy(), ref_off)
+
+
+def test_align_skips_out_of_range_ids():
+    rng = np.random.default_rng(0)
+    ids = rng.integers(0, 12, size=(50, 4)).astype(np.int32)
+    ids[3, 2] = -1
+    ids[10, 0] = 12
+    ids[11, 1] = 1 << 30
+    ref_sorted, ref_off, ref_n = oracle.moe_align(ids, 12, 16)
+    cap = 50 * 4 + 12 * 15
+    d_sorted = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    d_off = torch.zeros(13, dtype=torch.int32, device="cuda")
+    d_n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkg.moe_w4a16_align_debug(dev(ids), 50, 4, 12, 16, d_sorted, d_off, d_n)
+    torch.cuda.synchronize()
+    n = int(d_n.item())
+    assert n == ref_n
+    np.testing.assert_array_equal(d_sorted.cpu().numpy()[:n], ref_sorted)
+
+
+# ---------------------------------------------------------------------------- repack
+
+
+@pytest.mark.parametrize("E,K,N", [(8, 256, 128), (3, 1024, 512), (2, 7168, 2048)])
+def test_pack_roundtrip_bit_exact(E, K, N):
+    w1_q, w1_s, w2_q, w2_s = inputs.all_expert_weights(E, K, N, seed=5)
+    moe = pkg.MoEW4A16(E, K, N, 2)
+    moe.pack(dev(w1_q), dev(bits16(w1_s)), dev(w2_q), dev(bits16(w2_s)))
+    assert pkg.moe_w4a16_packed_bytes(moe.handle) == E * oracle.roofline_bytes_per_expert(K, N)
+    outs = [torch.zeros_like(dev(a)) for a in (w1_q, bits16(w1_s), w2_q, bits16(w2_s))]
+    pkg.moe_w4a16_unpack_debug(moe.handle, *outs)
+    torch.cuda.synchronize()
+    for got, ref in zip(outs, (w1_q, bits16(w1_s), w2_q, bits16(w2_s))):
+        np.testing.assert_array_equal(got.cpu().numpy(), ref)
+    moe.close()
+
+
+# ---------------------------------------------------------------------------- forward
+
+
+def check_forward(prob, hidden, ids, wts, what):
+    got = prob.run(hidden, ids, wts)
+    ref = prob.reference(hidden, ids, wts)
+    assert_close(got, ref, what)
+    assert prob.moe.status() == 0
+    return got
+
+
+def test_tiny_forward_and_intermediate():
+    wl = inputs.WORKLOADS["tiny"]
+    prob = Problem(wl.E, wl.K, wl.N, wl.topk)
+    hidden, ids, wts = inputs.workload_inputs(wl)
+    check_forward(prob, hidden, ids, wts, "tiny")
+    h_rows = bf16_tensor_to_f64(prob.moe.intermediate(wl.M))
+    x = oracle.bf16_to_f64(hidden)
+    ref_h = np.zeros_like(h_rows)
+    for t in range(wl.M):
+        for j in range(wl.topk):
+            w1, _ = oracle.expert_dense(*prob.w, int(ids[t, j]))
+            ref_h[t * wl.topk + j] = oracle.expert_hidden(x[t:t + 1], w1)[0]
+    assert_close(h_rows, ref_h, "tiny intermediate")
+    prob.close()
+
+
+@pytest.mark.parametrize("num_ctas", [None, 1, 3, 64, 256])
+@pytest.mark.parametrize("M", [1, 5, 37, 200])
+def test_mid_forward_grid_sizes(M, num_ctas):
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = inputs.workload_inputs(wl)
+    check_forward(prob, hidden, ids, wts, f"mid M={M} ctas={num_ctas}")
+    prob.close()
+
+
+def test_hot_expert_spans_several_token_tiles():
+    # one expert receives every token (> 128 rows: several token tiles of one expert)
+    E, K, N, k, M = 8, 768, 320, 2, 300
+    prob = Problem(E, K, N, k)
+    rng = np.random.default_rng(4)
+    hidden = inputs.hidden_states(M, K)
+    ids = np.stack([np.array([3, rng.choice([e for e in range(E) if e != 3])]) for _ in range(M)]).astype(np.int32)
+    wts = rng.uniform(0.2, 0.8, size=(M, k)).astype(np.float32)
+    for ctas in (None, 7):
+        if ctas:
+            prob.set_ctas(ctas)
+        check_forward(prob, hidden, ids, wts, f"hot expert ctas={ctas}")
+    prob.close()
+
+
+def test_bad_expert_ids_are_skipped_and_flagged():
+    wl = inputs.WORKLOADS["tiny"]
+    prob = Problem(wl.E, wl.K, wl.N, wl.topk)
+    hidden, ids, wts = inputs.workload_inputs(wl)
+    ids = ids.copy()
+    ids[1, 0] = -3
+    ids[2, 1] = wl.E
+    got = prob.run(hidden, ids, wts)
+    assert prob.moe.status() & pkg.STATUS_BAD_EXPERT_ID
+    assert_close(got, prob.reference(hidden, ids, wts), "bad ids")
+    prob.close()
+
+
+def test_zero_tokens_and_small_workspace():
+    wl = inputs.WORKLOADS["tiny"]
+    prob = Problem(wl.E, wl.K, wl.N, wl.topk)
+    h = prob.moe.handle
+    empty = torch.zeros((0, wl.K), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    pkg.moe_w4a16_forward(h, empty, empty, empty, empty, 0, ws)  # M == 0 is a no-op
+    hidden, ids, wts = inputs.workload_inputs(wl)
+    out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkg.MoeW4A16Error) as ei:
+        pkg.moe_w4a16_forward(h, dev(bits16(hidden)), dev(ids), dev(wts), out, wl.M, ws)
+    assert ei.value.code == -3
+    prob.close()
+
+
+def test_forward_host_matches_device_forward():
+    E, K, N, k, M = 16, 512, 256, 4, 23
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = inputs.workload_inputs(wl)
+    dev_out = prob.run(hidden, ids, wts)
+    h_hidden = torch.from_numpy(bits16(hidden)).pin_memory()
+    h_ids = torch.from_numpy(ids).pin_memory()
+    h_wts = torch.from_numpy(wts).pin_memory()
+    h_out = torch.zeros((M, K), dtype=torch.int16).pin_memory()
+    prob.moe.forward_host(h_hidden, h_ids, h_wts, h_out)
+    host_out = h_out.view(torch.bfloat16).float().numpy().astype(np.float64)
+    assert_close(host_out, prob.reference(hidden, ids, wts), "forward_host")
+    assert np.max(np.abs(host_out - dev_out)) <= 1e-2 * np.sqrt(np.mean(dev_out ** 2))
+    prob.close()
+
+
+def test_repeated_calls_agree():
+    E, K, N, k, M = 16, 512, 256, 4, 64
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = inputs.workload_inputs(wl)
+    a = prob.run(hidden, ids, wts)
+    b = prob.run(hidden, ids, wts)
+    # the down GEMM adds partial products with float atomics: only the order may differ
+    assert np.max(np.abs(a - b)) <= 1e-2 * np.sqrt(np.mean(a ** 2))
+    prob.close()
