@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 fused MoE forward (INT4 weights, group 32, bf16
+activations) at the MoE dimensions of the pages' benchmark: E=384 experts,
+hidden 7168, intermediate 2048, top-8.
+
+One "step" = one fused forward (align, gather, gate/up GEMM, down GEMM,
+finalize) over one batch of seeded synthetic tokens with all 384 experts'
+packed weights resident in HBM. The headline line is the decode workload
+(M = 1 token, uniform router logits); the M sweep of the pages' table
+(1, 9, 32, 90, 256, 512, 1024 uniform and Zipf-skewed) is reported under
+"sweep" with each batch's roofline fraction.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); the timed region is bracketed by barriers and
+the slowest rank's time is reported. ``--impl reference`` times the CPU oracle
+(float64 numpy) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from int4_weight_only_moe_gb300 import inputs  # noqa: E402
+
+HEADLINE = "decode"
+SWEEP = ["decode", "small9", "small32", "small90", "plateau256", "plateau512", "large_uniform",
+         "large_zipf"]
+METRIC = "MoE tokens/sec and µs/call vs M (1–1024); % HBM / tensor-pipe roofline"
+L2_FLUSH_BYTES = 512 << 20
+KERNELS = ["align", "gather", "gemm_gateup", "gemm_down", "finalize"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def expert_bytes(K, N, G=32):
+    """Packed INT4 codes + bf16 scales of one expert: (gate/up, down)."""
+    w1 = 2 * N * K // 2 + 2 * N * (K // G) * 2
+    w2 = K * N // 2 + K * (N // G) * 2
+    return w1, w2
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def file_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_src):
+    """DRAM bytes per launch of the gate/up GEMM from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "gemm_gateup_decode_ncu.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != file_hash(kernel_src):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+
+class GpuBench:
+    def __init__(self, device):
+        import torch
+
+        import int4_weight_only_moe_gb300 as pkg
+        self.torch, self.pkg = torch, pkg
+        wl = inputs.WORKLOADS[HEADLINE]
+        self.E, self.K, self.N, self.topk = wl.E, wl.K, wl.N, wl.topk
+        self.device = device
+        q1, s1, q2, s2 = inputs.all_expert_weights(self.E, self.K, self.N)
+        self.moe = pkg.MoEW4A16(self.E, self.K, self.N, self.topk)
+        d = [torch.from_numpy(a).to(device) for a in (q1, s1.view(np.int16), q2, s2.view(np.int16))]
+        self.moe.pack(*d)
+        torch.cuda.synchronize()
+        del d, q1, s1, q2, s2
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.current_stream()
+
+    def step_inputs(self, wl, n):
+        torch = self.torch
+        out = []
+        for s in range(n):
+            h, ids, w = inputs.workload_inputs(wl, step=s)
+            out.append((torch.from_numpy(h.view(np.int16)).to(self.device), torch.from_numpy(ids).to(self.device),
+                        torch.from_numpy(w).to(self.device)))
+        return out
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def time_forward(self, wl, steps, warmup, profile=False, barrier=None):
+        """Per-step device time (ms) of the forward, L2 flushed before every step."""
+        torch, pkg = self.torch, self.pkg
+        data = self.step_inputs(wl, steps + warmup)
+        out = torch.empty((wl.M, self.K), dtype=torch.bfloat16, device=self.device)
+        self.moe.ensure_workspace(wl.M)
+        pkg.moe_w4a16_set_option(self.moe.handle, pkg.OPT_PROFILE, 1 if profile else 0)
+        for i in range(warmup):
+            self.moe.forward(*data[i], out=out)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        ktimes = []
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            self.flush()
+            ev[i][0].record()
+            self.moe.forward(*data[warmup + i], out=out)
+            ev[i][1].record()
+            if profile:
+                ktimes.append(pkg.moe_w4a16_kernel_times(self.moe.handle))
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        pkg.moe_w4a16_set_option(self.moe.handle, pkg.OPT_PROFILE, 0)
+        status = self.moe.status()
+        if status != 0:
+            raise RuntimeError(f"device status word {status} after {wl.name}")
+        ms = [a.elapsed_time(b) for a, b in ev]
+        return ms, ktimes, data
+
+    def time_e2e(self, wl, steps, warmup):
+        """Same metric through the host-buffer C-ABI call (H2D + forward + D2H)."""
+        torch = self.torch
+        host = []
+        for s in range(steps + warmup):
+            h, ids, w = inputs.workload_inputs(wl, step=s)
+            host.append((torch.from_numpy(h.view(np.int16)).pin_memory(), torch.from_numpy(ids).pin_memory(),
+                         torch.from_numpy(w).pin_memory()))
+        out = torch.empty((wl.M, self.K), dtype=torch.int16).pin_memory()
+        for i in range(warmup):
+            self.moe.forward_host(*host[i], out)
+        ms = []
+        for i in range(steps):
+            self.flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            self.moe.forward_host(*host[warmup + i], out)  # synchronises before returning
+            ms.append((time.perf_counter() - t0) * 1e3)
+        h2d = wl.M * self.K * 2 + 2 * wl.M * self.topk * 4
+        d2h = wl.M * self.K * 2
+        return ms, h2d, d2h
+
+
+def roofline_entry(wl, us, active, hbm_gbs, tc_tflops):
+    w1b, w2b = expert_bytes(wl.K, wl.N)
+    t_hbm = active * (w1b + w2b) / (hbm_gbs * 1e9) * 1e6
+    t_tc = 2.0 * wl.M * wl.topk * 3 * wl.N * wl.K / (tc_tflops * 1e12) * 1e6
+    t_star = max(t_hbm, t_tc)
+    return {"M": wl.M, "routing": wl.routing, "active_experts": int(active), "us_per_call": round(us, 2),
+            "tok_per_s": round(wl.M / (us * 1e-6), 1), "us_per_token": round(us / wl.M, 3),
+            "roofline_us": round(t_star, 2), "binding_roof": "hbm" if t_hbm >= t_tc else "tensor",
+            "frac_of_roofline": round(t_star / us, 4)}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+        __graft_entry__.build()
+    hbm_gbs, tc_tflops, peak_src = peaks()
+    gb = GpuBench(device)
+    wl = inputs.WORKLOADS[HEADLINE]
+    barrier = dist.barrier if world > 1 else None
+
+    with ClockSampler(local_rank) as clk:
+        ms, _, data = gb.time_forward(wl, args.steps, args.warmup, barrier=barrier)
+    total_ms = sum(ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * wl.M * args.steps / (total_ms * 1e-3)
+
+    # kernel breakdown (events between kernels), roofline of the dominant kernel
+    _, ktimes, _ = gb.time_forward(wl, args.steps, args.warmup, profile=True)
+    kmean = [statistics.mean(k[i] for k in ktimes) for i in range(len(KERNELS))]
+    ids_all = np.stack([d[1].cpu().numpy() for d in data[args.warmup:]])
+    active = float(np.mean([len(np.unique(x)) for x in ids_all]))
+    w1b, w2b = expert_bytes(wl.K, wl.N)
+    gateup_bytes = active * w1b + wl.M * wl.K * 2 + wl.M * wl.topk * wl.N * 2
+    achieved = gateup_bytes / (kmean[2] * 1e-3) / 1e9
+    traffic = recorded_traffic(os.path.join(ROOT, "int4_weight_only_moe_gb300", "csrc", "gemm.cu"))
+
+    e2e_ms, h2d, d2h = gb.time_e2e(wl, max(3, args.steps), args.warmup)
+    e2e_value = wl.M / (statistics.mean(e2e_ms) * 1e-3) * world
+
+    sweep = {}
+    if not args.no_sweep:
+        for name in SWEEP:
+            w = inputs.WORKLOADS[name]
+            sms, _, sdata = gb.time_forward(w, args.sweep_steps, 3)
+            act = float(np.mean([len(np.unique(d[1].cpu().numpy())) for d in sdata[3:]]))
+            sweep[name] = roofline_entry(w, statistics.median(sms) * 1e3, act, hbm_gbs, tc_tflops)
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random INT4 weights for all 384 experts, N(0,1) bf16 hidden, "
+                "uniform router logits -> top-8 renormalised)",
+        "config": {"workload": "decode: E=384 K=7168 N=2048 top-8 INT4 g32, M=1 token per step",
+                   "M": wl.M, "E": wl.E, "K": wl.K, "N": wl.N, "topk": wl.topk, "group_size": 32,
+                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "inputs_per_step": "distinct seeded hidden/routing each step",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "kernel_ms": {k: round(v, 5) for k, v in zip(KERNELS, kmean)},
+        "roofline": {"kernel": "gemm_gateup", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm_gbs, "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4),
+                     "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                     "algorithmic_bytes_per_launch": int(gateup_bytes),
+                     "traffic": traffic},
+        "whole_forward_roofline": roofline_entry(wl, ms_step * 1e3, active, hbm_gbs, tc_tflops),
+        "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 4)},
+        "clocks": clk.summary(),
+        "sweep": sweep,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_samples)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+
+def oracle_step(wl, step):
+    """One oracle forward of ``wl`` at ``step`` (regenerating only the experts it routes to)."""
+    import oracle
+
+    hidden, ids, w = inputs.workload_inputs(wl, step=step)
+    cache = {}
+
+    def source(e):
+        if e not in cache:
+            cache[e] = inputs.expert_weights(e, wl.K, wl.N)
+        return cache[e]
+
+    t0 = time.perf_counter()
+    oracle.moe_forward(hidden, ids, w, None, None, None, None, expert_source=source)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(samples):
+    """Time the oracle in a single-threaded child process (BLAS pinned to one thread)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench._oracle_samples(%d)))" % (ROOT, samples))
+    p = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE, text=True, check=True)
+    secs = json.loads(p.stdout.strip().splitlines()[-1])
+    wl = inputs.WORKLOADS[HEADLINE]
+    return {"value": round(wl.M * len(secs) / sum(secs), 4), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{len(secs)} decode steps (M=1, 8 experts each) of the float64 numpy oracle, "
+                      "expert weights regenerated per step outside the timed region, 1 thread"}
+
+
+def _oracle_samples(n):
+    wl = inputs.WORKLOADS[HEADLINE]
+    return [oracle_step(wl, s) for s in range(n)]
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    wl = inputs.WORKLOADS[HEADLINE]
+    # the oracle has nothing to warm up beyond one call; cap the bounded sample
+    args.warmup = min(args.warmup, 1)
+    args.steps = min(args.steps, 8)
+    for s in range(args.warmup):
+        oracle_step(wl, s)
+    secs = [oracle_step(wl, args.warmup + s) for s in range(args.steps)]
+    total = sum(secs)
+    value = wl.M * args.steps / total
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": "decode: E=384 K=7168 N=2048 top-8 INT4 g32, M=1 token per step",
+                   "M": wl.M, "E": wl.E, "K": wl.K, "N": wl.N, "topk": wl.topk},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} decode steps of the float64 numpy oracle "
+                                   "(dequantise the 8 routed experts, SwiGLU, weighted sum)"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep-steps", type=int, default=20)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-samples", type=int, default=3)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -13,7 +13,11 @@
  * where W1 = [W1g; W1u] (gate rows [0, N), up rows [N, 2N)) is [2N, K] and W2 is
  * [K, N]. Weights are symmetric INT4 with one bf16 scale per group of 32 values
  * along each GEMM's reduction dimension: value = (u - 8) * scale for a stored
- * nibble u in 0..15. Activations (x, out) are bf16.
+ * nibble u in 0..15. Activations (x, out) are bf16. The tensor cores take fp16
+ * operands (kind::f16) with fp32 accumulation: the dequantised weights (u-8)*s
+ * are exact in fp16, bf16 hidden states convert to fp16 exactly within fp16's
+ * range (values beyond +-65504 saturate, as do intermediate activations), and
+ * the output is rounded once from fp32 to bf16.
  *
  * Conventions shared by every call:
  *  - Every function returns MOE_W4A16_OK (0) or a negative code; the message of
@@ -142,9 +146,10 @@ int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int b
 int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s,
                            int32_t* w2_q, uint16_t* w2_s, void* stream);
 
-/* Copy the intermediate activations SiLU(gate)*up (bf16) of the last forward
- * that used `workspace` into h_rows [M*topk, N] (device), row = flat slot id
- * t*topk+j; rows of skipped slots are left untouched. */
+/* Copy the intermediate activations SiLU(gate)*up (fp16 bit patterns, the
+ * tensor-core operand type) of the last forward that used `workspace` into
+ * h_rows [M*topk, N] (device), row = flat slot id t*topk+j; rows of skipped
+ * slots are left untouched. */
 int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M,
                                 uint16_t* h_rows, void* stream);
 

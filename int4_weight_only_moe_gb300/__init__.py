@@ -247,6 +247,6 @@ class MoEW4A16:
 
     def intermediate(self, M: int, stream=None):
         import torch
-        h_rows = torch.zeros((M * self.topk, self.N), dtype=torch.bfloat16, device="cuda")
+        h_rows = torch.zeros((M * self.topk, self.N), dtype=torch.float16, device="cuda")
         moe_w4a16_read_intermediate(self.handle, self.workspace, M, h_rows, stream)
         return h_rows

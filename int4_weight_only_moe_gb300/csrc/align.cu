@@ -1,6 +1,7 @@
 // Token->expert align, expert-sorted gather of the hidden states, output
 // finalisation and the intermediate-activation readback used by tests.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -137,8 +138,20 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl) {
   return launch_k(align_kernel, dim3(1), dim3(1024), smem, stream, pdl, a);
 }
 
-// Copy every expert-sorted row's hidden state into the blocked B-operand layout
-// (padding rows become zeros) and zero the fp32 output accumulator.
+// bf16 pair -> fp16 pair (exact inside fp16's range, saturated to +-65504 beyond).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.0f), 65504.0f);
+  const float hi = fminf(fmaxf(__uint_as_float(w & 0xFFFF0000u), -65504.0f), 65504.0f);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                    bf16x2_to_f16x2(v.w));
+}
+
+// Copy every expert-sorted row's hidden state, as fp16, into the blocked B-operand
+// layout (padding rows become zeros) and zero the fp32 output accumulator.
 __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
   pdl_wait();
   const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -153,8 +166,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
       const int sid = a.sorted_ids[g * kRowGroup + r];
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (sid < a.MK)
-        v = *reinterpret_cast<const uint4*>(a.x + static_cast<long long>(sid / a.topk) * a.K +
-                                            ch * 8);
+        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
+            a.x + static_cast<long long>(sid / a.topk) * a.K + ch * 8));
       uint8_t* dst = a.xs + (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
                      r * 128 + (((ch & 7) ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(dst) = v;

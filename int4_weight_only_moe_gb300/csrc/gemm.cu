@@ -2,8 +2,12 @@
 // tensor cores (tcgen05), one persistent warp-specialised kernel template:
 //
 //   gate/up:  [g; u] = W1[e] . x_t   (W1 rows interleaved gate/up), epilogue
-//             h = SiLU(g) * u -> bf16 intermediate (blocked layout)
+//             h = SiLU(g) * u -> fp16 intermediate (blocked layout)
 //   down:     y = W2[e] . h_r,  epilogue acc[t] += topk_weight * y  (fp32 red.add)
+//
+// Tensor-core operands are fp16 (kind::f16, fp32 accumulate): the dequantised
+// weights are exact in fp16, and the bf16 hidden states convert to fp16 exactly
+// inside fp16's range (the gather saturates beyond +-65504).
 //
 // "Swap-AB" orientation: the 128 weight rows of a tile are the MMA M dimension
 // and the routed tokens of one expert (16..128, a multiple of 16) are MMA N, so a
@@ -13,7 +17,7 @@
 //   warp 0       bulk-copies packed INT4 weight blocks (4.5 KB) into a 16-deep ring
 //   warp 1       bulk-copies the activation tile (B operand) into a 6-deep ring
 //   warp 2       allocates tensor memory; one thread issues tcgen05.mma
-//   warps 4..11  dequantise INT4 -> bf16 in registers and store the A operand
+//   warps 4..11  dequantise INT4 -> fp16 in registers and store the A operand
 //                straight into tensor memory (tcgen05.st), 4-deep ring
 //   warps 12..15 epilogue: tcgen05.ld of the fp32 accumulator (double-buffered)
 //
@@ -35,7 +39,7 @@
 // raises a CTA-wide abort flag, records MOE_W4A16_STATUS_TIMEOUT, and all roles
 // fall through to the teardown, which still waits for in-flight copies and MMAs
 // and frees tensor memory.
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 
@@ -49,7 +53,7 @@ constexpr int kNB = 6;                   // activation ring depth (shared memory
 constexpr int kNA = 4;                   // A-operand ring depth (tensor memory)
 constexpr int kBStage = kBNMax * 128;    // 16 KB
 constexpr int kTmemCols = 512;
-constexpr int kACols = 32;               // one k-block of bf16 A: 128 lanes x 32 columns
+constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
 constexpr int kAccCol0 = kNA * kACols;   // accumulators follow the A ring
 constexpr int kStatusTimeout = 2;
 
@@ -138,26 +142,35 @@ __device__ __forceinline__ Unit decode_unit(long long u, int R, const TokenTile*
   return r;
 }
 
-// 32 INT4 codes (one scale group) -> 16 bf16x2 words, columns of the A operand.
-// (128 + u) is built exactly by OR-ing the code into the mantissa of bf16 128;
-// subtracting 136 gives u - 8 exactly, and one rounding multiply by the scale
-// gives bf16((u - 8) * s).
-__device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t sc, uint32_t (&out)[16]) {
-  const uint32_t s2 = sc | (sc << 16);
+// 32 INT4 codes (one scale group) -> 16 f16x2 words, columns of the A operand.
+// OR-ing a code u into the mantissa of fp16 1024 gives exactly 1024 + u (code at
+// bits 0..3 of a half) or 1024 + 16u (code at bits 4..7); subtracting 1032, or
+// scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
+// scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
+// (for scales in fp16's normal range), so the dequantised weight carries no
+// rounding error. One shift and four masks unpack a word of eight codes.
+__device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t s_bf16, uint32_t (&out)[16]) {
+  const __half sh = __float2half_rn(__uint_as_float(s_bf16 << 16));
+  const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const uint32_t v = ((w[j] >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-      out[4 * j + p] = bf16x2_mul(bf16x2_sub(v, 0x43084308u), s2);
-    }
+    const uint32_t q = w[j], q8 = w[j] >> 8;
+    const uint32_t v0 = (q & 0x000F000Fu) | 0x64006400u;   // elements 0, 1: 1024 + u
+    const uint32_t v1 = (q & 0x00F000F0u) | 0x64006400u;   // elements 2, 3: 1024 + 16u
+    const uint32_t v2 = (q8 & 0x000F000Fu) | 0x64006400u;  // elements 4, 5
+    const uint32_t v3 = (q8 & 0x00F000F0u) | 0x64006400u;  // elements 6, 7
+    out[4 * j + 0] = f16x2_mul(f16x2_sub(v0, 0x64086408u), s2);
+    out[4 * j + 1] = f16x2_mul(f16x2_fma(v1, 0x2C002C00u, 0xD480D480u), s2);
+    out[4 * j + 2] = f16x2_mul(f16x2_sub(v2, 0x64086408u), s2);
+    out[4 * j + 3] = f16x2_mul(f16x2_fma(v3, 0x2C002C00u, 0xD480D480u), s2);
   }
 }
 
-__device__ __forceinline__ uint16_t bf16_bits(float x) {
-  __nv_bfloat16 b = __float2bfloat16_rn(x);
-  return *reinterpret_cast<uint16_t*>(&b);
+// fp16 bits of x, saturated to the finite range (+-65504).
+__device__ __forceinline__ uint16_t f16_bits_sat(float x) {
+  x = fminf(fmaxf(x, -65504.0f), 65504.0f);
+  return __half_as_ushort(__float2half_rn(x));
 }
 
 // SiLU(gate) * up for one 16-column chunk of the accumulator and store into the
@@ -177,7 +190,7 @@ __device__ __forceinline__ void swiglu_chunk(const float (&v)[16], int chunk, in
       const float u = is_gate ? p[i] : v[i];
       const float hv = g / (1.0f + __expf(-g)) * u;
       const int row = chunk * 16 + i;
-      st_shared_u16(s_stage + blocked_offset(row, f), bf16_bits(hv));
+      st_shared_u16(s_stage + blocked_offset(row, f), f16_bits_sat(hv));
     }
   }
 }
@@ -302,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       bool ok = true;
       while (ok && si.next(u, kb0, kb1)) {
         const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-        const uint32_t idesc = idesc_bf16_f32(kBM, un.ng * kRowGroup);
+        const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
         const int ab = acc_it & 1;
         if (!mbar_wait(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
                        kStatusTimeout)) {

@@ -10,7 +10,7 @@
 //   bytes [4096, 4608): bf16 scales, [half h][row r]; half h is the scale group
 //
 // Inside a word the eight 4-bit codes are interleaved so that one shift and one
-// mask put elements (2p, 2p+1) into the two bf16 halves of a 32-bit register:
+// mask put elements (2p, 2p+1) into the two 16-bit halves of a 32-bit register:
 // element 2p sits at bits 4p..4p+3 and element 2p+1 at bits 16+4p..16+4p+3.
 //
 // Blocks are ordered [expert][row tile][k-block]; a whole row tile is contiguous.
@@ -19,8 +19,8 @@
 // gate and up rows for 64 intermediate features.
 //
 // Activations feeding the tensor core as the B operand (expert-sorted hidden
-// states and the intermediate activations) are "blocked": [k-block][row group of
-// 16 rows][16 rows x 128 bytes], each 128-byte row holding 64 bf16 reduction
+// states and the intermediate activations, both fp16) are "blocked": [k-block][row
+// group of 16 rows][16 rows x 128 bytes], each 128-byte row holding 64 fp16 reduction
 // elements with the 16-byte chunks XOR-swizzled by (row % 8). A contiguous run of
 // row groups of one k-block is exactly the shared-memory image the tensor core
 // reads with a 128-byte-swizzle K-major descriptor.
@@ -40,7 +40,7 @@ constexpr int kRowGroupBytes = kRowGroup * 128;
 constexpr int kMaxCtas = 256;       // persistent grid limit (tickets / scratch slots)
 constexpr int kMaxExperts = 1024;
 
-// Byte offset of bf16 element (row, k) inside one 16-row group of a k-block
+// Byte offset of 16-bit element (row, k) inside one 16-row group of a k-block
 // (row in [0, 16), k in [0, 64)).
 __host__ __device__ __forceinline__ uint32_t blocked_offset(int row, int k) {
   return static_cast<uint32_t>(row * 128 + ((((k >> 3) ^ (row & 7)) & 7) << 4) + ((k & 7) << 1));

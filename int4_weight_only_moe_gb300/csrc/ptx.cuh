@@ -142,7 +142,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]; bf16 inputs, fp32 accumulate.
+// D[tmem] (+)= A[tmem] * B[smem]; 16-bit inputs, fp32 accumulate.
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -181,7 +181,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major bf16 operand stored as rows of
+// Shared-memory matrix descriptor of a K-major 16-bit operand stored as rows of
 // 128 bytes (64 elements) with the 128-byte swizzle: 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -193,11 +193,11 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor, kind::f16: f16 A and B (both K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4)                                 // D format: f32
-         | (1u << 7)                               // A format: bf16
-         | (1u << 10)                              // B format: bf16
+         | (0u << 7)                               // A format: f16
+         | (0u << 10)                              // B format: f16
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
@@ -229,15 +229,20 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// bf16x2 arithmetic, round to nearest even.
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+// f16x2 arithmetic, round to nearest even.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
