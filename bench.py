@@ -140,13 +140,13 @@ class ClockSampler:
 
 
 class GpuBench:
-    def __init__(self, device):
+    def __init__(self, device, experts=None):
         import torch
 
         import int4_weight_only_moe_gb300 as pkg
         self.torch, self.pkg = torch, pkg
         wl = inputs.WORKLOADS[HEADLINE]
-        self.E, self.K, self.N, self.topk = wl.E, wl.K, wl.N, wl.topk
+        self.E, self.K, self.N, self.topk = experts or wl.E, wl.K, wl.N, wl.topk
         self.device = device
         q1, s1, q2, s2 = inputs.all_expert_weights(self.E, self.K, self.N)
         self.moe = pkg.MoEW4A16(self.E, self.K, self.N, self.topk)
@@ -393,6 +393,29 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """A few forwards of one workload for profiler captures (ncu): no timing, no
+    extras. ``--experts`` shrinks the resident expert set to keep captures small."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    gb = GpuBench(torch.device("cuda", 0), experts=args.experts)
+    wl = inputs.WORKLOADS[args.workload]
+    if args.experts:
+        from dataclasses import replace
+        wl = replace(wl, E=args.experts)
+    data = gb.step_inputs(wl, args.warmup + args.steps)
+    out = torch.empty((wl.M, gb.K), dtype=torch.bfloat16, device="cuda")
+    gb.moe.ensure_workspace(wl.M)
+    for h, ids, w in data:
+        gb.flush()
+        gb.moe.forward(h, ids, w, out=out)
+    torch.cuda.synchronize()
+    assert gb.moe.status() == 0
+    print(f"profile case {wl.name} E={wl.E} M={wl.M}: {len(data)} forwards", flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,7 +426,14 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-samples", type=int, default=3)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="only run --warmup + --steps forwards of --workload (for ncu)")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--experts", type=int, default=None,
+                    help="resident experts in --profile-case (default: the workload's E)")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return run_profile_case(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -3,6 +3,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -158,28 +160,29 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   float4* acc4 = reinterpret_cast<float4*>(a.acc);
   for (long long i = gt; i < a.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int groups = a.hdr[kHdrNumPadded] / kRowGroup;
-  const int cpr = a.K / 8;  // 16-byte chunks per row
-  for (int g = blockIdx.x; g < groups; g += gridDim.x) {
-    for (int idx = threadIdx.x; idx < kRowGroup * cpr; idx += blockDim.x) {
-      const int r = idx / cpr, ch = idx - r * cpr;
-      const int sid = a.sorted_ids[g * kRowGroup + r];
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (sid < a.MK)
-        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
-            a.x + static_cast<long long>(sid / a.topk) * a.K + ch * 8));
-      uint8_t* dst = a.xs + (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
-                     r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = v;
-    }
+  // one thread per 16-byte chunk (8 elements) of every expert-sorted row
+  const int cpr = a.K / 8;
+  const long long chunks = static_cast<long long>(a.hdr[kHdrNumPadded]) * cpr;
+  for (long long idx = gt; idx < chunks; idx += nthr) {
+    const int p = static_cast<int>(idx / cpr), ch = static_cast<int>(idx - static_cast<long long>(p) * cpr);
+    const int sid = a.sorted_ids[p];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (sid < a.MK)
+      v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
+          a.x + static_cast<long long>(sid / a.topk) * a.K + ch * 8));
+    const int g = p / kRowGroup, r = p % kRowGroup;
+    uint8_t* dst = a.xs + (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
+                   r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst) = v;
   }
   pdl_launch_dependents();
 }
 
 cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
                           bool pdl) {
-  const long long zero_blocks = (a.acc_elems / 4 + 255) / 256;
-  long long grid = max_groups > zero_blocks ? max_groups : zero_blocks;
+  const long long work = std::max<long long>(static_cast<long long>(max_groups) * kRowGroup * (a.K / 8),
+                                             a.acc_elems / 4);
+  long long grid = (work + 255) / 256;
   const long long cap = 4LL * num_sms;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;

@@ -15,10 +15,10 @@
 //
 // Per CTA (one per SM), 16 warps:
 //   warp 0       bulk-copies packed INT4 weight blocks (4.5 KB) into a 16-deep ring
-//   warp 1       bulk-copies the activation tile (B operand) into a 6-deep ring
+//   warp 1       bulk-copies the activation tile (B operand) into an 8-deep ring
 //   warp 2       allocates tensor memory; one thread issues tcgen05.mma
 //   warps 4..11  dequantise INT4 -> fp16 in registers and store the A operand
-//                straight into tensor memory (tcgen05.st), 4-deep ring
+//                straight into tensor memory (tcgen05.st), 8-deep ring
 //   warps 12..15 epilogue: tcgen05.ld of the fp32 accumulator (double-buffered)
 //
 // The dequantisation writes the weight tile into tensor memory rather than
@@ -49,8 +49,8 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kNW = 16;                  // weight ring depth (shared memory)
-constexpr int kNB = 6;                   // activation ring depth (shared memory)
-constexpr int kNA = 4;                   // A-operand ring depth (tensor memory)
+constexpr int kNB = 8;                   // activation ring depth (shared memory)
+constexpr int kNA = 8;                   // A-operand ring depth (tensor memory)
 constexpr int kBStage = kBNMax * 128;    // 16 KB
 constexpr int kTmemCols = 512;
 constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
@@ -79,7 +79,7 @@ static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 2 * kBNMax <= kTmemCols, "tensor memory budget");
 
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMma = 2, kWarpDeq0 = 4, kWarpEpi0 = 12;
-constexpr int kDeqThreads = 256, kEpiThreads = 128;
+constexpr int kDeqWarps = 8, kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
 
 // Bounded wait that ignores the abort flag: used at teardown to let copies and
@@ -213,19 +213,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNW; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
-      mbar_init(bar(kBarWEmpty + i), kDeqThreads);
+      mbar_init(bar(kBarWEmpty + i), kDeqWarps);
     }
     for (int i = 0; i < kNB; ++i) {
       mbar_init(bar(kBarBFull + i), 1);
       mbar_init(bar(kBarBEmpty + i), 1);
     }
     for (int i = 0; i < kNA; ++i) {
-      mbar_init(bar(kBarAFull + i), kDeqThreads);
+      mbar_init(bar(kBarAFull + i), kDeqWarps);
       mbar_init(bar(kBarAEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarAccFull + i), 1);
-      mbar_init(bar(kBarAccEmpty + i), kEpiThreads);
+      mbar_init(bar(kBarAccEmpty + i), kEpiWarps);
     }
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
@@ -376,7 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const uint32_t scl = ld_shared_u16(wb + kWCodeBytes + half * 256 + r * 2);
         uint32_t out[16];
         dequant_group(qv, scl, out);
-        mbar_arrive(bar(kBarWEmpty + ws));
+        __syncwarp();  // every lane has consumed its shared-memory words
+        if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         w_ok = mbar_wait(bar(kBarAEmpty + sa), ((it / kNA) & 1) ^ 1, abort_flag, status,
                          kStatusTimeout);
         if (!__all_sync(0xffffffffu, w_ok)) {
@@ -387,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         tmem_st16(tmem + t_lane + sa * kACols + half * 16, out);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(kBarAFull + sa));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarAFull + sa));
       }
     }
   } else if (warp >= kWarpEpi0) {
@@ -447,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             swiglu_chunk(v, c, quad, lane, sStage);
           }
           tc_fence_before();
-          mbar_arrive(bar(kBarAccEmpty + ab));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
         } else {
           // split unit: park this CTA's partial sums, take a ticket
           const long long ustart = u * a.KBn;
@@ -462,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               __stcg(slot + (c * 16 + i) * kBM + r, __uint_as_float(raw_v[i]));
           }
           tc_fence_before();
-          mbar_arrive(bar(kBarAccEmpty + ab));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
           __threadfence();
           named_bar_sync(kEpiBar, kEpiThreads);
           const int c0 = sc.cta_of(ustart), c1 = sc.cta_of(ustart + a.KBn - 1);
@@ -480,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) v[i] = 0.f;
               for (int cc = c0; cc <= c1; ++cc) {
+                if (sc.start(cc) == sc.start(cc + 1)) continue;  // empty share: no partial
                 const int pc = (sc.start(cc) < ustart) ? 1 : 0;
                 const float* sl =
                     a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
@@ -523,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           }
         }
         tc_fence_before();
-        mbar_arrive(bar(kBarAccEmpty + ab));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
       }
       ++acc_it;
     }

@@ -56,15 +56,19 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 // in the global status word). Never spins without bound.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, int status_bit) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
+  // fast path: plain polling, no timer reads while the wait is short
+  for (int i = 0; i < 64; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      *abort_flag = 1;
-      atomicOr(status, status_bit);
-      return false;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if ((it & 1023u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(status, status_bit);
+        return false;
+      }
     }
   }
 }
