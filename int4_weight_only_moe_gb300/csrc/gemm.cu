@@ -13,13 +13,14 @@
 // and the routed tokens of one expert (16..128, a multiple of 16) are MMA N, so a
 // single token (decode) costs one N=16 tile instead of a 128-row tile.
 //
-// Per CTA (one per SM), 16 warps:
+// Per CTA (one per SM), 20 warps:
 //   warp 0       bulk-copies packed INT4 weight blocks (4.5 KB) into a 16-deep ring
 //   warp 1       bulk-copies the activation tile (B operand) into an 8-deep ring
 //   warp 2       allocates tensor memory; one thread issues tcgen05.mma
-//   warps 4..11  dequantise INT4 -> fp16 in registers and store the A operand
-//                straight into tensor memory (tcgen05.st), 8-deep ring
-//   warps 12..15 epilogue: tcgen05.ld of the fp32 accumulator (double-buffered)
+//   warps 4..15  dequantise INT4 -> fp16 in registers and store the A operand
+//                straight into tensor memory (tcgen05.st); three warps per lane
+//                quadrant take whole k-blocks in turn; 8-deep ring shared with B
+//   warps 16..19 epilogue: tcgen05.ld of the fp32 accumulator (double-buffered)
 //
 // The dequantisation writes the weight tile into tensor memory rather than
 // shared memory, so shared-memory bandwidth carries only the packed codes and the
@@ -47,28 +48,28 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
+constexpr int kWarpW = 0, kWarpB = 1, kWarpMma = 2, kWarpDeq0 = 4;
+constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
+constexpr int kThreads = (kWarpEpi0 + 4) * 32;
 constexpr int kNW = 16;                  // weight ring depth (shared memory)
-constexpr int kNB = 8;                   // activation ring depth (shared memory)
-constexpr int kNA = 8;                   // A-operand ring depth (tensor memory)
+constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
 constexpr int kBStage = kBNMax * 128;    // 16 KB
 constexpr int kTmemCols = 512;
 constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
-constexpr int kAccCol0 = kNA * kACols;   // accumulators follow the A ring
+constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
 constexpr int kStatusTimeout = 2;
 
 constexpr int kSmB = 0;
-constexpr int kSmW = kSmB + kNB * kBStage;
+constexpr int kSmW = kSmB + kNS * kBStage;
 constexpr int kSmStage = ((kSmW + kNW * kWBlockBytes + 1023) / 1024) * 1024;
 constexpr int kSmBar = kSmStage + kBNMax * 128;
 // barrier indices
-constexpr int kBarWFull = 0;
-constexpr int kBarWEmpty = kBarWFull + kNW;
-constexpr int kBarBFull = kBarWEmpty + kNW;
-constexpr int kBarBEmpty = kBarBFull + kNB;
-constexpr int kBarAFull = kBarBEmpty + kNB;
-constexpr int kBarAEmpty = kBarAFull + kNA;
-constexpr int kBarAccFull = kBarAEmpty + kNA;
+constexpr int kBarWFull = 0;                 // weight block landed (bulk-copy bytes)
+constexpr int kBarWEmpty = kBarWFull + kNW;  // weight block read by its 4 dequant warps
+constexpr int kBarFull = kBarWEmpty + kNW;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
+constexpr int kBarEmpty = kBarFull + kNS;    // stage consumed by the MMAs (tcgen05.commit)
+constexpr int kBarAccFull = kBarEmpty + kNS;
 constexpr int kBarAccEmpty = kBarAccFull + 2;
 constexpr int kBarDrain = kBarAccEmpty + 2;
 constexpr int kNumBars = kBarDrain + 1;
@@ -78,8 +79,7 @@ constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 by
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 2 * kBNMax <= kTmemCols, "tensor memory budget");
 
-constexpr int kWarpW = 0, kWarpB = 1, kWarpMma = 2, kWarpDeq0 = 4, kWarpEpi0 = 12;
-constexpr int kDeqWarps = 8, kEpiWarps = 4, kEpiThreads = 128;
+constexpr int kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
 
 // Bounded wait that ignores the abort flag: used at teardown to let copies and
@@ -213,15 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNW; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
-      mbar_init(bar(kBarWEmpty + i), kDeqWarps);
+      mbar_init(bar(kBarWEmpty + i), 4);
     }
-    for (int i = 0; i < kNB; ++i) {
-      mbar_init(bar(kBarBFull + i), 1);
-      mbar_init(bar(kBarBEmpty + i), 1);
-    }
-    for (int i = 0; i < kNA; ++i) {
-      mbar_init(bar(kBarAFull + i), kDeqWarps);
-      mbar_init(bar(kBarAEmpty + i), 1);
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(bar(kBarFull + i), 4 + 1);
+      mbar_init(bar(kBarEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarAccFull + i), 1);
@@ -288,21 +284,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
         const uint32_t bytes = static_cast<uint32_t>(un.ng) * kRowGroupBytes;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % kNB;
-          if (!mbar_wait(bar(kBarBEmpty + s), ((it / kNB) & 1) ^ 1, abort_flag, status,
+          const int s = it % kNS;
+          if (!mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
                          kStatusTimeout)) {
             ok = false;
             break;
           }
           const uint8_t* src =
               a.bsrc + (static_cast<long long>(kb) * a.Gcap + un.g0) * kRowGroupBytes;
-          mbar_arrive_expect_tx(bar(kBarBFull + s), bytes);
-          bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarBFull + s));
+          mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
+          bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
         }
       }
-      for (uint32_t j = 0; j < kNB && j < it; ++j) {
+      // the stage barriers also count dequant arrivals, so only the bytes can be
+      // drained here: wait until the last stages' copies have landed
+      for (uint32_t j = 0; j < kNS && j < it; ++j) {
         const uint32_t idx = it - 1 - j;
-        mbar_wait_drain(bar(kBarBFull + idx % kNB), (idx / kNB) & 1);
+        mbar_wait_drain(bar(kBarFull + idx % kNS), (idx / kNS) & 1);
       }
     }
   } else if (warp == kWarpMma) {
@@ -325,24 +323,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         tc_fence_after();
         const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int sa = it % kNA, sb = it % kNB;
-          if (!mbar_wait(bar(kBarAFull + sa), (it / kNA) & 1, abort_flag, status,
-                         kStatusTimeout) ||
-              !mbar_wait(bar(kBarBFull + sb), (it / kNB) & 1, abort_flag, status,
-                         kStatusTimeout)) {
+          const int st = it % kNS;
+          if (!mbar_wait(bar(kBarFull + st), (it / kNS) & 1, abort_flag, status, kStatusTimeout)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem + sa * kACols;
-          const uint32_t b_addr = sB + sb * kBStage;
+          const uint32_t a_tmem = tmem + st * kACols;
+          const uint64_t b_desc = sw128_kmajor_desc(sB + st * kBStage);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            tc_mma_ts(d_tmem, a_tmem + kk * 8, sw128_kmajor_desc(b_addr + kk * 32), idesc,
+            // +32 bytes of K per step inside the 128-byte swizzled row (+2 in the
+            // descriptor's 16-byte address units)
+            tc_mma_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc,
                       (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(kBarAEmpty + sa));
-          tc_commit(bar(kBarBEmpty + sb));
+          tc_commit(bar(kBarEmpty + st));
         }
         if (!ok) break;
         tc_commit(bar(kBarAccFull + ab));
@@ -353,18 +349,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     }
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
+    // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
+    // in this CTA's sequence is congruent to `phase` modulo kDeqPhases. The TMEM
+    // store of one k-block is retired (wait::st + arrival) only after the warp
+    // has loaded and converted its next k-block, which hides the store latency.
     const int quad = warp & 3;
-    const int half = (warp - kWarpDeq0) >> 2;  // scale group within the k-block
+    const int phase = (warp - kWarpDeq0) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t it = 0;
     SegIter si{my_begin, my_end, a.KBn};
     long long u;
     int kb0, kb1;
-    bool ok = true;
+    bool ok = true, pending = false;
+    int pend_stage = 0;
     while (ok && si.next(u, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        const int ws = it % kNW, sa = it % kNA;
+        if (static_cast<int>(it % kDeqPhases) != phase) continue;
+        const int ws = it % kNW, st = it % kNS;
         bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
                               kStatusTimeout);
         if (!__all_sync(0xffffffffu, w_ok)) {
@@ -372,25 +374,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           break;
         }
         const uint32_t wb = sW + ws * kWBlockBytes;
-        const uint4 qv = ld_shared_v4(wb + half * 2048 + r * 16);
-        const uint32_t scl = ld_shared_u16(wb + kWCodeBytes + half * 256 + r * 2);
-        uint32_t out[16];
-        dequant_group(qv, scl, out);
+        const uint4 q0 = ld_shared_v4(wb + r * 16);
+        const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
+        const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
+        const uint32_t s1 = ld_shared_u16(wb + kWCodeBytes + 256 + r * 2);
+        uint32_t out[32];
+        dequant_group(q0, s0, *reinterpret_cast<uint32_t(*)[16]>(&out[0]));
+        dequant_group(q1, s1, *reinterpret_cast<uint32_t(*)[16]>(&out[16]));
         __syncwarp();  // every lane has consumed its shared-memory words
         if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-        w_ok = mbar_wait(bar(kBarAEmpty + sa), ((it / kNA) & 1) ^ 1, abort_flag, status,
+        if (pending) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
+          pending = false;
+        }
+        w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
                          kStatusTimeout);
         if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        tmem_st16(tmem + t_lane + sa * kACols + half * 16, out);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarAFull + sa));
+        tmem_st32(tmem + t_lane + st * kACols, out);
+        pending = true;
+        pend_stage = st;
       }
+    }
+    if (pending) {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
     }
   } else if (warp >= kWarpEpi0) {
     // ------------------------------------------------ epilogue
