@@ -63,6 +63,17 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def reduce_max(value: float, device) -> float:
+    """Largest ``value`` over all ranks (the slowest replica sets the time)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def file_hash(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
@@ -258,11 +269,7 @@ def run_ours(args):
 
     with ClockSampler(local_rank) as clk:
         ms, _, data = gb.time_forward(wl, args.steps, args.warmup, barrier=barrier)
-    total_ms = sum(ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(ms), device)
     ms_step = total_ms / args.steps
     value = world * wl.M * args.steps / (total_ms * 1e-3)
 
