@@ -14,8 +14,8 @@
 // single token (decode) costs one N=16 tile instead of a 128-row tile.
 //
 // Per CTA (one per SM), 20 warps:
-//   warp 0       bulk-copies packed INT4 weight blocks (4.5 KB) into a 16-deep ring
-//   warp 1       bulk-copies the activation tile (B operand) into an 8-deep ring
+//   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
+//   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
 //   warp 2       allocates tensor memory; one thread issues tcgen05.mma
 //   warps 4..15  dequantise INT4 -> fp16 in registers and store the A operand
 //                straight into tensor memory (tcgen05.st); three warps per lane
@@ -59,6 +59,7 @@ constexpr int kTmemCols = 512;
 constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
 constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
 constexpr int kStatusTimeout = 2;
+constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
 
 constexpr int kSmB = 0;
 constexpr int kSmW = kSmB + kNS * kBStage;
@@ -246,8 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
   if (warp == kWarpW) {
     // ------------------------------------------------ packed-weight producer
-    if (lane == 0) {
-      uint32_t it = 0;
+    // kProducerLanes lanes issue the bulk copies of alternate k-blocks: several
+    // issuing threads keep small (4.5 KB) copies streaming at full HBM rate,
+    // where a single issuing thread reaches only about half of it.
+    if (lane < kProducerLanes) {
+      uint32_t it = 0, last = 0, mine = 0;
       SegIter si{my_begin, my_end, a.KBn};
       long long u;
       int kb0, kb1;
@@ -257,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const uint8_t* src =
             a.wpack + ((static_cast<long long>(un.e) * a.R + un.rt) * a.KBn + kb0) * kWBlockBytes;
         for (int kb = kb0; kb < kb1; ++kb, ++it, src += kWBlockBytes) {
+          if (static_cast<int>(it % kProducerLanes) != lane) continue;
           const int s = it % kNW;
           if (!mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
                          kStatusTimeout)) {
@@ -265,17 +270,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           }
           mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
           bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
+          last = it;
+          ++mine;
         }
       }
-      for (uint32_t j = 0; j < kNW && j < it; ++j) {
-        const uint32_t idx = it - 1 - j;
+      // let this lane's last copies land before shared memory is released
+      for (uint32_t j = 0; j < kNW / kProducerLanes && j < mine; ++j) {
+        const uint32_t idx = last - j * kProducerLanes;
         mbar_wait_drain(bar(kBarWFull + idx % kNW), (idx / kNW) & 1);
       }
     }
   } else if (warp == kWarpB) {
     // ------------------------------------------------ activation (B operand) producer
-    if (lane == 0) {
-      uint32_t it = 0;
+    if (lane < kProducerLanes) {
+      uint32_t it = 0, last = 0, mine = 0;
       SegIter si{my_begin, my_end, a.KBn};
       long long u;
       int kb0, kb1;
@@ -284,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
         const uint32_t bytes = static_cast<uint32_t>(un.ng) * kRowGroupBytes;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          if (static_cast<int>(it % kProducerLanes) != lane) continue;
           const int s = it % kNS;
           if (!mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
                          kStatusTimeout)) {
@@ -294,12 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               a.bsrc + (static_cast<long long>(kb) * a.Gcap + un.g0) * kRowGroupBytes;
           mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
           bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
+          last = it;
+          ++mine;
         }
       }
-      // the stage barriers also count dequant arrivals, so only the bytes can be
-      // drained here: wait until the last stages' copies have landed
-      for (uint32_t j = 0; j < kNS && j < it; ++j) {
-        const uint32_t idx = it - 1 - j;
+      // the stage barriers also count dequant arrivals, so this bounded wait only
+      // gives the last copies time to land before shared memory is released
+      for (uint32_t j = 0; j < kNS / kProducerLanes && j < mine; ++j) {
+        const uint32_t idx = last - j * kProducerLanes;
         mbar_wait_drain(bar(kBarFull + idx % kNS), (idx / kNS) & 1);
       }
     }
