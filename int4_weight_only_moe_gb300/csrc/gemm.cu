@@ -316,30 +316,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, acc_it = 0;
-      SegIter si{my_begin, my_end, a.KBn};
-      long long u;
-      int kb0, kb1;
-      bool ok = true;
-      while (ok && si.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-        const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-        const int ab = acc_it & 1;
-        if (!mbar_wait(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
-                       kStatusTimeout)) {
-          ok = false;
-          break;
-        }
+    // The whole warp runs the (uniform) loop and waits; one elected lane issues.
+    uint32_t it = 0, acc_it = 0;
+    SegIter si{my_begin, my_end, a.KBn};
+    long long u;
+    int kb0, kb1;
+    bool ok = true;
+    while (ok && si.next(u, kb0, kb1)) {
+      const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
+      const int ab = acc_it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1,
+                                            abort_flag, status, kStatusTimeout));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int st = it % kNS;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1, abort_flag,
+                                              status, kStatusTimeout));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int st = it % kNS;
-          if (!mbar_wait(bar(kBarFull + st), (it / kNS) & 1, abort_flag, status, kStatusTimeout)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (elect_one()) {
           const uint32_t a_tmem = tmem + st * kACols;
           const uint64_t b_desc = sw128_kmajor_desc(sB + st * kBStage);
 #pragma unroll
@@ -351,13 +349,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           }
           tc_commit(bar(kBarEmpty + st));
         }
-        if (!ok) break;
-        tc_commit(bar(kBarAccFull + ab));
-        ++acc_it;
+        __syncwarp();
       }
+      if (!ok) break;
+      if (elect_one()) tc_commit(bar(kBarAccFull + ab));
+      __syncwarp();
+      ++acc_it;
+    }
+    if (elect_one()) {
       tc_commit(bar(kBarDrain));
       mbar_wait_drain(bar(kBarDrain), 0);
     }
+    __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
     // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
