@@ -16,6 +16,7 @@
 // Per CTA (one per SM), 20 warps:
 //   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
 //   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
+//                (the lanes of a producer issue 4 consecutive k-blocks at once)
 //   warp 2       allocates tensor memory; one thread issues tcgen05.mma
 //   warps 4..15  dequantise INT4 -> fp16 in registers and store the A operand
 //                straight into tensor memory (tcgen05.st); three warps per lane
@@ -143,6 +144,37 @@ __device__ __forceinline__ Unit decode_unit(long long u, int R, const TokenTile*
   return r;
 }
 
+// Random access into this CTA's k-block sequence for lanes that step through it
+// together: seek(it) moves forward to the segment holding sequence index `it`.
+struct Cursor {
+  SegIter si;
+  long long u = 0, seg_it0 = 0;
+  int kb0 = 0, kb1 = 0, R = 0;
+  bool valid = false, decoded = false;
+  Unit un{};
+  const TokenTile* tiles;
+  const int32_t* expert_tiles;
+  __device__ Cursor(long long begin, long long end, int KBn, int R_, const TokenTile* t,
+                    const int32_t* et)
+      : si{begin, end, KBn}, R(R_), tiles(t), expert_tiles(et) {
+    valid = si.next(u, kb0, kb1);
+  }
+  __device__ __forceinline__ bool seek(long long it, int& kb) {
+    while (valid && it >= seg_it0 + (kb1 - kb0)) {
+      seg_it0 += kb1 - kb0;
+      valid = si.next(u, kb0, kb1);
+      decoded = false;
+    }
+    if (!valid) return false;
+    if (!decoded) {
+      un = decode_unit(u, R, tiles, expert_tiles);
+      decoded = true;
+    }
+    kb = kb0 + static_cast<int>(it - seg_it0);
+    return true;
+  }
+};
+
 // 32 INT4 codes (one scale group) -> 16 f16x2 words, columns of the A operand.
 // OR-ing a code u into the mantissa of fp16 1024 gives exactly 1024 + u (code at
 // bits 0..3 of a half) or 1024 + 16u (code at bits 4..7); subtracting 1032, or
@@ -245,73 +277,66 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   int* status = a.status;
   pdl_launch_dependents();
 
-  if (warp == kWarpW) {
-    // ------------------------------------------------ packed-weight producer
-    // kProducerLanes lanes issue the bulk copies of alternate k-blocks: several
-    // issuing threads keep small (4.5 KB) copies streaming at full HBM rate,
-    // where a single issuing thread reaches only about half of it.
+  if (warp == kWarpW || warp == kWarpB) {
+    // ------------------------------------------------ bulk-copy producers
+    // warp 0: packed weight blocks (W ring); warp 1: activation tiles (B operand,
+    // operand-stage ring). kProducerLanes lanes walk consecutive k-blocks in
+    // step and issue their copies in one warp instruction: a bulk-copy issue
+    // blocks its thread for a while, so several copies have to leave at once for
+    // small (2-4.5 KB) copies to keep HBM busy.
+    const bool is_w = warp == kWarpW;
+    const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
-      uint32_t it = 0, last = 0, mine = 0;
-      SegIter si{my_begin, my_end, a.KBn};
-      long long u;
-      int kb0, kb1;
-      bool ok = true;
-      while (ok && si.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-        const uint8_t* src =
-            a.wpack + ((static_cast<long long>(un.e) * a.R + un.rt) * a.KBn + kb0) * kWBlockBytes;
-        for (int kb = kb0; kb < kb1; ++kb, ++it, src += kWBlockBytes) {
-          if (static_cast<int>(it % kProducerLanes) != lane) continue;
-          const int s = it % kNW;
-          if (!mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
-                         kStatusTimeout)) {
-            ok = false;
-            break;
+      Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
+      long long last = -1;
+      uint32_t mine = 0;
+      for (long long base_it = 0; base_it < n_it; base_it += kProducerLanes) {
+        const long long it = base_it + lane;
+        const unsigned active = __ballot_sync(0x0000000fu, it < n_it) & 0xFu;
+        if (it < n_it) {
+          int kb = 0;
+          cur.seek(it, kb);
+          bool ok;
+          if (is_w) {
+            const int s = static_cast<int>(it % kNW);
+            ok = mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
+                           kStatusTimeout);
+            __syncwarp(active);
+            if (ok) {
+              const uint8_t* src =
+                  a.wpack +
+                  ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
+              mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
+              bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
+            }
+          } else {
+            const int s = static_cast<int>(it % kNS);
+            ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                           kStatusTimeout);
+            __syncwarp(active);
+            if (ok) {
+              const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
+              const uint8_t* src =
+                  a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
+              mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
+              bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
+            }
           }
-          mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
-          bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
-          last = it;
-          ++mine;
+          if (ok) {
+            last = it;
+            ++mine;
+          }
+          if (__any_sync(active, !ok)) break;
         }
       }
-      // let this lane's last copies land before shared memory is released
-      for (uint32_t j = 0; j < kNW / kProducerLanes && j < mine; ++j) {
-        const uint32_t idx = last - j * kProducerLanes;
-        mbar_wait_drain(bar(kBarWFull + idx % kNW), (idx / kNW) & 1);
-      }
-    }
-  } else if (warp == kWarpB) {
-    // ------------------------------------------------ activation (B operand) producer
-    if (lane < kProducerLanes) {
-      uint32_t it = 0, last = 0, mine = 0;
-      SegIter si{my_begin, my_end, a.KBn};
-      long long u;
-      int kb0, kb1;
-      bool ok = true;
-      while (ok && si.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-        const uint32_t bytes = static_cast<uint32_t>(un.ng) * kRowGroupBytes;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          if (static_cast<int>(it % kProducerLanes) != lane) continue;
-          const int s = it % kNS;
-          if (!mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                         kStatusTimeout)) {
-            ok = false;
-            break;
-          }
-          const uint8_t* src =
-              a.bsrc + (static_cast<long long>(kb) * a.Gcap + un.g0) * kRowGroupBytes;
-          mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
-          bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
-          last = it;
-          ++mine;
-        }
-      }
-      // the stage barriers also count dequant arrivals, so this bounded wait only
-      // gives the last copies time to land before shared memory is released
-      for (uint32_t j = 0; j < kNS / kProducerLanes && j < mine; ++j) {
-        const uint32_t idx = last - j * kProducerLanes;
-        mbar_wait_drain(bar(kBarFull + idx % kNS), (idx / kNS) & 1);
+      // bounded wait for this lane's last copies to land before shared memory is
+      // released (the operand-stage barriers also count dequant arrivals, so for
+      // them this only gives the copies time)
+      const int depth = is_w ? kNW : kNS;
+      for (uint32_t j = 0; j < static_cast<uint32_t>(depth / kProducerLanes) && j < mine; ++j) {
+        const long long idx = last - static_cast<long long>(j) * kProducerLanes;
+        mbar_wait_drain(bar((is_w ? kBarWFull : kBarFull) + static_cast<int>(idx % depth)),
+                        static_cast<uint32_t>((idx / depth) & 1));
       }
     }
   } else if (warp == kWarpMma) {
