@@ -340,52 +340,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       }
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------ MMA issuer
-    // The whole warp runs the (uniform) loop and waits; one elected lane issues.
-    uint32_t it = 0, acc_it = 0;
-    SegIter si{my_begin, my_end, a.KBn};
-    long long u;
-    int kb0, kb1;
-    bool ok = true;
-    while (ok && si.next(u, kb0, kb1)) {
-      const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-      const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-      const int ab = acc_it & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1,
-                                            abort_flag, status, kStatusTimeout));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        const int st = it % kNS;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1, abort_flag,
-                                              status, kStatusTimeout));
-        if (!ok) break;
-        tc_fence_after();
-        if (elect_one()) {
-          const uint32_t a_tmem = tmem + st * kACols;
-          const uint64_t b_desc = sw128_kmajor_desc(sB + st * kBStage);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // +32 bytes of K per step inside the 128-byte swizzled row (+2 in the
-            // descriptor's 16-byte address units)
-            tc_mma_ts(d_tmem, a_tmem + kk * 8, b_desc + 2 * kk, idesc,
-                      (kb > kb0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(bar(kBarEmpty + st));
+    // ------------------------------------------------ MMA issuer (one thread)
+    // The loop is on the critical path of every k-block: it polls with the
+    // non-blocking test and keeps descriptors in registers between k-blocks.
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      SegIter si{my_begin, my_end, a.KBn};
+      long long u;
+      int kb0, kb1;
+      bool ok = true;
+      const uint64_t b_desc0 = sw128_kmajor_desc(sB);
+      while (ok && si.next(u, kb0, kb1)) {
+        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
+        const int ab = acc_it & 1;
+        if (!mbar_wait_spin(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
+                            kStatusTimeout)) {
+          ok = false;
+          break;
         }
-        __syncwarp();
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
+        uint32_t acc_flag = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const uint32_t st = it % kNS;
+          if (!mbar_wait_spin(bar(kBarFull + st), (it / kNS) & 1, abort_flag, status,
+                              kStatusTimeout)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_tmem = tmem + st * kACols;
+          // B stage st starts st * kBStage bytes after stage 0 (16-byte units in the
+          // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
+          const uint64_t b_desc = b_desc0 + (st * kBStage >> 4);
+          tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
+          tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
+          tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
+          tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
+          tc_commit(bar(kBarEmpty + st));
+          acc_flag = 1u;
+        }
+        if (!ok) break;
+        tc_commit(bar(kBarAccFull + ab));
+        ++acc_it;
       }
-      if (!ok) break;
-      if (elect_one()) tc_commit(bar(kBarAccFull + ab));
-      __syncwarp();
-      ++acc_it;
-    }
-    if (elect_one()) {
       tc_commit(bar(kBarDrain));
       mbar_wait_drain(bar(kBarDrain), 0);
     }
-    __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
     // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
