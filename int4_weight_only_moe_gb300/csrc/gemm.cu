@@ -17,11 +17,13 @@
 //   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
 //   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
 //                (the lanes of a producer issue 4 consecutive k-blocks at once)
-//   warp 2       allocates tensor memory; one thread issues tcgen05.mma
+//   warps 2, 3   tcgen05.mma issuers for alternate k-blocks, each into its own
+//                accumulators (warp 2 also allocates tensor memory)
 //   warps 4..15  dequantise INT4 -> fp16 in registers and store the A operand
 //                straight into tensor memory (tcgen05.st); three warps per lane
 //                quadrant take whole k-blocks in turn; 8-deep ring shared with B
-//   warps 16..19 epilogue: tcgen05.ld of the fp32 accumulator (double-buffered)
+//   warps 16..19 epilogue: tcgen05.ld of both issuers' fp32 accumulators
+//                (double-buffered), summed
 //
 // The dequantisation writes the weight tile into tensor memory rather than
 // shared memory, so shared-memory bandwidth carries only the packed codes and the
@@ -50,12 +52,12 @@ namespace moe {
 namespace {
 
 constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
-constexpr int kWarpW = 0, kWarpB = 1, kWarpMma = 2, kWarpDeq0 = 4;
+constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 4;
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
 constexpr int kNW = 16;                  // weight ring depth (shared memory)
 constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
-constexpr int kBStage = kBNMax * 128;    // 16 KB
+constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
 constexpr int kTmemCols = 512;
 constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
 constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
@@ -71,18 +73,19 @@ constexpr int kBarWFull = 0;                 // weight block landed (bulk-copy b
 constexpr int kBarWEmpty = kBarWFull + kNW;  // weight block read by its 4 dequant warps
 constexpr int kBarFull = kBarWEmpty + kNW;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
 constexpr int kBarEmpty = kBarFull + kNS;    // stage consumed by the MMAs (tcgen05.commit)
-constexpr int kBarAccFull = kBarEmpty + kNS;
-constexpr int kBarAccEmpty = kBarAccFull + 2;
-constexpr int kBarDrain = kBarAccEmpty + 2;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarAccFull = kBarEmpty + kNS; // [issuer][buffer]: accumulator complete
+constexpr int kBarAccEmpty = kBarAccFull + 4;  // [buffer]: epilogue has read both issuers' sums
+constexpr int kBarDrain = kBarAccEmpty + 2;    // [issuer]
+constexpr int kNumBars = kBarDrain + 2;
 constexpr int kSmMisc = kSmBar + kNumBars * 8;
 constexpr int kSmBytes = kSmMisc + 64;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
-static_assert(kAccCol0 + 2 * kBNMax <= kTmemCols, "tensor memory budget");
+static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
 
 constexpr int kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
+constexpr int kRowRegs = kBNMax / 32;  // token rows per epilogue lane (routing prefetch)
 
 // Bounded wait that ignores the abort flag: used at teardown to let copies and
 // MMAs already in flight land before shared and tensor memory are released.
@@ -252,16 +255,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       mbar_init(bar(kBarFull + i), 4 + 1);
       mbar_init(bar(kBarEmpty + i), 1);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(bar(kBarAccFull + i), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarAccFull + i), 1);
       mbar_init(bar(kBarAccEmpty + i), kEpiWarps);
+      mbar_init(bar(kBarDrain + i), 1);
     }
-    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
@@ -339,55 +342,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                         static_cast<uint32_t>((idx / depth) & 1));
       }
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------ MMA issuer (one thread)
-    // The loop is on the critical path of every k-block: it polls with the
-    // non-blocking test and keeps descriptors in registers between k-blocks.
-    if (lane == 0) {
-      uint32_t it = 0, acc_it = 0;
-      SegIter si{my_begin, my_end, a.KBn};
-      long long u;
-      int kb0, kb1;
-      bool ok = true;
-      const uint64_t b_desc0 = sw128_kmajor_desc(sB);
-      while (ok && si.next(u, kb0, kb1)) {
+  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+    // ------------------------------------------------ MMA issuers
+    // Two warps issue alternate k-blocks of every unit into separate accumulators
+    // (the epilogue adds them), so one issuer's waits and commits overlap the
+    // other's MMAs. Each warp runs its loop uniformly; one elected lane issues.
+    const uint32_t par = static_cast<uint32_t>(warp - kWarpMma0);
+    uint32_t it_base = 0, acc_it = 0;
+    SegIter si{my_begin, my_end, a.KBn};
+    long long u;
+    int kb0, kb1;
+    bool ok = true;
+    const uint64_t b_desc0 = sw128_kmajor_desc(sB);
+    while (ok && si.next(u, kb0, kb1)) {
+      const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
+      const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
+      const int ab = acc_it & 1;
+      if (first < it_base + len) {
         const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-        const int ab = acc_it & 1;
-        if (!mbar_wait_spin(bar(kBarAccEmpty + ab), ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
-                            kStatusTimeout)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + kAccCol0 + ab * kBNMax;
+        ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarAccEmpty + ab),
+                                                    ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
+                                                    kStatusTimeout));
+        if (!ok) break;
+        const uint32_t d_tmem = tmem + kAccCol0 + (par * 2 + ab) * kBNMax;
         uint32_t acc_flag = 0;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (uint32_t it = first; it < it_base + len; it += 2) {
           const uint32_t st = it % kNS;
-          if (!mbar_wait_spin(bar(kBarFull + st), (it / kNS) & 1, abort_flag, status,
-                              kStatusTimeout)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarFull + st), (it / kNS) & 1,
+                                                      abort_flag, status, kStatusTimeout));
+          if (!ok) break;
           const uint32_t a_tmem = tmem + st * kACols;
-          // B stage st starts st * kBStage bytes after stage 0 (16-byte units in the
+          // B stage st is st * kBStage bytes after stage 0 (16-byte units in the
           // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
-          const uint64_t b_desc = b_desc0 + (st * kBStage >> 4);
-          tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
-          tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
-          tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
-          tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
-          tc_commit(bar(kBarEmpty + st));
+          const uint64_t b_desc = b_desc0 + ((st * kBStage) >> 4);
+          if (elect_one()) {
+            tc_fence_after();
+            tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
+            tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
+            tc_commit(bar(kBarEmpty + st));
+          }
           acc_flag = 1u;
         }
         if (!ok) break;
-        tc_commit(bar(kBarAccFull + ab));
-        ++acc_it;
+        if (elect_one()) tc_commit(bar(kBarAccFull + par * 2 + ab));
+        __syncwarp();
       }
-      tc_commit(bar(kBarDrain));
-      mbar_wait_drain(bar(kBarDrain), 0);
+      it_base += len;
+      ++acc_it;
     }
+    if (elect_one()) {
+      tc_commit(bar(kBarDrain + par));
+      mbar_wait_drain(bar(kBarDrain + par), 0);
+    }
+    __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
     // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
@@ -455,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     const int r = quad * 32 + lane;
     const int epi_tid = threadIdx.x - kWarpEpi0 * 32;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t acc_it = 0;
+    uint32_t acc_it = 0, it_base = 0, full_phase = 0;
     SegIter si{my_begin, my_end, a.KBn};
     long long u;
     int kb0, kb1;
@@ -463,14 +473,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
       const int nch = un.ng;  // 16-column chunks
       const int ab = acc_it & 1;
+      const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
+      // which MMA issuer (even / odd k-blocks of this CTA's sequence) has a sum
+      const bool has0 = len >= 2 || (it_base & 1u) == 0;
+      const bool has1 = len >= 2 || (it_base & 1u) == 1;
+      it_base += len;
 
       // routing of the tile's token rows (down GEMM), fetched before the wait
-      int sid_r[4] = {0, 0, 0, 0}, tok_r[4] = {0, 0, 0, 0};
-      float w_r[4] = {0.f, 0.f, 0.f, 0.f};
+      int sid_r[kRowRegs], tok_r[kRowRegs];
+      float w_r[kRowRegs];
+#pragma unroll
+      for (int j = 0; j < kRowRegs; ++j) {
+        sid_r[j] = a.MK;
+        tok_r[j] = 0;
+        w_r[j] = 0.f;
+      }
       if constexpr (kMode == 2) {
         const int pbase = un.g0 * kRowGroup;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kRowRegs; ++j) {
           const int row = 32 * j + lane;
           const int sid = row < nch * 16 ? a.sorted_ids[pbase + row] : a.MK;
           sid_r[j] = sid;
@@ -481,8 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         }
       }
 
-      bool w_ok = mbar_wait(bar(kBarAccFull + ab), (acc_it >> 1) & 1, abort_flag, status,
-                            kStatusTimeout);
+      bool w_ok = true;
+      if (has0) {
+        w_ok = mbar_wait(bar(kBarAccFull + ab), (full_phase >> ab) & 1u, abort_flag, status,
+                         kStatusTimeout);
+        full_phase ^= 1u << ab;
+      }
+      if (has1 && w_ok) {
+        w_ok = mbar_wait(bar(kBarAccFull + 2 + ab), (full_phase >> (2 + ab)) & 1u, abort_flag,
+                         status, kStatusTimeout);
+        full_phase ^= 1u << (2 + ab);
+      }
       w_ok = __all_sync(0xffffffffu, w_ok);
       if (lane == 0) epi_ok[(acc_it & 1) * 4 + quad] = w_ok ? 1 : 0;
       named_bar_sync(kEpiBar, kEpiThreads);
@@ -490,19 +520,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                           epi_ok[(acc_it & 1) * 4 + 2] && epi_ok[(acc_it & 1) * 4 + 3];
       if (!all_ok) break;
       tc_fence_after();
-      const uint32_t tacc = tmem + t_lane + kAccCol0 + ab * kBNMax;
+      const uint32_t tacc0 = tmem + t_lane + kAccCol0 + ab * kBNMax;
+      const uint32_t tacc1 = tmem + t_lane + kAccCol0 + (2 + ab) * kBNMax;
+      // fp32 sums of 16 token columns of this lane's row, both issuers added
+      auto load_chunk = [&](int c, float (&v)[16]) {
+        uint32_t rr[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if (has0) {
+          tmem_ld16(tacc0 + c * 16, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rr[i]);
+        }
+        if (has1) {
+          tmem_ld16(tacc1 + c * 16, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(rr[i]);
+        }
+      };
 
       if constexpr (kMode == 1) {
         const bool full = (kb0 == 0 && kb1 == a.KBn);
         bool write_tile = full;
         if (full) {
           for (int c = 0; c < nch; ++c) {
-            uint32_t raw_v[16];
-            tmem_ld16(tacc + c * 16, raw_v);
-            tmem_ld_wait();
             float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(raw_v[i]);
+            load_chunk(c, v);
             swiglu_chunk(v, c, quad, lane, sStage);
           }
           tc_fence_before();
@@ -514,12 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           const int part = (sc.start(blockIdx.x) < ustart) ? 1 : 0;
           float* slot = a.scratch + (static_cast<long long>(blockIdx.x) * 2 + part) * kBNMax * kBM;
           for (int c = 0; c < nch; ++c) {
-            uint32_t raw_v[16];
-            tmem_ld16(tacc + c * 16, raw_v);
-            tmem_ld_wait();
+            float v[16];
+            load_chunk(c, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              __stcg(slot + (c * 16 + i) * kBM + r, __uint_as_float(raw_v[i]));
+            for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
           }
           tc_fence_before();
           __syncwarp();
@@ -568,9 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 #pragma unroll
         for (int c = 0; c < kBNMax / 16; ++c) {
           if (c < nch) {
-            uint32_t raw_v[16];
-            tmem_ld16(tacc + c * 16, raw_v);
-            tmem_ld_wait();
+            float v[16];
+            load_chunk(c, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int row = c * 16 + i;
@@ -578,8 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               if (sid < a.MK) {
                 const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
                 const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
-                atomicAdd(acc_col + static_cast<long long>(tok) * a.Kout,
-                          wt * __uint_as_float(raw_v[i]));
+                atomicAdd(acc_col + static_cast<long long>(tok) * a.Kout, wt * v[i]);
               }
             }
           }
@@ -596,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   // ------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

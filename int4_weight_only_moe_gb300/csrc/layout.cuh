@@ -34,7 +34,7 @@ constexpr int kBM = 128;            // weight rows per tile (MMA M)
 constexpr int kBK = 64;             // reduction elements per k-block
 constexpr int kWBlockBytes = 4608;  // one packed (row tile, k-block) block
 constexpr int kWCodeBytes = 4096;
-constexpr int kBNMax = 128;         // largest token tile (MMA N)
+constexpr int kBNMax = 64;          // largest token tile (MMA N)
 constexpr int kRowGroup = 16;       // token rows per blocked row group
 constexpr int kRowGroupBytes = kRowGroup * 128;
 constexpr int kMaxCtas = 256;       // persistent grid limit (tickets / scratch slots)
