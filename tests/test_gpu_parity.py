@@ -102,6 +102,12 @@ def test_pack_roundtrip_bit_exact(E, K, N):
 # ---------------------------------------------------------------------------- forward
 
 
+def assert_within_one_ulp(a, b):
+    """Two bf16 results equal up to one unit in the last place of the larger one."""
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(a), np.abs(b)) + 1e-30)) - 7)
+    assert np.all(np.abs(a - b) <= ulp)
+
+
 def check_forward(prob, hidden, ids, wts, what):
     got = prob.run(hidden, ids, wts)
     ref = prob.reference(hidden, ids, wts)
@@ -193,7 +199,7 @@ def test_forward_host_matches_device_forward():
     prob.moe.forward_host(h_hidden, h_ids, h_wts, h_out)
     host_out = h_out.view(torch.bfloat16).float().numpy().astype(np.float64)
     assert_close(host_out, prob.reference(hidden, ids, wts), "forward_host")
-    assert np.max(np.abs(host_out - dev_out)) <= 1e-2 * np.sqrt(np.mean(dev_out ** 2))
+    assert_within_one_ulp(host_out, dev_out)
     prob.close()
 
 
@@ -204,6 +210,7 @@ def test_repeated_calls_agree():
     hidden, ids, wts = inputs.workload_inputs(wl)
     a = prob.run(hidden, ids, wts)
     b = prob.run(hidden, ids, wts)
-    # the down GEMM adds partial products with float atomics: only the order may differ
-    assert np.max(np.abs(a - b)) <= 1e-2 * np.sqrt(np.mean(a ** 2))
+    # the down GEMM adds partial products with float atomics: only the summation
+    # order may differ, which can flip the last bit of the bf16 output
+    assert_within_one_ulp(a, b)
     prob.close()
