@@ -153,6 +153,32 @@ int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s,
 int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M,
                                 uint16_t* h_rows, void* stream);
 
+/* ---- allocation-free variant ------------------------------------------ */
+
+/* The benchmark pages have no counterpart of this call; it exists for callers
+ * that cannot allocate device memory -- code running where cudaMalloc is not
+ * allowed or not wanted (inside a memory-pool-owning runtime, after device memory
+ * has been committed to a fixed budget, or in a plug-in that must not touch the
+ * host application's allocator) and so cannot provide the workspace that
+ * moe_w4a16_forward needs.
+ *
+ * Same computation, arguments and device pointers as moe_w4a16_forward, minus the
+ * workspace: the scratch lives in a fixed 48 MiB array in the library's device
+ * image (MOE_W4A16_NOALLOC_WORKSPACE_BYTES), present on every GPU that loads the
+ * library until the process exits. Calls whose moe_w4a16_workspace_size(h, M)
+ * exceeds it are rejected with MOE_W4A16_WORKSPACE_TOO_SMALL and a message giving
+ * both sizes (at E=384, K=7168, N=2048, top-8 this admits M <= 14 tokens).
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device); make that first call before any stream capture.
+ * Every call on a device shares the one array: calls that can overlap on the GPU
+ * (different streams without ordering between them) race and give wrong results;
+ * calls ordered on one stream are safe. Each call re-initialises what the
+ * forward needs zeroed, so leftovers of an earlier call do not matter.
+ * No cudaMalloc, cudaFree or other allocating routine is called. */
+#define MOE_W4A16_NOALLOC_WORKSPACE_BYTES (48u << 20)
+int moe_w4a16_forward_noalloc(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                              const float* topk_weights, uint16_t* out, int M, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ __all__ = [
     "moe_w4a16_forward_host", "moe_w4a16_status", "moe_w4a16_last_error",
     "moe_w4a16_set_option", "moe_w4a16_kernel_times", "moe_w4a16_packed_bytes",
     "moe_w4a16_align_debug", "moe_w4a16_unpack_debug", "moe_w4a16_read_intermediate",
-    "MoEW4A16", "OPT_NUM_CTAS", "OPT_PROFILE", "OPT_PDL", "STATUS_BAD_EXPERT_ID",
+    "moe_w4a16_forward_noalloc", "NOALLOC_WORKSPACE_BYTES", "MoEW4A16", "OPT_NUM_CTAS", "OPT_PROFILE", "OPT_PDL", "STATUS_BAD_EXPERT_ID",
     "STATUS_TIMEOUT",
 ]
 
@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libm
 OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR, NOT_PACKED = 0, -1, -2, -3, -4, -5
 STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT = 1, 2
 OPT_NUM_CTAS, OPT_PROFILE, OPT_PDL = 1, 2, 3
+NOALLOC_WORKSPACE_BYTES = 48 << 20
 
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 
@@ -46,6 +47,7 @@ _SIGNATURES = {
     "moe_w4a16_align_debug": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp]),
     "moe_w4a16_unpack_debug": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_w4a16_read_intermediate": (_c_int, [_vp, _vp, _c_int, _vp, _vp]),
+    "moe_w4a16_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp]),
 }
 
 _LIB = None
@@ -180,6 +182,13 @@ def moe_w4a16_unpack_debug(h, w1_q, w1_s, w2_q, w2_s, stream=None):
 
 def moe_w4a16_read_intermediate(h, workspace, M, h_rows, stream=None):
     _check(lib().moe_w4a16_read_intermediate(h, _ptr(workspace), M, _ptr(h_rows), _stream(stream)))
+
+
+def moe_w4a16_forward_noalloc(h, hidden, topk_ids, topk_weights, out, M, stream=None):
+    """The forward for callers that cannot allocate device memory: the workspace
+    is a fixed array inside the library (see include/moe_w4a16.h)."""
+    _check(lib().moe_w4a16_forward_noalloc(h, _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights),
+                                           _ptr(out), M, _stream(stream)))
 
 
 class MoEW4A16:

@@ -97,6 +97,12 @@ int check_handle(const moe_w4a16_ctx* h) {
 
 }  // namespace
 
+namespace moe {
+// Record `msg` as this thread's last error and return `code` (for entry points
+// defined in other translation units).
+int report_error(int code, const char* msg) { return fail(code, msg); }
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_w4a16_last_error(void) { return g_last_error.c_str(); }
