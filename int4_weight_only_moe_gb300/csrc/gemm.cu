@@ -14,7 +14,8 @@
 // single token (decode) costs one N=16 tile instead of a 128-row tile.
 //
 // Per CTA (one per SM), 20 warps:
-//   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
+//   warp 0       bulk-copies packed INT4 weight blocks, 4 k-blocks (18 KB) per copy,
+//                into a 6-chunk ring
 //   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
 //                (the lanes of a producer issue 4 consecutive k-blocks at once)
 //   warps 2, 3   tcgen05.mma issuers for alternate k-blocks, each into its own
@@ -55,7 +56,9 @@ constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 4;
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
-constexpr int kNW = 16;                  // weight ring depth (shared memory)
+constexpr int kWChunk = 4;               // k-blocks per weight copy (one 18 KB bulk copy)
+constexpr int kNWS = 6;                  // weight ring depth in chunks (shared memory)
+constexpr int kWChunkBytes = kWChunk * kWBlockBytes;
 constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
 constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
 constexpr int kTmemCols = 512;
@@ -66,12 +69,12 @@ constexpr int kProducerLanes = 4;        // copy-issuing threads per producer wa
 
 constexpr int kSmB = 0;
 constexpr int kSmW = kSmB + kNS * kBStage;
-constexpr int kSmStage = ((kSmW + kNW * kWBlockBytes + 1023) / 1024) * 1024;
+constexpr int kSmStage = ((kSmW + kNWS * kWChunkBytes + 1023) / 1024) * 1024;
 constexpr int kSmBar = kSmStage + kBNMax * 128;
 // barrier indices
-constexpr int kBarWFull = 0;                 // weight block landed (bulk-copy bytes)
-constexpr int kBarWEmpty = kBarWFull + kNW;  // weight block read by its 4 dequant warps
-constexpr int kBarFull = kBarWEmpty + kNW;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
+constexpr int kBarWFull = 0;                  // weight chunk landed (bulk-copy bytes)
+constexpr int kBarWEmpty = kBarWFull + kNWS;  // weight chunk read (4 dequant warps per k-block)
+constexpr int kBarFull = kBarWEmpty + kNWS;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
 constexpr int kBarEmpty = kBarFull + kNS;    // stage consumed by the MMAs (tcgen05.commit)
 constexpr int kBarAccFull = kBarEmpty + kNS; // [issuer][buffer]: accumulator complete
 constexpr int kBarAccEmpty = kBarAccFull + 4;  // [buffer]: epilogue has read both issuers' sums
@@ -247,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNW; ++i) {
+    for (int i = 0; i < kNWS; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
-      mbar_init(bar(kBarWEmpty + i), 4);
+      mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(kBarFull + i), 4 + 1);
@@ -280,14 +283,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   int* status = a.status;
   pdl_launch_dependents();
 
-  if (warp == kWarpW || warp == kWarpB) {
-    // ------------------------------------------------ bulk-copy producers
-    // warp 0: packed weight blocks (W ring); warp 1: activation tiles (B operand,
-    // operand-stage ring). kProducerLanes lanes walk consecutive k-blocks in
-    // step and issue their copies in one warp instruction: a bulk-copy issue
-    // blocks its thread for a while, so several copies have to leave at once for
-    // small (2-4.5 KB) copies to keep HBM busy.
-    const bool is_w = warp == kWarpW;
+  if (warp == kWarpW) {
+    // ------------------------------------------------ packed-weight producer
+    // One lane streams the weight blocks in chunks of kWChunk consecutive
+    // k-blocks: a row tile's k-blocks are contiguous, so a chunk is one 18 KB bulk
+    // copy (one per contiguous run where a chunk crosses units). Copies this
+    // large keep HBM busy from a single issuing thread; 4.5 KB ones do not.
+    if (lane == 0) {
+      const long long n_it = my_end - my_begin;
+      const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
+      Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
+      long long c = 0;
+      for (; c < n_chunks; ++c) {
+        const int s = static_cast<int>(c % kNWS);
+        if (!mbar_wait(bar(kBarWEmpty + s), ((c / kNWS) & 1) ^ 1, abort_flag, status,
+                       kStatusTimeout))
+          break;
+        const long long it0 = c * kWChunk;
+        const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
+        mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWBlockBytes);
+        for (long long it = it0; it < it1;) {
+          int kb = 0;
+          cur.seek(it, kb);
+          const long long left_in_unit = cur.kb1 - kb;
+          const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
+          const uint8_t* src =
+              a.wpack +
+              ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
+          bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWBlockBytes, src,
+                   static_cast<uint32_t>(run) * kWBlockBytes, bar(kBarWFull + s));
+          it += run;
+        }
+      }
+      // let the last chunks land before shared memory is released
+      for (long long j = 0; j < kNWS && j < c; ++j) {
+        const long long idx = c - 1 - j;
+        mbar_wait_drain(bar(kBarWFull + static_cast<int>(idx % kNWS)),
+                        static_cast<uint32_t>((idx / kNWS) & 1));
+      }
+    }
+  } else if (warp == kWarpB) {
+    // ------------------------------------------------ activation (B operand) producer
+    // kProducerLanes lanes walk consecutive k-blocks in step and issue their
+    // (2-8 KB) copies in one warp instruction: a bulk-copy issue holds its thread
+    // for a while, so small copies must leave several at a time.
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
       Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
@@ -299,47 +338,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (it < n_it) {
           int kb = 0;
           cur.seek(it, kb);
-          bool ok;
-          if (is_w) {
-            const int s = static_cast<int>(it % kNW);
-            ok = mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
-                           kStatusTimeout);
-            __syncwarp(active);
-            if (ok) {
-              const uint8_t* src =
-                  a.wpack +
-                  ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
-              mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
-              bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
-            }
-          } else {
-            const int s = static_cast<int>(it % kNS);
-            ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                           kStatusTimeout);
-            __syncwarp(active);
-            if (ok) {
-              const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
-              const uint8_t* src =
-                  a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
-              mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
-              bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
-            }
-          }
+          const int s = static_cast<int>(it % kNS);
+          const bool ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                                    kStatusTimeout);
+          __syncwarp(active);
           if (ok) {
+            const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
+            const uint8_t* src =
+                a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
+            mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
+            bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
             last = it;
             ++mine;
           }
           if (__any_sync(active, !ok)) break;
         }
       }
-      // bounded wait for this lane's last copies to land before shared memory is
-      // released (the operand-stage barriers also count dequant arrivals, so for
-      // them this only gives the copies time)
-      const int depth = is_w ? kNW : kNS;
-      for (uint32_t j = 0; j < static_cast<uint32_t>(depth / kProducerLanes) && j < mine; ++j) {
+      // bounded wait giving this lane's last copies time to land before shared
+      // memory is released (the stage barriers also count dequant arrivals)
+      for (uint32_t j = 0; j < static_cast<uint32_t>(kNS / kProducerLanes) && j < mine; ++j) {
         const long long idx = last - static_cast<long long>(j) * kProducerLanes;
-        mbar_wait_drain(bar((is_w ? kBarWFull : kBarFull) + static_cast<int>(idx % depth)),
-                        static_cast<uint32_t>((idx / depth) & 1));
+        mbar_wait_drain(bar(kBarFull + static_cast<int>(idx % kNS)),
+                        static_cast<uint32_t>((idx / kNS) & 1));
       }
     }
   } else if (warp == kWarpMma0 || warp == kWarpMma1) {
@@ -361,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       if (first < it_base + len) {
         const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-        ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarAccEmpty + ab),
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
                                                     kStatusTimeout));
         if (!ok) break;
@@ -369,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
           const uint32_t st = it % kNS;
-          ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarFull + st), (it / kNS) & 1,
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
                                                       abort_flag, status, kStatusTimeout));
           if (!ok) break;
           const uint32_t a_tmem = tmem + st * kACols;
@@ -417,14 +437,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     while (ok && si.next(u, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         if (static_cast<int>(it % kDeqPhases) != phase) continue;
-        const int ws = it % kNW, st = it % kNS;
-        bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
+        const uint32_t wc = it / kWChunk;  // weight chunk of this k-block
+        const int ws = static_cast<int>(wc % kNWS), st = it % kNS;
+        bool w_ok = mbar_wait(bar(kBarWFull + ws), (wc / kNWS) & 1, abort_flag, status,
                               kStatusTimeout);
         if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
           break;
         }
-        const uint32_t wb = sW + ws * kWBlockBytes;
+        const uint32_t wb = sW + ws * kWChunkBytes + (it % kWChunk) * kWBlockBytes;
         const uint4 q0 = ld_shared_v4(wb + r * 16);
         const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
         const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
