@@ -50,6 +50,28 @@
 
 namespace moe {
 
+// Optional pipeline timeline for performance work: built with -DMOE_GEMM_TRACE,
+// CTA 0 of the traced GEMM records clock64() at fixed points per k-block into a
+// device array read back with moe_gemm_trace_read(). Compiled out otherwise.
+#ifdef MOE_GEMM_TRACE
+__device__ long long g_gemm_trace[16][2048];
+extern "C" int moe_gemm_trace_read(long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_gemm_trace, sizeof(g_gemm_trace)));
+}
+#ifndef MOE_GEMM_TRACE_MODE
+#define MOE_GEMM_TRACE_MODE 1
+#endif
+#define TRACE_POINT(slot, idx)                                                      \
+  do {                                                                              \
+    if (blockIdx.x == 0 && kMode == MOE_GEMM_TRACE_MODE && (idx) < 2048)            \
+      g_gemm_trace[(slot)][(idx)] = clock64();                                      \
+  } while (0)
+#else
+#define TRACE_POINT(slot, idx) \
+  do {                         \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
@@ -301,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           break;
         const long long it0 = c * kWChunk;
         const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
+        TRACE_POINT(0, it0);
         mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWBlockBytes);
         for (long long it = it0; it < it1;) {
           int kb = 0;
@@ -346,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
             const uint8_t* src =
                 a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
+            TRACE_POINT(1, it);
             mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
             bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
             last = it;
@@ -389,9 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
           const uint32_t st = it % kNS;
+          if (lane == 0) TRACE_POINT(2, it);
           ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
                                                       abort_flag, status, kStatusTimeout));
           if (!ok) break;
+          if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
           // B stage st is st * kBStage bytes after stage 0 (16-byte units in the
           // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
@@ -403,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
             tc_commit(bar(kBarEmpty + st));
+            TRACE_POINT(4, it);
           }
           acc_flag = 1u;
         }
@@ -434,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     int kb0, kb1;
     bool ok = true, pending = false;
     int pend_stage = 0;
+    uint32_t pend_it = 0;
+    (void)pend_it;
     while (ok && si.next(u, kb0, kb1)) {
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         if (static_cast<int>(it % kDeqPhases) != phase) continue;
@@ -445,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           ok = false;
           break;
         }
+        if (lane == 0) TRACE_POINT(5 + (quad == 0 ? 0 : 10), it);
         const uint32_t wb = sW + ws * kWChunkBytes + (it % kWChunk) * kWBlockBytes;
         const uint4 q0 = ld_shared_v4(wb + r * 16);
         const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
@@ -454,11 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         dequant_group(q0, s0, *reinterpret_cast<uint32_t(*)[16]>(&out[0]));
         dequant_group(q1, s1, *reinterpret_cast<uint32_t(*)[16]>(&out[16]));
         __syncwarp();  // every lane has consumed its shared-memory words
+        if (lane == 0 && quad == 0) TRACE_POINT(6, it);
         if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
         if (pending) {
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
+          if (lane == 0) TRACE_POINT(8 + quad, pend_it);
           if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
           pending = false;
         }
@@ -468,10 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           ok = false;
           break;
         }
+        if (lane == 0 && quad == 0) TRACE_POINT(7, it);
         tc_fence_after();
         tmem_st32(tmem + t_lane + st * kACols, out);
         pending = true;
         pend_stage = st;
+        pend_it = it;
       }
     }
     if (pending) {
