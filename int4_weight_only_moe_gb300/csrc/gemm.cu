@@ -205,14 +205,24 @@ struct Cursor {
 
 // 32 INT4 codes (one scale group) -> 16 f16x2 words, columns of the A operand.
 // OR-ing a code u into the mantissa of fp16 1024 gives exactly 1024 + u (code at
-// bits 0..3 of a half) or 1024 + 16u (code at bits 4..7); subtracting 1032, or
-// scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
-// scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
-// (for scales in fp16's normal range), so the dequantised weight carries no
-// rounding error. One shift and four masks unpack a word of eight codes.
-__device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t s_bf16, uint32_t (&out)[16]) {
+// bits 0..3 of a half) or 1024 + 16u (code at bits 4..7). For the first form
+// (v - 1032) * s, for the second fma(v, s/16, -72 s) gives (u - 8) * s with a
+// single rounding; both are exact because (u - 8) * s and 72 s have at most 11
+// significant bits for a bf16 scale s (within fp16's normal range). One shift,
+// four masks and six f16x2 operations per word of eight codes.
+struct GroupScale {
+  uint32_t s2, s16, m72;  // s, s/16 and -72 s as f16x2 pairs
+};
+__device__ __forceinline__ GroupScale group_scale(uint32_t s_bf16) {
   const __half sh = __float2half_rn(__uint_as_float(s_bf16 << 16));
-  const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;
+  GroupScale g;
+  g.s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;
+  g.s16 = f16x2_mul(g.s2, 0x2C002C00u);  // * 1/16
+  g.m72 = f16x2_mul(g.s2, 0xD480D480u);  // * -72
+  return g;
+}
+__device__ __forceinline__ void dequant_group(const uint4 qv, const GroupScale g,
+                                              uint32_t* out) {
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -221,10 +231,10 @@ __device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t s_bf16, u
     const uint32_t v1 = (q & 0x00F000F0u) | 0x64006400u;   // elements 2, 3: 1024 + 16u
     const uint32_t v2 = (q8 & 0x000F000Fu) | 0x64006400u;  // elements 4, 5
     const uint32_t v3 = (q8 & 0x00F000F0u) | 0x64006400u;  // elements 6, 7
-    out[4 * j + 0] = f16x2_mul(f16x2_sub(v0, 0x64086408u), s2);
-    out[4 * j + 1] = f16x2_mul(f16x2_fma(v1, 0x2C002C00u, 0xD480D480u), s2);
-    out[4 * j + 2] = f16x2_mul(f16x2_sub(v2, 0x64086408u), s2);
-    out[4 * j + 3] = f16x2_mul(f16x2_fma(v3, 0x2C002C00u, 0xD480D480u), s2);
+    out[4 * j + 0] = f16x2_mul(f16x2_sub(v0, 0x64086408u), g.s2);
+    out[4 * j + 1] = f16x2_fma(v1, g.s16, g.m72);
+    out[4 * j + 2] = f16x2_mul(f16x2_sub(v2, 0x64086408u), g.s2);
+    out[4 * j + 3] = f16x2_fma(v3, g.s16, g.m72);
   }
 }
 
@@ -447,66 +457,55 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
-    // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
-    // in this CTA's sequence is congruent to `phase` modulo kDeqPhases. The TMEM
+    // Warp (quad, phase) converts rows 32*quad .. +31 of the k-blocks whose index
+    // in this CTA's sequence is phase, phase + kDeqPhases, ... (only the index
+    // matters here: it fixes the weight-ring slot and the operand stage). The TMEM
     // store of one k-block is retired (wait::st + arrival) only after the warp
     // has loaded and converted its next k-block, which hides the store latency.
     const int quad = warp & 3;
     const int phase = (warp - kWarpDeq0) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t it = 0;
-    SegIter si{my_begin, my_end, a.KBn};
-    long long u;
-    int kb0, kb1;
-    bool ok = true, pending = false;
-    int pend_stage = 0;
+    const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
+    bool pending = false;
+    uint32_t pend_stage = 0;
     uint32_t pend_it = 0;
     (void)pend_it;
-    while (ok && si.next(u, kb0, kb1)) {
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        if (static_cast<int>(it % kDeqPhases) != phase) continue;
-        const uint32_t wc = it / kWChunk;  // weight chunk of this k-block
-        const int ws = static_cast<int>(wc % kNWS), st = it % kNS;
-        bool w_ok = mbar_wait(bar(kBarWFull + ws), (wc / kNWS) & 1, abort_flag, status,
-                              kStatusTimeout);
-        if (!__all_sync(0xffffffffu, w_ok)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) TRACE_POINT(5 + (quad == 0 ? 0 : 10), it);
-        const uint32_t wb = sW + ws * kWChunkBytes + (it % kWChunk) * kWBlockBytes;
-        const uint4 q0 = ld_shared_v4(wb + r * 16);
-        const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
-        const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
-        const uint32_t s1 = ld_shared_u16(wb + kWCodeBytes + 256 + r * 2);
-        uint32_t out[32];
-        dequant_group(q0, s0, *reinterpret_cast<uint32_t(*)[16]>(&out[0]));
-        dequant_group(q1, s1, *reinterpret_cast<uint32_t(*)[16]>(&out[16]));
-        __syncwarp();  // every lane has consumed its shared-memory words
-        if (lane == 0 && quad == 0) TRACE_POINT(6, it);
-        if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-        if (pending) {
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) TRACE_POINT(8 + quad, pend_it);
-          if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
-          pending = false;
-        }
-        w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                         kStatusTimeout);
-        if (!__all_sync(0xffffffffu, w_ok)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0 && quad == 0) TRACE_POINT(7, it);
-        tc_fence_after();
-        tmem_st32(tmem + t_lane + st * kACols, out);
-        pending = true;
-        pend_stage = st;
-        pend_it = it;
+    for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
+      const uint32_t wc = it / kWChunk;  // weight chunk of this k-block
+      const uint32_t ws = wc % kNWS, st = it % kNS;
+      bool w_ok = mbar_wait(bar(kBarWFull + ws), (wc / kNWS) & 1, abort_flag, status,
+                            kStatusTimeout);
+      if (!__all_sync(0xffffffffu, w_ok)) break;
+      if (lane == 0 && quad == 0) TRACE_POINT(5, it);
+      const uint32_t wb = sW + ws * kWChunkBytes + (it % kWChunk) * kWBlockBytes;
+      const uint4 q0 = ld_shared_v4(wb + r * 16);
+      const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
+      const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
+      const uint32_t s1 = ld_shared_u16(wb + kWCodeBytes + 256 + r * 2);
+      uint32_t out[32];
+      dequant_group(q0, group_scale(s0), &out[0]);
+      dequant_group(q1, group_scale(s1), &out[16]);
+      __syncwarp();  // every lane has consumed its shared-memory words
+      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
+      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
+      if (pending) {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) TRACE_POINT(8 + quad, pend_it);
+        if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
+        pending = false;
       }
+      w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                       kStatusTimeout);
+      if (!__all_sync(0xffffffffu, w_ok)) break;
+      if (lane == 0 && quad == 0) TRACE_POINT(7, it);
+      tc_fence_after();
+      tmem_st32(tmem + t_lane + st * kACols, out);
+      pending = true;
+      pend_stage = st;
+      pend_it = it;
     }
     if (pending) {
       tmem_st_wait();
