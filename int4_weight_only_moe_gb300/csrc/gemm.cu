@@ -205,24 +205,16 @@ struct Cursor {
 
 // 32 INT4 codes (one scale group) -> 16 f16x2 words, columns of the A operand.
 // OR-ing a code u into the mantissa of fp16 1024 gives exactly 1024 + u (code at
-// bits 0..3 of a half) or 1024 + 16u (code at bits 4..7). For the first form
-// (v - 1032) * s, for the second fma(v, s/16, -72 s) gives (u - 8) * s with a
-// single rounding; both are exact because (u - 8) * s and 72 s have at most 11
-// significant bits for a bf16 scale s (within fp16's normal range). One shift,
-// four masks and six f16x2 operations per word of eight codes.
-struct GroupScale {
-  uint32_t s2, s16, m72;  // s, s/16 and -72 s as f16x2 pairs
-};
-__device__ __forceinline__ GroupScale group_scale(uint32_t s_bf16) {
+// bits 0..3 of a half) or 1024 + 16u (code at bits 4..7); subtracting 1032, or
+// scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
+// scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
+// (for scales in fp16's normal range), so the dequantised weight carries no
+// rounding error. One shift and four masks unpack a word of eight codes.
+__device__ __forceinline__ uint32_t group_scale(uint32_t s_bf16) {
   const __half sh = __float2half_rn(__uint_as_float(s_bf16 << 16));
-  GroupScale g;
-  g.s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;
-  g.s16 = f16x2_mul(g.s2, 0x2C002C00u);  // * 1/16
-  g.m72 = f16x2_mul(g.s2, 0xD480D480u);  // * -72
-  return g;
+  return static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;  // s as an f16x2 pair
 }
-__device__ __forceinline__ void dequant_group(const uint4 qv, const GroupScale g,
-                                              uint32_t* out) {
+__device__ __forceinline__ void dequant_group(const uint4 qv, const uint32_t s2, uint32_t* out) {
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -231,10 +223,10 @@ __device__ __forceinline__ void dequant_group(const uint4 qv, const GroupScale g
     const uint32_t v1 = (q & 0x00F000F0u) | 0x64006400u;   // elements 2, 3: 1024 + 16u
     const uint32_t v2 = (q8 & 0x000F000Fu) | 0x64006400u;  // elements 4, 5
     const uint32_t v3 = (q8 & 0x00F000F0u) | 0x64006400u;  // elements 6, 7
-    out[4 * j + 0] = f16x2_mul(f16x2_sub(v0, 0x64086408u), g.s2);
-    out[4 * j + 1] = f16x2_fma(v1, g.s16, g.m72);
-    out[4 * j + 2] = f16x2_mul(f16x2_sub(v2, 0x64086408u), g.s2);
-    out[4 * j + 3] = f16x2_fma(v3, g.s16, g.m72);
+    out[4 * j + 0] = f16x2_mul(f16x2_sub(v0, 0x64086408u), s2);
+    out[4 * j + 1] = f16x2_mul(f16x2_fma(v1, 0x2C002C00u, 0xD480D480u), s2);
+    out[4 * j + 2] = f16x2_mul(f16x2_sub(v2, 0x64086408u), s2);
+    out[4 * j + 3] = f16x2_mul(f16x2_fma(v3, 0x2C002C00u, 0xD480D480u), s2);
   }
 }
 
