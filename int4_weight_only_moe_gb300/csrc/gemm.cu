@@ -15,7 +15,7 @@
 //
 // Per CTA (one per SM), 20 warps:
 //   warp 0       bulk-copies packed INT4 weight blocks, 4 k-blocks (18 KB) per copy,
-//                into a 6-chunk ring
+//                into a 4-chunk ring
 //   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
 //                (the lanes of a producer issue 4 consecutive k-blocks at once)
 //   warps 2, 3   tcgen05.mma issuers for alternate k-blocks, each into its own
@@ -79,7 +79,7 @@ constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
 constexpr int kWChunk = 4;               // k-blocks per weight copy (one 18 KB bulk copy)
-constexpr int kNWS = 6;                  // weight ring depth in chunks (shared memory)
+constexpr int kNWS = 4;                  // weight ring depth in chunks (shared memory)
 constexpr int kWChunkBytes = kWChunk * kWBlockBytes;
 constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
 constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
@@ -209,11 +209,8 @@ struct Cursor {
 // scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
 // scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
 // (for scales in fp16's normal range), so the dequantised weight carries no
-// rounding error. One shift and four masks unpack a word of eight codes.
-__device__ __forceinline__ uint32_t group_scale(uint32_t s_bf16) {
-  const __half sh = __float2half_rn(__uint_as_float(s_bf16 << 16));
-  return static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;  // s as an f16x2 pair
-}
+// rounding error. One shift and four masks unpack a word of eight codes; `s2` is
+// the fp16 scale in both halves.
 __device__ __forceinline__ void dequant_group(const uint4 qv, const uint32_t s2, uint32_t* out) {
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
@@ -473,11 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const uint32_t wb = sW + ws * kWChunkBytes + (it % kWChunk) * kWBlockBytes;
       const uint4 q0 = ld_shared_v4(wb + r * 16);
       const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
-      const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
-      const uint32_t s1 = ld_shared_u16(wb + kWCodeBytes + 256 + r * 2);
+      const uint32_t sc = ld_shared_u32(wb + kWCodeBytes + r * 4);  // fp16 scales of both groups
       uint32_t out[32];
-      dequant_group(q0, group_scale(s0), &out[0]);
-      dequant_group(q1, group_scale(s1), &out[16]);
+      dequant_group(q0, __byte_perm(sc, 0, 0x1010), &out[0]);
+      dequant_group(q1, __byte_perm(sc, 0, 0x3232), &out[16]);
       __syncwarp();  // every lane has consumed its shared-memory words
       if (lane == 0 && quad == 0) TRACE_POINT(6, it);
       if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
