@@ -78,13 +78,19 @@ constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 4;
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
-constexpr int kWChunk = 4;               // k-blocks per weight copy (one 18 KB bulk copy)
+// A pipeline step covers kSub consecutive 64-element k-blocks (128 reduction
+// elements): every per-step cost (barrier waits and arrivals, MMA commit, address
+// arithmetic) is paid once per 128 elements.
+constexpr int kSub = 2;
+constexpr int kWStepBytes = kSub * kWBlockBytes;  // packed weights of one step (9 KB)
+constexpr int kWChunk = 2;               // steps per weight copy (one 18 KB bulk copy)
 constexpr int kNWS = 4;                  // weight ring depth in chunks (shared memory)
-constexpr int kWChunkBytes = kWChunk * kWBlockBytes;
-constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
-constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
+constexpr int kWChunkBytes = kWChunk * kWStepBytes;
+constexpr int kNS = 4;                   // operand stage ring: A in tensor memory, B in shared memory
+constexpr int kBSub = kBNMax * 128;      // B tile of one 64-element k-block
+constexpr int kBStage = kSub * kBSub;    // B tiles of one step
 constexpr int kTmemCols = 512;
-constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
+constexpr int kACols = kSub * 32;        // one step of fp16 A: 128 lanes x 64 columns
 constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
 constexpr int kStatusTimeout = 2;
 constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
@@ -95,7 +101,7 @@ constexpr int kSmStage = ((kSmW + kNWS * kWChunkBytes + 1023) / 1024) * 1024;
 constexpr int kSmBar = kSmStage + kBNMax * 128;
 // barrier indices
 constexpr int kBarWFull = 0;                  // weight chunk landed (bulk-copy bytes)
-constexpr int kBarWEmpty = kBarWFull + kNWS;  // weight chunk read (4 dequant warps per k-block)
+constexpr int kBarWEmpty = kBarWFull + kNWS;  // weight chunk read (4 dequant warps per step)
 constexpr int kBarFull = kBarWEmpty + kNWS;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
 constexpr int kBarEmpty = kBarFull + kNS;    // stage consumed by the MMAs (tcgen05.commit)
 constexpr int kBarAccFull = kBarEmpty + kNS; // [issuer][buffer]: accumulator complete
@@ -107,6 +113,8 @@ constexpr int kSmBytes = kSmMisc + 64;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
+static_assert((kNWS & (kNWS - 1)) == 0 && (kNS & (kNS - 1)) == 0 && kWChunk == 2,
+              "ring index arithmetic below assumes power-of-two rings and 2-step chunks");
 
 constexpr int kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
@@ -273,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNWS; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
-      mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);
+      mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);  // 4 quadrant warps x steps
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(kBarFull + i), 4 + 1);
@@ -306,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
   if (warp == kWarpW) {
     // ------------------------------------------------ packed-weight producer
-    // One lane streams the weight blocks in chunks of kWChunk consecutive
-    // k-blocks: a row tile's k-blocks are contiguous, so a chunk is one 18 KB bulk
-    // copy (one per contiguous run where a chunk crosses units). Copies this
-    // large keep HBM busy from a single issuing thread; 4.5 KB ones do not.
+    // One lane streams the weight blocks in chunks of kWChunk consecutive steps:
+    // a row tile's k-blocks are contiguous, so a chunk is one 18 KB bulk copy (one
+    // per contiguous run where a chunk crosses units). Copies this large keep HBM
+    // busy from a single issuing thread; 4.5 KB ones do not.
     if (lane == 0) {
       const long long n_it = my_end - my_begin;
       const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
@@ -323,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const long long it0 = c * kWChunk;
         const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
         TRACE_POINT(0, it0);
-        mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWBlockBytes);
+        mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWStepBytes);
         for (long long it = it0; it < it1;) {
           int kb = 0;
           cur.seek(it, kb);
@@ -331,9 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
           const uint8_t* src =
               a.wpack +
-              ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
-          bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWBlockBytes, src,
-                   static_cast<uint32_t>(run) * kWBlockBytes, bar(kBarWFull + s));
+              ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWStepBytes;
+          bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes, src,
+                   static_cast<uint32_t>(run) * kWStepBytes, bar(kBarWFull + s));
           it += run;
         }
       }
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   } else if (warp == kWarpB) {
     // ------------------------------------------------ activation (B operand) producer
     // kProducerLanes lanes walk consecutive k-blocks in step and issue their
-    // (2-8 KB) copies in one warp instruction: a bulk-copy issue holds its thread
+    // (2-8 KB) copies in one go: a bulk-copy issue holds its thread
     // for a while, so small copies must leave several at a time.
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
@@ -365,12 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                                     kStatusTimeout);
           __syncwarp(active);
           if (ok) {
+            // the step's two 64-element k-blocks are two planes of the blocked layout
             const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
-            const uint8_t* src =
-                a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
+            const uint8_t* src = a.bsrc + (static_cast<long long>(kb) * kSub * a.Gcap + cur.un.g0) *
+                                              kRowGroupBytes;
+            const long long plane = static_cast<long long>(a.Gcap) * kRowGroupBytes;
             TRACE_POINT(1, it);
-            mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
+            mbar_arrive_expect_tx(bar(kBarFull + s), kSub * bytes);
             bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
+            bulk_g2s(sB + s * kBStage + kBSub, src + plane, bytes, bar(kBarFull + s));
             last = it;
             ++mine;
           }
@@ -418,15 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           if (!ok) break;
           if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
-          // B stage st is st * kBStage bytes after stage 0 (16-byte units in the
-          // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
+          // B stage st is st * kBStage bytes after stage 0, its second 64-element
+          // half kBSub bytes further (16-byte units in the descriptor); +32 bytes of
+          // K per MMA inside the 128-byte swizzled rows.
           const uint64_t b_desc = b_desc0 + ((st * kBStage) >> 4);
+          const uint64_t b_desc1 = b_desc + (kBSub >> 4);
           if (elect_one()) {
             tc_fence_after();
             tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
             tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 32, b_desc1, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 40, b_desc1 + 2, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 48, b_desc1 + 4, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 56, b_desc1 + 6, idesc, 1u);
             tc_commit(bar(kBarEmpty + st));
             TRACE_POINT(4, it);
           }
@@ -460,23 +477,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     uint32_t pend_stage = 0;
     uint32_t pend_it = 0;
     (void)pend_it;
+    const uint32_t a_lane = tmem + t_lane;
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
-      const uint32_t wc = it / kWChunk;  // weight chunk of this k-block
-      const uint32_t ws = wc % kNWS, st = it % kNS;
-      bool w_ok = mbar_wait(bar(kBarWFull + ws), (wc / kNWS) & 1, abort_flag, status,
+      const uint32_t ws = (it >> 1) & (kNWS - 1);  // weight chunk slot (2 steps per chunk)
+      const uint32_t st = it & (kNS - 1);
+      bool w_ok = mbar_wait(bar(kBarWFull + ws), (it >> 3) & 1, abort_flag, status,
                             kStatusTimeout);
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(5, it);
-      const uint32_t wb = sW + ws * kWChunkBytes + (it % kWChunk) * kWBlockBytes;
-      const uint4 q0 = ld_shared_v4(wb + r * 16);
-      const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
-      const uint32_t sc = ld_shared_u32(wb + kWCodeBytes + r * 4);  // fp16 scales of both groups
+      // the step's weights: slot ws, step (it & 1) of the chunk = (it & 7) steps in
+      const uint32_t wb = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + r * 16;
+      const uint32_t wsc = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + kWCodeBytes + r * 4;
+      const uint4 q0 = ld_shared_v4(wb);
+      const uint4 q1 = ld_shared_v4(wb + 2048);
+      const uint4 q2 = ld_shared_v4(wb + kWBlockBytes);
+      const uint4 q3 = ld_shared_v4(wb + kWBlockBytes + 2048);
+      const uint32_t sc0 = ld_shared_u32(wsc);  // fp16 scales of the two groups
+      const uint32_t sc1 = ld_shared_u32(wsc + kWBlockBytes);
       uint32_t out[32];
-      dequant_group(q0, __byte_perm(sc, 0, 0x1010), &out[0]);
-      dequant_group(q1, __byte_perm(sc, 0, 0x3232), &out[16]);
-      __syncwarp();  // every lane has consumed its shared-memory words
-      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
-      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
+      dequant_group(q0, __byte_perm(sc0, 0, 0x1010), &out[0]);
+      dequant_group(q1, __byte_perm(sc0, 0, 0x3232), &out[16]);
       if (pending) {
         tmem_st_wait();
         tc_fence_before();
@@ -485,12 +505,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
         pending = false;
       }
-      w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
+      w_ok = mbar_wait(bar(kBarEmpty + st), ((it >> 2) & 1) ^ 1, abort_flag, status,
                        kStatusTimeout);
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(7, it);
       tc_fence_after();
-      tmem_st32(tmem + t_lane + st * kACols, out);
+      tmem_st32(a_lane + st * kACols, out);
+      dequant_group(q2, __byte_perm(sc1, 0, 0x1010), &out[0]);
+      dequant_group(q3, __byte_perm(sc1, 0, 0x3232), &out[16]);
+      __syncwarp();  // every lane has consumed its shared-memory words
+      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
+      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
+      tmem_st32(a_lane + st * kACols + 32, out);
       pending = true;
       pend_stage = st;
       pend_it = it;
