@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
       const int rank = __popc(peers & ((1u << lane) - 1u));
-      a.sorted_ids[seg_sm[e] + hist[w * E + e] + rank] = i;
+      const int pos = seg_sm[e] + hist[w * E + e] + rank;
+      if (MOE_CHECK(a.sorted_cap <= 0 || pos < a.sorted_cap, a.hdr, a.dbg, 21, pos, e))
+        a.sorted_ids[pos] = i;
     }
     __syncwarp();
     if (e >= 0 && lane == __ffs(peers) - 1) hist[w * E + e] += __popc(peers);
@@ -105,7 +107,9 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
   }
 
   if (tid < E) {
-    for (int p = seg + my_cnt; p < seg + my_pad; ++p) a.sorted_ids[p] = a.MK;
+    for (int p = seg + my_cnt; p < seg + my_pad; ++p)
+      if (MOE_CHECK(a.sorted_cap <= 0 || p < a.sorted_cap, a.hdr, a.dbg, 22, p, tid))
+        a.sorted_ids[p] = a.MK;
     if (a.expert_offsets) {
       a.expert_offsets[tid] = seg;
       if (tid == E - 1) a.expert_offsets[E] = tot_pad;
@@ -117,7 +121,8 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
         tt.g0 = (seg + t * a.bn_max) / kRowGroup;
         tt.ngroups = min(a.bn_max, my_pad - t * a.bn_max) / kRowGroup;
         tt.first = tstart;
-        a.tiles[tstart + t] = tt;
+        if (MOE_CHECK(tstart + t < a.tiles_cap, a.hdr, a.dbg, 23, tstart + t, tid))
+          a.tiles[tstart + t] = tt;
       }
       a.expert_tiles[tid] = my_tiles;
     }
@@ -167,13 +172,15 @@ __global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
     const int p = static_cast<int>(idx / cpr), ch = static_cast<int>(idx - static_cast<long long>(p) * cpr);
     const int sid = a.sorted_ids[p];
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (sid < a.MK)
+    if (sid < a.MK && MOE_CHECK(sid >= 0 && sid / a.topk < a.M, const_cast<int32_t*>(a.hdr),
+                                a.dbg, 24, sid, p))
       v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
           a.x + static_cast<long long>(sid / a.topk) * a.K + ch * 8));
     const int g = p / kRowGroup, r = p % kRowGroup;
-    uint8_t* dst = a.xs + (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
-                   r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst) = v;
+    const long long off = (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
+                          r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    if (MOE_CHECK(off + 16 <= a.xs_bytes, const_cast<int32_t*>(a.hdr), a.dbg, 25, off, p))
+      *reinterpret_cast<uint4*>(a.xs + off) = v;
   }
   pdl_launch_dependents();
 }

@@ -271,6 +271,9 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   aa.hdr = hdr;
   aa.tickets = tickets;
   aa.n_tickets = kMaxCtas;
+  aa.sorted_cap = L.Pcap;
+  aa.tiles_cap = L.Gcap;
+  aa.dbg = hdr + 8;
   MOE_CUDA_TRY(launch_align(aa, s, false));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
 
@@ -285,6 +288,9 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   ga.xs = xs;
   ga.acc = acc;
   ga.acc_elems = static_cast<long long>(M) * h->K;
+  ga.xs_bytes = static_cast<long long>(L.Pcap) * h->K * 2;
+  ga.M = M;
+  ga.dbg = hdr + 8;
   MOE_CUDA_TRY(launch_gather(ga, L.Gcap, h->num_sms, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[2], s));
 
@@ -303,6 +309,14 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g1.MK = static_cast<int>(MK);
   g1.topk = h->topk;
   g1.status = hdr + kHdrStatus;
+  g1.wpack_bytes = static_cast<long long>(h->w1p_bytes);
+  g1.bsrc_bytes = static_cast<long long>(L.Pcap) * h->K * 2;
+  g1.hout_bytes = static_cast<long long>(L.Pcap) * h->N * 2;
+  g1.scratch_elems = static_cast<long long>(kMaxCtas) * 2 * kBNMax * kBM;
+  g1.sorted_cap = L.Pcap;
+  g1.tiles_cap = L.Gcap;
+  g1.E = h->E;
+  g1.dbg = hdr + 8;
   MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
@@ -322,6 +336,13 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g2.MK = static_cast<int>(MK);
   g2.topk = h->topk;
   g2.status = hdr + kHdrStatus;
+  g2.wpack_bytes = static_cast<long long>(h->w2p_bytes);
+  g2.bsrc_bytes = static_cast<long long>(L.Pcap) * h->N * 2;
+  g2.acc_elems = static_cast<long long>(M) * h->K;
+  g2.sorted_cap = L.Pcap;
+  g2.tiles_cap = L.Gcap;
+  g2.E = h->E;
+  g2.dbg = hdr + 8;
   MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 

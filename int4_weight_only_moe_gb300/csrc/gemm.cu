@@ -337,11 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           cur.seek(it, kb);
           const long long left_in_unit = cur.kb1 - kb;
           const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
-          const uint8_t* src =
-              a.wpack +
+          const long long woff =
               ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWStepBytes;
-          bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes, src,
-                   static_cast<uint32_t>(run) * kWStepBytes, bar(kBarWFull + s));
+          if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kWStepBytes <= a.wpack_bytes &&
+                            cur.un.e >= 0 && cur.un.e < a.E && cur.un.rt < a.R && kb + run <= a.KBn &&
+                            run >= 1 && (it - it0) + run <= kWChunk,
+                        a.status, a.dbg, 1, woff, run * 100 + (it - it0)))
+            bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
+                     a.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes, bar(kBarWFull + s));
           it += run;
         }
       }
@@ -368,6 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (it < n_it) {
           int kb = 0;
           cur.seek(it, kb);
+          if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 && cur.un.e >= 0 && cur.un.e < a.E &&
+                             cur.un.g0 >= 0 && cur.un.g0 + cur.un.ng <= a.tiles_cap && kb >= 0 && kb < a.KBn,
+                         a.status, a.dbg, 11, cur.un.ng * 1000 + cur.un.e, cur.un.g0 * 1000 + kb))
+            cur.un.ng = 1;
           const int s = static_cast<int>(it % kNS);
           const bool ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
                                     kStatusTimeout);
@@ -375,13 +382,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           if (ok) {
             // the step's two 64-element k-blocks are two planes of the blocked layout
             const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
-            const uint8_t* src = a.bsrc + (static_cast<long long>(kb) * kSub * a.Gcap + cur.un.g0) *
-                                              kRowGroupBytes;
+            const long long boff =
+                (static_cast<long long>(kb) * kSub * a.Gcap + cur.un.g0) * kRowGroupBytes;
             const long long plane = static_cast<long long>(a.Gcap) * kRowGroupBytes;
             TRACE_POINT(1, it);
             mbar_arrive_expect_tx(bar(kBarFull + s), kSub * bytes);
-            bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
-            bulk_g2s(sB + s * kBStage + kBSub, src + plane, bytes, bar(kBarFull + s));
+            if (MOE_CHECK(boff >= 0 && boff + bytes <= a.bsrc_bytes && bytes <= kBSub && bytes > 0 &&
+                              s >= 0 && s < kNS,
+                          a.status, a.dbg, 2, boff, bytes))
+              bulk_g2s(sB + s * kBStage, a.bsrc + boff, bytes, bar(kBarFull + s));
+            if (MOE_CHECK(boff + plane + bytes <= a.bsrc_bytes, a.status, a.dbg, 3, boff + plane,
+                          bytes))
+              bulk_g2s(sB + s * kBStage + kBSub, a.bsrc + boff + plane, bytes, bar(kBarFull + s));
             last = it;
             ++mine;
           }
@@ -413,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
       const int ab = acc_it & 1;
       if (first < it_base + len) {
-        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16, a.status, a.dbg, 12, un.ng, u)) un.ng = 1;
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
@@ -538,7 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     long long u;
     int kb0, kb1;
     while (si.next(u, kb0, kb1)) {
-      const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16 && un.rt >= 0 && un.rt < a.R, a.status, a.dbg,
+                     13, un.ng, un.rt))
+        un.ng = 1;
       const int nch = un.ng;  // 16-column chunks
       const int ab = acc_it & 1;
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
@@ -561,7 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 #pragma unroll
         for (int j = 0; j < kRowRegs; ++j) {
           const int row = 32 * j + lane;
-          const int sid = row < nch * 16 ? a.sorted_ids[pbase + row] : a.MK;
+          const bool in_tile = row < nch * 16 &&
+                               MOE_CHECK(pbase + row < a.sorted_cap, a.status, a.dbg, 9, pbase + row, nch);
+          const int sid = in_tile ? a.sorted_ids[pbase + row] : a.MK;
           sid_r[j] = sid;
           if (sid < a.MK) {
             w_r[j] = a.topk_weights[sid];
@@ -629,8 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           for (int c = 0; c < nch; ++c) {
             float v[16];
             load_chunk(c, v);
+            const long long so = (slot - a.scratch) + (c * 16) * kBM + r;
+            if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 6, so, c)) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
+              for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -656,8 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                 const int pc = (sc.start(cc) < ustart) ? 1 : 0;
                 const float* sl =
                     a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
+                const long long so = (sl - a.scratch) + (c * 16) * kBM + r;
+                if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 7, so, cc)) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
+                  for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
+                }
               }
               swiglu_chunk(v, c, quad, lane, sStage);
             }
@@ -667,8 +691,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           fence_proxy_async_smem();
           named_bar_sync(kEpiBar, kEpiThreads);
           if (epi_tid == 0) {
-            bulk_s2g(a.hout + (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes,
-                     sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
+            const long long hoff = (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes;
+            if (MOE_CHECK(hoff >= 0 && hoff + nch * kRowGroupBytes <= a.hout_bytes && nch > 0 &&
+                              nch <= kBNMax / 16,
+                          a.status, a.dbg, 5, hoff, nch))
+              bulk_s2g(a.hout + hoff, sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
             bulk_commit();
             bulk_wait_read_all();
           }
@@ -688,7 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               if (sid < a.MK) {
                 const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
                 const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
-                atomicAdd(acc_col + static_cast<long long>(tok) * a.Kout, wt * v[i]);
+                const long long ai = (acc_col - a.acc) + static_cast<long long>(tok) * a.Kout;
+                if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 8, ai, sid))
+                  atomicAdd(a.acc + ai, wt * v[i]);
               }
             }
           }

@@ -30,6 +30,8 @@ struct AlignArgs {
   int32_t* tickets;         // zeroed, or null
   int n_tickets;
   int32_t* num_padded_out;  // optional extra copy of num_padded
+  int sorted_cap, tiles_cap;  // extents for the self-checking build
+  int32_t* dbg;
 };
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl);
 
@@ -42,6 +44,9 @@ struct GatherArgs {
   uint8_t* xs;        // blocked [K/64][Gcap][16 x 128 B]
   float* acc;         // [M, K] fp32, zeroed
   long long acc_elems;
+  long long xs_bytes;  // extents for the self-checking build
+  int M;
+  int32_t* dbg;
 };
 cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
                           bool pdl);
@@ -65,6 +70,10 @@ struct GemmArgs {
   float* acc;              // [M, Kout] fp32
   int Kout, MK, topk;
   int32_t* status;
+  // buffer extents, read only by the self-checking build (-DMOE_CHECKS)
+  long long wpack_bytes, bsrc_bytes, hout_bytes, acc_elems, scratch_elems;
+  int sorted_cap, tiles_cap, E;
+  int32_t* dbg;  // first failed check: site, values, block, thread
 };
 cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
@@ -76,6 +85,30 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int nu
 cudaError_t launch_read_intermediate(const uint8_t* hbuf, const int32_t* sorted_ids,
                                      const int32_t* hdr, int MK, int N, int Gcap, int max_rows,
                                      uint16_t* h_rows, cudaStream_t stream);
+
+// Self-checking build (-DMOE_CHECKS): every global access is range-checked first;
+// a failed check sets status bit 8, records the first failure (site, two values,
+// block, thread) in dbg[0..5] and skips the access.
+#ifdef MOE_CHECKS
+__device__ __forceinline__ bool moe_check(bool ok, int32_t* status, int32_t* dbg, int site,
+                                          long long v0, long long v1) {
+  if (!ok) {
+    if (status) atomicOr(status, 8);
+    if (dbg && atomicCAS(dbg, 0, site) == 0) {
+      dbg[1] = static_cast<int32_t>(v0);
+      dbg[2] = static_cast<int32_t>(v1);
+      dbg[3] = static_cast<int32_t>(blockIdx.x);
+      dbg[4] = static_cast<int32_t>(threadIdx.x);
+      dbg[5] = static_cast<int32_t>(v0 >> 32);
+    }
+  }
+  return ok;
+}
+#define MOE_CHECK(cond, status, dbg, site, v0, v1) \
+  moe_check((cond), (status), (dbg), (site), (long long)(v0), (long long)(v1))
+#else
+#define MOE_CHECK(cond, status, dbg, site, v0, v1) true
+#endif
 
 // Launch helper: optional programmatic dependent launch attribute.
 template <typename... KArgs, typename... Args>
