@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
   pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (tid == 0 && a.hdr) a.hdr[kHdrStatus] = 0;
+  if (tid < 8 && a.dbg) a.dbg[tid] = 0;
   for (int i = tid; i < 32 * E; i += blockDim.x) hist[i] = 0;
   if (a.tickets)
     for (int i = tid; i < a.n_tickets; i += blockDim.x) a.tickets[i] = 0;

@@ -40,6 +40,10 @@
 // order (deterministic), applies SiLU*up and writes the tile. No CTA ever waits
 // for another.
 //
+// Warp-collective tcgen05 instructions (.sync.aligned: st, ld, wait, alloc,
+// dealloc) are always preceded by a warp-wide synchronisation, never issued right
+// after lane-divergent code.
+//
 // Every mbarrier wait is bounded in time (see mbar_wait); a wait that gives up
 // raises a CTA-wide abort flag, records MOE_W4A16_STATUS_TIMEOUT, and all roles
 // fall through to the teardown, which still waits for in-flight copies and MMAs
@@ -511,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       dequant_group(q0, __byte_perm(sc0, 0, 0x1010), &out[0]);
       dequant_group(q1, __byte_perm(sc0, 0, 0x3232), &out[16]);
       if (pending) {
+        __syncwarp();
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -523,18 +528,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(7, it);
       tc_fence_after();
+      __syncwarp();
       tmem_st32(a_lane + st * kACols, out);
       dequant_group(q2, __byte_perm(sc1, 0, 0x1010), &out[0]);
       dequant_group(q3, __byte_perm(sc1, 0, 0x3232), &out[16]);
-      __syncwarp();  // every lane has consumed its shared-memory words
+      // converge before the warp-collective store; every lane has also consumed
+      // its shared-memory words by now, so the slot can be released after it
+      __syncwarp();
+      tmem_st32(a_lane + st * kACols + 32, out);
       if (lane == 0 && quad == 0) TRACE_POINT(6, it);
       if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-      tmem_st32(a_lane + st * kACols + 32, out);
       pending = true;
       pend_stage = st;
       pend_it = it;
     }
     if (pending) {
+      __syncwarp();
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -611,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       // fp32 sums of 16 token columns of this lane's row, both issuers added
       auto load_chunk = [&](int c, float (&v)[16]) {
         uint32_t rr[16];
+        __syncwarp();  // tcgen05.ld is warp-collective: converge after per-lane code
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = 0.f;
         if (has0) {
