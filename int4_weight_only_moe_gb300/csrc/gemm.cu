@@ -742,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   }
 
   // ------------------------------------------------ teardown
+  __syncwarp();  // lanes that skipped a single-lane role wait for it here
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma0) {

@@ -54,7 +54,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// One lane of the (whole, converged) warp; synchronises the warp first because
+// elect.sync with a full member mask must not run while lanes are diverged.
 __device__ __forceinline__ bool elect_one() {
+  __syncwarp();
   uint32_t pred;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -261,8 +264,10 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
 }
 
 // ---------------------------------------------------------------- misc
+// Named barrier over `nthreads` threads; the non-aligned form, so lanes of a warp
+// may arrive after lane-divergent code.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
