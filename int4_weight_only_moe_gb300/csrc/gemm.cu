@@ -10,12 +10,11 @@
 // inside fp16's range (the gather saturates beyond +-65504).
 //
 // "Swap-AB" orientation: the 128 weight rows of a tile are the MMA M dimension
-// and the routed tokens of one expert (16..128, a multiple of 16) are MMA N, so a
+// and the routed tokens of one expert (16..64, a multiple of 16) are MMA N, so a
 // single token (decode) costs one N=16 tile instead of a 128-row tile.
 //
 // Per CTA (one per SM), 20 warps:
-//   warp 0       bulk-copies packed INT4 weight blocks, 4 k-blocks (18 KB) per copy,
-//                into a 4-chunk ring
+//   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
 //   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
 //                (the lanes of a producer issue 4 consecutive k-blocks at once)
 //   warps 2, 3   tcgen05.mma issuers for alternate k-blocks, each into its own
@@ -40,10 +39,6 @@
 // order (deterministic), applies SiLU*up and writes the tile. No CTA ever waits
 // for another.
 //
-// Warp-collective tcgen05 instructions (.sync.aligned: st, ld, wait, alloc,
-// dealloc) are always preceded by a warp-wide synchronisation, never issued right
-// after lane-divergent code.
-//
 // Every mbarrier wait is bounded in time (see mbar_wait); a wait that gives up
 // raises a CTA-wide abort flag, records MOE_W4A16_STATUS_TIMEOUT, and all roles
 // fall through to the teardown, which still waits for in-flight copies and MMAs
@@ -54,59 +49,29 @@
 
 namespace moe {
 
-// Optional pipeline timeline for performance work: built with -DMOE_GEMM_TRACE,
-// CTA 0 of the traced GEMM records clock64() at fixed points per k-block into a
-// device array read back with moe_gemm_trace_read(). Compiled out otherwise.
-#ifdef MOE_GEMM_TRACE
-__device__ long long g_gemm_trace[16][2048];
-extern "C" int moe_gemm_trace_read(long long* host) {
-  return static_cast<int>(cudaMemcpyFromSymbol(host, g_gemm_trace, sizeof(g_gemm_trace)));
-}
-#ifndef MOE_GEMM_TRACE_MODE
-#define MOE_GEMM_TRACE_MODE 1
-#endif
-#define TRACE_POINT(slot, idx)                                                      \
-  do {                                                                              \
-    if (blockIdx.x == 0 && kMode == MOE_GEMM_TRACE_MODE && (idx) < 2048)            \
-      g_gemm_trace[(slot)][(idx)] = clock64();                                      \
-  } while (0)
-#else
-#define TRACE_POINT(slot, idx) \
-  do {                         \
-  } while (0)
-#endif
-
 namespace {
 
 constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 4;
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
-// A pipeline step covers kSub consecutive 64-element k-blocks (128 reduction
-// elements): every per-step cost (barrier waits and arrivals, MMA commit, address
-// arithmetic) is paid once per 128 elements.
-constexpr int kSub = 2;
-constexpr int kWStepBytes = kSub * kWBlockBytes;  // packed weights of one step (9 KB)
-constexpr int kWChunk = 2;               // steps per weight copy (one 18 KB bulk copy)
-constexpr int kNWS = 4;                  // weight ring depth in chunks (shared memory)
-constexpr int kWChunkBytes = kWChunk * kWStepBytes;
-constexpr int kNS = 4;                   // operand stage ring: A in tensor memory, B in shared memory
-constexpr int kBSub = kBNMax * 128;      // B tile of one 64-element k-block
-constexpr int kBStage = kSub * kBSub;    // B tiles of one step
+constexpr int kNW = 16;                  // weight ring depth (shared memory)
+constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
+constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
 constexpr int kTmemCols = 512;
-constexpr int kACols = kSub * 32;        // one step of fp16 A: 128 lanes x 64 columns
+constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
 constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
 constexpr int kStatusTimeout = 2;
 constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
 
 constexpr int kSmB = 0;
 constexpr int kSmW = kSmB + kNS * kBStage;
-constexpr int kSmStage = ((kSmW + kNWS * kWChunkBytes + 1023) / 1024) * 1024;
+constexpr int kSmStage = ((kSmW + kNW * kWBlockBytes + 1023) / 1024) * 1024;
 constexpr int kSmBar = kSmStage + kBNMax * 128;
 // barrier indices
-constexpr int kBarWFull = 0;                  // weight chunk landed (bulk-copy bytes)
-constexpr int kBarWEmpty = kBarWFull + kNWS;  // weight chunk read (4 dequant warps per step)
-constexpr int kBarFull = kBarWEmpty + kNWS;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
+constexpr int kBarWFull = 0;                 // weight block landed (bulk-copy bytes)
+constexpr int kBarWEmpty = kBarWFull + kNW;  // weight block read by its 4 dequant warps
+constexpr int kBarFull = kBarWEmpty + kNW;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
 constexpr int kBarEmpty = kBarFull + kNS;    // stage consumed by the MMAs (tcgen05.commit)
 constexpr int kBarAccFull = kBarEmpty + kNS; // [issuer][buffer]: accumulator complete
 constexpr int kBarAccEmpty = kBarAccFull + 4;  // [buffer]: epilogue has read both issuers' sums
@@ -117,8 +82,6 @@ constexpr int kSmBytes = kSmMisc + 64;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
-static_assert((kNWS & (kNWS - 1)) == 0 && (kNS & (kNS - 1)) == 0 && kWChunk == 2,
-              "ring index arithmetic below assumes power-of-two rings and 2-step chunks");
 
 constexpr int kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
@@ -221,9 +184,10 @@ struct Cursor {
 // scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
 // scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
 // (for scales in fp16's normal range), so the dequantised weight carries no
-// rounding error. One shift and four masks unpack a word of eight codes; `s2` is
-// the fp16 scale in both halves.
-__device__ __forceinline__ void dequant_group(const uint4 qv, const uint32_t s2, uint32_t* out) {
+// rounding error. One shift and four masks unpack a word of eight codes.
+__device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t s_bf16, uint32_t (&out)[16]) {
+  const __half sh = __float2half_rn(__uint_as_float(s_bf16 << 16));
+  const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -283,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNWS; ++i) {
+    for (int i = 0; i < kNW; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
-      mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);  // 4 quadrant warps x steps
+      mbar_init(bar(kBarWEmpty + i), 4);
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(kBarFull + i), 4 + 1);
@@ -316,54 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   int* status = a.status;
   pdl_launch_dependents();
 
-  if (warp == kWarpW) {
-    // ------------------------------------------------ packed-weight producer
-    // One lane streams the weight blocks in chunks of kWChunk consecutive steps:
-    // a row tile's k-blocks are contiguous, so a chunk is one 18 KB bulk copy (one
-    // per contiguous run where a chunk crosses units). Copies this large keep HBM
-    // busy from a single issuing thread; 4.5 KB ones do not.
-    if (lane == 0) {
-      const long long n_it = my_end - my_begin;
-      const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
-      Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
-      long long c = 0;
-      for (; c < n_chunks; ++c) {
-        const int s = static_cast<int>(c % kNWS);
-        if (!mbar_wait(bar(kBarWEmpty + s), ((c / kNWS) & 1) ^ 1, abort_flag, status,
-                       kStatusTimeout))
-          break;
-        const long long it0 = c * kWChunk;
-        const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
-        TRACE_POINT(0, it0);
-        mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWStepBytes);
-        for (long long it = it0; it < it1;) {
-          int kb = 0;
-          cur.seek(it, kb);
-          const long long left_in_unit = cur.kb1 - kb;
-          const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
-          const long long woff =
-              ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWStepBytes;
-          if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kWStepBytes <= a.wpack_bytes &&
-                            cur.un.e >= 0 && cur.un.e < a.E && cur.un.rt < a.R && kb + run <= a.KBn &&
-                            run >= 1 && (it - it0) + run <= kWChunk,
-                        a.status, a.dbg, 1, woff, run * 100 + (it - it0)))
-            bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
-                     a.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes, bar(kBarWFull + s));
-          it += run;
-        }
-      }
-      // let the last chunks land before shared memory is released
-      for (long long j = 0; j < kNWS && j < c; ++j) {
-        const long long idx = c - 1 - j;
-        mbar_wait_drain(bar(kBarWFull + static_cast<int>(idx % kNWS)),
-                        static_cast<uint32_t>((idx / kNWS) & 1));
-      }
-    }
-  } else if (warp == kWarpB) {
-    // ------------------------------------------------ activation (B operand) producer
-    // kProducerLanes lanes walk consecutive k-blocks in step and issue their
-    // (2-8 KB) copies in one go: a bulk-copy issue holds its thread
-    // for a while, so small copies must leave several at a time.
+  if (warp == kWarpW || warp == kWarpB) {
+    // ------------------------------------------------ bulk-copy producers
+    // warp 0: packed weight blocks (W ring); warp 1: activation tiles (B operand,
+    // operand-stage ring). kProducerLanes lanes walk consecutive k-blocks in
+    // step and issue their copies in one warp instruction: a bulk-copy issue
+    // blocks its thread for a while, so several copies have to leave at once for
+    // small (2-4.5 KB) copies to keep HBM busy.
+    const bool is_w = warp == kWarpW;
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
       Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
@@ -375,41 +299,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (it < n_it) {
           int kb = 0;
           cur.seek(it, kb);
-          if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 && cur.un.e >= 0 && cur.un.e < a.E &&
-                             cur.un.g0 >= 0 && cur.un.g0 + cur.un.ng <= a.tiles_cap && kb >= 0 && kb < a.KBn,
-                         a.status, a.dbg, 11, cur.un.ng * 1000 + cur.un.e, cur.un.g0 * 1000 + kb))
-            cur.un.ng = 1;
-          const int s = static_cast<int>(it % kNS);
-          const bool ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                                    kStatusTimeout);
-          __syncwarp(active);
+          bool ok;
+          if (is_w) {
+            const int s = static_cast<int>(it % kNW);
+            ok = mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
+                           kStatusTimeout);
+            __syncwarp(active);
+            if (ok) {
+              const uint8_t* src =
+                  a.wpack +
+                  ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
+              mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
+              bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
+            }
+          } else {
+            const int s = static_cast<int>(it % kNS);
+            ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                           kStatusTimeout);
+            __syncwarp(active);
+            if (ok) {
+              const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
+              const uint8_t* src =
+                  a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
+              mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
+              bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
+            }
+          }
           if (ok) {
-            // the step's two 64-element k-blocks are two planes of the blocked layout
-            const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
-            const long long boff =
-                (static_cast<long long>(kb) * kSub * a.Gcap + cur.un.g0) * kRowGroupBytes;
-            const long long plane = static_cast<long long>(a.Gcap) * kRowGroupBytes;
-            TRACE_POINT(1, it);
-            mbar_arrive_expect_tx(bar(kBarFull + s), kSub * bytes);
-            if (MOE_CHECK(boff >= 0 && boff + bytes <= a.bsrc_bytes && bytes <= kBSub && bytes > 0 &&
-                              s >= 0 && s < kNS,
-                          a.status, a.dbg, 2, boff, bytes))
-              bulk_g2s(sB + s * kBStage, a.bsrc + boff, bytes, bar(kBarFull + s));
-            if (MOE_CHECK(boff + plane + bytes <= a.bsrc_bytes, a.status, a.dbg, 3, boff + plane,
-                          bytes))
-              bulk_g2s(sB + s * kBStage + kBSub, a.bsrc + boff + plane, bytes, bar(kBarFull + s));
             last = it;
             ++mine;
           }
           if (__any_sync(active, !ok)) break;
         }
       }
-      // bounded wait giving this lane's last copies time to land before shared
-      // memory is released (the stage barriers also count dequant arrivals)
-      for (uint32_t j = 0; j < static_cast<uint32_t>(kNS / kProducerLanes) && j < mine; ++j) {
+      // bounded wait for this lane's last copies to land before shared memory is
+      // released (the operand-stage barriers also count dequant arrivals, so for
+      // them this only gives the copies time)
+      const int depth = is_w ? kNW : kNS;
+      for (uint32_t j = 0; j < static_cast<uint32_t>(depth / kProducerLanes) && j < mine; ++j) {
         const long long idx = last - static_cast<long long>(j) * kProducerLanes;
-        mbar_wait_drain(bar(kBarFull + static_cast<int>(idx % kNS)),
-                        static_cast<uint32_t>((idx / kNS) & 1));
+        mbar_wait_drain(bar((is_w ? kBarWFull : kBarFull) + static_cast<int>(idx % depth)),
+                        static_cast<uint32_t>((idx / depth) & 1));
       }
     }
   } else if (warp == kWarpMma0 || warp == kWarpMma1) {
@@ -429,10 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
       const int ab = acc_it & 1;
       if (first < it_base + len) {
-        Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-        if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16, a.status, a.dbg, 12, un.ng, u)) un.ng = 1;
+        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
+        ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarAccEmpty + ab),
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
                                                     kStatusTimeout));
         if (!ok) break;
@@ -440,29 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
           const uint32_t st = it % kNS;
-          if (lane == 0) TRACE_POINT(2, it);
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
+          ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarFull + st), (it / kNS) & 1,
                                                       abort_flag, status, kStatusTimeout));
           if (!ok) break;
-          if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
-          // B stage st is st * kBStage bytes after stage 0, its second 64-element
-          // half kBSub bytes further (16-byte units in the descriptor); +32 bytes of
-          // K per MMA inside the 128-byte swizzled rows.
+          // B stage st is st * kBStage bytes after stage 0 (16-byte units in the
+          // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
           const uint64_t b_desc = b_desc0 + ((st * kBStage) >> 4);
-          const uint64_t b_desc1 = b_desc + (kBSub >> 4);
           if (elect_one()) {
             tc_fence_after();
             tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
             tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 32, b_desc1, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 40, b_desc1 + 2, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 48, b_desc1 + 4, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 56, b_desc1 + 6, idesc, 1u);
             tc_commit(bar(kBarEmpty + st));
-            TRACE_POINT(4, it);
           }
           acc_flag = 1u;
         }
@@ -480,67 +400,60 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
-    // Warp (quad, phase) converts rows 32*quad .. +31 of the k-blocks whose index
-    // in this CTA's sequence is phase, phase + kDeqPhases, ... (only the index
-    // matters here: it fixes the weight-ring slot and the operand stage). The TMEM
+    // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
+    // in this CTA's sequence is congruent to `phase` modulo kDeqPhases. The TMEM
     // store of one k-block is retired (wait::st + arrival) only after the warp
     // has loaded and converted its next k-block, which hides the store latency.
     const int quad = warp & 3;
     const int phase = (warp - kWarpDeq0) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
-    bool pending = false;
-    uint32_t pend_stage = 0;
-    uint32_t pend_it = 0;
-    (void)pend_it;
-    const uint32_t a_lane = tmem + t_lane;
-    for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
-      const uint32_t ws = (it >> 1) & (kNWS - 1);  // weight chunk slot (2 steps per chunk)
-      const uint32_t st = it & (kNS - 1);
-      bool w_ok = mbar_wait(bar(kBarWFull + ws), (it >> 3) & 1, abort_flag, status,
-                            kStatusTimeout);
-      if (!__all_sync(0xffffffffu, w_ok)) break;
-      if (lane == 0 && quad == 0) TRACE_POINT(5, it);
-      // the step's weights: slot ws, step (it & 1) of the chunk = (it & 7) steps in
-      const uint32_t wb = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + r * 16;
-      const uint32_t wsc = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + kWCodeBytes + r * 4;
-      const uint4 q0 = ld_shared_v4(wb);
-      const uint4 q1 = ld_shared_v4(wb + 2048);
-      const uint4 q2 = ld_shared_v4(wb + kWBlockBytes);
-      const uint4 q3 = ld_shared_v4(wb + kWBlockBytes + 2048);
-      const uint32_t sc0 = ld_shared_u32(wsc);  // fp16 scales of the two groups
-      const uint32_t sc1 = ld_shared_u32(wsc + kWBlockBytes);
-      uint32_t out[32];
-      dequant_group(q0, __byte_perm(sc0, 0, 0x1010), &out[0]);
-      dequant_group(q1, __byte_perm(sc0, 0, 0x3232), &out[16]);
-      if (pending) {
+    uint32_t it = 0;
+    SegIter si{my_begin, my_end, a.KBn};
+    long long u;
+    int kb0, kb1;
+    bool ok = true, pending = false;
+    int pend_stage = 0;
+    while (ok && si.next(u, kb0, kb1)) {
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        if (static_cast<int>(it % kDeqPhases) != phase) continue;
+        const int ws = it % kNW, st = it % kNS;
+        bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
+                              kStatusTimeout);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        const uint32_t wb = sW + ws * kWBlockBytes;
+        const uint4 q0 = ld_shared_v4(wb + r * 16);
+        const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
+        const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
+        const uint32_t s1 = ld_shared_u16(wb + kWCodeBytes + 256 + r * 2);
+        uint32_t out[32];
+        dequant_group(q0, s0, *reinterpret_cast<uint32_t(*)[16]>(&out[0]));
+        dequant_group(q1, s1, *reinterpret_cast<uint32_t(*)[16]>(&out[16]));
+        __syncwarp();  // every lane has consumed its shared-memory words
+        if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
+        if (pending) {
+          __syncwarp();  // tcgen05.wait is warp-collective: converge after the lane-0 arrival
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
+          pending = false;
+        }
+        w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                         kStatusTimeout);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         __syncwarp();
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) TRACE_POINT(8 + quad, pend_it);
-        if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
-        pending = false;
+        tmem_st32(tmem + t_lane + st * kACols, out);
+        pending = true;
+        pend_stage = st;
       }
-      w_ok = mbar_wait(bar(kBarEmpty + st), ((it >> 2) & 1) ^ 1, abort_flag, status,
-                       kStatusTimeout);
-      if (!__all_sync(0xffffffffu, w_ok)) break;
-      if (lane == 0 && quad == 0) TRACE_POINT(7, it);
-      tc_fence_after();
-      __syncwarp();
-      tmem_st32(a_lane + st * kACols, out);
-      dequant_group(q2, __byte_perm(sc1, 0, 0x1010), &out[0]);
-      dequant_group(q3, __byte_perm(sc1, 0, 0x3232), &out[16]);
-      // converge before the warp-collective store; every lane has also consumed
-      // its shared-memory words by now, so the slot can be released after it
-      __syncwarp();
-      tmem_st32(a_lane + st * kACols + 32, out);
-      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
-      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-      pending = true;
-      pend_stage = st;
-      pend_it = it;
     }
     if (pending) {
       __syncwarp();
@@ -560,10 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     long long u;
     int kb0, kb1;
     while (si.next(u, kb0, kb1)) {
-      Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
-      if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16 && un.rt >= 0 && un.rt < a.R, a.status, a.dbg,
-                     13, un.ng, un.rt))
-        un.ng = 1;
+      const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
       const int nch = un.ng;  // 16-column chunks
       const int ab = acc_it & 1;
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
@@ -586,9 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 #pragma unroll
         for (int j = 0; j < kRowRegs; ++j) {
           const int row = 32 * j + lane;
-          const bool in_tile = row < nch * 16 &&
-                               MOE_CHECK(pbase + row < a.sorted_cap, a.status, a.dbg, 9, pbase + row, nch);
-          const int sid = in_tile ? a.sorted_ids[pbase + row] : a.MK;
+          const int sid = row < nch * 16 ? a.sorted_ids[pbase + row] : a.MK;
           sid_r[j] = sid;
           if (sid < a.MK) {
             w_r[j] = a.topk_weights[sid];
@@ -657,11 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           for (int c = 0; c < nch; ++c) {
             float v[16];
             load_chunk(c, v);
-            const long long so = (slot - a.scratch) + (c * 16) * kBM + r;
-            if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 6, so, c)) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
-            }
+            for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
           }
           tc_fence_before();
           __syncwarp();
@@ -687,11 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                 const int pc = (sc.start(cc) < ustart) ? 1 : 0;
                 const float* sl =
                     a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
-                const long long so = (sl - a.scratch) + (c * 16) * kBM + r;
-                if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 7, so, cc)) {
 #pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
-                }
+                for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
               }
               swiglu_chunk(v, c, quad, lane, sStage);
             }
@@ -701,11 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           fence_proxy_async_smem();
           named_bar_sync(kEpiBar, kEpiThreads);
           if (epi_tid == 0) {
-            const long long hoff = (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes;
-            if (MOE_CHECK(hoff >= 0 && hoff + nch * kRowGroupBytes <= a.hout_bytes && nch > 0 &&
-                              nch <= kBNMax / 16,
-                          a.status, a.dbg, 5, hoff, nch))
-              bulk_s2g(a.hout + hoff, sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
+            bulk_s2g(a.hout + (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes,
+                     sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
             bulk_commit();
             bulk_wait_read_all();
           }
@@ -725,9 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               if (sid < a.MK) {
                 const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
                 const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
-                const long long ai = (acc_col - a.acc) + static_cast<long long>(tok) * a.Kout;
-                if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 8, ai, sid))
-                  atomicAdd(a.acc + ai, wt * v[i]);
+                atomicAdd(acc_col + static_cast<long long>(tok) * a.Kout, wt * v[i]);
               }
             }
           }
