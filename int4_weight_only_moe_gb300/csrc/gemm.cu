@@ -184,10 +184,9 @@ struct Cursor {
 // scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
 // scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
 // (for scales in fp16's normal range), so the dequantised weight carries no
-// rounding error. One shift and four masks unpack a word of eight codes.
-__device__ __forceinline__ void dequant_group(const uint4 qv, uint32_t s_bf16, uint32_t (&out)[16]) {
-  const __half sh = __float2half_rn(__uint_as_float(s_bf16 << 16));
-  const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sh)) * 0x10001u;
+// rounding error. One shift and four masks unpack a word of eight codes; `s2` is
+// the fp16 scale in both halves.
+__device__ __forceinline__ void dequant_group(const uint4 qv, const uint32_t s2, uint32_t* out) {
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -400,60 +399,48 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
-    // Warp (quad, phase) converts rows 32*quad .. +31 of every k-block whose index
-    // in this CTA's sequence is congruent to `phase` modulo kDeqPhases. The TMEM
+    // Warp (quad, phase) converts rows 32*quad .. +31 of the k-blocks whose index
+    // in this CTA's sequence is phase, phase + kDeqPhases, ... (only the index
+    // matters here: it fixes the weight-ring slot and the operand stage). The TMEM
     // store of one k-block is retired (wait::st + arrival) only after the warp
     // has loaded and converted its next k-block, which hides the store latency.
     const int quad = warp & 3;
     const int phase = (warp - kWarpDeq0) >> 2;
     const int r = quad * 32 + lane;
-    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t it = 0;
-    SegIter si{my_begin, my_end, a.KBn};
-    long long u;
-    int kb0, kb1;
-    bool ok = true, pending = false;
-    int pend_stage = 0;
-    while (ok && si.next(u, kb0, kb1)) {
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
-        if (static_cast<int>(it % kDeqPhases) != phase) continue;
-        const int ws = it % kNW, st = it % kNS;
-        bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
-                              kStatusTimeout);
-        if (!__all_sync(0xffffffffu, w_ok)) {
-          ok = false;
-          break;
-        }
-        const uint32_t wb = sW + ws * kWBlockBytes;
-        const uint4 q0 = ld_shared_v4(wb + r * 16);
-        const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
-        const uint32_t s0 = ld_shared_u16(wb + kWCodeBytes + r * 2);
-        const uint32_t s1 = ld_shared_u16(wb + kWCodeBytes + 256 + r * 2);
-        uint32_t out[32];
-        dequant_group(q0, s0, *reinterpret_cast<uint32_t(*)[16]>(&out[0]));
-        dequant_group(q1, s1, *reinterpret_cast<uint32_t(*)[16]>(&out[16]));
-        __syncwarp();  // every lane has consumed its shared-memory words
-        if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-        if (pending) {
-          __syncwarp();  // tcgen05.wait is warp-collective: converge after the lane-0 arrival
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
-          pending = false;
-        }
-        w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                         kStatusTimeout);
-        if (!__all_sync(0xffffffffu, w_ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
+    bool pending = false;
+    uint32_t pend_stage = 0;
+    for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
+      const uint32_t ws = it % kNW, st = it % kNS;
+      bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
+                            kStatusTimeout);
+      if (!__all_sync(0xffffffffu, w_ok)) break;
+      const uint32_t wb = sW + ws * kWBlockBytes;
+      const uint4 q0 = ld_shared_v4(wb + r * 16);
+      const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
+      const uint32_t sc = ld_shared_u32(wb + kWCodeBytes + r * 4);  // fp16 scales of both groups
+      uint32_t out[32];
+      dequant_group(q0, __byte_perm(sc, 0, 0x1010), &out[0]);
+      dequant_group(q1, __byte_perm(sc, 0, 0x3232), &out[16]);
+      __syncwarp();  // every lane has consumed its shared-memory words
+      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
+      if (pending) {
+        __syncwarp();  // tcgen05.wait is warp-collective: converge after the lane-0 arrival
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        tmem_st32(tmem + t_lane + st * kACols, out);
-        pending = true;
-        pend_stage = st;
+        if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
+        pending = false;
       }
+      w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                       kStatusTimeout);
+      if (!__all_sync(0xffffffffu, w_ok)) break;
+      tc_fence_after();
+      __syncwarp();
+      tmem_st32(a_lane + st * kACols, out);
+      pending = true;
+      pend_stage = st;
     }
     if (pending) {
       __syncwarp();

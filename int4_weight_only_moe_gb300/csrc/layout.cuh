@@ -7,7 +7,8 @@
 //
 //   bytes [0, 4096):    codes, [half h (0..1)][row r (0..127)][4 words]; word j of
 //                       (h, r) holds reduction elements 32h + 8j .. 32h + 8j + 7
-//   bytes [4096, 4608): bf16 scales, [half h][row r]; half h is the scale group
+//   bytes [4096, 4608): fp16 scales, [row r][half h]; half h is the scale group
+//                       (both scales of a row in one 32-bit word)
 //
 // Inside a word the eight 4-bit codes are interleaved so that one shift and one
 // mask put elements (2p, 2p+1) into the two 16-bit halves of a 32-bit register:

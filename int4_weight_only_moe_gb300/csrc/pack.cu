@@ -3,6 +3,9 @@
 // checks). Counterpart of the repack step of "The Pivot to Real Hardware ...",
 // Step 2 (GPTQ in, hardware-friendly layout out, no act-order permutation);
 // the byte count is unchanged.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -38,6 +41,17 @@ __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t dst) {
   return src;
 }
 
+// Scales are kept as fp16 in the packed layout (the tensor-core operand type):
+// exact for bf16 scales inside fp16's normal range, which the dequantisation
+// needs anyway; the inverse conversion restores the bf16 bits exactly there.
+__device__ __forceinline__ uint16_t bf16_to_f16_bits(uint16_t b) {
+  return __half_as_ushort(__float2half_rn(__uint_as_float(static_cast<uint32_t>(b) << 16)));
+}
+__device__ __forceinline__ uint16_t f16_to_bf16_bits(uint16_t h) {
+  const __nv_bfloat16 v = __float2bfloat16_rn(__half2float(__ushort_as_half(h)));
+  return *reinterpret_cast<const uint16_t*>(&v);
+}
+
 // One CTA per (expert, row tile, k-block) block. `q` is [E, Kred/8, Nout] int32,
 // `s` is [E, Kred/32, Nout] bf16; `R` row tiles of 128 rows, `KBn` k-blocks.
 __global__ void __launch_bounds__(256) repack_kernel(const uint32_t* __restrict__ q,
@@ -63,7 +77,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint32_t* __restrict_
   for (int t = threadIdx.x; t < 256; t += blockDim.x) {
     const int r = t & 127, h = t >> 7;
     const int f = tile_row_source(rt, r, Nout, interleave);
-    ds[h * 128 + r] = s[(e * srows + kb * 2 + h) * Nout + f];
+    ds[r * 2 + h] = bf16_to_f16_bits(s[(e * srows + kb * 2 + h) * Nout + f]);
   }
 }
 
@@ -88,7 +102,7 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
   for (int t = threadIdx.x; t < 256; t += blockDim.x) {
     const int r = t & 127, h = t >> 7;
     const int f = tile_row_source(rt, r, Nout, interleave);
-    s[(e * srows + kb * 2 + h) * Nout + f] = ss[h * 128 + r];
+    s[(e * srows + kb * 2 + h) * Nout + f] = f16_to_bf16_bits(ss[r * 2 + h]);
   }
 }
 
