@@ -49,9 +49,35 @@
 
 namespace moe {
 
+// Optional pipeline timeline for performance work: built with -DMOE_GEMM_TRACE,
+// CTA 0 of the traced GEMM records clock64() at fixed points per k-block into a
+// device array read back with moe_gemm_trace_read(). Compiled out otherwise.
+#ifdef MOE_GEMM_TRACE
+__device__ long long g_gemm_trace[16][2048];
+extern "C" int moe_gemm_trace_read(long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_gemm_trace, sizeof(g_gemm_trace)));
+}
+#ifndef MOE_GEMM_TRACE_MODE
+#define MOE_GEMM_TRACE_MODE 1
+#endif
+#define TRACE_POINT(slot, idx)                                                      \
+  do {                                                                              \
+    if (blockIdx.x == 0 && kMode == MOE_GEMM_TRACE_MODE && (idx) < 2048)            \
+      g_gemm_trace[(slot)][(idx)] = clock64();                                      \
+  } while (0)
+#else
+#define TRACE_POINT(slot, idx) \
+  do {                         \
+  } while (0)
+#endif
+
 namespace {
 
-constexpr int kDeqPhases = 3;            // dequant warps per TMEM lane quadrant
+// Dequantisation warps per TMEM lane quadrant (compile-time; 3 by default).
+#ifndef MOE_DEQ_PHASES
+#define MOE_DEQ_PHASES 3
+#endif
+constexpr int kDeqPhases = MOE_DEQ_PHASES;
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 4;
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
@@ -308,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               const uint8_t* src =
                   a.wpack +
                   ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
+              TRACE_POINT(0, it);
               mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
               bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
             }
@@ -320,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
               const uint8_t* src =
                   a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
+              TRACE_POINT(1, it);
               mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
               bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
             }
@@ -360,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       if (first < it_base + len) {
         const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-        ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarAccEmpty + ab),
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
                                                     kStatusTimeout));
         if (!ok) break;
@@ -368,9 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
           const uint32_t st = it % kNS;
-          ok = __all_sync(0xffffffffu, mbar_wait_spin(bar(kBarFull + st), (it / kNS) & 1,
+          if (lane == 0) TRACE_POINT(2, it);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
                                                       abort_flag, status, kStatusTimeout));
           if (!ok) break;
+          if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
           // B stage st is st * kBStage bytes after stage 0 (16-byte units in the
           // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
@@ -382,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
             tc_commit(bar(kBarEmpty + st));
+            TRACE_POINT(4, it);
           }
           acc_flag = 1u;
         }
@@ -410,12 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
     bool pending = false;
-    uint32_t pend_stage = 0;
+    uint32_t pend_stage = 0, pend_it = 0;
+    (void)pend_it;
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
       const uint32_t ws = it % kNW, st = it % kNS;
+      if (lane == 0 && quad == 0) TRACE_POINT(12, it);
       bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
                             kStatusTimeout);
       if (!__all_sync(0xffffffffu, w_ok)) break;
+      if (lane == 0 && quad == 0) TRACE_POINT(5, it);
       const uint32_t wb = sW + ws * kWBlockBytes;
       const uint4 q0 = ld_shared_v4(wb + r * 16);
       const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
@@ -424,23 +458,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       dequant_group(q0, __byte_perm(sc, 0, 0x1010), &out[0]);
       dequant_group(q1, __byte_perm(sc, 0, 0x3232), &out[16]);
       __syncwarp();  // every lane has consumed its shared-memory words
+      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
       if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
       if (pending) {
         __syncwarp();  // tcgen05.wait is warp-collective: converge after the lane-0 arrival
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
+        if (lane == 0) TRACE_POINT(8 + quad, pend_it);
         if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
         pending = false;
       }
       w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
                        kStatusTimeout);
       if (!__all_sync(0xffffffffu, w_ok)) break;
+      if (lane == 0 && quad == 0) TRACE_POINT(7, it);
       tc_fence_after();
       __syncwarp();
       tmem_st32(a_lane + st * kACols, out);
       pending = true;
       pend_stage = st;
+      pend_it = it;
     }
     if (pending) {
       __syncwarp();
