@@ -15,13 +15,15 @@
 //
 // Per CTA (one per SM), 20 warps:
 //   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
-//   warp 1       4 lanes bulk-copy the activation tile (B operand) into an 8-deep ring
-//                (the lanes of a producer issue 4 consecutive k-blocks at once)
+//   warp 1       4 lanes bulk-copy the activation tile (B operand) into a 16-deep
+//                ring of its own (the lanes of a producer issue 4 consecutive
+//                k-blocks at once); the activations are small and L2-resident, so
+//                running them 16 k-blocks ahead takes their latency off the MMA path
 //   warps 2, 3   tcgen05.mma issuers for alternate k-blocks, each into its own
 //                accumulators (warp 2 also allocates tensor memory)
 //   warps 4..15  dequantise INT4 -> fp16 in registers and store the A operand
-//                straight into tensor memory (tcgen05.st); three warps per lane
-//                quadrant take whole k-blocks in turn; 8-deep ring shared with B
+//                straight into tensor memory (tcgen05.st) through an 8-stage ring;
+//                three warps per lane quadrant take whole k-blocks in turn
 //   warps 16..19 epilogue: tcgen05.ld of both issuers' fp32 accumulators
 //                (double-buffered), summed
 //
@@ -82,7 +84,8 @@ constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
 constexpr int kNW = 16;                  // weight ring depth (shared memory)
-constexpr int kNS = 8;                   // operand stage ring: A in tensor memory, B in shared memory
+constexpr int kNS = 8;                   // A operand stage ring (tensor memory)
+constexpr int kNB = 16;                  // B operand ring (shared memory), deeper than the A ring
 constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
 constexpr int kTmemCols = 512;
 constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
@@ -91,15 +94,17 @@ constexpr int kStatusTimeout = 2;
 constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
 
 constexpr int kSmB = 0;
-constexpr int kSmW = kSmB + kNS * kBStage;
+constexpr int kSmW = kSmB + kNB * kBStage;
 constexpr int kSmStage = ((kSmW + kNW * kWBlockBytes + 1023) / 1024) * 1024;
 constexpr int kSmBar = kSmStage + kBNMax * 128;
 // barrier indices
 constexpr int kBarWFull = 0;                 // weight block landed (bulk-copy bytes)
 constexpr int kBarWEmpty = kBarWFull + kNW;  // weight block read by its 4 dequant warps
-constexpr int kBarFull = kBarWEmpty + kNW;   // stage ready: A stored (4 warps) + B landed (1 + bytes)
-constexpr int kBarEmpty = kBarFull + kNS;    // stage consumed by the MMAs (tcgen05.commit)
-constexpr int kBarAccFull = kBarEmpty + kNS; // [issuer][buffer]: accumulator complete
+constexpr int kBarFull = kBarWEmpty + kNW;   // A stage ready: stored by its 4 dequant warps
+constexpr int kBarEmpty = kBarFull + kNS;    // A stage consumed by the MMAs (tcgen05.commit)
+constexpr int kBarBFull = kBarEmpty + kNS;   // B stage landed (bulk-copy bytes)
+constexpr int kBarBEmpty = kBarBFull + kNB;  // B stage consumed by the MMAs (tcgen05.commit)
+constexpr int kBarAccFull = kBarBEmpty + kNB; // [issuer][buffer]: accumulator complete
 constexpr int kBarAccEmpty = kBarAccFull + 4;  // [buffer]: epilogue has read both issuers' sums
 constexpr int kBarDrain = kBarAccEmpty + 2;    // [issuer]
 constexpr int kNumBars = kBarDrain + 2;
@@ -277,8 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       mbar_init(bar(kBarWEmpty + i), 4);
     }
     for (int i = 0; i < kNS; ++i) {
-      mbar_init(bar(kBarFull + i), 4 + 1);
+      mbar_init(bar(kBarFull + i), 4);
       mbar_init(bar(kBarEmpty + i), 1);
+    }
+    for (int i = 0; i < kNB; ++i) {
+      mbar_init(bar(kBarBFull + i), 1);
+      mbar_init(bar(kBarBEmpty + i), 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(kBarAccFull + i), 1);
     for (int i = 0; i < 2; ++i) {
@@ -339,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
             }
           } else {
-            const int s = static_cast<int>(it % kNS);
-            ok = mbar_wait(bar(kBarEmpty + s), ((it / kNS) & 1) ^ 1, abort_flag, status,
+            const int s = static_cast<int>(it % kNB);
+            ok = mbar_wait(bar(kBarBEmpty + s), ((it / kNB) & 1) ^ 1, abort_flag, status,
                            kStatusTimeout);
             __syncwarp(active);
             if (ok) {
@@ -348,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               const uint8_t* src =
                   a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
               TRACE_POINT(1, it);
-              mbar_arrive_expect_tx(bar(kBarFull + s), bytes);
-              bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarFull + s));
+              mbar_arrive_expect_tx(bar(kBarBFull + s), bytes);
+              bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarBFull + s));
             }
           }
           if (ok) {
@@ -360,12 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         }
       }
       // bounded wait for this lane's last copies to land before shared memory is
-      // released (the operand-stage barriers also count dequant arrivals, so for
-      // them this only gives the copies time)
-      const int depth = is_w ? kNW : kNS;
+      // released
+      const int depth = is_w ? kNW : kNB;
       for (uint32_t j = 0; j < static_cast<uint32_t>(depth / kProducerLanes) && j < mine; ++j) {
         const long long idx = last - static_cast<long long>(j) * kProducerLanes;
-        mbar_wait_drain(bar((is_w ? kBarWFull : kBarFull) + static_cast<int>(idx % depth)),
+        mbar_wait_drain(bar((is_w ? kBarWFull : kBarBFull) + static_cast<int>(idx % depth)),
                         static_cast<uint32_t>((idx / depth) & 1));
       }
     }
@@ -395,16 +403,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const uint32_t d_tmem = tmem + kAccCol0 + (par * 2 + ab) * kBNMax;
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
-          const uint32_t st = it % kNS;
+          const uint32_t st = it % kNS, sb = it % kNB;
           if (lane == 0) TRACE_POINT(2, it);
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarBFull + sb), (it / kNB) & 1,
                                                       abort_flag, status, kStatusTimeout));
+          if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
+                                                        abort_flag, status, kStatusTimeout));
           if (!ok) break;
           if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
-          // B stage st is st * kBStage bytes after stage 0 (16-byte units in the
+          // B stage sb is sb * kBStage bytes after stage 0 (16-byte units in the
           // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
-          const uint64_t b_desc = b_desc0 + ((st * kBStage) >> 4);
+          const uint64_t b_desc = b_desc0 + ((sb * kBStage) >> 4);
           if (elect_one()) {
             tc_fence_after();
             tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
@@ -412,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
             tc_commit(bar(kBarEmpty + st));
+            tc_commit(bar(kBarBEmpty + sb));
             TRACE_POINT(4, it);
           }
           acc_flag = 1u;
@@ -445,6 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     (void)pend_it;
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
       const uint32_t ws = it % kNW, st = it % kNS;
+      // non-blocking test of the stage-free barrier now; its latency overlaps the
+      // conversion and the blocking wait below runs only if it was not ready
+      const bool e_early = mbar_test_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1);
       if (lane == 0 && quad == 0) TRACE_POINT(12, it);
       bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
                             kStatusTimeout);
@@ -469,9 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
         pending = false;
       }
-      w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                       kStatusTimeout);
-      if (!__all_sync(0xffffffffu, w_ok)) break;
+      if (!__all_sync(0xffffffffu, e_early)) {
+        w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
+                         kStatusTimeout);
+        if (!__all_sync(0xffffffffu, w_ok)) break;
+      }
       if (lane == 0 && quad == 0) TRACE_POINT(7, it);
       tc_fence_after();
       __syncwarp();

@@ -77,13 +77,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Normal waits last micro- to milliseconds; this only ends a broken pipeline.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
-// Wait for the phase of parity `parity` of `bar` to complete. Returns false if
-// another thread of the CTA has raised `abort_flag`, or if the wait has lasted
-// longer than kWaitTimeoutNs (then it raises the flag and records `status_bit`
-// in the global status word). Never spins without bound.
+// Wait for the phase of parity `parity` of `bar` to complete: a non-blocking test
+// first (cheapest when the phase is already complete, the common case), then
+// suspended tries. Returns false if another thread of the CTA has raised
+// `abort_flag`, or if the wait has lasted longer than kWaitTimeoutNs (then it
+// raises the flag and records `status_bit` in the global status word). Never
+// spins without bound.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, int status_bit) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -92,27 +94,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       *abort_flag = 1;
       atomicOr(status, status_bit);
       return false;
-    }
-  }
-}
-
-// Same contract as mbar_wait, polling with the non-blocking test: for the single
-// thread on the critical path (the MMA issuer), where wake-up latency matters more
-// than the issue slots a short spin costs.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, int* status,
-                                               int status_bit) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *abort_flag = 1;
-        atomicOr(status, status_bit);
-        return false;
-      }
     }
   }
 }
