@@ -114,6 +114,23 @@ constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 by
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
 
+// Stage-reuse safety. A dequantisation warp reuses A stage st for k-block it after
+// a parity test of Empty[st], meaning "the MMA of k-block it - kNS is done". A
+// parity test cannot tell that phase from the one two uses back, so the warp must
+// already know that the MMA of it - 2*kNS has completed, or it may overwrite the
+// stage under a running MMA and arrive in the wrong phase of Full[st]. It knows
+// this from its own earlier waits: j iterations back it waited for the MMA of
+// it - j*kDeqPhases - kNS, and each issuer (issuers alternate by k-block parity)
+// completes its k-blocks in order, so that wait covers it - 2*kNS whenever
+// j*kDeqPhases <= kNS and j*kDeqPhases - kNS is even.
+constexpr bool stage_reuse_is_safe(int phases, int stages) {
+  for (int j = 1; j * phases <= stages; ++j)
+    if ((stages - j * phases) % 2 == 0) return true;
+  return false;
+}
+static_assert(stage_reuse_is_safe(kDeqPhases, kNS),
+              "a dequantisation warp could pass a stale Empty phase (parity aliasing)");
+
 constexpr int kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
 constexpr int kRowRegs = kBNMax / 32;  // token rows per epilogue lane (routing prefetch)
