@@ -43,7 +43,7 @@ extern "C" {
 enum {
   MOE_W4A16_OK = 0,
   MOE_W4A16_INVALID_ARG = -1,         /* null pointer, negative size, bad handle */
-  MOE_W4A16_UNSUPPORTED_SHAPE = -2,   /* K % 128, N % 64, group_size != 32, E or topk out of range */
+  MOE_W4A16_UNSUPPORTED_SHAPE = -2,   /* K % 128, N % 128, group_size != 32, E or topk out of range */
   MOE_W4A16_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < moe_w4a16_workspace_size(h, M) */
   MOE_W4A16_CUDA_ERROR = -4,          /* a CUDA runtime call failed (message has the CUDA error) */
   MOE_W4A16_NOT_PACKED = -5           /* forward before moe_w4a16_pack */
@@ -61,7 +61,7 @@ typedef struct moe_w4a16_ctx* moe_w4a16_t;
  * routing and INT4 group size (must be 32). Binds to the current CUDA device and
  * allocates the packed weight storage there (cudaMalloc, same byte count as the
  * GPTQ-style inputs: E*(3*N*K/2 + 2*(2N*K/32 + K*N/32)) bytes).
- * Requirements: K % 128 == 0, N % 64 == 0, 1 <= E <= 1024, 1 <= topk <= E.
+ * Requirements: K % 128 == 0, N % 128 == 0, 1 <= E <= 1024, 1 <= topk <= E.
  * Host-synchronous. */
 int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t* out);
 

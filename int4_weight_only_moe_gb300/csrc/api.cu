@@ -114,7 +114,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   if (E < 1 || E > kMaxExperts) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "E must be in [1, 1024]");
   if (topk < 1 || topk > E) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "topk must be in [1, E]");
   if (K <= 0 || K % 128 != 0) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "K must be a positive multiple of 128");
-  if (N <= 0 || N % 64 != 0) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "N must be a positive multiple of 64");
+  if (N <= 0 || N % 128 != 0) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "N must be a positive multiple of 128");
   auto* h = new moe_w4a16_ctx();
   std::memset(h, 0, sizeof(*h));
   h->E = E;
@@ -301,7 +301,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g1.tiles = tiles;
   g1.expert_tiles = expert_tiles;
   g1.R = 2 * h->N / kBM;
-  g1.KBn = h->K / kBK;
+  g1.KBn = h->K / (2 * kBK);  // GEMM pipeline steps of 128 reduction elements
   g1.Gcap = L.Gcap;
   g1.hout = hbuf;
   g1.scratch = scratch;
@@ -327,7 +327,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g2.tiles = tiles;
   g2.expert_tiles = expert_tiles;
   g2.R = h->K / kBM;
-  g2.KBn = h->N / kBK;
+  g2.KBn = h->N / (2 * kBK);
   g2.Gcap = L.Gcap;
   g2.sorted_ids = sorted;
   g2.topk_weights = topk_weights;

@@ -13,18 +13,24 @@
 // and the routed tokens of one expert (16..64, a multiple of 16) are MMA N, so a
 // single token (decode) costs one N=16 tile instead of a 128-row tile.
 //
-// Per CTA (one per SM), 20 warps:
-//   warp 0       4 lanes bulk-copy packed INT4 weight blocks (4.5 KB) into a 16-deep ring
-//   warp 1       4 lanes bulk-copy the activation tile (B operand) into a 16-deep
-//                ring of its own (the lanes of a producer issue 4 consecutive
-//                k-blocks at once); the activations are small and L2-resident, so
-//                running them 16 k-blocks ahead takes their latency off the MMA path
-//   warps 2, 3   tcgen05.mma issuers for alternate k-blocks, each into its own
-//                accumulators (warp 2 also allocates tensor memory)
-//   warps 4..15  dequantise INT4 -> fp16 in registers and store the A operand
-//                straight into tensor memory (tcgen05.st) through an 8-stage ring;
-//                three warps per lane quadrant take whole k-blocks in turn
-//   warps 16..19 epilogue: tcgen05.ld of both issuers' fp32 accumulators
+// The pipeline moves in steps of 128 reduction elements (two 64-element k-blocks
+// of the packed layout): every per-step cost (barrier tests and arrivals, MMA
+// commits, copy issue, address arithmetic) is paid once per 128 elements.
+//
+// Per CTA (one per SM), 24 warps:
+//   warp 0       one lane bulk-copies the packed INT4 weights, 2 steps (18 KB) per
+//                copy, into a 4-chunk ring
+//   warp 1       4 lanes bulk-copy the activation tile (B operand, both 64-element
+//                planes of a step) into an 8-step ring of its own (the lanes issue
+//                4 consecutive steps at once); running the small, L2-resident
+//                copies that far ahead takes their latency off the MMA path
+//   warps 2, 3   tcgen05.mma issuers for alternate steps (8 MMAs each), each into
+//                its own accumulators (warp 2 also allocates tensor memory)
+//   warps 4..19  dequantise INT4 -> fp16 in registers and store the A operand
+//                straight into tensor memory (tcgen05.st) through a 4-stage ring;
+//                four warps per lane quadrant, warp `phase` converting the steps
+//                phase, phase + 4, ... and so always writing stage `phase`
+//   warps 20..23 epilogue: tcgen05.ld of both issuers' fp32 accumulators
 //                (double-buffered), summed
 //
 // The dequantisation writes the weight tile into tensor memory rather than
@@ -32,14 +38,18 @@
 // activations; the MMA reads A from tensor memory and B from shared memory.
 //
 // Work split (stream-K): the units (expert, 128-row weight tile, token tile) each
-// have KBn k-blocks of 64 reduction elements; all units' k-blocks are laid end to
-// end and every CTA takes an equal contiguous share. Every SM therefore streams the
+// have KBn steps of 128 reduction elements; all units' steps are laid end to end
+// and every CTA takes an equal contiguous share. Every SM therefore streams the
 // same number of weight bytes whatever the routing. A unit cut between CTAs is
 // finished by its last contributor: down-GEMM partials are simply added into the
 // fp32 accumulator; gate/up partials go to a per-CTA scratch slot, and the CTA
-// whose atomic ticket completes the unit's k-block count sums the slots in CTA
+// whose atomic ticket completes the unit's step count sums the slots in CTA
 // order (deterministic), applies SiLU*up and writes the tile. No CTA ever waits
 // for another.
+//
+// Warp-collective tcgen05 instructions (.sync.aligned: st, ld, wait, alloc,
+// dealloc) are always preceded by a warp-wide synchronisation, never issued right
+// after lane-divergent code.
 //
 // Every mbarrier wait is bounded in time (see mbar_wait); a wait that gives up
 // raises a CTA-wide abort flag, records MOE_W4A16_STATUS_TIMEOUT, and all roles
@@ -52,7 +62,7 @@
 namespace moe {
 
 // Optional pipeline timeline for performance work: built with -DMOE_GEMM_TRACE,
-// CTA 0 of the traced GEMM records clock64() at fixed points per k-block into a
+// CTA 0 of the traced GEMM records clock64() at fixed points per step into a
 // device array read back with moe_gemm_trace_read(). Compiled out otherwise.
 #ifdef MOE_GEMM_TRACE
 __device__ long long g_gemm_trace[16][2048];
@@ -75,32 +85,41 @@ extern "C" int moe_gemm_trace_read(long long* host) {
 
 namespace {
 
-// Dequantisation warps per TMEM lane quadrant (compile-time; 3 by default).
+// Dequantisation warps per TMEM lane quadrant (compile-time; 4 by default, one
+// per operand stage).
 #ifndef MOE_DEQ_PHASES
-#define MOE_DEQ_PHASES 3
+#define MOE_DEQ_PHASES 4
 #endif
 constexpr int kDeqPhases = MOE_DEQ_PHASES;
 constexpr int kWarpW = 0, kWarpB = 1, kWarpMma0 = 2, kWarpMma1 = 3, kWarpDeq0 = 4;
 constexpr int kWarpEpi0 = kWarpDeq0 + 4 * kDeqPhases;
 constexpr int kThreads = (kWarpEpi0 + 4) * 32;
-constexpr int kNW = 16;                  // weight ring depth (shared memory)
-constexpr int kNS = 8;                   // A operand stage ring (tensor memory)
-constexpr int kNB = 16;                  // B operand ring (shared memory), deeper than the A ring
-constexpr int kBStage = kBNMax * 128;    // B tile of one k-block
+// A pipeline step covers kSub consecutive 64-element k-blocks (128 reduction
+// elements): every per-step cost (barrier waits and arrivals, MMA commit, address
+// arithmetic) is paid once per 128 elements.
+constexpr int kSub = 2;
+constexpr int kWStepBytes = kSub * kWBlockBytes;  // packed weights of one step (9 KB)
+constexpr int kWChunk = 2;               // steps per weight copy (one 18 KB bulk copy)
+constexpr int kNWS = 4;                  // weight ring depth in chunks (shared memory)
+constexpr int kWChunkBytes = kWChunk * kWStepBytes;
+constexpr int kNS = 4;                   // A operand stage ring (tensor memory)
+constexpr int kNB = 8;                   // B operand ring (shared memory), deeper than the A ring
+constexpr int kBSub = kBNMax * 128;      // B tile of one 64-element k-block
+constexpr int kBStage = kSub * kBSub;    // B tiles of one step
 constexpr int kTmemCols = 512;
-constexpr int kACols = 32;               // one k-block of fp16 A: 128 lanes x 32 columns
+constexpr int kACols = kSub * 32;        // one step of fp16 A: 128 lanes x 64 columns
 constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
 constexpr int kStatusTimeout = 2;
 constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
 
 constexpr int kSmB = 0;
 constexpr int kSmW = kSmB + kNB * kBStage;
-constexpr int kSmStage = ((kSmW + kNW * kWBlockBytes + 1023) / 1024) * 1024;
+constexpr int kSmStage = ((kSmW + kNWS * kWChunkBytes + 1023) / 1024) * 1024;
 constexpr int kSmBar = kSmStage + kBNMax * 128;
 // barrier indices
-constexpr int kBarWFull = 0;                 // weight block landed (bulk-copy bytes)
-constexpr int kBarWEmpty = kBarWFull + kNW;  // weight block read by its 4 dequant warps
-constexpr int kBarFull = kBarWEmpty + kNW;   // A stage ready: stored by its 4 dequant warps
+constexpr int kBarWFull = 0;                  // weight chunk landed (bulk-copy bytes)
+constexpr int kBarWEmpty = kBarWFull + kNWS;  // weight chunk read (4 dequant warps per step)
+constexpr int kBarFull = kBarWEmpty + kNWS;   // A stage ready: stored by its 4 dequant warps
 constexpr int kBarEmpty = kBarFull + kNS;    // A stage consumed by the MMAs (tcgen05.commit)
 constexpr int kBarBFull = kBarEmpty + kNS;   // B stage landed (bulk-copy bytes)
 constexpr int kBarBEmpty = kBarBFull + kNB;  // B stage consumed by the MMAs (tcgen05.commit)
@@ -113,15 +132,18 @@ constexpr int kSmBytes = kSmMisc + 64;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
+static_assert((kNWS & (kNWS - 1)) == 0 && (kNS & (kNS - 1)) == 0 && (kNB & (kNB - 1)) == 0 &&
+                  kWChunk == 2,
+              "ring index arithmetic below assumes power-of-two rings and 2-step chunks");
 
-// Stage-reuse safety. A dequantisation warp reuses A stage st for k-block it after
-// a parity test of Empty[st], meaning "the MMA of k-block it - kNS is done". A
+// Stage-reuse safety. A dequantisation warp reuses A stage st for step it after
+// a parity test of Empty[st], meaning "the MMA of step it - kNS is done". A
 // parity test cannot tell that phase from the one two uses back, so the warp must
 // already know that the MMA of it - 2*kNS has completed, or it may overwrite the
 // stage under a running MMA and arrive in the wrong phase of Full[st]. It knows
 // this from its own earlier waits: j iterations back it waited for the MMA of
-// it - j*kDeqPhases - kNS, and each issuer (issuers alternate by k-block parity)
-// completes its k-blocks in order, so that wait covers it - 2*kNS whenever
+// it - j*kDeqPhases - kNS, and each issuer (issuers alternate by step parity)
+// completes its steps in order, so that wait covers it - 2*kNS whenever
 // j*kDeqPhases <= kNS and j*kDeqPhases - kNS is even.
 constexpr bool stage_reuse_is_safe(int phases, int stages) {
   for (int j = 1; j * phases <= stages; ++j)
@@ -145,12 +167,12 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 struct Sched {
-  long long W;  // total k-blocks
+  long long W;  // total steps
   int G;        // CTAs
   __device__ __forceinline__ long long start(int c) const {
     return static_cast<long long>(c) * W / G;
   }
-  // CTA whose share contains k-block g.
+  // CTA whose share contains step g.
   __device__ int cta_of(long long g) const {
     int c = static_cast<int>((g * G) / (W > 0 ? W : 1));
     if (c > G - 1) c = G - 1;
@@ -163,7 +185,7 @@ struct Sched {
 struct SegIter {
   long long g, gend;
   int KBn;
-  // Next (unit, k-block range) of this CTA's share.
+  // Next (unit, step range) of this CTA's share.
   __device__ __forceinline__ bool next(long long& u, int& kb0, int& kb1) {
     if (g >= gend) return false;
     u = g / KBn;
@@ -195,7 +217,7 @@ __device__ __forceinline__ Unit decode_unit(long long u, int R, const TokenTile*
   return r;
 }
 
-// Random access into this CTA's k-block sequence for lanes that step through it
+// Random access into this CTA's step sequence for lanes that walk through it
 // together: seek(it) moves forward to the segment holding sequence index `it`.
 struct Cursor {
   SegIter si;
@@ -294,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNW; ++i) {
+    for (int i = 0; i < kNWS; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
-      mbar_init(bar(kBarWEmpty + i), 4);
+      mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);  // 4 quadrant warps x steps
     }
     for (int i = 0; i < kNS; ++i) {
       mbar_init(bar(kBarFull + i), 4);
@@ -331,14 +353,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   int* status = a.status;
   pdl_launch_dependents();
 
-  if (warp == kWarpW || warp == kWarpB) {
-    // ------------------------------------------------ bulk-copy producers
-    // warp 0: packed weight blocks (W ring); warp 1: activation tiles (B operand,
-    // operand-stage ring). kProducerLanes lanes walk consecutive k-blocks in
-    // step and issue their copies in one warp instruction: a bulk-copy issue
-    // blocks its thread for a while, so several copies have to leave at once for
-    // small (2-4.5 KB) copies to keep HBM busy.
-    const bool is_w = warp == kWarpW;
+  if (warp == kWarpW) {
+    // ------------------------------------------------ packed-weight producer
+    // One lane streams the weight blocks in chunks of kWChunk consecutive steps:
+    // a row tile's k-blocks are contiguous, so a chunk is one 18 KB bulk copy (one
+    // per contiguous run where a chunk crosses units). Copies this large keep HBM
+    // busy from a single issuing thread; 4.5 KB ones do not.
+    if (lane == 0) {
+      const long long n_it = my_end - my_begin;
+      const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
+      Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
+      long long c = 0;
+      for (; c < n_chunks; ++c) {
+        const int s = static_cast<int>(c % kNWS);
+        if (!mbar_wait(bar(kBarWEmpty + s), ((c / kNWS) & 1) ^ 1, abort_flag, status,
+                       kStatusTimeout))
+          break;
+        const long long it0 = c * kWChunk;
+        const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
+        TRACE_POINT(0, it0);
+        mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWStepBytes);
+        for (long long it = it0; it < it1;) {
+          int kb = 0;
+          cur.seek(it, kb);
+          const long long left_in_unit = cur.kb1 - kb;
+          const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
+          const long long woff =
+              ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWStepBytes;
+          if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kWStepBytes <= a.wpack_bytes &&
+                            cur.un.e >= 0 && cur.un.e < a.E && cur.un.rt < a.R && kb + run <= a.KBn &&
+                            run >= 1 && (it - it0) + run <= kWChunk,
+                        a.status, a.dbg, 1, woff, run * 100 + (it - it0)))
+            bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
+                     a.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes, bar(kBarWFull + s));
+          it += run;
+        }
+      }
+      // let the last chunks land before shared memory is released
+      for (long long j = 0; j < kNWS && j < c; ++j) {
+        const long long idx = c - 1 - j;
+        mbar_wait_drain(bar(kBarWFull + static_cast<int>(idx % kNWS)),
+                        static_cast<uint32_t>((idx / kNWS) & 1));
+      }
+    }
+  } else if (warp == kWarpB) {
+    // ------------------------------------------------ activation (B operand) producer
+    // kProducerLanes lanes walk consecutive k-blocks in step and issue their
+    // (2-8 KB) copies in one go: a bulk-copy issue holds its thread
+    // for a while, so small copies must leave several at a time.
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
       Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
@@ -350,35 +412,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (it < n_it) {
           int kb = 0;
           cur.seek(it, kb);
-          bool ok;
-          if (is_w) {
-            const int s = static_cast<int>(it % kNW);
-            ok = mbar_wait(bar(kBarWEmpty + s), ((it / kNW) & 1) ^ 1, abort_flag, status,
-                           kStatusTimeout);
-            __syncwarp(active);
-            if (ok) {
-              const uint8_t* src =
-                  a.wpack +
-                  ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWBlockBytes;
-              TRACE_POINT(0, it);
-              mbar_arrive_expect_tx(bar(kBarWFull + s), kWBlockBytes);
-              bulk_g2s(sW + s * kWBlockBytes, src, kWBlockBytes, bar(kBarWFull + s));
-            }
-          } else {
-            const int s = static_cast<int>(it % kNB);
-            ok = mbar_wait(bar(kBarBEmpty + s), ((it / kNB) & 1) ^ 1, abort_flag, status,
-                           kStatusTimeout);
-            __syncwarp(active);
-            if (ok) {
-              const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
-              const uint8_t* src =
-                  a.bsrc + (static_cast<long long>(kb) * a.Gcap + cur.un.g0) * kRowGroupBytes;
-              TRACE_POINT(1, it);
-              mbar_arrive_expect_tx(bar(kBarBFull + s), bytes);
-              bulk_g2s(sB + s * kBStage, src, bytes, bar(kBarBFull + s));
-            }
-          }
+          if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 && cur.un.e >= 0 && cur.un.e < a.E &&
+                             cur.un.g0 >= 0 && cur.un.g0 + cur.un.ng <= a.tiles_cap && kb >= 0 && kb < a.KBn,
+                         a.status, a.dbg, 11, cur.un.ng * 1000 + cur.un.e, cur.un.g0 * 1000 + kb))
+            cur.un.ng = 1;
+          const int s = static_cast<int>(it % kNB);
+          const bool ok = mbar_wait(bar(kBarBEmpty + s), ((it / kNB) & 1) ^ 1, abort_flag, status,
+                                    kStatusTimeout);
+          __syncwarp(active);
           if (ok) {
+            // the step's two 64-element k-blocks are two planes of the blocked layout
+            const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
+            const long long boff =
+                (static_cast<long long>(kb) * kSub * a.Gcap + cur.un.g0) * kRowGroupBytes;
+            const long long plane = static_cast<long long>(a.Gcap) * kRowGroupBytes;
+            TRACE_POINT(1, it);
+            mbar_arrive_expect_tx(bar(kBarBFull + s), kSub * bytes);
+            if (MOE_CHECK(boff >= 0 && boff + bytes <= a.bsrc_bytes && bytes <= kBSub && bytes > 0 &&
+                              s >= 0 && s < kNB,
+                          a.status, a.dbg, 2, boff, bytes))
+              bulk_g2s(sB + s * kBStage, a.bsrc + boff, bytes, bar(kBarBFull + s));
+            if (MOE_CHECK(boff + plane + bytes <= a.bsrc_bytes, a.status, a.dbg, 3, boff + plane,
+                          bytes))
+              bulk_g2s(sB + s * kBStage + kBSub, a.bsrc + boff + plane, bytes, bar(kBarBFull + s));
             last = it;
             ++mine;
           }
@@ -387,11 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       }
       // bounded wait for this lane's last copies to land before shared memory is
       // released
-      const int depth = is_w ? kNW : kNB;
-      for (uint32_t j = 0; j < static_cast<uint32_t>(depth / kProducerLanes) && j < mine; ++j) {
+      for (uint32_t j = 0; j < static_cast<uint32_t>(kNB / kProducerLanes) && j < mine; ++j) {
         const long long idx = last - static_cast<long long>(j) * kProducerLanes;
-        mbar_wait_drain(bar((is_w ? kBarWFull : kBarBFull) + static_cast<int>(idx % depth)),
-                        static_cast<uint32_t>((idx / depth) & 1));
+        mbar_wait_drain(bar(kBarBFull + static_cast<int>(idx % kNB)),
+                        static_cast<uint32_t>((idx / kNB) & 1));
       }
     }
   } else if (warp == kWarpMma0 || warp == kWarpMma1) {
@@ -411,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
       const int ab = acc_it & 1;
       if (first < it_base + len) {
-        const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16, a.status, a.dbg, 12, un.ng, u)) un.ng = 1;
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
@@ -430,15 +486,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           if (!ok) break;
           if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
-          // B stage sb is sb * kBStage bytes after stage 0 (16-byte units in the
-          // descriptor); +32 bytes of K per MMA inside the 128-byte swizzled row.
+          // B stage sb is sb * kBStage bytes after stage 0, its second 64-element
+          // half kBSub bytes further (16-byte units in the descriptor); +32 bytes of
+          // K per MMA inside the 128-byte swizzled rows.
           const uint64_t b_desc = b_desc0 + ((sb * kBStage) >> 4);
+          const uint64_t b_desc1 = b_desc + (kBSub >> 4);
           if (elect_one()) {
             tc_fence_after();
             tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
             tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
             tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 32, b_desc1, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 40, b_desc1 + 2, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 48, b_desc1 + 4, idesc, 1u);
+            tc_mma_ts(d_tmem, a_tmem + 56, b_desc1 + 6, idesc, 1u);
             tc_commit(bar(kBarEmpty + st));
             tc_commit(bar(kBarBEmpty + sb));
             TRACE_POINT(4, it);
@@ -459,48 +521,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     __syncwarp();
   } else if (warp >= kWarpDeq0 && warp < kWarpEpi0) {
     // ------------------------------------------------ dequantisation into tensor memory
-    // Warp (quad, phase) converts rows 32*quad .. +31 of the k-blocks whose index
-    // in this CTA's sequence is phase, phase + kDeqPhases, ... (only the index
-    // matters here: it fixes the weight-ring slot and the operand stage). The TMEM
-    // store of one k-block is retired (wait::st + arrival) only after the warp
-    // has loaded and converted its next k-block, which hides the store latency.
+    // Warp (quad, phase) converts rows 32*quad .. +31 of the steps whose index in
+    // this CTA's sequence is phase, phase + kDeqPhases, ... (only the index matters
+    // here: it fixes the weight-ring slot and the operand stage). A step's two
+    // 32-column stores are retired (wait::st + arrival) right after they are
+    // issued, so the step's MMAs run while the warp converts its next step.
     const int quad = warp & 3;
     const int phase = (warp - kWarpDeq0) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
-    bool pending = false;
-    uint32_t pend_stage = 0, pend_it = 0;
-    (void)pend_it;
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
-      const uint32_t ws = it % kNW, st = it % kNS;
+      const uint32_t ws = (it >> 1) & (kNWS - 1);  // weight chunk slot (2 steps per chunk)
+      const uint32_t st = it & (kNS - 1);
       // non-blocking test of the stage-free barrier now; its latency overlaps the
       // conversion and the blocking wait below runs only if it was not ready
       const bool e_early = mbar_test_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1);
       if (lane == 0 && quad == 0) TRACE_POINT(12, it);
-      bool w_ok = mbar_wait(bar(kBarWFull + ws), (it / kNW) & 1, abort_flag, status,
+      bool w_ok = mbar_wait(bar(kBarWFull + ws), (it >> 3) & 1, abort_flag, status,
                             kStatusTimeout);
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(5, it);
-      const uint32_t wb = sW + ws * kWBlockBytes;
-      const uint4 q0 = ld_shared_v4(wb + r * 16);
-      const uint4 q1 = ld_shared_v4(wb + 2048 + r * 16);
-      const uint32_t sc = ld_shared_u32(wb + kWCodeBytes + r * 4);  // fp16 scales of both groups
+      // the step's weights: slot ws, step (it & 1) of the chunk = (it & 7) steps in
+      const uint32_t wb = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + r * 16;
+      const uint32_t wsc = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + kWCodeBytes + r * 4;
+      const uint4 q0 = ld_shared_v4(wb);
+      const uint4 q1 = ld_shared_v4(wb + 2048);
+      const uint4 q2 = ld_shared_v4(wb + kWBlockBytes);
+      const uint4 q3 = ld_shared_v4(wb + kWBlockBytes + 2048);
+      const uint32_t sc0 = ld_shared_u32(wsc);  // fp16 scales of the two groups
+      const uint32_t sc1 = ld_shared_u32(wsc + kWBlockBytes);
       uint32_t out[32];
-      dequant_group(q0, __byte_perm(sc, 0, 0x1010), &out[0]);
-      dequant_group(q1, __byte_perm(sc, 0, 0x3232), &out[16]);
-      __syncwarp();  // every lane has consumed its shared-memory words
-      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
-      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
-      if (pending) {
-        __syncwarp();  // tcgen05.wait is warp-collective: converge after the lane-0 arrival
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) TRACE_POINT(8 + quad, pend_it);
-        if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
-        pending = false;
-      }
+      dequant_group(q0, __byte_perm(sc0, 0, 0x1010), &out[0]);
+      dequant_group(q1, __byte_perm(sc0, 0, 0x3232), &out[16]);
       if (!__all_sync(0xffffffffu, e_early)) {
         w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
                          kStatusTimeout);
@@ -510,16 +563,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       tc_fence_after();
       __syncwarp();
       tmem_st32(a_lane + st * kACols, out);
-      pending = true;
-      pend_stage = st;
-      pend_it = it;
-    }
-    if (pending) {
+      dequant_group(q2, __byte_perm(sc1, 0, 0x1010), &out[0]);
+      dequant_group(q3, __byte_perm(sc1, 0, 0x3232), &out[16]);
+      // converge before the warp-collective store; every lane has also consumed
+      // its shared-memory words by now, so the slot can be released after it
       __syncwarp();
+      tmem_st32(a_lane + st * kACols + 32, out);
+      if (lane == 0 && quad == 0) TRACE_POINT(6, it);
+      if (lane == 0) mbar_arrive(bar(kBarWEmpty + ws));
+      __syncwarp();  // tcgen05.wait is warp-collective: converge after the lane-0 arrival
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarFull + pend_stage));
+      if (lane == 0) TRACE_POINT(8 + quad, it);
+      if (lane == 0) mbar_arrive(bar(kBarFull + st));
     }
   } else if (warp >= kWarpEpi0) {
     // ------------------------------------------------ epilogue
@@ -532,7 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     long long u;
     int kb0, kb1;
     while (si.next(u, kb0, kb1)) {
-      const Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16 && un.rt >= 0 && un.rt < a.R, a.status, a.dbg,
+                     13, un.ng, un.rt))
+        un.ng = 1;
       const int nch = un.ng;  // 16-column chunks
       const int ab = acc_it & 1;
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
@@ -555,7 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 #pragma unroll
         for (int j = 0; j < kRowRegs; ++j) {
           const int row = 32 * j + lane;
-          const int sid = row < nch * 16 ? a.sorted_ids[pbase + row] : a.MK;
+          const bool in_tile = row < nch * 16 &&
+                               MOE_CHECK(pbase + row < a.sorted_cap, a.status, a.dbg, 9, pbase + row, nch);
+          const int sid = in_tile ? a.sorted_ids[pbase + row] : a.MK;
           sid_r[j] = sid;
           if (sid < a.MK) {
             w_r[j] = a.topk_weights[sid];
@@ -624,8 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           for (int c = 0; c < nch; ++c) {
             float v[16];
             load_chunk(c, v);
+            const long long so = (slot - a.scratch) + (c * 16) * kBM + r;
+            if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 6, so, c)) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
+              for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -651,8 +716,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                 const int pc = (sc.start(cc) < ustart) ? 1 : 0;
                 const float* sl =
                     a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
+                const long long so = (sl - a.scratch) + (c * 16) * kBM + r;
+                if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 7, so, cc)) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
+                  for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
+                }
               }
               swiglu_chunk(v, c, quad, lane, sStage);
             }
@@ -662,8 +730,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           fence_proxy_async_smem();
           named_bar_sync(kEpiBar, kEpiThreads);
           if (epi_tid == 0) {
-            bulk_s2g(a.hout + (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes,
-                     sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
+            const long long hoff = (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes;
+            if (MOE_CHECK(hoff >= 0 && hoff + nch * kRowGroupBytes <= a.hout_bytes && nch > 0 &&
+                              nch <= kBNMax / 16,
+                          a.status, a.dbg, 5, hoff, nch))
+              bulk_s2g(a.hout + hoff, sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
             bulk_commit();
             bulk_wait_read_all();
           }
@@ -683,7 +754,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
               if (sid < a.MK) {
                 const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
                 const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
-                atomicAdd(acc_col + static_cast<long long>(tok) * a.Kout, wt * v[i]);
+                const long long ai = (acc_col - a.acc) + static_cast<long long>(tok) * a.Kout;
+                if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 8, ai, sid))
+                  atomicAdd(a.acc + ai, wt * v[i]);
               }
             }
           }

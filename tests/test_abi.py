@@ -45,7 +45,7 @@ def test_binding_wraps_every_symbol():
 
 def test_create_rejects_bad_shapes_without_touching_the_gpu(lib):
     h = ctypes.c_void_p()
-    cases = [(8, 256, 128, 2, 16), (8, 200, 128, 2, 32), (8, 256, 96, 2, 32),
+    cases = [(8, 256, 128, 2, 16), (8, 200, 128, 2, 32), (8, 256, 96, 2, 32), (8, 256, 192, 2, 32),
              (0, 256, 128, 2, 32), (8, 256, 128, 9, 32), (2000, 256, 128, 2, 32)]
     for E, K, N, k, g in cases:
         rc = lib.moe_w4a16_create(E, K, N, k, g, ctypes.byref(h))

@@ -145,7 +145,7 @@ def test_mid_forward_grid_sizes(M, num_ctas):
 
 def test_hot_expert_spans_several_token_tiles():
     # one expert receives every token (> 128 rows: several token tiles of one expert)
-    E, K, N, k, M = 8, 768, 320, 2, 300
+    E, K, N, k, M = 8, 768, 384, 2, 300
     prob = Problem(E, K, N, k)
     rng = np.random.default_rng(4)
     hidden = inputs.hidden_states(M, K)
