@@ -100,10 +100,17 @@ constexpr int kThreads = (kWarpEpi0 + 4) * 32;
 constexpr int kSub = 2;
 constexpr int kWStepBytes = kSub * kWBlockBytes;  // packed weights of one step (9 KB)
 constexpr int kWChunk = 2;               // steps per weight copy (one 18 KB bulk copy)
-constexpr int kNWS = 4;                  // weight ring depth in chunks (shared memory)
+// Ring depths (compile-time; shared memory is shared between the two rings).
+#ifndef MOE_W_CHUNKS
+#define MOE_W_CHUNKS 4
+#endif
+#ifndef MOE_B_STEPS
+#define MOE_B_STEPS 8
+#endif
+constexpr int kNWS = MOE_W_CHUNKS;       // weight ring depth in chunks (shared memory)
 constexpr int kWChunkBytes = kWChunk * kWStepBytes;
 constexpr int kNS = 4;                   // A operand stage ring (tensor memory)
-constexpr int kNB = 8;                   // B operand ring (shared memory), deeper than the A ring
+constexpr int kNB = MOE_B_STEPS;         // B operand ring depth in steps (shared memory)
 constexpr int kBSub = kBNMax * 128;      // B tile of one 64-element k-block
 constexpr int kBStage = kSub * kBSub;    // B tiles of one step
 constexpr int kTmemCols = 512;
@@ -132,9 +139,8 @@ constexpr int kSmBytes = kSmMisc + 64;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
-static_assert((kNWS & (kNWS - 1)) == 0 && (kNS & (kNS - 1)) == 0 && (kNB & (kNB - 1)) == 0 &&
-                  kWChunk == 2,
-              "ring index arithmetic below assumes power-of-two rings and 2-step chunks");
+static_assert((kNS & (kNS - 1)) == 0 && kWChunk == 2,
+              "stage index arithmetic below assumes a power-of-two A ring and 2-step chunks");
 
 // Stage-reuse safety. A dequantisation warp reuses A stage st for step it after
 // a parity test of Empty[st], meaning "the MMA of step it - kNS is done". A
@@ -152,6 +158,11 @@ constexpr bool stage_reuse_is_safe(int phases, int stages) {
 }
 static_assert(stage_reuse_is_safe(kDeqPhases, kNS),
               "a dequantisation warp could pass a stale Empty phase (parity aliasing)");
+// The MMA issuer that waits on a B (or A) stage for step it consumed the
+// previous phase itself (step it - depth) only if the depth is even; a B
+// producer lane reuses a slot only after an earlier lockstep iteration.
+static_assert(kNB % 2 == 0 && kNS % 2 == 0 && kNB >= kProducerLanes,
+              "ring depths must be even and the B ring at least as deep as the producer lanes");
 
 constexpr int kEpiWarps = 4, kEpiThreads = 128;
 constexpr int kEpiBar = 1;  // named barrier id of the epilogue warps
@@ -280,23 +291,24 @@ __device__ __forceinline__ uint16_t f16_bits_sat(float x) {
 
 // SiLU(gate) * up for one 16-column chunk of the accumulator and store into the
 // staging tile (blocked, swizzled). Lanes (2i, 2i+1) hold the gate and up rows of
-// feature i; the even lane writes tokens 0..7 of the chunk, the odd lane 8..15.
+// feature i for the chunk's 16 tokens; the even lane finishes tokens 0..7 and the
+// odd lane tokens 8..15, so each sends its partner the half the partner finishes.
+// No lane-divergent code: every lane evaluates 8 SiLUs. The sigmoid uses the fast
+// reciprocal (a few fp32 ulps, far below the fp16 rounding of h; it tends to 0 as
+// e^-g overflows to infinity).
 __device__ __forceinline__ void swiglu_chunk(const float (&v)[16], int chunk, int quad, int lane,
                                              uint32_t s_stage) {
-  float p[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) p[i] = __shfl_xor_sync(0xffffffffu, v[i], 1);
   const bool is_gate = (lane & 1) == 0;
   const int f = quad * 16 + (lane >> 1);
+  const int row0 = chunk * 16 + (is_gate ? 0 : 8);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if ((i < 8) == is_gate) {
-      const float g = is_gate ? v[i] : p[i];
-      const float u = is_gate ? p[i] : v[i];
-      const float hv = g / (1.0f + __expf(-g)) * u;
-      const int row = chunk * 16 + i;
-      st_shared_u16(s_stage + blocked_offset(row, f), f16_bits_sat(hv));
-    }
+  for (int j = 0; j < 8; ++j) {
+    const float mine = is_gate ? v[j] : v[j + 8];
+    const float other = __shfl_xor_sync(0xffffffffu, is_gate ? v[j + 8] : v[j], 1);
+    const float g = is_gate ? mine : other;
+    const float u = is_gate ? other : mine;
+    const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
+    st_shared_u16(s_stage + blocked_offset(row0 + j, f), f16_bits_sat(g * sig * u));
   }
 }
 
@@ -315,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   volatile int* epi_ok = reinterpret_cast<volatile int*>(gbase + kSmMisc + 16);  // [2][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) TRACE_POINT(13, 0);  // kernel entry
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNWS; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
@@ -346,7 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  pdl_wait();  // the align/gather (or gate/up) kernel's outputs are read below
+  // Programmatic dependent launch: wait for the preceding kernel (its outputs are
+  // read below), then let the next one launch as this grid's CTAs retire. Starting
+  // the weight stream before the wait (only the B operand depends on the
+  // preceding kernel) was measured: the early weight traffic slowed the preceding
+  // kernel's last CTAs more than it saved. The routing reads stay ordinary cached
+  // loads: they sit on the producers' path at every unit boundary.
+  pdl_wait();
+  if (threadIdx.x == 0) TRACE_POINT(13, 1);
   const int num_tiles = a.hdr[kHdrNumTiles];
   const Sched sc{static_cast<long long>(num_tiles) * a.R * a.KBn, static_cast<int>(gridDim.x)};
   const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
@@ -405,9 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     if (lane < kProducerLanes) {
       Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
       long long last = -1;
+      long long issued_hi = 0;  // no lane has issued a step at or beyond this index
       uint32_t mine = 0;
       for (long long base_it = 0; base_it < n_it; base_it += kProducerLanes) {
         const long long it = base_it + lane;
+        issued_hi = base_it + kProducerLanes < n_it ? base_it + kProducerLanes : n_it;
         const unsigned active = __ballot_sync(0x0000000fu, it < n_it) & 0xFu;
         if (it < n_it) {
           int kb = 0;
@@ -443,8 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       }
       // bounded wait for this lane's last copies to land before shared memory is
       // released
-      for (uint32_t j = 0; j < static_cast<uint32_t>(kNB / kProducerLanes) && j < mine; ++j) {
-        const long long idx = last - static_cast<long long>(j) * kProducerLanes;
+      // (exactly the copies of the last kNB steps issued: no later copy reused
+      // their slots, so their phases cannot alias; earlier ones were consumed)
+      for (long long idx = last; mine > 0 && idx >= 0 && idx + kNB >= issued_hi;
+           idx -= kProducerLanes) {
         mbar_wait_drain(bar(kBarBFull + static_cast<int>(idx % kNB)),
                         static_cast<uint32_t>((idx / kNB) & 1));
       }
@@ -508,7 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           acc_flag = 1u;
         }
         if (!ok) break;
-        if (elect_one()) tc_commit(bar(kBarAccFull + par * 2 + ab));
+        if (elect_one()) {
+          tc_commit(bar(kBarAccFull + par * 2 + ab));
+          TRACE_POINT(14, 32 + acc_it * 2 + par);  // issuer done with a segment
+        }
         __syncwarp();
       }
       it_base += len;
@@ -532,19 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
-      const uint32_t ws = (it >> 1) & (kNWS - 1);  // weight chunk slot (2 steps per chunk)
+      const uint32_t wc = it >> 1;                 // weight chunk (2 steps per chunk)
+      const uint32_t ws = wc % kNWS;               // its ring slot
       const uint32_t st = it & (kNS - 1);
       // non-blocking test of the stage-free barrier now; its latency overlaps the
       // conversion and the blocking wait below runs only if it was not ready
       const bool e_early = mbar_test_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1);
       if (lane == 0 && quad == 0) TRACE_POINT(12, it);
-      bool w_ok = mbar_wait(bar(kBarWFull + ws), (it >> 3) & 1, abort_flag, status,
+      bool w_ok = mbar_wait(bar(kBarWFull + ws), (wc / kNWS) & 1, abort_flag, status,
                             kStatusTimeout);
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(5, it);
-      // the step's weights: slot ws, step (it & 1) of the chunk = (it & 7) steps in
-      const uint32_t wb = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + r * 16;
-      const uint32_t wsc = sW + (it & (kNWS * kWChunk - 1)) * kWStepBytes + kWCodeBytes + r * 4;
+      // the step's weights: slot ws, step (it & 1) of the chunk
+      const uint32_t wstep = ws * kWChunk + (it & 1);
+      const uint32_t wb = sW + wstep * kWStepBytes + r * 16;
+      const uint32_t wsc = sW + wstep * kWStepBytes + kWCodeBytes + r * 4;
       const uint4 q0 = ld_shared_v4(wb);
       const uint4 q1 = ld_shared_v4(wb + 2048);
       const uint4 q2 = ld_shared_v4(wb + kWBlockBytes);
@@ -638,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         full_phase ^= 1u << (2 + ab);
       }
       w_ok = __all_sync(0xffffffffu, w_ok);
+      if (epi_tid == 0) TRACE_POINT(14, 512 + acc_it);  // epilogue's accumulator wait done
       if (lane == 0) epi_ok[(acc_it & 1) * 4 + quad] = w_ok ? 1 : 0;
       named_bar_sync(kEpiBar, kEpiThreads);
       const bool all_ok = epi_ok[(acc_it & 1) * 4 + 0] && epi_ok[(acc_it & 1) * 4 + 1] &&
@@ -673,8 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           for (int c = 0; c < nch; ++c) {
             float v[16];
             load_chunk(c, v);
+            if (epi_tid == 0 && c == 0) TRACE_POINT(14, 600 + acc_it * 8 + 0);  // accumulators loaded
             swiglu_chunk(v, c, quad, lane, sStage);
           }
+          if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 1);  // SwiGLU staged
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
@@ -704,6 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             *last_flag = (old + add == a.KBn) ? 1 : 0;
           }
           named_bar_sync(kEpiBar, kEpiThreads);
+          if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 5);  // ticket taken
           write_tile = *last_flag != 0;
           if (write_tile) {
             __threadfence();
@@ -727,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           }
         }
         if (write_tile) {
+          if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 2);  // tile ready to store
           fence_proxy_async_smem();
           named_bar_sync(kEpiBar, kEpiThreads);
           if (epi_tid == 0) {
@@ -736,7 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                           a.status, a.dbg, 5, hoff, nch))
               bulk_s2g(a.hout + hoff, sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
             bulk_commit();
+            TRACE_POINT(14, 600 + acc_it * 8 + 3);  // bulk store issued
             bulk_wait_read_all();
+            TRACE_POINT(14, 600 + acc_it * 8 + 4);  // staging tile read by the store
           }
           named_bar_sync(kEpiBar, kEpiThreads);
         }
@@ -765,12 +801,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
       }
+      if (epi_tid == 0) TRACE_POINT(15, acc_it);  // epilogue done with a segment
       ++acc_it;
     }
     if (epi_tid == 0) bulk_wait_all();
   }
 
   // ------------------------------------------------ teardown
+  if (lane == 0) TRACE_POINT(14, warp);  // each warp reaching the teardown
   __syncwarp();  // lanes that skipped a single-lane role wait for it here
   tc_fence_before();
   __syncthreads();
