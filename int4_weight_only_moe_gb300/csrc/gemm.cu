@@ -135,7 +135,9 @@ constexpr int kBarAccEmpty = kBarAccFull + 4;  // [buffer]: epilogue has read bo
 constexpr int kBarDrain = kBarAccEmpty + 2;    // [issuer]
 constexpr int kNumBars = kBarDrain + 2;
 constexpr int kSmMisc = kSmBar + kNumBars * 8;
-constexpr int kSmBytes = kSmMisc + 64;
+constexpr int kMaxSegs = 512;            // units decoded into shared memory up front
+constexpr int kSmSeg = kSmMisc + 64;
+constexpr int kSmBytes = kSmSeg + kMaxSegs * 16;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
@@ -228,19 +230,34 @@ __device__ __forceinline__ Unit decode_unit(long long u, int R, const TokenTile*
   return r;
 }
 
+// The units of this CTA's share, decoded once at kernel start into shared memory
+// (consecutive segments are consecutive units): the roles then never stall at a
+// unit boundary on the dependent global loads of decode_unit. Units beyond the
+// table are decoded on the fly.
+static_assert(sizeof(Unit) == 16, "segment table entry size");
+struct SegTable {
+  const Unit* t;
+  long long u0;
+  int n, R;
+  const TokenTile* tiles;
+  const int32_t* expert_tiles;
+  __device__ __forceinline__ Unit get(long long u) const {
+    const long long s = u - u0;
+    return (s >= 0 && s < n) ? t[s] : decode_unit(u, R, tiles, expert_tiles);
+  }
+};
+
 // Random access into this CTA's step sequence for lanes that walk through it
 // together: seek(it) moves forward to the segment holding sequence index `it`.
 struct Cursor {
   SegIter si;
   long long u = 0, seg_it0 = 0;
-  int kb0 = 0, kb1 = 0, R = 0;
+  int kb0 = 0, kb1 = 0;
   bool valid = false, decoded = false;
   Unit un{};
-  const TokenTile* tiles;
-  const int32_t* expert_tiles;
-  __device__ Cursor(long long begin, long long end, int KBn, int R_, const TokenTile* t,
-                    const int32_t* et)
-      : si{begin, end, KBn}, R(R_), tiles(t), expert_tiles(et) {
+  SegTable segs;
+  __device__ Cursor(long long begin, long long end, int KBn, const SegTable& st)
+      : si{begin, end, KBn}, segs(st) {
     valid = si.next(u, kb0, kb1);
   }
   __device__ __forceinline__ bool seek(long long it, int& kb) {
@@ -251,7 +268,7 @@ struct Cursor {
     }
     if (!valid) return false;
     if (!decoded) {
-      un = decode_unit(u, R, tiles, expert_tiles);
+      un = segs.get(u);
       decoded = true;
     }
     kb = kb0 + static_cast<int>(it - seg_it0);
@@ -373,6 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   int* status = a.status;
   pdl_launch_dependents();
 
+  // decode this CTA's units in parallel (one round of global loads for all)
+  Unit* seg_tab = reinterpret_cast<Unit*>(gbase + kSmSeg);
+  const long long u_first = my_begin / a.KBn;
+  const long long n_units = my_end > my_begin ? (my_end - 1) / a.KBn - u_first + 1 : 0;
+  const int n_tab = static_cast<int>(n_units < kMaxSegs ? n_units : kMaxSegs);
+  for (int i = threadIdx.x; i < n_tab; i += blockDim.x)
+    seg_tab[i] = decode_unit(u_first + i, a.R, a.tiles, a.expert_tiles);
+  __syncthreads();
+  const SegTable segs{seg_tab, u_first, n_tab, a.R, a.tiles, a.expert_tiles};
+
   if (warp == kWarpW) {
     // ------------------------------------------------ packed-weight producer
     // One lane streams the weight blocks in chunks of kWChunk consecutive steps:
@@ -382,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     if (lane == 0) {
       const long long n_it = my_end - my_begin;
       const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
-      Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
+      Cursor cur(my_begin, my_end, a.KBn, segs);
       long long c = 0;
       for (; c < n_chunks; ++c) {
         const int s = static_cast<int>(c % kNWS);
@@ -423,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // for a while, so small copies must leave several at a time.
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
-      Cursor cur(my_begin, my_end, a.KBn, a.R, a.tiles, a.expert_tiles);
+      Cursor cur(my_begin, my_end, a.KBn, segs);
       long long last = -1;
       long long issued_hi = 0;  // no lane has issued a step at or beyond this index
       uint32_t mine = 0;
@@ -490,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
       const int ab = acc_it & 1;
       if (first < it_base + len) {
-        Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+        Unit un = segs.get(u);
         if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16, a.status, a.dbg, 12, un.ng, u)) un.ng = 1;
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
@@ -618,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     long long u;
     int kb0, kb1;
     while (si.next(u, kb0, kb1)) {
-      Unit un = decode_unit(u, a.R, a.tiles, a.expert_tiles);
+      Unit un = segs.get(u);
       if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16 && un.rt >= 0 && un.rt < a.R, a.status, a.dbg,
                      13, un.ng, un.rt))
         un.ng = 1;
