@@ -410,6 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const long long n_it = my_end - my_begin;
       const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
       Cursor cur(my_begin, my_end, a.KBn, segs);
+      // The weights are read exactly once: stream them through L2 with an
+      // evict-first policy, so they do not displace the activations (re-read by
+      // every row tile of their expert) or the intermediate.
+      const uint64_t w_policy = l2_policy_evict_first();
       long long c = 0;
       for (; c < n_chunks; ++c) {
         const int s = static_cast<int>(c % kNWS);
@@ -431,8 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                             cur.un.e >= 0 && cur.un.e < a.E && cur.un.rt < a.R && kb + run <= a.KBn &&
                             run >= 1 && (it - it0) + run <= kWChunk,
                         a.status, a.dbg, 1, woff, run * 100 + (it - it0)))
-            bulk_g2s(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
-                     a.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes, bar(kBarWFull + s));
+            bulk_g2s_hint(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
+                          a.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes,
+                          bar(kBarWFull + s), w_policy);
           it += run;
         }
       }
@@ -746,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             float v[16];
             load_chunk(c, v);
             const long long so = (slot - a.scratch) + (c * 16) * kBM + r;
+            (void)so;  // read only by the self-checking build
             if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 6, so, c)) {
 #pragma unroll
               for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
@@ -777,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                 const float* sl =
                     a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
                 const long long so = (sl - a.scratch) + (c * 16) * kBM + r;
+                (void)so;  // read only by the self-checking build
                 if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 7, so, cc)) {
 #pragma unroll
                   for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
