@@ -123,7 +123,9 @@ enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL 
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order
- * (align, gather, gemm1, gemm2, finalize). Synchronises on the recorded events.
+ * (align, gather, gemm1, gemm2, finalize); when M * topk <= 32 the routing and
+ * the gather run as one kernel, reported as align (gather then reads ~0).
+ * Synchronises on the recorded events.
  * `n` is the capacity of `ms`; returns the number written or a negative code. */
 int moe_w4a16_kernel_times(moe_w4a16_t h, float* ms, int n);
 

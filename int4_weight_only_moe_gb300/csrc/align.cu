@@ -138,7 +138,120 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
   pdl_launch_dependents();
 }
 
+// Small batches (at most 32 routed slots, e.g. decode) take one warp, with no
+// E-wide histograms, scans or block barriers: lane l holds flat slot l; lanes
+// routed to the same expert find each other with __match_any_sync; a slot's rank
+// among them counts the lower lanes (slot ids ascending, the same stable order as
+// the general kernel); the padded segment and first tile of an expert add up the
+// experts present (at most 32) with a smaller id. Experts without rows get no
+// segment and no tiles (the GEMMs read only the tiles' experts).
+struct SmallRoute {
+  int e;          // this lane's expert, or -1 (no slot or a bad id)
+  int rank, cnt;  // position among the slots of its expert, and their number
+  bool leader;    // lowest lane of its expert
+  int pad, ntile; // leader only: padded rows and token tiles of the expert
+  int seg, tile0; // first padded row and first tile of the expert
+  int tot_pad, tot_tiles;
+  bool any_bad;
+};
+
+__device__ SmallRoute small_route(const AlignArgs& a, int lane) {
+  SmallRoute r;
+  r.e = -1;
+  bool bad = false;
+  if (lane < a.MK) {
+    const int v = a.topk_ids[lane];
+    if (v >= 0 && v < a.E)
+      r.e = v;
+    else
+      bad = true;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, r.e);
+  const bool valid = r.e >= 0;
+  r.rank = __popc(peers & ((1u << lane) - 1u));
+  r.cnt = __popc(peers);
+  r.leader = valid && r.rank == 0;
+  r.pad = r.leader ? (r.cnt + a.block - 1) / a.block * a.block : 0;
+  r.ntile = (r.leader && a.bn_max > 0) ? (r.pad + a.bn_max - 1) / a.bn_max : 0;
+  const int lead_e = r.leader ? r.e : -1;
+  r.seg = r.tile0 = r.tot_pad = r.tot_tiles = 0;
+  for (int j = 0; j < 32; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, lead_e, j);
+    const int pj = __shfl_sync(0xffffffffu, r.pad, j);
+    const int tj = __shfl_sync(0xffffffffu, r.ntile, j);
+    if (ej >= 0) {
+      r.tot_pad += pj;
+      r.tot_tiles += tj;
+      if (ej < r.e) {
+        r.seg += pj;
+        r.tile0 += tj;
+      }
+    }
+  }
+  r.any_bad = __any_sync(0xffffffffu, bad);
+  return r;
+}
+
+// Write the routing outputs of a small batch (one warp): header, counters, sorted
+// slot ids, token tiles, and (debug entry) the offsets of all E experts.
+__device__ void small_route_write(const AlignArgs& a, const SmallRoute& r, int lane) {
+  // header first: the range checks below may OR bits into the status word
+  if (lane == 0) {
+    if (a.hdr) {
+      a.hdr[kHdrStatus] = r.any_bad ? 1 : 0;
+      a.hdr[kHdrNumPadded] = r.tot_pad;
+      a.hdr[kHdrNumTiles] = r.tot_tiles;
+    }
+    if (a.num_padded_out) *a.num_padded_out = r.tot_pad;
+  }
+  if (lane < 8 && a.dbg) a.dbg[lane] = 0;
+  if (a.tickets)
+    for (int i = lane; i < a.n_tickets; i += 32) a.tickets[i] = 0;
+  __syncwarp();
+  if (r.e >= 0 &&
+      MOE_CHECK(a.sorted_cap <= 0 || r.seg + r.rank < a.sorted_cap, a.hdr, a.dbg, 26, r.seg + r.rank, r.e))
+    a.sorted_ids[r.seg + r.rank] = lane;
+  if (r.leader) {
+    for (int p = r.seg + r.cnt; p < r.seg + r.pad; ++p)
+      if (MOE_CHECK(a.sorted_cap <= 0 || p < a.sorted_cap, a.hdr, a.dbg, 27, p, r.e))
+        a.sorted_ids[p] = a.MK;
+    if (a.bn_max > 0) {
+      for (int t = 0; t < r.ntile; ++t) {
+        TokenTile tt;
+        tt.expert = r.e;
+        tt.g0 = (r.seg + t * a.bn_max) / kRowGroup;
+        tt.ngroups = min(a.bn_max, r.pad - t * a.bn_max) / kRowGroup;
+        tt.first = r.tile0;
+        if (MOE_CHECK(r.tile0 + t < a.tiles_cap, a.hdr, a.dbg, 28, r.tile0 + t, r.e))
+          a.tiles[r.tile0 + t] = tt;
+      }
+      a.expert_tiles[r.e] = r.ntile;
+    }
+  }
+  if (a.expert_offsets) {
+    const int lead_e = r.leader ? r.e : -1;
+    for (int x0 = 0; x0 <= a.E; x0 += 32) {  // uniform trip count: shuffles stay converged
+      const int x = x0 + lane;
+      int off = 0;
+      for (int j = 0; j < 32; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, lead_e, j);
+        const int pj = __shfl_sync(0xffffffffu, r.pad, j);
+        if (ej >= 0 && ej < x) off += pj;
+      }
+      if (x <= a.E) a.expert_offsets[x] = off;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(32) align_small_kernel(const AlignArgs a) {
+  pdl_wait();
+  const SmallRoute r = small_route(a, threadIdx.x);
+  small_route_write(a, r, threadIdx.x);
+  pdl_launch_dependents();
+}
+
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl) {
+  if (a.MK <= 32) return launch_k(align_small_kernel, dim3(1), dim3(32), 0, stream, pdl, a);
   const size_t smem = (33 * static_cast<size_t>(a.E)) * sizeof(int);
   cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -156,6 +269,63 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
                     bf16x2_to_f16x2(v.w));
+}
+
+// Small batches in one launch: routing and gather. Every CTA's first warp
+// recomputes the one-warp routing (cheap) and lays the padded sorted-slot list
+// into shared memory; CTA 0 also publishes the routing for the GEMMs (they read
+// it after waiting for this kernel). Then every thread gathers its share of the
+// expert-sorted rows and zeroes its share of the accumulator, as gather_kernel.
+constexpr int kSmallPadRows = 32 + 32 * (kRowGroup - 1);  // at most 32 slots, padded to 16 each
+
+__global__ void __launch_bounds__(256) route_gather_small_kernel(const AlignArgs a, const GatherArgs g) {
+  __shared__ int s_sorted[kSmallPadRows];
+  __shared__ int s_npad;
+  pdl_wait();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const SmallRoute r = small_route(a, lane);
+    const int npad = r.tot_pad < kSmallPadRows ? r.tot_pad : kSmallPadRows;
+    for (int p = lane; p < npad; p += 32) s_sorted[p] = a.MK;
+    __syncwarp();
+    if (r.e >= 0 && r.seg + r.rank < kSmallPadRows) s_sorted[r.seg + r.rank] = lane;
+    if (lane == 0) s_npad = npad;
+    if (blockIdx.x == 0) small_route_write(a, r, lane);
+  }
+  __syncthreads();
+  const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  float4* acc4 = reinterpret_cast<float4*>(g.acc);
+  for (long long i = gt; i < g.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int cpr = g.K / 8;
+  const long long chunks = static_cast<long long>(s_npad) * cpr;
+  for (long long idx = gt; idx < chunks; idx += nthr) {
+    const int p = static_cast<int>(idx / cpr), ch = static_cast<int>(idx - static_cast<long long>(p) * cpr);
+    const int sid = s_sorted[p];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (sid < g.MK && MOE_CHECK(sid >= 0 && sid / g.topk < g.M, const_cast<int32_t*>(g.hdr), g.dbg, 29,
+                                sid, p))
+      v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
+          g.x + static_cast<long long>(sid / g.topk) * g.K + ch * 8));
+    const int grp = p / kRowGroup, row = p % kRowGroup;
+    const long long off = (static_cast<long long>(ch >> 3) * g.Gcap + grp) * kRowGroupBytes +
+                          row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+    if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 30, off, p))
+      *reinterpret_cast<uint4*>(g.xs + off) = v;
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
+                                      int num_sms, cudaStream_t stream, bool pdl) {
+  const long long rows = max_rows < kSmallPadRows ? max_rows : kSmallPadRows;
+  const long long work = std::max<long long>(rows * (g.K / 8), g.acc_elems / 4);
+  long long grid = (work + 255) / 256;
+  const long long cap = 4LL * num_sms;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  return launch_k(route_gather_small_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
+                  pdl, a, g);
 }
 
 // Copy every expert-sorted row's hidden state, as fp16, into the blocked B-operand

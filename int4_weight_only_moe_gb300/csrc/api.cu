@@ -274,8 +274,6 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   aa.sorted_cap = L.Pcap;
   aa.tiles_cap = L.Gcap;
   aa.dbg = hdr + 8;
-  MOE_CUDA_TRY(launch_align(aa, s, false));
-  if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
 
   GatherArgs ga{};
   ga.x = hidden;
@@ -291,7 +289,15 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   ga.xs_bytes = static_cast<long long>(L.Pcap) * h->K * 2;
   ga.M = M;
   ga.dbg = hdr + 8;
-  MOE_CUDA_TRY(launch_gather(ga, L.Gcap, h->num_sms, s, pdl));
+  if (MK <= 32) {
+    // small batch (decode): routing and gather in one launch, timed as "align"
+    MOE_CUDA_TRY(launch_route_gather_small(aa, ga, L.Pcap, h->num_sms, s, false));
+    if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
+  } else {
+    MOE_CUDA_TRY(launch_align(aa, s, false));
+    if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
+    MOE_CUDA_TRY(launch_gather(ga, L.Gcap, h->num_sms, s, pdl));
+  }
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[2], s));
 
   GemmArgs g1{};

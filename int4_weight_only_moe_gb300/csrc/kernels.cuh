@@ -50,6 +50,10 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
                           bool pdl);
+// M * topk <= 32: the routing (as the align kernel) and the gather in one launch.
+// max_rows bounds the padded rows (the workspace's capacity).
+cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
+                                      int num_sms, cudaStream_t stream, bool pdl);
 
 struct GemmArgs {
   const uint8_t* wpack;    // packed weights of this GEMM

@@ -39,6 +39,9 @@ def zipf_ids(rng, M, E, k, s=1.1):
     (9, 8, 384, 16, "uniform"), (90, 8, 384, 16, "uniform"), (1024, 8, 384, 16, "uniform"),
     (1024, 8, 384, 16, "zipf"), (333, 3, 1024, 64, "uniform"), (77, 5, 40, 1, "zipf"),
     (500, 4, 7, 5, "dup"), (4096, 8, 384, 16, "zipf"),
+    # at most 32 slots: the one-warp path
+    (3, 8, 384, 16, "dup"), (2, 8, 40, 5, "zipf"), (4, 8, 384, 1, "uniform"), (1, 4, 3, 64, "dup"),
+    (16, 2, 1024, 16, "uniform"), (5, 6, 12, 16, "dup"),
 ])
 def test_align_bit_exact(M, k, E, block, dist):
     rng = np.random.default_rng(M * 31 + E)
@@ -57,6 +60,22 @@ def test_align_bit_exact(M, k, E, block, dist):
     d_off = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
     d_n = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkg.moe_w4a16_align_debug(d_ids, M, k, E, block, d_sorted, d_off, d_n)
+    torch.cuda.synchronize()
+    n = int(d_n.item())
+    assert n == ref_n
+    np.testing.assert_array_equal(d_sorted.cpu().numpy()[:n], ref_sorted)
+    np.testing.assert_array_equal(d_off.cpu().numpy(), ref_off)
+
+
+def test_align_small_batch_skips_out_of_range_ids():
+    # the one-warp path (at most 32 slots) flags and skips bad ids like the general one
+    ids = np.array([[3, 3, -1, 7], [12, 0, 3, 1 << 30], [5, 5, 5, 11]], dtype=np.int32)
+    ref_sorted, ref_off, ref_n = oracle.moe_align(ids, 12, 16)
+    cap = 12 + 12 * 15
+    d_sorted = torch.zeros(cap, dtype=torch.int32, device="cuda")
+    d_off = torch.zeros(13, dtype=torch.int32, device="cuda")
+    d_n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkg.moe_w4a16_align_debug(dev(ids), 3, 4, 12, 16, d_sorted, d_off, d_n)
     torch.cuda.synchronize()
     n = int(d_n.item())
     assert n == ref_n
