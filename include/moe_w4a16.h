@@ -97,10 +97,18 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
                       const float* topk_weights, uint16_t* out, int M,
                       void* workspace, size_t workspace_bytes, void* stream);
 
-/* End-to-end variant with HOST buffers (same shapes as moe_w4a16_forward):
- * copies the inputs host->device into the workspace, runs the forward, copies
- * `out` back and synchronises the stream before returning. The workspace must
- * hold moe_w4a16_workspace_size(h, M) + moe_w4a16_host_staging_size(h, M) bytes. */
+/* End-to-end variant with HOST buffers (same shapes as moe_w4a16_forward); it
+ * synchronises `stream` before returning, so the buffers may be reused at once.
+ * Batches whose hidden states take at most 1 MiB are zero-copy: when all four
+ * buffers are pinned host memory (page-locked or registered; hidden and out
+ * 16-byte aligned) the kernels read the inputs and write `out` in place over the
+ * host-device link; pageable buffers are first copied into a pinned staging block
+ * the handle allocates on first use (kept until moe_w4a16_destroy) and read from
+ * there. Larger batches are copied host->device into the workspace, and `out`
+ * back, by the copy engines. The workspace must hold
+ * moe_w4a16_workspace_size(h, M) + moe_w4a16_host_staging_size(h, M) bytes
+ * whichever route is taken. Not safe to call on one handle from two threads at
+ * once (the staging block is shared). */
 size_t moe_w4a16_host_staging_size(moe_w4a16_t h, int M);
 int moe_w4a16_forward_host(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
                            const float* topk_weights, uint16_t* out, int M,

@@ -92,14 +92,28 @@ def _ptr(t) -> int:
 def _stream(stream) -> int:
     if stream is None:
         import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:  # the current stream's handle without building a Stream object
+            return int(raw(torch.cuda.current_device()))
         return int(torch.cuda.current_stream().cuda_stream)
     return int(getattr(stream, "cuda_stream", stream))
 
 
+_DTYPES: dict = {}
+
+
+def _dtypes(names):
+    d = _DTYPES.get(names)
+    if d is None:
+        import torch
+        d = _DTYPES[names] = tuple(getattr(torch, n) for n in names if hasattr(torch, n))
+    return d
+
+
 def _need(t, dtype_names, shape, name, device=True):
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
-    if str(t.dtype).replace("torch.", "") not in dtype_names:
+    if t.dtype not in _dtypes(dtype_names):
         raise ValueError(f"{name}: dtype {t.dtype}, expected one of {dtype_names}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -198,6 +212,7 @@ class MoEW4A16:
         self.E, self.K, self.N, self.topk = E, K, N, topk
         self.handle = moe_w4a16_create(E, K, N, topk, group_size)
         self.workspace = None
+        self._ws_bytes = {}  # (M, host staging) -> workspace bytes
 
     def close(self):
         if self.handle:
@@ -220,11 +235,14 @@ class MoEW4A16:
         moe_w4a16_pack(self.handle, w1_q, w1_s, w2_q, w2_s, stream)
 
     def ensure_workspace(self, M: int, host_staging: bool = False):
-        import torch
-        need = moe_w4a16_workspace_size(self.handle, M)
-        if host_staging:
-            need += moe_w4a16_host_staging_size(self.handle, M)
+        need = self._ws_bytes.get((M, host_staging))
+        if need is None:
+            need = moe_w4a16_workspace_size(self.handle, M)
+            if host_staging:
+                need += moe_w4a16_host_staging_size(self.handle, M)
+            self._ws_bytes[(M, host_staging)] = need
         if self.workspace is None or self.workspace.numel() < need:
+            import torch
             self.workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
         return self.workspace
 

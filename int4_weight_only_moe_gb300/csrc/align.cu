@@ -250,12 +250,17 @@ __global__ void __launch_bounds__(32) align_small_kernel(const AlignArgs a) {
   pdl_launch_dependents();
 }
 
+cudaError_t align_set_attributes(int E) {
+  (void)E;
+  // the limit covers every expert count a handle may have, so it is set once and
+  // never again inside a forward (which may be under stream capture)
+  return cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(33 * kMaxExperts * sizeof(int)));
+}
+
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl) {
   if (a.MK <= 32) return launch_k(align_small_kernel, dim3(1), dim3(32), 0, stream, pdl, a);
   const size_t smem = (33 * static_cast<size_t>(a.E)) * sizeof(int);
-  cudaError_t err = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
   return launch_k(align_kernel, dim3(1), dim3(1024), smem, stream, pdl, a);
 }
 

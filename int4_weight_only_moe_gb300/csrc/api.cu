@@ -23,6 +23,9 @@ struct moe_w4a16_ctx {
   bool packed;
   cudaEvent_t ev[6];
   bool ev_valid;
+  // pinned staging of small host-buffer forwards whose buffers are pageable
+  uint8_t* hstage;
+  size_t hstage_bytes;
 };
 
 namespace {
@@ -42,6 +45,23 @@ int fail(int code, const std::string& msg) {
   } while (0)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Host-buffer forwards whose hidden states are at most this large let the kernels
+// read the inputs and write the output in host memory over the host-device link
+// (zero-copy); larger ones move them with the copy engines, which stream large
+// transfers faster than the gather and finalize kernels' loads and stores would.
+constexpr size_t kZeroCopyMaxBytes = 1u << 20;
+
+// Device address of a pinned (page-locked or registered) host buffer, or null if
+// `p` is pageable memory the device cannot address.
+const void* pinned_device_pointer(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
 
 struct WsLayout {
   size_t hdr, tickets, sorted, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
@@ -126,6 +146,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = gemm_set_attributes();
+  if (e == cudaSuccess) e = align_set_attributes(E);
   if (e != cudaSuccess) {
     delete h;
     return fail(MOE_W4A16_CUDA_ERROR, std::string("device setup: ") + cudaGetErrorString(e));
@@ -150,6 +171,7 @@ int moe_w4a16_destroy(moe_w4a16_t h) {
   cudaDeviceSynchronize();
   cudaFree(h->w1p);
   cudaFree(h->w2p);
+  if (h->hstage) cudaFreeHost(h->hstage);
   if (h->ev_valid)
     for (auto& ev : h->ev) cudaEventDestroy(ev);
   delete h;
@@ -371,12 +393,57 @@ int moe_w4a16_forward_host(moe_w4a16_t h, const uint16_t* hidden, const int32_t*
     return fail(MOE_W4A16_WORKSPACE_TOO_SMALL,
                 "workspace too small: need " + std::to_string(need + stage) + " bytes");
   auto s = static_cast<cudaStream_t>(stream);
+  // device staging after the workspace (batches moved by the copy engines):
+  // [hidden | ids | weights | out]
   uint8_t* st = static_cast<uint8_t*>(workspace) + need;
   const size_t xb = static_cast<size_t>(M) * h->K * 2, rb = static_cast<size_t>(M) * h->topk * 4;
+  const size_t xa = align_up(xb, 256), ra = align_up(rb, 256), in_bytes = xa + 2 * ra;
   uint16_t* d_x = reinterpret_cast<uint16_t*>(st);
-  uint16_t* d_out = reinterpret_cast<uint16_t*>(st + align_up(xb, 256));
-  int32_t* d_ids = reinterpret_cast<int32_t*>(st + 2 * align_up(xb, 256));
-  float* d_w = reinterpret_cast<float*>(st + 2 * align_up(xb, 256) + align_up(rb, 256));
+  int32_t* d_ids = reinterpret_cast<int32_t*>(st + xa);
+  float* d_w = reinterpret_cast<float*>(st + xa + ra);
+  uint16_t* d_out = reinterpret_cast<uint16_t*>(st + in_bytes);
+
+  // Small batches: zero-copy. The kernels read the inputs from, and the finalize
+  // kernel writes the output to, pinned host memory: the caller's buffers when
+  // they are pinned, else the handle's pinned staging block. This spares the copy
+  // engines' per-transfer latency, which at decode sizes exceeds the transfer.
+  if (xb <= kZeroCopyMaxBytes) {
+    const void* px = pinned_device_pointer(hidden);
+    const void* pi = px ? pinned_device_pointer(topk_ids) : nullptr;
+    const void* pw = pi ? pinned_device_pointer(topk_weights) : nullptr;
+    const void* po = pw ? pinned_device_pointer(out) : nullptr;
+    if (po && ((reinterpret_cast<uintptr_t>(px) | reinterpret_cast<uintptr_t>(po)) % 16) == 0) {
+      if (int rc = moe_w4a16_forward(h, static_cast<const uint16_t*>(px), static_cast<const int32_t*>(pi),
+                                     static_cast<const float*>(pw), static_cast<uint16_t*>(const_cast<void*>(po)),
+                                     M, workspace, need, stream))
+        return rc;
+      MOE_CUDA_TRY(cudaStreamSynchronize(s));
+      return MOE_W4A16_OK;
+    }
+    // pageable buffers: [hidden | ids | weights | out] in the pinned staging block
+    if (h->hstage_bytes < in_bytes + xa) {
+      if (h->hstage) cudaFreeHost(h->hstage);
+      h->hstage = nullptr;
+      h->hstage_bytes = 0;
+      MOE_CUDA_TRY(cudaHostAlloc(reinterpret_cast<void**>(&h->hstage), in_bytes + xa, cudaHostAllocMapped));
+      h->hstage_bytes = in_bytes + xa;
+    }
+    uint8_t* hs = h->hstage;
+    void* dev = nullptr;
+    MOE_CUDA_TRY(cudaHostGetDevicePointer(&dev, hs, 0));
+    uint8_t* ds = static_cast<uint8_t*>(dev);
+    std::memcpy(hs, hidden, xb);
+    std::memcpy(hs + xa, topk_ids, rb);
+    std::memcpy(hs + xa + ra, topk_weights, rb);
+    if (int rc = moe_w4a16_forward(h, reinterpret_cast<const uint16_t*>(ds), reinterpret_cast<const int32_t*>(ds + xa),
+                                   reinterpret_cast<const float*>(ds + xa + ra),
+                                   reinterpret_cast<uint16_t*>(ds + in_bytes), M, workspace, need, stream))
+      return rc;
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    std::memcpy(out, hs + in_bytes, xb);
+    return MOE_W4A16_OK;
+  }
+
   MOE_CUDA_TRY(cudaMemcpyAsync(d_x, hidden, xb, cudaMemcpyHostToDevice, s));
   MOE_CUDA_TRY(cudaMemcpyAsync(d_ids, topk_ids, rb, cudaMemcpyHostToDevice, s));
   MOE_CUDA_TRY(cudaMemcpyAsync(d_w, topk_weights, rb, cudaMemcpyHostToDevice, s));
@@ -429,6 +496,7 @@ int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int b
   aa.sorted_ids = sorted_ids;
   aa.expert_offsets = expert_offsets;
   aa.num_padded_out = num_padded;
+  MOE_CUDA_TRY(align_set_attributes(E));
   MOE_CUDA_TRY(launch_align(aa, static_cast<cudaStream_t>(stream), false));
   return MOE_W4A16_OK;
 }

@@ -34,6 +34,9 @@ struct AlignArgs {
   int32_t* dbg;
 };
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl);
+// At handle creation: the general align kernel's dynamic shared memory limit,
+// sized for the largest expert count.
+cudaError_t align_set_attributes(int E);
 
 // Expert-sorted, blocked copy of the hidden states; also zeroes the fp32 accumulator.
 struct GatherArgs {
