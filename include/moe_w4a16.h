@@ -92,7 +92,9 @@ size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M);
  *   topk_weights fp32  [M, topk]
  *   out          bf16  [M, K]      written completely (rounded to nearest even)
  *   workspace    >= moe_w4a16_workspace_size(h, M) bytes, 256-byte aligned
- * M == 0 is a no-op. Launches 5 kernels on `stream`, allocates nothing. */
+ * M == 0 is a no-op. Launches 5 kernels on `stream` (4 when M * topk <= 32),
+ * allocates nothing and makes no host-synchronising call, so it may be captured
+ * into a CUDA graph and replayed with new inputs in the same buffers. */
 int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
                       const float* topk_weights, uint16_t* out, int M,
                       void* workspace, size_t workspace_bytes, void* stream);

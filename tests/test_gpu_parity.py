@@ -268,6 +268,40 @@ def test_forward_host_zero_copy_and_staged_paths():
     prob.close()
 
 
+@pytest.mark.parametrize("M", [1, 37])
+def test_forward_replays_from_a_cuda_graph(M):
+    # the forward allocates nothing and makes no host-synchronising call, so it can
+    # be captured once and replayed on new inputs copied into the same buffers
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    steps = [inputs.workload_inputs(wl, step=s) for s in range(3)]
+    static = [dev(bits16(steps[0][0])), dev(steps[0][1]), dev(steps[0][2])]
+    out = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    prob.moe.ensure_workspace(M)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        prob.moe.forward(*static, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        prob.moe.forward(*static, out=out)
+    for s, (hidden, ids, wts) in enumerate(steps[1:] + steps[:1]):
+        for dst, src in zip(static, (dev(bits16(hidden)), dev(ids), dev(wts))):
+            dst.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        got = bf16_tensor_to_f64(out)
+        assert prob.moe.status() == 0
+        assert_within_one_ulp(got, prob.run(hidden, ids, wts))
+        if s == 0:
+            assert_close(got, prob.reference(hidden, ids, wts), f"graph replay M={M}")
+    del g
+    prob.close()
+
+
 def test_repeated_calls_agree():
     E, K, N, k, M = 16, 512, 256, 4, 64
     prob = Problem(E, K, N, k)
