@@ -15,6 +15,7 @@ struct moe_w4a16_ctx {
   int device;
   int num_sms;
   int num_ctas;
+  int step_cost;  // extra stream-K cost per row group of a token tile (0: even split)
   bool pdl;
   bool profile;
   uint8_t* w1p;
@@ -52,6 +53,10 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // transfers faster than the gather and finalize kernels' loads and stores would.
 constexpr size_t kZeroCopyMaxBytes = 1u << 20;
 
+// Default extra stream-K cost of a pipeline step per row group of its token tile
+// beyond the first, in eighths of a one-group step (measured on GB300).
+constexpr int kDefaultStepCost = 2;
+
 // Device address of a pinned (page-locked or registered) host buffer, or null if
 // `p` is pageable memory the device cannot address.
 const void* pinned_device_pointer(const void* p) {
@@ -64,7 +69,7 @@ const void* pinned_device_pointer(const void* p) {
 }
 
 struct WsLayout {
-  size_t hdr, tickets, sorted, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
+  size_t hdr, tickets, sched, sorted, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
   int Pcap, Gcap;
 };
 
@@ -84,6 +89,8 @@ WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   off = align_up(off, 256);
   L.tickets = off;
   off = align_up(off + kMaxCtas * sizeof(int32_t), 256);
+  L.sched = off;  // stream-K boundaries of the two GEMMs
+  off = align_up(off + 2 * (kMaxCtas + 1) * sizeof(long long), 256);
   L.sorted = off;
   off = align_up(off + static_cast<size_t>(L.Pcap) * sizeof(int32_t), 256);
   L.tiles = off;
@@ -143,6 +150,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->topk = topk;
   h->group = group_size;
   h->pdl = true;
+  h->step_cost = kDefaultStepCost;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = gemm_set_attributes();
@@ -233,6 +241,10 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
     case MOE_W4A16_OPT_PDL:
       h->pdl = value != 0;
       return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_STEP_COST:
+      if (value < 0 || value > 64) return fail(MOE_W4A16_INVALID_ARG, "step cost must be in [0, 64]");
+      h->step_cost = value;
+      return MOE_W4A16_OK;
     default:
       return fail(MOE_W4A16_INVALID_ARG, "unknown option");
   }
@@ -296,6 +308,14 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   aa.sorted_cap = L.Pcap;
   aa.tiles_cap = L.Gcap;
   aa.dbg = hdr + 8;
+  long long* sched = reinterpret_cast<long long*>(ws + L.sched);
+  aa.sched = sched;
+  aa.sched_ctas = h->num_ctas;
+  aa.sched_R[0] = 2 * h->N / kBM;
+  aa.sched_KBn[0] = h->K / (2 * kBK);
+  aa.sched_R[1] = h->K / kBM;
+  aa.sched_KBn[1] = h->N / (2 * kBK);
+  aa.step_cost_per_group = h->step_cost;
 
   GatherArgs ga{};
   ga.x = hidden;
@@ -345,6 +365,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g1.tiles_cap = L.Gcap;
   g1.E = h->E;
   g1.dbg = hdr + 8;
+  g1.sched = sched;
   MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
@@ -371,6 +392,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g2.tiles_cap = L.Gcap;
   g2.E = h->E;
   g2.dbg = hdr + 8;
+  g2.sched = sched + (h->num_ctas + 1);
   MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 

@@ -137,7 +137,8 @@ constexpr int kNumBars = kBarDrain + 2;
 constexpr int kSmMisc = kSmBar + kNumBars * 8;
 constexpr int kMaxSegs = 512;            // units decoded into shared memory up front
 constexpr int kSmSeg = kSmMisc + 64;
-constexpr int kSmBytes = kSmSeg + kMaxSegs * 16;
+constexpr int kSmSched = kSmSeg + kMaxSegs * 16;  // [kMaxCtas + 1] stream-K boundaries
+constexpr int kSmBytes = kSmSched + (kMaxCtas + 1) * 8 + 8;
 constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
 static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
@@ -180,13 +181,25 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 struct Sched {
-  long long W;  // total steps
-  int G;        // CTAs
+  long long W;           // total steps
+  int G;                 // CTAs
+  const long long* tab;  // [G + 1] cost-weighted first steps (shared memory), or null: even split
   __device__ __forceinline__ long long start(int c) const {
-    return static_cast<long long>(c) * W / G;
+    return tab ? tab[c] : static_cast<long long>(c) * W / G;
   }
   // CTA whose share contains step g.
   __device__ int cta_of(long long g) const {
+    if (tab) {  // the last CTA whose share starts at or before g
+      int lo = 0, hi = G - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab[mid] <= g)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      return lo;
+    }
     int c = static_cast<int>((g * G) / (W > 0 ? W : 1));
     if (c > G - 1) c = G - 1;
     while (c + 1 < G && start(c + 1) <= g) ++c;
@@ -385,8 +398,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   pdl_wait();
   if (threadIdx.x == 0) TRACE_POINT(13, 1);
   const int num_tiles = a.hdr[kHdrNumTiles];
-  const Sched sc{static_cast<long long>(num_tiles) * a.R * a.KBn, static_cast<int>(gridDim.x)};
-  const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
+  // cost-weighted boundaries when the align kernel wrote them (loaded alongside the
+  // header; ignored otherwise), else an even split of the steps
+  const bool weighted = a.sched != nullptr && a.hdr[kHdrSched] == 1;
+  const long long wb0 = a.sched ? a.sched[blockIdx.x] : 0, wb1 = a.sched ? a.sched[blockIdx.x + 1] : 0;
+  long long* sched_sm = reinterpret_cast<long long*>(gbase + kSmSched);
+  const Sched sc{static_cast<long long>(num_tiles) * a.R * a.KBn, static_cast<int>(gridDim.x),
+                 weighted ? sched_sm : nullptr};
+  long long my_begin, my_end;
+  if (weighted) {  // clamped: a malformed table can misbalance, never overrun
+    my_begin = wb0 < 0 ? 0 : (wb0 > sc.W ? sc.W : wb0);
+    my_end = wb1 < my_begin ? my_begin : (wb1 > sc.W ? sc.W : wb1);
+  } else {
+    my_begin = sc.start(blockIdx.x);
+    my_end = sc.start(blockIdx.x + 1);
+  }
   int* status = a.status;
   pdl_launch_dependents();
 
@@ -397,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   const int n_tab = static_cast<int>(n_units < kMaxSegs ? n_units : kMaxSegs);
   for (int i = threadIdx.x; i < n_tab; i += blockDim.x)
     seg_tab[i] = decode_unit(u_first + i, a.R, a.tiles, a.expert_tiles);
+  if (weighted)
+    for (int i = threadIdx.x; i <= static_cast<int>(gridDim.x); i += blockDim.x) sched_sm[i] = a.sched[i];
   __syncthreads();
   const SegTable segs{seg_tab, u_first, n_tab, a.R, a.tiles, a.expert_tiles};
 

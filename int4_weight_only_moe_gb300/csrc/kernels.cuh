@@ -32,6 +32,13 @@ struct AlignArgs {
   int32_t* num_padded_out;  // optional extra copy of num_padded
   int sorted_cap, tiles_cap;  // extents for the self-checking build
   int32_t* dbg;
+  // cost-weighted stream-K boundaries (general path; null: not computed):
+  // sched[w * (sched_ctas + 1) + c] = first step of CTA c in GEMM w (0 gate/up,
+  // 1 down), whose units are (row tiles sched_R[w]) x (steps sched_KBn[w])
+  long long* sched;
+  int sched_ctas;
+  int sched_R[2], sched_KBn[2];
+  int step_cost_per_group;
 };
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl);
 // At handle creation: the general align kernel's dynamic shared memory limit,
@@ -81,6 +88,7 @@ struct GemmArgs {
   long long wpack_bytes, bsrc_bytes, hout_bytes, acc_elems, scratch_elems;
   int sorted_cap, tiles_cap, E;
   int32_t* dbg;  // first failed check: site, values, block, thread
+  const long long* sched;  // [gridDim.x + 1] weighted boundaries, used when hdr[kHdrSched] == 1
 };
 cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);

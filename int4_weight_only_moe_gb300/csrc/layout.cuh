@@ -56,6 +56,18 @@ struct TokenTile {
 };
 
 // Header words at the start of the workspace.
-enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrWords = 64 };
+// kHdrSched: 1 when the align kernel wrote cost-weighted stream-K boundaries for
+// both GEMMs (the general path), 0 for an even split of the steps.
+enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrSched = 3, kHdrWords = 64 };
+
+// Relative cost of one pipeline step of a unit whose token tile holds ng row
+// groups: a base of 8 plus `per_group` for every row group beyond the second. The
+// weight stream (9 KB a step from HBM) and its conversion are the same for every
+// tile; the activation copy from L2 is 4 KB per row group a step, which costs
+// nothing extra while the weight stream sets the pace and starts to, alongside
+// the larger MMAs and epilogue, at three and four row groups.
+__host__ __device__ __forceinline__ int step_cost(int ng, int per_group) {
+  return 8 + per_group * (ng > 2 ? ng - 2 : 0);
+}
 
 }  // namespace moe

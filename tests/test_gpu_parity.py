@@ -186,6 +186,26 @@ def test_hot_expert_spans_several_token_tiles():
     prob.close()
 
 
+@pytest.mark.parametrize("step_cost", [0, 1, 8, 64])
+@pytest.mark.parametrize("num_ctas", [None, 5, 256])
+def test_cost_weighted_stream_k_shares(step_cost, num_ctas):
+    # Zipf-skewed routing gives token tiles of 1 to 4 row groups; the align kernel
+    # then splits each GEMM's steps by cost, not by count (0 = even split). Every
+    # split must give the oracle's result. (Two splits are not compared with each
+    # other bit for bit: where a gate/up unit is cut moves the fp32 partial sums,
+    # and a one-unit change in the bf16 intermediate carries into the output.)
+    E, K, N, k, M = 16, 512, 256, 4, 300
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    rng = np.random.default_rng(11)
+    ids = zipf_ids(rng, M, E, k, s=1.6)
+    hidden = inputs.hidden_states(M, K)
+    wts = rng.uniform(0.1, 1.0, size=(M, k)).astype(np.float32)
+    wts /= wts.sum(axis=1, keepdims=True)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_STEP_COST, step_cost)
+    check_forward(prob, hidden, ids, wts, f"step cost {step_cost} ctas {num_ctas}")
+    prob.close()
+
+
 def test_bad_expert_ids_are_skipped_and_flagged():
     wl = inputs.WORKLOADS["tiny"]
     prob = Problem(wl.E, wl.K, wl.N, wl.topk)
