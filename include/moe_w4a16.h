@@ -129,12 +129,13 @@ const char* moe_w4a16_last_error(void);
  *                            (read with moe_w4a16_kernel_times; perturbs overlap)
  *   MOE_W4A16_OPT_PDL        1 = launch dependent kernels with programmatic
  *                            dependent launch (default 1)
- *   MOE_W4A16_OPT_STEP_COST  stream-K balance of the GEMMs (batches with
- *                            M * topk > 32): a pipeline step whose token tile has
+ *   MOE_W4A16_OPT_STEP_COST_GATEUP, MOE_W4A16_OPT_STEP_COST_DOWN
+ *                            stream-K balance of each GEMM for batches with
+ *                            M * topk > 32: a pipeline step whose token tile has
  *                            ng row groups of 16 counts as 8 + value * max(0, ng - 2);
  *                            0 = split the steps evenly (range 0..64) */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
-       MOE_W4A16_OPT_STEP_COST = 4 };
+       MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5 };
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order

@@ -25,7 +25,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libm
 
 OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR, NOT_PACKED = 0, -1, -2, -3, -4, -5
 STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT = 1, 2
-OPT_NUM_CTAS, OPT_PROFILE, OPT_PDL, OPT_STEP_COST = 1, 2, 3, 4
+OPT_NUM_CTAS, OPT_PROFILE, OPT_PDL = 1, 2, 3
+OPT_STEP_COST_GATEUP, OPT_STEP_COST_DOWN = 4, 5
 NOALLOC_WORKSPACE_BYTES = 48 << 20
 
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p

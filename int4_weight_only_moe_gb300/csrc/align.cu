@@ -139,71 +139,75 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
     if (a.num_padded_out) *a.num_padded_out = tot_pad;
   }
 
-  // Cost-weighted stream-K boundaries for the two GEMMs. Each GEMM's steps run in
-  // unit order [expert][row tile][token tile of the expert]; a step of a unit whose
-  // token tile has ng row groups costs step_cost(ng). CTA c starts at the first
-  // step where the cost so far reaches c/G of the total, so CTAs that draw a hot
-  // expert's full 64-row tiles get fewer steps than those that draw 16-row ones.
-  if (a.sched != nullptr && a.bn_max > 0 && a.step_cost_per_group > 0) {
-    __syncthreads();  // the per-warp histograms are no longer read: reuse them
+  // Cost-weighted stream-K boundaries, per GEMM. Each GEMM's steps run in unit
+  // order [expert][row tile][token tile of the expert]; a step of a unit whose
+  // token tile has ng row groups costs step_cost(ng, c) with that GEMM's c. CTA j
+  // starts at the first step where the cost so far reaches j/G of the total, so
+  // CTAs that draw a hot expert's full 64-row tiles get fewer steps. A GEMM with
+  // c = 0 keeps the even split (its header bit stays clear).
+  if (a.sched != nullptr && a.bn_max > 0) {
     long long* Pe = reinterpret_cast<long long*>(hist);  // [E + 1] cost before expert e's tiles
     int* fe = reinterpret_cast<int*>(Pe + E + 1);        // [E] first tile
     int* tee = fe + E;                                   // [E] tiles
     int* cle = tee + E;                                  // [E] step cost of the last tile
-    const int cpg = a.step_cost_per_group;
-    const int cfull = step_cost(a.bn_max / kRowGroup, cpg);
-    int my_cost = 0, c_last = 0;
-    if (tid < E && my_tiles > 0) {
-      c_last = step_cost((my_pad - (my_tiles - 1) * a.bn_max) / kRowGroup, cpg);
-      my_cost = (my_tiles - 1) * cfull + c_last;
-    }
-    int tot_cost = 0;
-    const int before = block_exclusive_scan(my_cost, warp_tmp, &tot_cost);
-    if (tid < E) {
-      Pe[tid] = before;
-      fe[tid] = tstart;
-      tee[tid] = my_tiles;
-      cle[tid] = c_last;
-    }
-    if (tid == 0) Pe[E] = tot_cost;
-    __syncthreads();
     const int G = a.sched_ctas;
-    for (int i = tid; i < 2 * (G + 1); i += blockDim.x) {
-      const int w = i / (G + 1), c = i - w * (G + 1);
+    int bits = 0;
+    for (int w = 0; w < 2; ++w) {
+      const int cpg = a.step_cost_per_group[w];
+      if (cpg <= 0) continue;  // uniform across the block
+      bits |= 1 << w;
+      __syncthreads();  // the histograms, or the previous GEMM's costs, are no longer read
+      const int cfull = step_cost(a.bn_max / kRowGroup, cpg);
+      int my_cost = 0, c_last = 0;
+      if (tid < E && my_tiles > 0) {
+        c_last = step_cost((my_pad - (my_tiles - 1) * a.bn_max) / kRowGroup, cpg);
+        my_cost = (my_tiles - 1) * cfull + c_last;
+      }
+      int tot_cost = 0;
+      const int before = block_exclusive_scan(my_cost, warp_tmp, &tot_cost);
+      if (tid < E) {
+        Pe[tid] = before;
+        fe[tid] = tstart;
+        tee[tid] = my_tiles;
+        cle[tid] = c_last;
+      }
+      if (tid == 0) Pe[E] = tot_cost;
+      __syncthreads();
       const long long R = a.sched_R[w], KB = a.sched_KBn[w];
       const long long W = static_cast<long long>(tot_tiles) * R * KB;
-      long long g = 0;
-      if (c == G) {
-        g = W;
-      } else if (tot_cost > 0) {
-        const long long T = static_cast<long long>(c) * tot_cost * R * KB / G;
-        int lo = 0, hi = E - 1;  // the last expert whose tiles start at cost <= T
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (KB * R * Pe[mid] <= T)
-            lo = mid;
-          else
-            hi = mid - 1;
+      for (int c = tid; c <= G; c += blockDim.x) {
+        long long g = 0;
+        if (c == G) {
+          g = W;
+        } else if (tot_cost > 0) {
+          const long long T = static_cast<long long>(c) * tot_cost * R * KB / G;
+          int lo = 0, hi = E - 1;  // the last expert whose tiles start at cost <= T
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (KB * R * Pe[mid] <= T)
+              lo = mid;
+            else
+              hi = mid - 1;
+          }
+          const int e = lo;
+          const long long T1 = T - KB * R * Pe[e];
+          const long long Ce = Pe[e + 1] - Pe[e];  // > 0: T lies inside expert e's units
+          const long long rt = T1 / (KB * Ce);
+          const long long T2 = T1 - rt * KB * Ce;
+          const int te = tee[e];
+          long long tt = T2 / (KB * cfull);  // every tile but the last is full
+          if (tt > te - 1) tt = te - 1;
+          const long long T3 = T2 - tt * KB * cfull;
+          const long long ct = (tt == te - 1) ? cle[e] : cfull;
+          long long kb = (T3 + ct - 1) / ct;
+          if (kb > KB) kb = KB;
+          g = (R * fe[e] + rt * te + tt) * KB + kb;
+          if (g > W) g = W;
         }
-        const int e = lo;
-        const long long T1 = T - KB * R * Pe[e];
-        const long long Ce = Pe[e + 1] - Pe[e];  // > 0: T lies inside expert e's units
-        const long long rt = T1 / (KB * Ce);
-        const long long T2 = T1 - rt * KB * Ce;
-        const int te = tee[e];
-        long long tt = T2 / (KB * cfull);  // every tile but the last is full
-        if (tt > te - 1) tt = te - 1;
-        const long long T3 = T2 - tt * KB * cfull;
-        const long long ct = (tt == te - 1) ? cle[e] : cfull;
-        long long kb = (T3 + ct - 1) / ct;
-        if (kb > KB) kb = KB;
-        g = (R * fe[e] + rt * te + tt) * KB + kb;
-        if (g > W) g = W;
+        a.sched[w * (G + 1) + c] = g;
       }
-      a.sched[i] = g;
     }
-    __syncthreads();
-    if (tid == 0 && a.hdr) a.hdr[kHdrSched] = 1;
+    if (tid == 0 && a.hdr) a.hdr[kHdrSched] = bits;
   }
   pdl_launch_dependents();
 }

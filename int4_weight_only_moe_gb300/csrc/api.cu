@@ -15,7 +15,7 @@ struct moe_w4a16_ctx {
   int device;
   int num_sms;
   int num_ctas;
-  int step_cost;  // extra stream-K cost per row group of a token tile (0: even split)
+  int step_cost[2];  // per GEMM (gate/up, down): stream-K cost per row group beyond two (0: even split)
   bool pdl;
   bool profile;
   uint8_t* w1p;
@@ -53,9 +53,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // transfers faster than the gather and finalize kernels' loads and stores would.
 constexpr size_t kZeroCopyMaxBytes = 1u << 20;
 
-// Default extra stream-K cost of a pipeline step per row group of its token tile
-// beyond the first, in eighths of a one-group step (measured on GB300).
-constexpr int kDefaultStepCost = 2;
+// Default stream-K cost of a pipeline step per row group of its token tile beyond
+// the second, in eighths of a one-group step, per GEMM. Measured on GB300 with
+// Zipf-routed M = 1024 (hot experts in full 64-row tiles): weighting the down
+// GEMM by 2 took the forward from 2,923 to 2,653 us; weighting the gate/up GEMM,
+// or the down GEMM by more, was slower; other batch sizes do not change.
+constexpr int kDefaultStepCostGateUp = 0;
+constexpr int kDefaultStepCostDown = 2;
 
 // Device address of a pinned (page-locked or registered) host buffer, or null if
 // `p` is pageable memory the device cannot address.
@@ -150,7 +154,8 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->topk = topk;
   h->group = group_size;
   h->pdl = true;
-  h->step_cost = kDefaultStepCost;
+  h->step_cost[0] = kDefaultStepCostGateUp;
+  h->step_cost[1] = kDefaultStepCostDown;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = gemm_set_attributes();
@@ -241,9 +246,10 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
     case MOE_W4A16_OPT_PDL:
       h->pdl = value != 0;
       return MOE_W4A16_OK;
-    case MOE_W4A16_OPT_STEP_COST:
+    case MOE_W4A16_OPT_STEP_COST_GATEUP:
+    case MOE_W4A16_OPT_STEP_COST_DOWN:
       if (value < 0 || value > 64) return fail(MOE_W4A16_INVALID_ARG, "step cost must be in [0, 64]");
-      h->step_cost = value;
+      h->step_cost[option == MOE_W4A16_OPT_STEP_COST_DOWN ? 1 : 0] = value;
       return MOE_W4A16_OK;
     default:
       return fail(MOE_W4A16_INVALID_ARG, "unknown option");
@@ -308,14 +314,19 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   aa.sorted_cap = L.Pcap;
   aa.tiles_cap = L.Gcap;
   aa.dbg = hdr + 8;
-  long long* sched = reinterpret_cast<long long*>(ws + L.sched);
+  // weighted stream-K boundaries: written by the general align kernel only, so
+  // small batches pass no table and their GEMMs skip the lookup altogether
+  long long* sched = (MK <= 32 || (h->step_cost[0] == 0 && h->step_cost[1] == 0))
+                         ? nullptr
+                         : reinterpret_cast<long long*>(ws + L.sched);
   aa.sched = sched;
   aa.sched_ctas = h->num_ctas;
   aa.sched_R[0] = 2 * h->N / kBM;
   aa.sched_KBn[0] = h->K / (2 * kBK);
   aa.sched_R[1] = h->K / kBM;
   aa.sched_KBn[1] = h->N / (2 * kBK);
-  aa.step_cost_per_group = h->step_cost;
+  aa.step_cost_per_group[0] = h->step_cost[0];
+  aa.step_cost_per_group[1] = h->step_cost[1];
 
   GatherArgs ga{};
   ga.x = hidden;
@@ -365,7 +376,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g1.tiles_cap = L.Gcap;
   g1.E = h->E;
   g1.dbg = hdr + 8;
-  g1.sched = sched;
+  g1.sched = (sched && h->step_cost[0] > 0) ? sched : nullptr;
   MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
@@ -392,7 +403,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g2.tiles_cap = L.Gcap;
   g2.E = h->E;
   g2.dbg = hdr + 8;
-  g2.sched = sched + (h->num_ctas + 1);
+  g2.sched = (sched && h->step_cost[1] > 0) ? sched + (h->num_ctas + 1) : nullptr;
   MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 

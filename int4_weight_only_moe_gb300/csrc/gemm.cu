@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   const int num_tiles = a.hdr[kHdrNumTiles];
   // cost-weighted boundaries when the align kernel wrote them (loaded alongside the
   // header; ignored otherwise), else an even split of the steps
-  const bool weighted = a.sched != nullptr && a.hdr[kHdrSched] == 1;
+  const bool weighted = a.sched != nullptr && ((a.hdr[kHdrSched] >> (kMode - 1)) & 1) != 0;
   const long long wb0 = a.sched ? a.sched[blockIdx.x] : 0, wb1 = a.sched ? a.sched[blockIdx.x + 1] : 0;
   long long* sched_sm = reinterpret_cast<long long*>(gbase + kSmSched);
   const Sched sc{static_cast<long long>(num_tiles) * a.R * a.KBn, static_cast<int>(gridDim.x),

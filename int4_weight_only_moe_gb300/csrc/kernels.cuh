@@ -38,7 +38,7 @@ struct AlignArgs {
   long long* sched;
   int sched_ctas;
   int sched_R[2], sched_KBn[2];
-  int step_cost_per_group;
+  int step_cost_per_group[2];  // per GEMM; 0 = even split for that GEMM
 };
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl);
 // At handle creation: the general align kernel's dynamic shared memory limit,
@@ -88,7 +88,8 @@ struct GemmArgs {
   long long wpack_bytes, bsrc_bytes, hout_bytes, acc_elems, scratch_elems;
   int sorted_cap, tiles_cap, E;
   int32_t* dbg;  // first failed check: site, values, block, thread
-  const long long* sched;  // [gridDim.x + 1] weighted boundaries, used when hdr[kHdrSched] == 1
+  const long long* sched;  // [gridDim.x + 1] weighted boundaries, used when this GEMM's
+                           // bit of hdr[kHdrSched] is set (bit 0 gate/up, bit 1 down)
 };
 cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);

@@ -56,8 +56,9 @@ struct TokenTile {
 };
 
 // Header words at the start of the workspace.
-// kHdrSched: 1 when the align kernel wrote cost-weighted stream-K boundaries for
-// both GEMMs (the general path), 0 for an even split of the steps.
+// kHdrSched: bit w set when the align kernel wrote cost-weighted stream-K
+// boundaries for GEMM w (0 gate/up, 1 down; the general path only), clear for an
+// even split of that GEMM's steps.
 enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrSched = 3, kHdrWords = 64 };
 
 // Relative cost of one pipeline step of a unit whose token tile holds ng row

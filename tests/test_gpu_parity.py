@@ -201,7 +201,8 @@ def test_cost_weighted_stream_k_shares(step_cost, num_ctas):
     hidden = inputs.hidden_states(M, K)
     wts = rng.uniform(0.1, 1.0, size=(M, k)).astype(np.float32)
     wts /= wts.sum(axis=1, keepdims=True)
-    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_STEP_COST, step_cost)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_STEP_COST_GATEUP, step_cost)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_STEP_COST_DOWN, (step_cost * 3) % 65)
     check_forward(prob, hidden, ids, wts, f"step cost {step_cost} ctas {num_ctas}")
     prob.close()
 
