@@ -15,15 +15,17 @@ Formats produced (the GPTQ-style "logical" input format that the repack step of
   32 consecutive reduction elements.
 * ``w2_q``  int32 ``[E, N/8, K]`` and ``w2_s`` uint16 ``[E, N/32, K]``: the down
   projection, reduction axis N.
-* ``hidden`` uint16 (bf16) ``[M, K]``; ``topk_ids`` int32 ``[M, k]``;
-  ``topk_weights`` float32 ``[M, k]``.
+* ``hidden`` uint16 (bf16) ``[M, K]``; router ``logits`` float32 ``[M, E]``.
+  (Turning logits into ``topk_ids`` / ``topk_weights`` is the router, a step of
+  the method: the library's router kernel does it on the device, the oracle's
+  ``route`` on the host; nothing here does.)
 
 Every random 32-bit word is uniform, so all eight codes of a word are uniform
 on ``0..15`` (stored value ``u``; the symmetric code is ``u - 8`` in ``[-8, 7]``).
 Scales are uniform on ``[0.005, 0.02]`` rounded to bf16, hidden states are
 standard normal rounded to bf16, and router logits follow the workload recipe
-(normal, uniform, or Zipf-skewed expert popularity with Gumbel noise). Routing
-picks the k largest logits per token and renormalises the softmax over them.
+(normal, uniform, or Zipf-skewed expert popularity with Gumbel noise), rounded to
+float32.
 
 Expert weights are drawn from a per-expert stream, so a caller that needs only
 a few experts (a sampled oracle check at full size) regenerates just those.
@@ -120,7 +122,11 @@ def hidden_states(M: int, K: int, seed: int = HIDDEN_SEED, step: int = 0) -> np.
 
 def router_logits(M: int, E: int, routing: str, seed: int = ROUTING_SEED,
                   step: int = 0, zipf_s: float = 1.1) -> np.ndarray:
-    """Router logits ``[M, E]`` (float64) following the workload's recipe."""
+    """Router logits ``[M, E]`` (float32) following the workload's recipe."""
+    return _router_logits64(M, E, routing, seed, step, zipf_s).astype(np.float32)
+
+
+def _router_logits64(M, E, routing, seed, step, zipf_s):
     g = _rng(seed, 11, step)
     if routing == "normal":
         return g.standard_normal((M, E))
@@ -138,27 +144,10 @@ def router_logits(M: int, E: int, routing: str, seed: int = ROUTING_SEED,
     raise ValueError(f"unknown routing recipe {routing!r}")
 
 
-def route(logits: np.ndarray, topk: int):
-    """Top-k expert ids (int32, descending logit) and renormalised softmax weights (float32)."""
-    M, E = logits.shape
-    ids = np.argsort(-logits, axis=1, kind="stable")[:, :topk]
-    sel = np.take_along_axis(logits, ids, axis=1)
-    w = np.exp(sel - sel.max(axis=1, keepdims=True))
-    w /= w.sum(axis=1, keepdims=True)
-    return ids.astype(np.int32), w.astype(np.float32)
-
-
-def routing_for(wl: Workload, seed: int = ROUTING_SEED, step: int = 0, M: int | None = None):
-    m = wl.M if M is None else M
-    return route(router_logits(m, wl.E, wl.routing, seed, step, wl.zipf_s), wl.topk)
-
-
 def workload_inputs(wl: Workload, step: int = 0, M: int | None = None):
-    """Activations and routing of one step of ``wl``: (hidden, topk_ids, topk_weights)."""
+    """Activations and router logits of one step of ``wl``: (hidden bf16 bits, logits float32)."""
     m = wl.M if M is None else M
-    hidden = hidden_states(m, wl.K, step=step)
-    ids, w = routing_for(wl, step=step, M=m)
-    return hidden, ids, w
+    return hidden_states(m, wl.K, step=step), router_logits(m, wl.E, wl.routing, step=step, zipf_s=wl.zipf_s)
 
 
 def active_experts(topk_ids: np.ndarray) -> np.ndarray:

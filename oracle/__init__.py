@@ -12,6 +12,7 @@ from .moe_oracle import (  # noqa: F401
     moe_align,
     moe_forward,
     roofline_bytes_per_expert,
+    route,
     silu,
     unpack_codes,
 )

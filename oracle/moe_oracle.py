@@ -18,6 +18,11 @@ against the definitions it follows:
 * Expert MLP: ``down(SiLU(gate . x) * (up . x))`` with ``SiLU(z) = z / (1 + e^-z)``.
 * Mixture: every token is routed to its top-k experts and the k expert outputs
   are summed with the top-k weights (Input Knowledge item 1: 384 experts, top-8).
+* Routing (the gating network that chooses which experts a token is sent to --
+  "The Weight-Streaming Threshold", Input Knowledge Required; the workloads'
+  recipe "router logits -> softmax top-k, renormalised"): softmax over all E
+  router logits of a token, keep the k most probable experts, divide their
+  probabilities by their sum. Equal logits rank the lower expert id first.
 * Align (the token->expert counting sort that groups routed rows by expert and
   pads every expert's rows to a block size) -- the pages only mention "sorting
   indices"; the definition used here is the plainest one: experts in id order,
@@ -140,6 +145,29 @@ def moe_forward(hidden_bf16, topk_ids, topk_weights, w1_q, w1_s, w2_q, w2_s,
         y *= wts[rows[r_idx], j_idx][:, None]
         np.add.at(out, r_idx, y)
     return out
+
+
+def route(logits: np.ndarray, topk: int):
+    """Top-k routing of router logits ``[M, E]``: ``(topk_ids int32 [M, k], topk_weights float64 [M, k])``.
+
+    For every token: ``p = softmax(logits)`` over all ``E`` experts; the ids are
+    the ``k`` experts of largest ``p`` (equivalently largest logit) in descending
+    order, equal logits taken in ascending expert id; the weights are those
+    ``p`` divided by their sum (renormalised to 1).
+    """
+    lg = np.asarray(logits, dtype=np.float64)
+    M, E = lg.shape
+    ids = np.empty((M, topk), dtype=np.int32)
+    wts = np.empty((M, topk), dtype=np.float64)
+    for t in range(M):
+        row = lg[t]
+        p = np.exp(row - row.max())
+        p /= p.sum()
+        order = sorted(range(E), key=lambda e: (-row[e], e))[:topk]
+        sel = p[order]
+        ids[t] = order
+        wts[t] = sel / sel.sum()
+    return ids, wts
 
 
 def moe_align(topk_ids: np.ndarray, num_experts: int, block: int):

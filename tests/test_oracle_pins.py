@@ -376,3 +376,89 @@ def test_planted_align_mistakes_are_caught():
         assert bad.tolist() != bf
     unpadded = [v for v in good.tolist() if v < 60]
     assert unpadded != bf or all(np.diff(bf_off) % 4 == 0)
+
+
+# ---------------------------------------------------------------------------
+# routing (softmax -> top-k -> renormalise)
+
+
+def test_route_golden():
+    from fractions import Fraction
+    for k, logits, want_ids, want_w in read_golden_rows("route_examples.txt"):
+        lg = np.array([[float(v) for v in logits.split(",")]], dtype=np.float64)
+        ids, w = oracle.route(lg, int(k))
+        assert ids[0].tolist() == [int(v) for v in want_ids.split(",")], (logits, ids)
+        np.testing.assert_allclose(w[0], [float(Fraction(v)) for v in want_w.split(",")], rtol=1e-12)
+
+
+def read_golden_rows(name):
+    rows = []
+    for fields in read_golden(name):
+        rows.append([f.strip() for f in " ".join(fields).split("|")])
+    return rows
+
+
+def _beats(l, a, b):
+    return l[a] > l[b] or (l[a] == l[b] and a < b)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_route_matches_subset_enumeration(seed):
+    """Brute force: the top-k set is the one k-subset whose every member beats every
+    non-member; the order inside it is by how many members each beats; weights are
+    probabilities exp(l)/sum exp(l) (plain math.exp) renormalised over the set."""
+    import itertools
+    import math
+    rng = np.random.default_rng(seed)
+    E, k = int(rng.integers(3, 8)), int(rng.integers(1, 4))
+    k = min(k, E)
+    lg = np.round(rng.standard_normal((5, E)) * 2) / 2  # coarse grid: ties happen
+    ids, w = oracle.route(lg, k)
+    for t in range(lg.shape[0]):
+        l = [float(v) for v in lg[t]]
+        winners = [S for S in itertools.combinations(range(E), k)
+                   if all(_beats(l, a, b) for a in S for b in range(E) if b not in S)]
+        assert len(winners) == 1
+        S = winners[0]
+        order = sorted(S, key=lambda a: -sum(_beats(l, a, b) for b in S))
+        assert ids[t].tolist() == order
+        z = sum(math.exp(v) for v in l)
+        p = [math.exp(l[a]) / z for a in order]
+        np.testing.assert_allclose(w[t], [v / sum(p) for v in p], rtol=1e-12)
+
+
+def test_route_full_softmax_and_shift_invariance():
+    rng = np.random.default_rng(3)
+    lg = rng.standard_normal((7, 12))
+    ids, w = oracle.route(lg, 12)  # k = E: the whole softmax, in descending order
+    ref = torch.softmax(torch.from_numpy(lg), dim=1).numpy()
+    np.testing.assert_allclose(w, np.take_along_axis(ref, ids.astype(np.int64), axis=1), rtol=1e-12)
+    ids2, w2 = oracle.route(lg + 17.25, 4)
+    ids3, w3 = oracle.route(lg, 4)
+    assert (ids2 == ids3).all()
+    np.testing.assert_allclose(w2, w3, rtol=1e-12)
+    np.testing.assert_allclose(w3.sum(axis=1), 1.0, rtol=1e-12)
+
+
+def test_planted_route_mistakes_are_caught(monkeypatch):
+    """A router that forgets to renormalise, or breaks ties towards the higher id,
+    fails the golden rows."""
+    real = oracle.route
+
+    def no_renorm(logits, topk):
+        lg = np.asarray(logits, dtype=np.float64)
+        ids, _ = real(lg, topk)
+        p = np.exp(lg - lg.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        return ids, np.take_along_axis(p, ids.astype(np.int64), axis=1)
+
+    def high_id_ties(logits, topk):
+        lg = np.asarray(logits, dtype=np.float64)
+        flipped_ids, w = real(lg[:, ::-1], topk)
+        return (lg.shape[1] - 1 - flipped_ids).astype(np.int32), w
+
+    for bad in (no_renorm, high_id_ties):
+        monkeypatch.setattr(oracle, "route", bad)
+        with pytest.raises(AssertionError):
+            test_route_golden()
+    monkeypatch.setattr(oracle, "route", real)
