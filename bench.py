@@ -78,23 +78,32 @@ def file_hash(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel_src):
-    """DRAM bytes per launch of the gate/up GEMM from the committed ncu summary,
-    valid only while the kernel source is unchanged since the capture."""
-    path = os.path.join(ROOT, "profiles", "gemm_gateup_decode_ncu.md")
+def kernel_sources_hash():
+    """Hash of the GEMM kernel's sources (the kernel file and the headers it includes)."""
+    csrc = os.path.join(ROOT, "int4_weight_only_moe_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "layout.cuh", "kernels.cuh", "small_route.cuh"):
+        path = os.path.join(csrc, f)
+        if os.path.exists(path):
+            h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the gate/up GEMM at the headline workload, from the
+    committed ncu record (profiles/gemm_gateup_decode_ncu.json), valid only while the
+    kernel's sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "gemm_gateup_decode_ncu.json")
     if not os.path.exists(path):
         return None
-    vals = {}
-    for line in open(path):
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256_16") != file_hash(kernel_src):
-        return None
     try:
-        return float(vals["dram_bytes_per_launch_full_size"])
-    except (KeyError, ValueError):
+        rec = json.load(open(path))
+    except ValueError:
         return None
+    if rec.get("kernel_sources_sha256_16") != kernel_sources_hash():
+        return None
+    v = rec.get("dram_bytes_per_launch_full_size")
+    return float(v) if v is not None else None
 
 
 class ClockSampler:
@@ -169,12 +178,17 @@ class GpuBench:
         self.stream = torch.cuda.current_stream()
 
     def step_inputs(self, wl, n):
+        """Per step: device hidden states and their routing by the library's router
+        kernel (outside any timed region)."""
         torch = self.torch
         out = []
         for s in range(n):
-            h, ids, w = inputs.workload_inputs(wl, step=s)
-            out.append((torch.from_numpy(h.view(np.int16)).to(self.device), torch.from_numpy(ids).to(self.device),
-                        torch.from_numpy(w).to(self.device)))
+            h, logits = inputs.workload_inputs(wl, step=s)
+            d_logits = torch.from_numpy(logits).to(self.device)
+            if wl.E != self.E:  # a resident expert set smaller than the workload's: route among them
+                d_logits = d_logits[:, :self.E].contiguous()
+            ids, w = self.moe.route(d_logits)
+            out.append((torch.from_numpy(h.view(np.int16)).to(self.device), ids, w))
         return out
 
     def flush(self):
@@ -257,10 +271,8 @@ class GpuBench:
         """Same metric through the host-buffer C-ABI call (H2D + forward + D2H)."""
         torch = self.torch
         host = []
-        for s in range(steps + warmup):
-            h, ids, w = inputs.workload_inputs(wl, step=s)
-            host.append((torch.from_numpy(h.view(np.int16)).pin_memory(), torch.from_numpy(ids).pin_memory(),
-                         torch.from_numpy(w).pin_memory()))
+        for h, ids, w in self.step_inputs(wl, steps + warmup):
+            host.append((h.cpu().pin_memory(), ids.cpu().pin_memory(), w.cpu().pin_memory()))
         out = torch.empty((wl.M, self.K), dtype=torch.int16).pin_memory()
         for i in range(warmup):
             self.moe.forward_host(*host[i], out)
@@ -281,10 +293,12 @@ def roofline_entry(wl, us, active, hbm_gbs, tc_tflops):
     t_hbm = active * (w1b + w2b) / (hbm_gbs * 1e9) * 1e6
     t_tc = 2.0 * wl.M * wl.topk * 3 * wl.N * wl.K / (tc_tflops * 1e12) * 1e6
     t_star = max(t_hbm, t_tc)
+    t_hbm8 = active * (w1b + w2b) / 8e12 * 1e6  # the same roof at 8 TB/s
     return {"M": wl.M, "routing": wl.routing, "active_experts": int(active), "us_per_call": round(us, 2),
             "tok_per_s": round(wl.M / (us * 1e-6), 1), "us_per_token": round(us / wl.M, 3),
             "roofline_us": round(t_star, 2), "binding_roof": "hbm" if t_hbm >= t_tc else "tensor",
-            "frac_of_roofline": round(t_star / us, 4)}
+            "frac_of_roofline": round(t_star / us, 4),
+            "frac_of_roofline_8000_gbs": round(max(t_hbm8, t_tc) / us, 4)}
 
 
 def run_ours(args):
@@ -303,6 +317,8 @@ def run_ours(args):
         dist.barrier()
         __graft_entry__.build()
     hbm_gbs, tc_tflops, peak_src = peaks()
+    # the oracle's worker pool starts before any GPU work (spawned processes)
+    cpu_pool = OraclePool() if (not args.no_cpu_baseline and world == 1 and rank == 0) else None
     gb = GpuBench(device)
     wl = inputs.WORKLOADS[HEADLINE]
     barrier = dist.barrier if world > 1 else None
@@ -321,7 +337,7 @@ def run_ours(args):
     w1b, w2b = expert_bytes(wl.K, wl.N)
     gateup_bytes = active * w1b + wl.M * wl.K * 2 + wl.M * wl.topk * wl.N * 2
     achieved = gateup_bytes / (kmean[2] * 1e-3) / 1e9
-    traffic = recorded_traffic(os.path.join(ROOT, "int4_weight_only_moe_gb300", "csrc", "gemm.cu"))
+    traffic = recorded_traffic()
 
     # timing detail of the headline workload: spread, hot L2, graph-captured launches
     hot_ms, _, _ = gb.time_forward(wl, args.steps, args.warmup, flush=False)
@@ -350,20 +366,19 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "dtype_detail": "INT4 weights dequantised exactly to f16 tensor-core operands, f32 accumulate, "
+                        "bf16 in/out",
         "data": "synthetic (seeded random INT4 weights for all 384 experts, N(0,1) bf16 hidden, "
-                "uniform router logits -> top-8 renormalised)",
-        "config": {"workload": "decode: E=384 K=7168 N=2048 top-8 INT4 g32, M=1 token per step",
-                   "M": wl.M, "E": wl.E, "K": wl.K, "N": wl.N, "topk": wl.topk, "group_size": 32,
-                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write)",
-                   "inputs_per_step": "distinct seeded hidden/routing each step",
-                   "parallelism": f"replicas x{world}"},
+                "uniform router logits -> top-8 renormalised by the library's router)",
+        "config": headline_config(wl, world),
         # the library runs the routing and the gather as one kernel when M * topk <= 32
         "gpu_launches": (len(KERNELS) - (1 if wl.M * wl.topk <= 32 else 0)) * args.steps,
         "kernel_ms": {k: round(v, 5) for k, v in zip(KERNELS, kmean)},
         "roofline": {"kernel": "gemm_gateup", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": hbm_gbs, "unit": "GB/s", "frac": round(achieved / hbm_gbs, 4),
                      "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                     "frac_of_8000_gbs": round(achieved / 8000.0, 4),
                      "algorithmic_bytes_per_launch": int(gateup_bytes),
                      "traffic": traffic},
         "whole_forward_roofline": roofline_entry(wl, ms_step * 1e3, active, hbm_gbs, tc_tflops),
@@ -373,8 +388,9 @@ def run_ours(args):
         "clocks": clk.summary(),
         "sweep": sweep,
     }
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_samples)
+    if cpu_pool is not None:
+        line["cpu_baseline"] = cpu_baseline(cpu_pool, args.cpu_samples)
+        cpu_pool.close()
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -382,42 +398,116 @@ def run_ours(args):
 
 
 # --------------------------------------------------------------------------- CPU oracle arm
+#
+# The oracle (float64 numpy) is timed expert by expert: a call's experts are
+# independent, so a pool of worker processes (one BLAS thread each, "spawn" start
+# method) runs them concurrently on the host cores. Each worker regenerates the
+# seeded inputs and its expert's weights untimed and times only the oracle's
+# arithmetic (dequantise, SwiGLU MLP, weighted sum) for the tokens routed to it.
+
+_ROUTED = {}
 
 
-def oracle_step(wl, step):
-    """One oracle forward of ``wl`` at ``step`` (regenerating only the experts it routes to)."""
+def _routed(fields, step):
+    key = (fields, step)
+    if key not in _ROUTED:
+        import oracle
+        wl = inputs.Workload(*fields)
+        hidden, logits = inputs.workload_inputs(wl, step=step)
+        ids, w = oracle.route(logits, wl.topk)
+        _ROUTED.clear()
+        _ROUTED[key] = (hidden, ids, w.astype(np.float32))
+    return _ROUTED[key]
+
+
+def _oracle_expert_seconds(task):
+    """Seconds of oracle arithmetic for expert ``e``'s share of one call."""
     import oracle
-
-    hidden, ids, w = inputs.workload_inputs(wl, step=step)
-    cache = {}
-
-    def source(e):
-        if e not in cache:
-            cache[e] = inputs.expert_weights(e, wl.K, wl.N)
-        return cache[e]
-
+    fields, step, e = task
+    wl = inputs.Workload(*fields)
+    hidden, ids, w = _routed(fields, step)
+    weights = inputs.expert_weights(int(e), wl.K, wl.N)
+    masked = np.where(ids == e, ids, -1).astype(np.int32)
+    toks = np.unique(np.nonzero(ids == e)[0])
     t0 = time.perf_counter()
-    oracle.moe_forward(hidden, ids, w, None, None, None, None, expert_source=source)
+    oracle.moe_forward(hidden, masked, w, None, None, None, None, tokens=toks,
+                       expert_source=lambda _e: weights)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(samples):
-    """Time the oracle in a single-threaded child process (BLAS pinned to one thread)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench._oracle_samples(%d)))" % (ROOT, samples))
-    p = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE, text=True, check=True)
-    secs = json.loads(p.stdout.strip().splitlines()[-1])
+def _fields(wl):
+    return (wl.name, wl.E, wl.K, wl.N, wl.topk, wl.M, wl.routing, wl.zipf_s)
+
+
+class OraclePool:
+    """Worker processes for the oracle, one BLAS thread each."""
+
+    def __init__(self, procs=None):
+        import multiprocessing as mp
+        self.procs = procs or max(1, min(os.cpu_count() or 1, 16))
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+        self.pool = mp.get_context("spawn").Pool(self.procs)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+    def call_seconds(self, wl, step, experts):
+        """Per-expert seconds for ``experts`` of ``wl``'s call at ``step``."""
+        return self.pool.map(_oracle_expert_seconds, [(_fields(wl), step, int(e)) for e in experts])
+
+
+def oracle_call(pool, wl, step):
+    """Wall seconds of one whole oracle call: its experts run concurrently, so the
+    call takes as long as the busiest worker's share (experts dealt round-robin)."""
+    import oracle
+    _, logits = inputs.workload_inputs(wl, step=step)
+    experts = np.unique(oracle.route(logits, wl.topk)[0])
+    secs = pool.call_seconds(wl, step, experts)
+    loads = [sum(secs[i::pool.procs]) for i in range(pool.procs)]
+    return max(loads), len(experts)
+
+
+def cpu_baseline_sweep(pool, max_experts=16):
+    """Oracle throughput for every workload of the sweep on a bounded sample: up to
+    ``max_experts`` of a call's routed experts are timed (one per worker); the call's
+    time is their mean times its expert count, spread over the pool's workers."""
+    import oracle
+    out = {}
+    for name in SWEEP:
+        wl = inputs.WORKLOADS[name]
+        _, logits = inputs.workload_inputs(wl)
+        experts = np.unique(oracle.route(logits, wl.topk)[0])
+        sample = experts[np.linspace(0, len(experts) - 1, min(max_experts, len(experts))).astype(int)]
+        secs = pool.call_seconds(wl, 0, sample)
+        per_expert = float(np.mean(secs))
+        wall = per_expert * -(-len(experts) // pool.procs)
+        out[name] = {"M": wl.M, "s_per_call": round(wall, 3), "tok_per_s": round(wl.M / wall, 4),
+                     "cpu_s_per_expert": round(per_expert, 4), "active_experts": int(len(experts)),
+                     "sampled_experts": int(len(sample))}
+    return out
+
+
+def cpu_baseline(pool, steps):
+    """The headline (decode) oracle throughput plus the sweep, on ``pool.procs`` cores."""
     wl = inputs.WORKLOADS[HEADLINE]
-    return {"value": round(wl.M * len(secs) / sum(secs), 4), "unit": "tokens/s", "cores": 1,
+    walls = [oracle_call(pool, wl, s)[0] for s in range(steps)]
+    return {"value": round(wl.M * steps / sum(walls), 4), "unit": "tokens/s", "cores": pool.procs,
             "kind": "oracle",
-            "sample": f"{len(secs)} decode steps (M=1, 8 experts each) of the float64 numpy oracle, "
-                      "expert weights regenerated per step outside the timed region, 1 thread"}
+            "sample": f"{steps} decode steps (M=1, 8 routed experts each) of the float64 numpy oracle, "
+                      f"experts run concurrently on {pool.procs} worker processes with one BLAS "
+                      "thread each; input and weight generation untimed. sweep: per workload, up to "
+                      "16 routed experts timed and the call extrapolated to all its experts",
+            "sweep": cpu_baseline_sweep(pool)}
 
 
-def _oracle_samples(n):
-    wl = inputs.WORKLOADS[HEADLINE]
-    return [oracle_step(wl, s) for s in range(n)]
+def headline_config(wl, world):
+    return {"workload": "decode: E=384 K=7168 N=2048 top-8 INT4 g32, M=1 token per step",
+            "M": wl.M, "E": wl.E, "K": wl.K, "N": wl.N, "topk": wl.topk, "group_size": 32,
+            "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MiB write)",
+            "inputs_per_step": "distinct seeded hidden/routing each step",
+            "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args):
@@ -425,25 +515,26 @@ def run_reference(args):
     if rank != 0:
         return
     wl = inputs.WORKLOADS[HEADLINE]
-    # the oracle has nothing to warm up beyond one call; cap the bounded sample
-    args.warmup = min(args.warmup, 1)
-    args.steps = min(args.steps, 8)
-    for s in range(args.warmup):
-        oracle_step(wl, s)
-    secs = [oracle_step(wl, args.warmup + s) for s in range(args.steps)]
+    pool = OraclePool()
+    try:
+        for s in range(args.warmup):
+            oracle_call(pool, wl, s)
+        secs = [oracle_call(pool, wl, args.warmup + s)[0] for s in range(args.steps)]
+    finally:
+        pool.close()
     total = sum(secs)
     value = wl.M * args.steps / total
-    cores = os.cpu_count()
+    cores = min(pool.procs, 8)  # a decode call has 8 experts: at most 8 workers are busy
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
-        "config": {"workload": "decode: E=384 K=7168 N=2048 top-8 INT4 g32, M=1 token per step",
-                   "M": wl.M, "E": wl.E, "K": wl.K, "N": wl.N, "topk": wl.topk},
+        "config": headline_config(wl, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} decode steps of the float64 numpy oracle "
-                                   "(dequantise the 8 routed experts, SwiGLU, weighted sum)"},
+                         "sample": f"{args.steps} decode steps of the float64 numpy oracle (route, "
+                                   "dequantise the 8 routed experts, SwiGLU, weighted sum), experts "
+                                   "concurrently on worker processes with one BLAS thread each"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

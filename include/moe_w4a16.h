@@ -15,9 +15,13 @@
  * along each GEMM's reduction dimension: value = (u - 8) * scale for a stored
  * nibble u in 0..15. Activations (x, out) are bf16. The tensor cores take fp16
  * operands (kind::f16) with fp32 accumulation: the dequantised weights (u-8)*s
- * are exact in fp16, bf16 hidden states convert to fp16 exactly within fp16's
- * range (values beyond +-65504 saturate, as do intermediate activations), and
- * the output is rounded once from fp32 to bf16.
+ * are exact in fp16 (pack rejects scales for which they would not be), every
+ * token row is fed in as x * 2^-e with a power of two chosen from the row's
+ * largest magnitude (exact, and undone in fp32 in the GEMM epilogues, so any
+ * finite bf16 row is within range), the intermediate SiLU(g)*u is rounded once to
+ * fp16 (stored as h * 2^-2e; a value that still exceeds fp16's range saturates
+ * and sets MOE_W4A16_STATUS_H_SATURATED), and the output is rounded once from
+ * fp32 to bf16.
  *
  * Conventions shared by every call:
  *  - Every function returns MOE_W4A16_OK (0) or a negative code; the message of
@@ -46,13 +50,18 @@ enum {
   MOE_W4A16_UNSUPPORTED_SHAPE = -2,   /* K % 128, N % 128, group_size != 32, E or topk out of range */
   MOE_W4A16_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < moe_w4a16_workspace_size(h, M) */
   MOE_W4A16_CUDA_ERROR = -4,          /* a CUDA runtime call failed (message has the CUDA error) */
-  MOE_W4A16_NOT_PACKED = -5           /* forward before moe_w4a16_pack */
+  MOE_W4A16_NOT_PACKED = -5,          /* forward before moe_w4a16_pack */
+  MOE_W4A16_UNSUPPORTED_SCALE = -6    /* pack: a scale outside {0} U [2^-14, 8160] in magnitude */
 };
 
 /* Device status bits (see moe_w4a16_status). */
 enum {
   MOE_W4A16_STATUS_BAD_EXPERT_ID = 1, /* a topk_ids entry was outside [0, E); that slot was skipped */
-  MOE_W4A16_STATUS_TIMEOUT = 2        /* a pipeline wait in a GEMM kernel gave up; output is invalid */
+  MOE_W4A16_STATUS_TIMEOUT = 2,       /* a pipeline wait in a GEMM kernel gave up; output is invalid */
+  MOE_W4A16_STATUS_H_SATURATED = 4,   /* an intermediate activation exceeded fp16's range and was
+                                         saturated to +-65504; the output is inexact */
+  MOE_W4A16_STATUS_BAD_SCHEDULE = 16  /* malformed stream-K boundaries were ignored (the GEMMs split
+                                         their steps evenly instead); the output is still correct */
 };
 
 typedef struct moe_w4a16_ctx* moe_w4a16_t;
@@ -75,7 +84,11 @@ int moe_w4a16_destroy(moe_w4a16_t h);
  *   w1_s bf16  [E, K/32, 2N]
  *   w2_q int32 [E, N/8, K]
  *   w2_s bf16  [E, N/32, K]
- * The inputs may be freed once the stream has passed this call. */
+ * Every scale must be 0 or have a finite magnitude in [2^-14, 8160], the range in
+ * which each dequantised weight (u - 8) * s is an exact fp16 number; otherwise
+ * the call returns MOE_W4A16_UNSUPPORTED_SCALE and the handle stays unpacked.
+ * Synchronises `stream` (to read the scale check); the inputs may be freed once
+ * it returns. */
 int moe_w4a16_pack(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s,
                    const int32_t* w2_q, const uint16_t* w2_s, void* stream);
 
@@ -98,6 +111,28 @@ size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M);
 int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
                       const float* topk_weights, uint16_t* out, int M,
                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router ("The Weight-Streaming Threshold", Input Knowledge Required: the gating
+ * network picks the k experts a token is sent to; the workloads route by
+ * "router logits -> softmax top-k, renormalised"). Device pointers:
+ *   router_logits fp32  [M, E]
+ *   topk_ids      int32 [M, topk]  out: the k largest logits' experts, in
+ *                                  descending order, equal logits by ascending id
+ *   topk_weights  fp32  [M, topk]  out: softmax over all E restricted to those k
+ *                                  and renormalised, exp(l_j - l_0) / sum_i exp(l_i - l_0)
+ * 1 <= topk <= min(E, 32), E <= 1024. Logits should be finite (a NaN ranks as
+ * -infinity). One launch on `stream`, no host synchronisation. */
+int moe_w4a16_route(const float* router_logits, int M, int E, int topk, int32_t* topk_ids,
+                    float* topk_weights, void* stream);
+
+/* moe_w4a16_forward with the router in front: routes router_logits fp32 [M, E]
+ * (as moe_w4a16_route, topk <= 32), writes topk_ids / topk_weights (device
+ * outputs, [M, topk]) and runs the forward on them. For M * topk <= 32 the
+ * routing runs inside the forward's first launch (4 launches in all); otherwise
+ * a router launch precedes the forward's 5. Same workspace as moe_w4a16_forward. */
+int moe_w4a16_forward_logits(moe_w4a16_t h, const uint16_t* hidden, const float* router_logits,
+                             int32_t* topk_ids, float* topk_weights, uint16_t* out, int M,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* End-to-end variant with HOST buffers (same shapes as moe_w4a16_forward); it
  * synchronises `stream` before returning, so the buffers may be reused at once.
@@ -133,9 +168,22 @@ const char* moe_w4a16_last_error(void);
  *                            stream-K balance of each GEMM for batches with
  *                            M * topk > 32: a pipeline step whose token tile has
  *                            ng row groups of 16 counts as 8 + value * max(0, ng - 2);
- *                            0 = split the steps evenly (range 0..64) */
+ *                            0 = split the steps evenly (range 0..64)
+ *   MOE_W4A16_OPT_WAIT_LIMIT_US
+ *                            longest time a GEMM pipeline wait may take before the
+ *                            kernel gives up, sets MOE_W4A16_STATUS_TIMEOUT, lets
+ *                            its in-flight copies and MMAs land and returns: value
+ *                            microseconds at clocks up to 4 GHz, counted in SM
+ *                            cycles (0 = the default, about 4 s at 2 GHz). The
+ *                            output of a call that gave up is invalid; the next
+ *                            call is not affected.
+ *   MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES
+ *                            test hook: 1 makes each GEMM's epilogue first wait on
+ *                            a barrier nothing arrives on, so that the give-up path
+ *                            above runs (use with a short wait limit). 0 = off. */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
-       MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5 };
+       MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5,
+       MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7 };
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order
@@ -164,12 +212,27 @@ int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int b
 int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s,
                            int32_t* w2_q, uint16_t* w2_s, void* stream);
 
-/* Copy the intermediate activations SiLU(gate)*up (fp16 bit patterns, the
- * tensor-core operand type) of the last forward that used `workspace` into
- * h_rows [M*topk, N] (device), row = flat slot id t*topk+j; rows of skipped
- * slots are left untouched. */
+/* Copy the intermediate activations SiLU(gate)*up of the last forward that used
+ * `workspace` into h_rows fp32 [M*topk, N] (device), row = flat slot id
+ * t*topk+j: the fp16 tensor-core operand with the row's prescale undone; rows of
+ * skipped slots are left untouched. */
 int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M,
-                                uint16_t* h_rows, void* stream);
+                                float* h_rows, void* stream);
+
+/* Copy the fp32 accumulator of the last forward that used `workspace` (with M
+ * tokens) -- sum_j w * W2[e] . h before the output's rounding to bf16 -- into acc
+ * fp32 [M, K] (device). */
+int moe_w4a16_read_accumulator(moe_w4a16_t h, const void* workspace, int M, float* acc,
+                               void* stream);
+
+/* Copy the stream-K boundaries of the last forward that used `workspace` (with M
+ * tokens) to host memory: bounds[w * (G + 1) + c] = first pipeline step of CTA c
+ * in GEMM w (0 gate/up, 1 down), G = the grid size (MOE_W4A16_OPT_NUM_CTAS);
+ * *flags = bit w set when GEMM w used those boundaries (else it split its steps
+ * evenly and the table is stale). `n` is the capacity of `bounds`. Synchronises
+ * `stream`; returns the number of entries written or a negative code. */
+int moe_w4a16_schedule_debug(moe_w4a16_t h, const void* workspace, int M, int64_t* bounds,
+                             int n, int* flags, void* stream);
 
 /* ---- allocation-free variant ------------------------------------------ */
 
@@ -187,7 +250,9 @@ int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M,
  * exceeds it are rejected with MOE_W4A16_WORKSPACE_TOO_SMALL and a message giving
  * both sizes (at E=384, K=7168, N=2048, top-8 this admits M <= 14 tokens).
  * The first call on a device looks up the array's device address (a one-time
- * set-up per device); make that first call before any stream capture.
+ * set-up per device, repeated automatically if the device's context has been
+ * re-created since, e.g. after cudaDeviceReset); make that first call before any
+ * stream capture.
  * Every call on a device shares the one array: calls that can overlap on the GPU
  * (different streams without ordering between them) race and give wrong results;
  * calls ordered on one stream are safe. Each call re-initialises what the

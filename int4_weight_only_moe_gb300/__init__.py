@@ -17,16 +17,20 @@ __all__ = [
     "moe_w4a16_forward_host", "moe_w4a16_status", "moe_w4a16_last_error",
     "moe_w4a16_set_option", "moe_w4a16_kernel_times", "moe_w4a16_packed_bytes",
     "moe_w4a16_align_debug", "moe_w4a16_unpack_debug", "moe_w4a16_read_intermediate",
-    "moe_w4a16_forward_noalloc", "NOALLOC_WORKSPACE_BYTES", "MoEW4A16", "OPT_NUM_CTAS", "OPT_PROFILE", "OPT_PDL", "STATUS_BAD_EXPERT_ID",
-    "STATUS_TIMEOUT",
+    "moe_w4a16_schedule_debug", "moe_w4a16_read_accumulator", "moe_w4a16_route", "moe_w4a16_forward_logits", "moe_w4a16_forward_noalloc", "NOALLOC_WORKSPACE_BYTES", "MoEW4A16",
+    "OPT_NUM_CTAS", "OPT_PROFILE", "OPT_PDL", "OPT_STEP_COST_GATEUP", "OPT_STEP_COST_DOWN",
+    "OPT_WAIT_LIMIT_US", "OPT_TEST_WAIT_NEVER_COMPLETES", "STATUS_BAD_EXPERT_ID", "STATUS_TIMEOUT", "STATUS_H_SATURATED",
+    "STATUS_BAD_SCHEDULE",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmoe_w4a16.so")
 
 OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR, NOT_PACKED = 0, -1, -2, -3, -4, -5
-STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT = 1, 2
+UNSUPPORTED_SCALE = -6
+STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT, STATUS_H_SATURATED, STATUS_BAD_SCHEDULE = 1, 2, 4, 16
 OPT_NUM_CTAS, OPT_PROFILE, OPT_PDL = 1, 2, 3
-OPT_STEP_COST_GATEUP, OPT_STEP_COST_DOWN = 4, 5
+OPT_STEP_COST_GATEUP, OPT_STEP_COST_DOWN, OPT_WAIT_LIMIT_US = 4, 5, 6
+OPT_TEST_WAIT_NEVER_COMPLETES = 7
 NOALLOC_WORKSPACE_BYTES = 48 << 20
 
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
@@ -40,6 +44,8 @@ _SIGNATURES = {
     "moe_w4a16_host_staging_size": (_c_size, [_vp, _c_int]),
     "moe_w4a16_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_size, _vp]),
     "moe_w4a16_forward_host": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_size, _vp]),
+    "moe_w4a16_route": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_w4a16_forward_logits": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_size, _vp]),
     "moe_w4a16_status": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), _vp]),
     "moe_w4a16_last_error": (ctypes.c_char_p, []),
     "moe_w4a16_set_option": (_c_int, [_vp, _c_int, _c_int]),
@@ -48,6 +54,9 @@ _SIGNATURES = {
     "moe_w4a16_align_debug": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp]),
     "moe_w4a16_unpack_debug": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_w4a16_read_intermediate": (_c_int, [_vp, _vp, _c_int, _vp, _vp]),
+    "moe_w4a16_read_accumulator": (_c_int, [_vp, _vp, _c_int, _vp, _vp]),
+    "moe_w4a16_schedule_debug": (_c_int, [_vp, _vp, _c_int, ctypes.POINTER(ctypes.c_int64), _c_int,
+                                          ctypes.POINTER(_c_int), _vp]),
     "moe_w4a16_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp]),
 }
 
@@ -155,6 +164,18 @@ def moe_w4a16_forward(h, hidden, topk_ids, topk_weights, out, M, workspace, stre
                                    _stream(stream)))
 
 
+def moe_w4a16_route(router_logits, M, E, topk, topk_ids, topk_weights, stream=None):
+    _check(lib().moe_w4a16_route(_ptr(router_logits), M, E, topk, _ptr(topk_ids), _ptr(topk_weights),
+                                 _stream(stream)))
+
+
+def moe_w4a16_forward_logits(h, hidden, router_logits, topk_ids, topk_weights, out, M, workspace,
+                             stream=None):
+    _check(lib().moe_w4a16_forward_logits(h, _ptr(hidden), _ptr(router_logits), _ptr(topk_ids),
+                                          _ptr(topk_weights), _ptr(out), M, _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def moe_w4a16_forward_host(h, hidden, topk_ids, topk_weights, out, M, workspace, stream=None):
     _check(lib().moe_w4a16_forward_host(h, _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights),
                                         _ptr(out), M, _ptr(workspace),
@@ -197,6 +218,23 @@ def moe_w4a16_unpack_debug(h, w1_q, w1_s, w2_q, w2_s, stream=None):
 
 def moe_w4a16_read_intermediate(h, workspace, M, h_rows, stream=None):
     _check(lib().moe_w4a16_read_intermediate(h, _ptr(workspace), M, _ptr(h_rows), _stream(stream)))
+
+
+def moe_w4a16_read_accumulator(h, workspace, M, acc, stream=None):
+    _check(lib().moe_w4a16_read_accumulator(h, _ptr(workspace), M, _ptr(acc), _stream(stream)))
+
+
+def moe_w4a16_schedule_debug(h, workspace, M, n_ctas, stream=None):
+    """Both GEMMs' stream-K boundaries of the last forward on ``workspace``:
+    ``(bounds [2, n_ctas + 1] int64 list of lists, flags)``."""
+    n = 2 * (n_ctas + 1)
+    buf = (ctypes.c_int64 * n)()
+    flags = _c_int(0)
+    w = lib().moe_w4a16_schedule_debug(h, _ptr(workspace), M, buf, n, ctypes.byref(flags), _stream(stream))
+    if w < 0:
+        _check(w)
+    vals = [int(buf[i]) for i in range(n)]
+    return [vals[:n_ctas + 1], vals[n_ctas + 1:]], int(flags.value)
 
 
 def moe_w4a16_forward_noalloc(h, hidden, topk_ids, topk_weights, out, M, stream=None):
@@ -260,6 +298,31 @@ class MoEW4A16:
         moe_w4a16_forward(self.handle, hidden, topk_ids, topk_weights, out, M, ws, stream)
         return out
 
+    def route(self, router_logits, stream=None):
+        """Top-k routing of ``router_logits`` fp32 [M, E] on the device: (ids, weights)."""
+        import torch
+        M = router_logits.shape[0]
+        _need(router_logits, ("float32",), (M, self.E), "router_logits")
+        ids = torch.empty((M, self.topk), dtype=torch.int32, device=router_logits.device)
+        w = torch.empty((M, self.topk), dtype=torch.float32, device=router_logits.device)
+        moe_w4a16_route(router_logits, M, self.E, self.topk, ids, w, stream)
+        return ids, w
+
+    def forward_logits(self, hidden, router_logits, out=None, stream=None):
+        """Routing plus forward: (out, topk_ids, topk_weights)."""
+        import torch
+        M = hidden.shape[0]
+        _need(hidden, _BITS16, (M, self.K), "hidden")
+        _need(router_logits, ("float32",), (M, self.E), "router_logits")
+        if out is None:
+            out = torch.empty((M, self.K), dtype=torch.bfloat16, device=hidden.device)
+        _need(out, _BITS16, (M, self.K), "out")
+        ids = torch.empty((M, self.topk), dtype=torch.int32, device=hidden.device)
+        w = torch.empty((M, self.topk), dtype=torch.float32, device=hidden.device)
+        ws = self.ensure_workspace(M)
+        moe_w4a16_forward_logits(self.handle, hidden, router_logits, ids, w, out, M, ws, stream)
+        return out, ids, w
+
     def forward_host(self, hidden, topk_ids, topk_weights, out, stream=None):
         M = hidden.shape[0]
         _need(hidden, _BITS16, (M, self.K), "hidden", device=False)
@@ -273,8 +336,15 @@ class MoEW4A16:
     def status(self, stream=None) -> int:
         return moe_w4a16_status(self.handle, self.workspace, stream)
 
+    def accumulator(self, M: int, stream=None):
+        """fp32 [M, K] output accumulator of the last forward (before the bf16 rounding)."""
+        import torch
+        acc = torch.zeros((M, self.K), dtype=torch.float32, device="cuda")
+        moe_w4a16_read_accumulator(self.handle, self.workspace, M, acc, stream)
+        return acc
+
     def intermediate(self, M: int, stream=None):
         import torch
-        h_rows = torch.zeros((M * self.topk, self.N), dtype=torch.float16, device="cuda")
+        h_rows = torch.zeros((M * self.topk, self.N), dtype=torch.float32, device="cuda")
         moe_w4a16_read_intermediate(self.handle, self.workspace, M, h_rows, stream)
         return h_rows

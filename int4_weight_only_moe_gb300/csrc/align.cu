@@ -6,6 +6,8 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "route.cuh"
+#include "small_route.cuh"
 
 namespace moe {
 
@@ -212,58 +214,8 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
   pdl_launch_dependents();
 }
 
-// Small batches (at most 32 routed slots, e.g. decode) take one warp, with no
-// E-wide histograms, scans or block barriers: lane l holds flat slot l; lanes
-// routed to the same expert find each other with __match_any_sync; a slot's rank
-// among them counts the lower lanes (slot ids ascending, the same stable order as
-// the general kernel); the padded segment and first tile of an expert add up the
-// experts present (at most 32) with a smaller id. Experts without rows get no
-// segment and no tiles (the GEMMs read only the tiles' experts).
-struct SmallRoute {
-  int e;          // this lane's expert, or -1 (no slot or a bad id)
-  int rank, cnt;  // position among the slots of its expert, and their number
-  bool leader;    // lowest lane of its expert
-  int pad, ntile; // leader only: padded rows and token tiles of the expert
-  int seg, tile0; // first padded row and first tile of the expert
-  int tot_pad, tot_tiles;
-  bool any_bad;
-};
-
 __device__ SmallRoute small_route(const AlignArgs& a, int lane) {
-  SmallRoute r;
-  r.e = -1;
-  bool bad = false;
-  if (lane < a.MK) {
-    const int v = a.topk_ids[lane];
-    if (v >= 0 && v < a.E)
-      r.e = v;
-    else
-      bad = true;
-  }
-  const unsigned peers = __match_any_sync(0xffffffffu, r.e);
-  const bool valid = r.e >= 0;
-  r.rank = __popc(peers & ((1u << lane) - 1u));
-  r.cnt = __popc(peers);
-  r.leader = valid && r.rank == 0;
-  r.pad = r.leader ? (r.cnt + a.block - 1) / a.block * a.block : 0;
-  r.ntile = (r.leader && a.bn_max > 0) ? (r.pad + a.bn_max - 1) / a.bn_max : 0;
-  const int lead_e = r.leader ? r.e : -1;
-  r.seg = r.tile0 = r.tot_pad = r.tot_tiles = 0;
-  for (int j = 0; j < 32; ++j) {
-    const int ej = __shfl_sync(0xffffffffu, lead_e, j);
-    const int pj = __shfl_sync(0xffffffffu, r.pad, j);
-    const int tj = __shfl_sync(0xffffffffu, r.ntile, j);
-    if (ej >= 0) {
-      r.tot_pad += pj;
-      r.tot_tiles += tj;
-      if (ej < r.e) {
-        r.seg += pj;
-        r.tile0 += tj;
-      }
-    }
-  }
-  r.any_bad = __any_sync(0xffffffffu, bad);
-  return r;
+  return small_route(a.topk_ids, a.MK, a.E, a.block, a.bn_max, lane);
 }
 
 // Write the routing outputs of a small batch (one warp): header, counters, sorted
@@ -339,29 +291,136 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl) {
   return launch_k(align_kernel, dim3(1), dim3(1024), smem, stream, pdl, a);
 }
 
-// bf16 pair -> fp16 pair (exact inside fp16's range, saturated to +-65504 beyond).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.0f), 65504.0f);
-  const float hi = fminf(fmaxf(__uint_as_float(w & 0xFFFF0000u), -65504.0f), 65504.0f);
+// Largest magnitude among eight bf16 values, as bf16 magnitude bits: for finite
+// values the order of |x| is the order of the low 15 bits.
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  return m;
+}
+
+// Prescale exponent of a token row whose largest magnitude has bf16 bits `m`:
+// the e for which that magnitude times 2^-e lies in [4, 8) (clamped to
+// +-kMaxRowExp); 0 for an all-zero row, and for a row holding an infinity or a
+// NaN (outside the supported input range: such values saturate).
+__device__ __forceinline__ int row_exponent(uint32_t m) {
+  if (m == 0 || m >= 0x7F80u) return 0;
+  const int biased = static_cast<int>(m >> 7);
+  // floor(log2 |x|): from the exponent field, or for a subnormal (m * 2^-133) from
+  // the leading mantissa bit
+  const int lg = biased > 0 ? biased - 127 : (31 - __clz(static_cast<int>(m))) - 133;
+  const int e = lg - 2;
+  return e < -kMaxRowExp ? -kMaxRowExp : (e > kMaxRowExp ? kMaxRowExp : e);
+}
+
+// bf16 pair times f -> fp16 pair (f = 2^-e is exact; values stay below 8 for a
+// finite row, the clamp only bounds non-finite ones).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float f) {
+  const float lo = fminf(fmaxf(__uint_as_float(w << 16) * f, -65504.0f), 65504.0f);
+  const float hi = fminf(fmaxf(__uint_as_float(w & 0xFFFF0000u) * f, -65504.0f), 65504.0f);
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                    bf16x2_to_f16x2(v.w));
+
+// One CTA copies expert-sorted row p (flat slot `sid`, or padding when sid is the
+// sentinel) into the blocked fp16 B-operand layout: every thread loads its
+// 16-byte chunks of the token's row at once (up to kGatherChunks each), the CTA
+// reduces the row's largest magnitude, records the row's prescale exponent e and
+// writes x * 2^-e. A padding row only gets the exponent kPadRowExp: its operand
+// rows are never written (they only feed output columns that nothing reads, and
+// the gate/up epilogue stores zeros for them).
+constexpr int kGatherThreads = 256;
+constexpr int kGatherChunks = 8;  // chunks of 8 elements per thread and pass: K <= 16384 in one pass
+__device__ void gather_row(const GatherArgs& g, int p, int sid, int* red) {
+  const int tid = threadIdx.x;
+  const bool real = sid < g.MK && MOE_CHECK(sid >= 0 && sid / g.topk < g.M, const_cast<int32_t*>(g.hdr),
+                                            g.dbg, 24, sid, p);
+  if (!real) {  // uniform across the CTA
+    if (tid == 0) g.rowexp[p] = kPadRowExp;
+    return;
+  }
+  const int cpr = g.K / 8;  // 16-byte chunks per row
+  const uint4* src = reinterpret_cast<const uint4*>(g.x + static_cast<long long>(sid / g.topk) * g.K);
+  const int grp = p / kRowGroup, row = p % kRowGroup;
+  constexpr int kPass = kGatherThreads * kGatherChunks;
+  const bool one_pass = cpr <= kPass;  // the whole row stays in registers (K <= 16384)
+  uint4 v[kGatherChunks];
+  uint32_t m = 0;
+  for (int c0 = 0; c0 < cpr; c0 += kPass) {
+#pragma unroll
+    for (int i = 0; i < kGatherChunks; ++i) {
+      const int ch = c0 + i * kGatherThreads + tid;
+      v[i] = ch < cpr ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+      m = max(m, bf16x8_absmax_bits(v[i]));
+    }
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((tid & 31) == 0) red[tid >> 5] = static_cast<int>(m);
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t x = tid < kGatherThreads / 32 ? static_cast<uint32_t>(red[tid]) : 0u;
+    x = __reduce_max_sync(0xffffffffu, x);
+    if (tid == 0) red[kGatherThreads / 32] = static_cast<int>(x);
+  }
+  __syncthreads();
+  const int e = row_exponent(static_cast<uint32_t>(red[kGatherThreads / 32]));
+  __syncthreads();  // red is reused by the next row
+  if (tid == 0) g.rowexp[p] = e;
+  const float f = exp2_int(-e);
+  for (int c0 = 0; c0 < cpr; c0 += kPass) {
+#pragma unroll
+    for (int i = 0; i < kGatherChunks; ++i) {
+      const int ch = c0 + i * kGatherThreads + tid;
+      if (ch >= cpr) continue;
+      const uint4 x = one_pass ? v[i] : src[ch];
+      const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
+                                 bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
+      const long long off = (static_cast<long long>(ch >> 3) * g.Gcap + grp) * kRowGroupBytes +
+                            row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+      if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 25, off, p))
+        *reinterpret_cast<uint4*>(g.xs + off) = o;
+    }
+  }
 }
 
 // Small batches in one launch: routing and gather. Every CTA's first warp
 // recomputes the one-warp routing (cheap) and lays the padded sorted-slot list
 // into shared memory; CTA 0 also publishes the routing for the GEMMs (they read
-// it after waiting for this kernel). Then every thread gathers its share of the
-// expert-sorted rows and zeroes its share of the accumulator, as gather_kernel.
+// it after waiting for this kernel). Then every warp gathers its share of the
+// expert-sorted rows, one row at a time, and every thread zeroes its share of the
+// accumulator, as gather_kernel.
 constexpr int kSmallPadRows = 32 + 32 * (kRowGroup - 1);  // at most 32 slots, padded to 16 each
+constexpr int kGatherWarps = kGatherThreads / 32;
 
-__global__ void __launch_bounds__(256) route_gather_small_kernel(const AlignArgs a, const GatherArgs g) {
+__global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(const AlignArgs a_in,
+                                                                           const GatherArgs g) {
   __shared__ int s_sorted[kSmallPadRows];
   __shared__ int s_npad;
+  __shared__ int32_t s_ids[32];
+  __shared__ int s_red[kGatherWarps + 1];
   pdl_wait();
+  AlignArgs a = a_in;
+  if (a.logits) {
+    // route the (at most 32 / k) tokens first: warp w takes tokens w, w + 8, ...;
+    // CTA 0 publishes ids and weights, every CTA keeps the ids for its own use
+    const int lane = threadIdx.x & 31;
+    for (int t = threadIdx.x >> 5; t < a.M_tokens; t += kGatherWarps) {
+      int id;
+      float w;
+      warp_topk(a.logits + static_cast<long long>(t) * a.E, a.E, a.topk, lane, &id, &w);
+      if (lane < a.topk) {
+        s_ids[t * a.topk + lane] = id;
+        if (blockIdx.x == 0) {
+          a.ids_out[t * a.topk + lane] = id;
+          a.wts_out[t * a.topk + lane] = w;
+        }
+      }
+    }
+    __syncthreads();
+    a.topk_ids = s_ids;
+  }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const SmallRoute r = small_route(a, lane);
@@ -377,74 +436,46 @@ __global__ void __launch_bounds__(256) route_gather_small_kernel(const AlignArgs
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   float4* acc4 = reinterpret_cast<float4*>(g.acc);
   for (long long i = gt; i < g.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int cpr = g.K / 8;
-  const long long chunks = static_cast<long long>(s_npad) * cpr;
-  for (long long idx = gt; idx < chunks; idx += nthr) {
-    const int p = static_cast<int>(idx / cpr), ch = static_cast<int>(idx - static_cast<long long>(p) * cpr);
-    const int sid = s_sorted[p];
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (sid < g.MK && MOE_CHECK(sid >= 0 && sid / g.topk < g.M, const_cast<int32_t*>(g.hdr), g.dbg, 29,
-                                sid, p))
-      v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
-          g.x + static_cast<long long>(sid / g.topk) * g.K + ch * 8));
-    const int grp = p / kRowGroup, row = p % kRowGroup;
-    const long long off = (static_cast<long long>(ch >> 3) * g.Gcap + grp) * kRowGroupBytes +
-                          row * 128 + (((ch & 7) ^ (row & 7)) << 4);
-    if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 30, off, p))
-      *reinterpret_cast<uint4*>(g.xs + off) = v;
-  }
+  for (int p = blockIdx.x; p < s_npad; p += gridDim.x) gather_row(g, p, s_sorted[p], s_red);
   pdl_launch_dependents();
 }
 
 cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
                                       int num_sms, cudaStream_t stream, bool pdl) {
   const long long rows = max_rows < kSmallPadRows ? max_rows : kSmallPadRows;
-  const long long work = std::max<long long>(rows * (g.K / 8), g.acc_elems / 4);
-  long long grid = (work + 255) / 256;
+  const long long ctas = std::max<long long>(rows, (g.acc_elems / 4 + kGatherThreads - 1) / kGatherThreads);
+  long long grid = ctas;
   const long long cap = 4LL * num_sms;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return launch_k(route_gather_small_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream,
-                  pdl, a, g);
+  return launch_k(route_gather_small_kernel, dim3(static_cast<unsigned>(grid)), dim3(kGatherThreads), 0,
+                  stream, pdl, a, g);
 }
 
-// Copy every expert-sorted row's hidden state, as fp16, into the blocked B-operand
-// layout (padding rows become zeros) and zero the fp32 output accumulator.
-__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+// Copy every expert-sorted row's hidden state, prescaled and as fp16, into the
+// blocked B-operand layout, one CTA per row, and zero the fp32 output accumulator.
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs a) {
+  __shared__ int s_red[kGatherWarps + 1];
   pdl_wait();
   const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   float4* acc4 = reinterpret_cast<float4*>(a.acc);
   for (long long i = gt; i < a.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // one thread per 16-byte chunk (8 elements) of every expert-sorted row
-  const int cpr = a.K / 8;
-  const long long chunks = static_cast<long long>(a.hdr[kHdrNumPadded]) * cpr;
-  for (long long idx = gt; idx < chunks; idx += nthr) {
-    const int p = static_cast<int>(idx / cpr), ch = static_cast<int>(idx - static_cast<long long>(p) * cpr);
-    const int sid = a.sorted_ids[p];
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (sid < a.MK && MOE_CHECK(sid >= 0 && sid / a.topk < a.M, const_cast<int32_t*>(a.hdr),
-                                a.dbg, 24, sid, p))
-      v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
-          a.x + static_cast<long long>(sid / a.topk) * a.K + ch * 8));
-    const int g = p / kRowGroup, r = p % kRowGroup;
-    const long long off = (static_cast<long long>(ch >> 3) * a.Gcap + g) * kRowGroupBytes +
-                          r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-    if (MOE_CHECK(off + 16 <= a.xs_bytes, const_cast<int32_t*>(a.hdr), a.dbg, 25, off, p))
-      *reinterpret_cast<uint4*>(a.xs + off) = v;
-  }
+  const int num_padded = a.hdr[kHdrNumPadded];
+  for (int p = blockIdx.x; p < num_padded; p += gridDim.x) gather_row(a, p, a.sorted_ids[p], s_red);
   pdl_launch_dependents();
 }
 
 cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
                           bool pdl) {
-  const long long work = std::max<long long>(static_cast<long long>(max_groups) * kRowGroup * (a.K / 8),
-                                             a.acc_elems / 4);
-  long long grid = (work + 255) / 256;
-  const long long cap = 4LL * num_sms;
+  const long long rows = static_cast<long long>(max_groups) * kRowGroup;
+  const long long ctas = std::max<long long>(rows, (a.acc_elems / 4 + kGatherThreads - 1) / kGatherThreads);
+  long long grid = ctas;
+  const long long cap = 8LL * num_sms;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return launch_k(gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, stream, pdl, a);
+  return launch_k(gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(kGatherThreads), 0, stream,
+                  pdl, a);
 }
 
 // out = bf16(acc), round to nearest even; eight elements per thread step.
@@ -482,26 +513,32 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int nu
 
 __global__ void read_intermediate_kernel(const uint8_t* __restrict__ hbuf,
                                          const int32_t* __restrict__ sorted_ids,
+                                         const int32_t* __restrict__ rowexp,
                                          const int32_t* __restrict__ hdr, int MK, int N, int Gcap,
-                                         uint16_t* __restrict__ h_rows) {
+                                         float* __restrict__ h_rows) {
   const int num_padded = hdr[kHdrNumPadded];
   for (int p = blockIdx.x; p < num_padded; p += gridDim.x) {
     const int sid = sorted_ids[p];
     if (sid >= MK) continue;
+    int e = rowexp[p];  // (a real row: never the padding sentinel)
+    e = e < -kMaxRowExp ? -kMaxRowExp : (e > kMaxRowExp ? kMaxRowExp : e);
+    const float scale = exp2_int(2 * e);  // h was stored as h * 2^-2e
     const int g = p / kRowGroup, r = p % kRowGroup;
     for (int n = threadIdx.x; n < N; n += blockDim.x) {
       const int kb = n >> 6, k = n & 63;
-      h_rows[static_cast<long long>(sid) * N + n] = *reinterpret_cast<const uint16_t*>(
+      const uint16_t bits = *reinterpret_cast<const uint16_t*>(
           hbuf + (static_cast<long long>(kb) * Gcap + g) * kRowGroupBytes + blocked_offset(r, k));
+      h_rows[static_cast<long long>(sid) * N + n] = __half2float(__ushort_as_half(bits)) * scale;
     }
   }
 }
 
 cudaError_t launch_read_intermediate(const uint8_t* hbuf, const int32_t* sorted_ids,
-                                     const int32_t* hdr, int MK, int N, int Gcap, int max_rows,
-                                     uint16_t* h_rows, cudaStream_t stream) {
+                                     const int32_t* rowexp, const int32_t* hdr, int MK, int N,
+                                     int Gcap, int max_rows, float* h_rows, cudaStream_t stream) {
   int grid = max_rows < 1024 ? (max_rows > 0 ? max_rows : 1) : 1024;
-  read_intermediate_kernel<<<grid, 256, 0, stream>>>(hbuf, sorted_ids, hdr, MK, N, Gcap, h_rows);
+  read_intermediate_kernel<<<grid, 256, 0, stream>>>(hbuf, sorted_ids, rowexp, hdr, MK, N, Gcap,
+                                                     h_rows);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,9 @@ struct moe_w4a16_ctx {
   int step_cost[2];  // per GEMM (gate/up, down): stream-K cost per row group beyond two (0: even split)
   bool pdl;
   bool profile;
+  unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
+  bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
+  int32_t* dflag;              // device word: pack's scale check
   uint8_t* w1p;
   uint8_t* w2p;
   size_t w1p_bytes, w2p_bytes;
@@ -73,7 +76,7 @@ const void* pinned_device_pointer(const void* p) {
 }
 
 struct WsLayout {
-  size_t hdr, tickets, sched, sorted, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
+  size_t hdr, tickets, sched, sorted, rowexp, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
   int Pcap, Gcap;
 };
 
@@ -96,6 +99,8 @@ WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   L.sched = off;  // stream-K boundaries of the two GEMMs
   off = align_up(off + 2 * (kMaxCtas + 1) * sizeof(long long), 256);
   L.sorted = off;
+  off = align_up(off + static_cast<size_t>(L.Pcap) * sizeof(int32_t), 256);
+  L.rowexp = off;
   off = align_up(off + static_cast<size_t>(L.Pcap) * sizeof(int32_t), 256);
   L.tiles = off;
   off = align_up(off + static_cast<size_t>(L.Gcap) * sizeof(TokenTile), 256);
@@ -170,8 +175,10 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->w2p_bytes = static_cast<size_t>(E) * (K / kBM) * (N / kBK) * kWBlockBytes;
   e = cudaMalloc(&h->w1p, h->w1p_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->w2p, h->w2p_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->dflag, 256);
   if (e != cudaSuccess) {
     cudaFree(h->w1p);
+    cudaFree(h->w2p);
     delete h;
     return fail(MOE_W4A16_CUDA_ERROR, std::string("cudaMalloc packed weights: ") + cudaGetErrorString(e));
   }
@@ -184,6 +191,7 @@ int moe_w4a16_destroy(moe_w4a16_t h) {
   cudaDeviceSynchronize();
   cudaFree(h->w1p);
   cudaFree(h->w2p);
+  cudaFree(h->dflag);
   if (h->hstage) cudaFreeHost(h->hstage);
   if (h->ev_valid)
     for (auto& ev : h->ev) cudaEventDestroy(ev);
@@ -198,10 +206,19 @@ int moe_w4a16_pack(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s, con
   if (int rc = check_handle(h)) return rc;
   if (!w1_q || !w1_s || !w2_q || !w2_s) return fail(MOE_W4A16_INVALID_ARG, "null weight pointer");
   auto s = static_cast<cudaStream_t>(stream);
+  h->packed = false;
+  MOE_CUDA_TRY(cudaMemsetAsync(h->dflag, 0, sizeof(int32_t), s));
   MOE_CUDA_TRY(launch_repack(reinterpret_cast<const uint32_t*>(w1_q), w1_s, h->w1p, h->E, h->K,
-                             2 * h->N, 2 * h->N / kBM, h->K / kBK, 1, s));
+                             2 * h->N, 2 * h->N / kBM, h->K / kBK, 1, h->dflag, s));
   MOE_CUDA_TRY(launch_repack(reinterpret_cast<const uint32_t*>(w2_q), w2_s, h->w2p, h->E, h->N,
-                             h->K, h->K / kBM, h->N / kBK, 0, s));
+                             h->K, h->K / kBM, h->N / kBK, 0, h->dflag, s));
+  int32_t bad = 0;
+  MOE_CUDA_TRY(cudaMemcpyAsync(&bad, h->dflag, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaStreamSynchronize(s));
+  if (bad)
+    return fail(MOE_W4A16_UNSUPPORTED_SCALE,
+                "a scale is outside the supported range (0, or 2^-14 <= |s| <= 8160, finite): "
+                "its fp16 dequantised weights would not be exact");
   h->packed = true;
   return MOE_W4A16_OK;
 }
@@ -246,6 +263,13 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
     case MOE_W4A16_OPT_PDL:
       h->pdl = value != 0;
       return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_WAIT_LIMIT_US:
+      if (value < 0) return fail(MOE_W4A16_INVALID_ARG, "wait limit must be >= 0");
+      h->wait_us = static_cast<unsigned long long>(value);
+      return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES:
+      h->test_never_wait = value != 0;
+      return MOE_W4A16_OK;
     case MOE_W4A16_OPT_STEP_COST_GATEUP:
     case MOE_W4A16_OPT_STEP_COST_DOWN:
       if (value < 0 || value > 64) return fail(MOE_W4A16_INVALID_ARG, "step cost must be in [0, 64]");
@@ -265,14 +289,22 @@ int moe_w4a16_kernel_times(moe_w4a16_t h, float* ms, int n) {
   return w;
 }
 
-int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
-                      const float* topk_weights, uint16_t* out, int M, void* workspace,
-                      size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward's launch sequence. With `logits` the top-k routing runs first and
+// writes topk_ids / topk_weights (outputs then); without, they are inputs.
+int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, const int32_t* topk_ids,
+                 const float* topk_weights, uint16_t* out, int M, void* workspace,
+                 size_t workspace_bytes, void* stream) {
   if (int rc = check_handle(h)) return rc;
   if (M < 0) return fail(MOE_W4A16_INVALID_ARG, "M must be >= 0");
   if (M == 0) return MOE_W4A16_OK;
   if (!hidden || !topk_ids || !topk_weights || !out || !workspace)
     return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  if (logits && h->topk > 32)
+    return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "the router supports topk <= 32");
   if (!h->packed) return fail(MOE_W4A16_NOT_PACKED, "moe_w4a16_pack has not been called");
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return fail(MOE_W4A16_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -289,6 +321,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
   int32_t* tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  int32_t* rowexp = reinterpret_cast<int32_t*>(ws + L.rowexp);
   TokenTile* tiles = reinterpret_cast<TokenTile*>(ws + L.tiles);
   int32_t* expert_tiles = reinterpret_cast<int32_t*>(ws + L.expert_tiles);
   uint8_t* xs = ws + L.xs;
@@ -301,6 +334,13 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[0], s));
   AlignArgs aa{};
   aa.topk_ids = topk_ids;
+  aa.M_tokens = M;
+  aa.topk = h->topk;
+  if (logits && MK <= 32) {  // routed inside the small-batch routing + gather launch
+    aa.logits = logits;
+    aa.ids_out = const_cast<int32_t*>(topk_ids);
+    aa.wts_out = const_cast<float*>(topk_weights);
+  }
   aa.MK = static_cast<int>(MK);
   aa.E = h->E;
   aa.block = kRowGroup;
@@ -337,6 +377,7 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   ga.K = h->K;
   ga.Gcap = L.Gcap;
   ga.xs = xs;
+  ga.rowexp = rowexp;
   ga.acc = acc;
   ga.acc_elems = static_cast<long long>(M) * h->K;
   ga.xs_bytes = static_cast<long long>(L.Pcap) * h->K * 2;
@@ -347,7 +388,10 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
     MOE_CUDA_TRY(launch_route_gather_small(aa, ga, L.Pcap, h->num_sms, s, false));
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
   } else {
-    MOE_CUDA_TRY(launch_align(aa, s, false));
+    if (logits)  // router kernel first; the align reads what it wrote
+      MOE_CUDA_TRY(launch_route(logits, M, h->E, h->topk, const_cast<int32_t*>(topk_ids),
+                                const_cast<float*>(topk_weights), h->num_sms, s, false));
+    MOE_CUDA_TRY(launch_align(aa, s, logits != nullptr && pdl));
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
     MOE_CUDA_TRY(launch_gather(ga, L.Gcap, h->num_sms, s, pdl));
   }
@@ -359,6 +403,13 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g1.hdr = hdr;
   g1.tiles = tiles;
   g1.expert_tiles = expert_tiles;
+  g1.rowexp = rowexp;
+  g1.wait_kcycles = wait_limit_kcycles(h->wait_us);
+  g1.test_never_wait = h->test_never_wait ? 1 : 0;
+  // a small batch whose ids are an input: the GEMMs recompute its routing tiles and
+  // start their weight streams without waiting for the routing + gather launch
+  const int32_t* small_ids = (MK <= 32 && !logits) ? topk_ids : nullptr;
+  g1.small_ids = small_ids;
   g1.R = 2 * h->N / kBM;
   g1.KBn = h->K / (2 * kBK);  // GEMM pipeline steps of 128 reduction elements
   g1.Gcap = L.Gcap;
@@ -386,6 +437,10 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
   g2.hdr = hdr;
   g2.tiles = tiles;
   g2.expert_tiles = expert_tiles;
+  g2.rowexp = rowexp;
+  g2.wait_kcycles = wait_limit_kcycles(h->wait_us);
+  g2.test_never_wait = h->test_never_wait ? 1 : 0;
+  g2.small_ids = small_ids;
   g2.R = h->K / kBM;
   g2.KBn = h->N / (2 * kBK);
   g2.Gcap = L.Gcap;
@@ -409,6 +464,40 @@ int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk
 
   MOE_CUDA_TRY(launch_finalize(acc, out, static_cast<long long>(M) * h->K, h->num_sms, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[5], s));
+  return MOE_W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                      const float* topk_weights, uint16_t* out, int M, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return forward_impl(h, hidden, nullptr, topk_ids, topk_weights, out, M, workspace, workspace_bytes,
+                      stream);
+}
+
+int moe_w4a16_forward_logits(moe_w4a16_t h, const uint16_t* hidden, const float* router_logits,
+                             int32_t* topk_ids, float* topk_weights, uint16_t* out, int M,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!router_logits && M > 0) return fail(MOE_W4A16_INVALID_ARG, "null router_logits");
+  return forward_impl(h, hidden, router_logits, topk_ids, topk_weights, out, M, workspace,
+                      workspace_bytes, stream);
+}
+
+int moe_w4a16_route(const float* router_logits, int M, int E, int topk, int32_t* topk_ids,
+                    float* topk_weights, void* stream) {
+  if (M < 0 || E < 1 || E > kMaxExperts || topk < 1 || topk > E)
+    return fail(MOE_W4A16_INVALID_ARG, "bad shape (need M >= 0, 1 <= topk <= E <= 1024)");
+  if (topk > 32) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "the router supports topk <= 32");
+  if (M == 0) return MOE_W4A16_OK;
+  if (!router_logits || !topk_ids || !topk_weights) return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  int dev = 0, sms = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  MOE_CUDA_TRY(launch_route(router_logits, M, E, topk, topk_ids, topk_weights, sms,
+                            static_cast<cudaStream_t>(stream), false));
   return MOE_W4A16_OK;
 }
 
@@ -496,17 +585,46 @@ int moe_w4a16_status(moe_w4a16_t h, const void* workspace, int32_t* status, void
   return MOE_W4A16_OK;
 }
 
-int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M, uint16_t* h_rows,
+int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M, float* h_rows,
                                 void* stream) {
   if (int rc = check_handle(h)) return rc;
   if (!workspace || !h_rows || M <= 0) return fail(MOE_W4A16_INVALID_ARG, "bad argument");
   const WsLayout L = ws_layout(h, M);
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   MOE_CUDA_TRY(launch_read_intermediate(ws + L.hbuf, reinterpret_cast<const int32_t*>(ws + L.sorted),
+                                        reinterpret_cast<const int32_t*>(ws + L.rowexp),
                                         reinterpret_cast<const int32_t*>(ws + L.hdr), M * h->topk,
                                         h->N, L.Gcap, L.Pcap, h_rows,
                                         static_cast<cudaStream_t>(stream)));
   return MOE_W4A16_OK;
+}
+
+int moe_w4a16_read_accumulator(moe_w4a16_t h, const void* workspace, int M, float* acc,
+                               void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (!workspace || !acc || M <= 0) return fail(MOE_W4A16_INVALID_ARG, "bad argument");
+  const WsLayout L = ws_layout(h, M);
+  MOE_CUDA_TRY(cudaMemcpyAsync(acc, static_cast<const uint8_t*>(workspace) + L.acc,
+                               static_cast<size_t>(M) * h->K * sizeof(float), cudaMemcpyDeviceToDevice,
+                               static_cast<cudaStream_t>(stream)));
+  return MOE_W4A16_OK;
+}
+
+int moe_w4a16_schedule_debug(moe_w4a16_t h, const void* workspace, int M, int64_t* bounds, int n,
+                             int* flags, void* stream) {
+  if (int rc = check_handle(h)) return rc;
+  if (!workspace || !bounds || !flags || M <= 0) return fail(MOE_W4A16_INVALID_ARG, "bad argument");
+  if (n < 2 * (h->num_ctas + 1)) return fail(MOE_W4A16_INVALID_ARG, "bounds holds fewer than 2 * (ctas + 1) entries");
+  const WsLayout L = ws_layout(h, M);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  auto s = static_cast<cudaStream_t>(stream);
+  int32_t hdr[kHdrWords];
+  MOE_CUDA_TRY(cudaMemcpyAsync(hdr, ws + L.hdr, sizeof(hdr), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaMemcpyAsync(bounds, ws + L.sched, 2 * (h->num_ctas + 1) * sizeof(int64_t),
+                               cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaStreamSynchronize(s));
+  *flags = hdr[kHdrSched];
+  return 2 * (h->num_ctas + 1);
 }
 
 int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int block,

@@ -58,6 +58,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "small_route.cuh"
 
 namespace moe {
 
@@ -100,50 +101,76 @@ constexpr int kThreads = (kWarpEpi0 + 4) * 32;
 constexpr int kSub = 2;
 constexpr int kWStepBytes = kSub * kWBlockBytes;  // packed weights of one step (9 KB)
 constexpr int kWChunk = 2;               // steps per weight copy (one 18 KB bulk copy)
-// Ring depths (compile-time; shared memory is shared between the two rings).
-#ifndef MOE_W_CHUNKS
-#define MOE_W_CHUNKS 4
-#endif
-#ifndef MOE_B_STEPS
-#define MOE_B_STEPS 8
-#endif
-constexpr int kNWS = MOE_W_CHUNKS;       // weight ring depth in chunks (shared memory)
 constexpr int kWChunkBytes = kWChunk * kWStepBytes;
 constexpr int kNS = 4;                   // A operand stage ring (tensor memory)
-constexpr int kNB = MOE_B_STEPS;         // B operand ring depth in steps (shared memory)
-constexpr int kBSub = kBNMax * 128;      // B tile of one 64-element k-block
-constexpr int kBStage = kSub * kBSub;    // B tiles of one step
 constexpr int kTmemCols = 512;
 constexpr int kACols = kSub * 32;        // one step of fp16 A: 128 lanes x 64 columns
 constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
-constexpr int kStatusTimeout = 2;
 constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
 
-constexpr int kSmB = 0;
-constexpr int kSmW = kSmB + kNB * kBStage;
-constexpr int kSmStage = ((kSmW + kNWS * kWChunkBytes + 1023) / 1024) * 1024;
-constexpr int kSmBar = kSmStage + kBNMax * 128;
+// The two shared-memory rings (packed weights, activation tiles) divide one
+// region between them per CTA: a B stage holds a step of the CTA's widest token
+// tile (16..64 rows), and the rings are as deep as that allows. Both rings hold
+// the same number of steps: the bulk-copy engine serves an SM's copies in issue
+// order, so an activation copy issued behind a long run of weight copies lands
+// late and stalls the MMA. With equal depths the B copy of a step is issued just
+// after the weight copy of the same step (its slot frees with the MMA that
+// follows the conversion which frees the weight slot) and lands with it.
+constexpr int kMaxNWS = 8;               // weight ring depth limit in chunks
+constexpr int kMaxNB = 2 * kMaxNWS;      // B ring depth limit in steps
+constexpr int kBRowGroupStep = kSub * kRowGroupBytes;  // B bytes of one row group per step
 // barrier indices
-constexpr int kBarWFull = 0;                  // weight chunk landed (bulk-copy bytes)
-constexpr int kBarWEmpty = kBarWFull + kNWS;  // weight chunk read (4 dequant warps per step)
-constexpr int kBarFull = kBarWEmpty + kNWS;   // A stage ready: stored by its 4 dequant warps
-constexpr int kBarEmpty = kBarFull + kNS;    // A stage consumed by the MMAs (tcgen05.commit)
-constexpr int kBarBFull = kBarEmpty + kNS;   // B stage landed (bulk-copy bytes)
-constexpr int kBarBEmpty = kBarBFull + kNB;  // B stage consumed by the MMAs (tcgen05.commit)
-constexpr int kBarAccFull = kBarBEmpty + kNB; // [issuer][buffer]: accumulator complete
-constexpr int kBarAccEmpty = kBarAccFull + 4;  // [buffer]: epilogue has read both issuers' sums
-constexpr int kBarDrain = kBarAccEmpty + 2;    // [issuer]
-constexpr int kNumBars = kBarDrain + 2;
+constexpr int kBarWFull = 0;                     // weight chunk landed (bulk-copy bytes)
+constexpr int kBarWEmpty = kBarWFull + kMaxNWS;  // weight chunk read (4 dequant warps per step)
+constexpr int kBarFull = kBarWEmpty + kMaxNWS;   // A stage ready: stored by its 4 dequant warps
+constexpr int kBarEmpty = kBarFull + kNS;        // A stage consumed by the MMAs (tcgen05.commit)
+constexpr int kBarBFull = kBarEmpty + kNS;       // B stage landed (bulk-copy bytes)
+constexpr int kBarBEmpty = kBarBFull + kMaxNB;   // B stage consumed by the MMAs (tcgen05.commit)
+constexpr int kBarAccFull = kBarBEmpty + kMaxNB; // [issuer][buffer]: accumulator complete
+constexpr int kBarAccEmpty = kBarAccFull + 4;    // [buffer]: epilogue has read both issuers' sums
+constexpr int kBarDrain = kBarAccEmpty + 2;      // [issuer]
+constexpr int kBarNever = kBarDrain + 2;         // nothing ever arrives (the give-up test hook)
+constexpr int kNumBars = kBarNever + 1;
+// fixed part of shared memory first, then the ring region
+constexpr int kSmStage = 0;                              // SwiGLU staging tile (1024-aligned)
+constexpr int kSmBar = kSmStage + kBNMax * 128;
 constexpr int kSmMisc = kSmBar + kNumBars * 8;
-constexpr int kMaxSegs = 512;            // units decoded into shared memory up front
+constexpr int kMaxSegs = 256;            // units decoded into shared memory up front
 constexpr int kSmSeg = kSmMisc + 64;
 constexpr int kSmSched = kSmSeg + kMaxSegs * 16;  // [kMaxCtas + 1] stream-K boundaries
-constexpr int kSmBytes = kSmSched + (kMaxCtas + 1) * 8 + 8;
-constexpr int kSmAlloc = kSmBytes + 1024;  // slack to align the base to 1024 bytes
-static_assert(kSmAlloc <= 227 * 1024, "shared memory budget");
+constexpr int kSmallTiles = 32;          // token tiles of a batch of at most 32 routed slots
+constexpr int kSmSmall = kSmSched + (kMaxCtas + 1) * 8 + 8;  // [kSmallTiles] TokenTile + count
+constexpr int kSmRings = ((kSmSmall + kSmallTiles * 16 + 16 + 1023) / 1024) * 1024;
+constexpr int kSmAlloc = 227 * 1024;     // the whole per-CTA limit (base aligned to 1024 inside)
+constexpr int kRingBytes = kSmAlloc - 1024 - kSmRings;
+static_assert(kSmRings < kSmAlloc - 1024, "shared memory budget");
 static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
 static_assert((kNS & (kNS - 1)) == 0 && kWChunk == 2,
               "stage index arithmetic below assumes a power-of-two A ring and 2-step chunks");
+
+// Ring depths for a CTA whose widest token tile has `ng` row groups: nws weight
+// chunks (an even number: the parity arguments below need even depths) and
+// nb = 2 * nws B stages of ng row groups -- 8 chunks / 16 steps for one-group
+// tiles, 6 / 12 for two, 4 / 8 for three or four.
+struct RingCfg {
+  int nb, nws;
+  uint32_t b_stage, b_plane;  // bytes of one B stage, and of one 64-element plane in it
+};
+__host__ __device__ constexpr RingCfg ring_cfg(int ng) {
+  const int g = ng < 1 ? 1 : (ng > kBNMax / kRowGroup ? kBNMax / kRowGroup : ng);
+  const int b_stage = g * kBRowGroupStep;
+  int nws = kRingBytes / (kWChunkBytes + 2 * b_stage);
+  nws = nws > kMaxNWS ? kMaxNWS : nws;
+  nws &= ~1;
+  return RingCfg{2 * nws, nws, static_cast<uint32_t>(b_stage), static_cast<uint32_t>(g * kRowGroupBytes)};
+}
+static_assert(ring_cfg(1).nws == 8 && ring_cfg(2).nws == 6 && ring_cfg(3).nws == 4 &&
+                  ring_cfg(4).nws == 4,
+              "ring depths as documented");
+static_assert(ring_cfg(1).nb * ring_cfg(1).b_stage + ring_cfg(1).nws * kWChunkBytes <= kRingBytes &&
+                  ring_cfg(2).nb * ring_cfg(2).b_stage + ring_cfg(2).nws * kWChunkBytes <= kRingBytes &&
+                  ring_cfg(4).nb * ring_cfg(4).b_stage + ring_cfg(4).nws * kWChunkBytes <= kRingBytes,
+              "rings fit the region");
 
 // Stage-reuse safety. A dequantisation warp reuses A stage st for step it after
 // a parity test of Empty[st], meaning "the MMA of step it - kNS is done". A
@@ -163,8 +190,12 @@ static_assert(stage_reuse_is_safe(kDeqPhases, kNS),
               "a dequantisation warp could pass a stale Empty phase (parity aliasing)");
 // The MMA issuer that waits on a B (or A) stage for step it consumed the
 // previous phase itself (step it - depth) only if the depth is even; a B
-// producer lane reuses a slot only after an earlier lockstep iteration.
-static_assert(kNB % 2 == 0 && kNS % 2 == 0 && kNB >= kProducerLanes,
+// producer lane reuses a slot only after an earlier lockstep iteration. A
+// dequantisation warp sees every second weight chunk (its steps are 4 apart, 2
+// steps a chunk), so with an even weight ring it has itself waited for the
+// previous phase of every chunk slot it waits on.
+static_assert(kMaxNB % 2 == 0 && kNS % 2 == 0 && ring_cfg(4).nb >= kProducerLanes &&
+                  kDeqPhases == 2 * kWChunk,
               "ring depths must be even and the B ring at least as deep as the producer lanes");
 
 constexpr int kEpiWarps = 4, kEpiThreads = 128;
@@ -173,10 +204,11 @@ constexpr int kRowRegs = kBNMax / 32;  // token rows per epilogue lane (routing 
 
 // Bounded wait that ignores the abort flag: used at teardown to let copies and
 // MMAs already in flight land before shared and tensor memory are released.
+// (8e8 SM cycles: about 0.4 s.)
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
+  const long long c0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > 200000000ull) return;
+    if (clock64() - c0 > 800000000ll) return;
   }
 }
 
@@ -208,17 +240,51 @@ struct Sched {
   }
 };
 
+// The segments (unit, step range) of a CTA's share [begin, end): a share starts
+// and ends inside units that other CTAs share. Those partial units come first
+// (the one the share starts in, then the one it ends in), then the whole units in
+// order: every contributor to a split unit then reaches it early in its share, so
+// the split unit's cross-CTA reduction (partial sums, ticket, last arriver)
+// overlaps the whole units that follow instead of adding to the kernel's tail.
+// Every role walks the same sequence.
 struct SegIter {
-  long long g, gend;
+  long long g, gend;  // the share
+  long long uw;       // next whole unit (stage 2)
   int KBn;
+  int stage;          // 0: first partial unit, 1: last partial unit, 2: whole units
+  __device__ SegIter(long long begin, long long end, int kbn)
+      : g(begin), gend(end), uw(0), KBn(kbn), stage(0) {}
+  __device__ __forceinline__ void range(long long u, int& kb0, int& kb1) const {
+    const long long lo = g - u * KBn, hi = gend - u * KBn;
+    kb0 = static_cast<int>(lo > 0 ? lo : 0);
+    kb1 = static_cast<int>(hi < KBn ? hi : KBn);
+  }
   // Next (unit, step range) of this CTA's share.
   __device__ __forceinline__ bool next(long long& u, int& kb0, int& kb1) {
-    if (g >= gend) return false;
-    u = g / KBn;
-    kb0 = static_cast<int>(g - u * KBn);
-    const long long lim = gend - u * KBn;
-    kb1 = static_cast<int>(lim < KBn ? lim : KBn);
-    g = u * KBn + kb1;
+    if (gend <= g) return false;
+    const long long u0 = g / KBn, u1 = (gend - 1) / KBn;
+    const bool p0 = g > u0 * KBn || gend < (u0 + 1) * KBn;  // the share starts inside u0 (or ends in it)
+    const bool p1 = u1 != u0 && gend < (u1 + 1) * KBn;       // the share ends inside u1
+    if (stage == 0) {
+      stage = 1;
+      uw = p0 ? u0 + 1 : u0;
+      if (p0) {
+        u = u0;
+        range(u, kb0, kb1);
+        return true;
+      }
+    }
+    if (stage == 1) {
+      stage = 2;
+      if (p1) {
+        u = u1;
+        range(u, kb0, kb1);
+        return true;
+      }
+    }
+    if (uw > (p1 ? u1 - 1 : u1)) return false;
+    u = uw++;
+    range(u, kb0, kb1);
     return true;
   }
 };
@@ -248,15 +314,29 @@ __device__ __forceinline__ Unit decode_unit(long long u, int R, const TokenTile*
 // unit boundary on the dependent global loads of decode_unit. Units beyond the
 // table are decoded on the fly.
 static_assert(sizeof(Unit) == 16, "segment table entry size");
+// A batch of at most 32 routed slots has at most one token tile per expert, so
+// unit u is (tile u / R, row tile u % R); its tiles live in shared memory.
+__device__ __forceinline__ Unit decode_unit_small(long long u, int R, const TokenTile* tiles) {
+  const TokenTile a = tiles[u / R];
+  Unit r;
+  r.e = a.expert;
+  r.rt = static_cast<int>(u % R);
+  r.g0 = a.g0;
+  r.ng = a.ngroups;
+  return r;
+}
+
 struct SegTable {
   const Unit* t;
   long long u0;
   int n, R;
   const TokenTile* tiles;
   const int32_t* expert_tiles;
+  const TokenTile* small_tiles;  // the small-batch tile list (shared memory), or null
   __device__ __forceinline__ Unit get(long long u) const {
     const long long s = u - u0;
-    return (s >= 0 && s < n) ? t[s] : decode_unit(u, R, tiles, expert_tiles);
+    if (s >= 0 && s < n) return t[s];
+    return small_tiles ? decode_unit_small(u, R, small_tiles) : decode_unit(u, R, tiles, expert_tiles);
   }
 };
 
@@ -270,7 +350,7 @@ struct Cursor {
   Unit un{};
   SegTable segs;
   __device__ Cursor(long long begin, long long end, int KBn, const SegTable& st)
-      : si{begin, end, KBn}, segs(st) {
+      : si(begin, end, KBn), segs(st) {
     valid = si.next(u, kb0, kb1);
   }
   __device__ __forceinline__ bool seek(long long it, int& kb) {
@@ -326,20 +406,34 @@ __device__ __forceinline__ uint16_t f16_bits_sat(float x) {
 // No lane-divergent code: every lane evaluates 8 SiLUs. The sigmoid uses the fast
 // reciprocal (a few fp32 ulps, far below the fp16 rounding of h; it tends to 0 as
 // e^-g overflows to infinity).
-__device__ __forceinline__ void swiglu_chunk(const float (&v)[16], int chunk, int quad, int lane,
-                                             uint32_t s_stage) {
+// Token row R of the tile was fed in as x * 2^-e (e = the row's prescale
+// exponent, held by lane R % 32 in e_reg, the register of R / 32): the sums are
+// multiplied back by 2^e before SiLU, and h is stored as h * 2^-2e (the down
+// GEMM's epilogue multiplies by 2^2e). A padding row (exponent kPadRowExp) has no
+// operand data: its h is stored as zero. Returns true if a stored value had to be
+// saturated to fp16's range.
+__device__ __forceinline__ bool swiglu_chunk(const float (&v)[16], int chunk, int quad, int lane,
+                                             uint32_t s_stage, int e_reg) {
   const bool is_gate = (lane & 1) == 0;
   const int f = quad * 16 + (lane >> 1);
   const int row0 = chunk * 16 + (is_gate ? 0 : 8);
+  bool sat = false;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float mine = is_gate ? v[j] : v[j + 8];
     const float other = __shfl_xor_sync(0xffffffffu, is_gate ? v[j + 8] : v[j], 1);
-    const float g = is_gate ? mine : other;
-    const float u = is_gate ? other : mine;
+    const int e_raw = __shfl_sync(0xffffffffu, e_reg, (row0 + j) & 31);
+    const bool pad = e_raw == kPadRowExp;
+    const int e = pad ? 0 : (e_raw < -kMaxRowExp ? -kMaxRowExp : (e_raw > kMaxRowExp ? kMaxRowExp : e_raw));
+    const float up_scale = exp2_int(e);
+    const float g = (is_gate ? mine : other) * up_scale;
+    const float u = (is_gate ? other : mine) * up_scale;
     const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
-    st_shared_u16(s_stage + blocked_offset(row0 + j, f), f16_bits_sat(g * sig * u));
+    const float h = pad ? 0.0f : g * sig * u * exp2_int(-2 * e);
+    sat = sat || fabsf(h) > 65504.0f;
+    st_shared_u16(s_stage + blocked_offset(row0 + j, f), f16_bits_sat(h));
   }
+  return sat;
 }
 
 template <int kMode>  // 1: gate/up + SwiGLU, 2: down + weighted scatter-add
@@ -348,18 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sB = base + kSmB, sW = base + kSmW, sStage = base + kSmStage;
+  const uint32_t sStage = base + kSmStage, sRings = base + kSmRings;
   const uint32_t sBar = base + kSmBar;
   auto bar = [sBar](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kSmMisc);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + kSmMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(gbase + kSmMisc + 8);
+  int* ng_max_sm = reinterpret_cast<int*>(gbase + kSmMisc + 12);
   volatile int* epi_ok = reinterpret_cast<volatile int*>(gbase + kSmMisc + 16);  // [2][4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t wait_ns = a.wait_kcycles;  // (the wait limit, in units of 1024 cycles)
   if (threadIdx.x == 0) TRACE_POINT(13, 0);  // kernel entry
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNWS; ++i) {
+    for (int i = 0; i < kMaxNWS; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
       mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);  // 4 quadrant warps x steps
     }
@@ -367,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       mbar_init(bar(kBarFull + i), 4);
       mbar_init(bar(kBarEmpty + i), 1);
     }
-    for (int i = 0; i < kNB; ++i) {
+    for (int i = 0; i < kMaxNB; ++i) {
       mbar_init(bar(kBarBFull + i), 1);
       mbar_init(bar(kBarBEmpty + i), 1);
     }
@@ -376,8 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       mbar_init(bar(kBarAccEmpty + i), kEpiWarps);
       mbar_init(bar(kBarDrain + i), 1);
     }
+    mbar_init(bar(kBarNever), 1);
     *abort_flag = 0;
     *last_flag = 0;
+    *ng_max_sm = 1;
     fence_mbar_init();
   }
   if (warp == kWarpMma0) {
@@ -389,44 +487,86 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // Programmatic dependent launch: wait for the preceding kernel (its outputs are
-  // read below), then let the next one launch as this grid's CTAs retire. Starting
-  // the weight stream before the wait (only the B operand depends on the
-  // preceding kernel) was measured: the early weight traffic slowed the preceding
-  // kernel's last CTAs more than it saved. The routing reads stay ordinary cached
-  // loads: they sit on the producers' path at every unit boundary.
-  pdl_wait();
-  if (threadIdx.x == 0) TRACE_POINT(13, 1);
-  const int num_tiles = a.hdr[kHdrNumTiles];
-  // cost-weighted boundaries when the align kernel wrote them (loaded alongside the
-  // header; ignored otherwise), else an even split of the steps
-  const bool weighted = a.sched != nullptr && ((a.hdr[kHdrSched] >> (kMode - 1)) & 1) != 0;
-  const long long wb0 = a.sched ? a.sched[blockIdx.x] : 0, wb1 = a.sched ? a.sched[blockIdx.x + 1] : 0;
-  long long* sched_sm = reinterpret_cast<long long*>(gbase + kSmSched);
-  const Sched sc{static_cast<long long>(num_tiles) * a.R * a.KBn, static_cast<int>(gridDim.x),
-                 weighted ? sched_sm : nullptr};
-  long long my_begin, my_end;
-  if (weighted) {  // clamped: a malformed table can misbalance, never overrun
-    my_begin = wb0 < 0 ? 0 : (wb0 > sc.W ? sc.W : wb0);
-    my_end = wb1 < my_begin ? my_begin : (wb1 > sc.W ? sc.W : wb1);
+  // Programmatic dependent launch. The general path waits for the preceding
+  // kernel here (the routing tiles are among its outputs), then lets the next one
+  // launch as this grid's CTAs retire. Starting the weight stream before that
+  // wait was measured on this path: the early weight traffic slowed the
+  // preceding kernel's last CTAs more than it saved.
+  // A small batch (at most 32 routed slots, small_ids set) instead recomputes its
+  // routing tiles here from the caller's topk_ids: one warp, one load. Only the
+  // activation producer and the epilogue read the preceding kernel's outputs, so
+  // only they wait; the weight stream starts right away (it has a whole decode
+  // step's latency to hide and the preceding kernels are small).
+  const bool small = a.small_ids != nullptr;
+  TokenTile* small_tiles = reinterpret_cast<TokenTile*>(gbase + kSmSmall);
+  int* small_ntiles = reinterpret_cast<int*>(gbase + kSmSmall + kSmallTiles * 16);
+  int num_tiles;
+  if (small) {
+    if (warp == 0) {
+      const SmallRoute r = small_route(a.small_ids, a.MK, a.E, kRowGroup, kBNMax, lane);
+      if (r.leader && r.tile0 < kSmallTiles) {  // one tile per expert present
+        TokenTile tt;
+        tt.expert = r.e;
+        tt.g0 = r.seg / kRowGroup;
+        tt.ngroups = r.pad / kRowGroup;
+        tt.first = r.tile0;
+        small_tiles[r.tile0] = tt;
+      }
+      if (lane == 0) *small_ntiles = r.tot_tiles < kSmallTiles ? r.tot_tiles : kSmallTiles;
+    }
+    __syncthreads();
+    num_tiles = *small_ntiles;
   } else {
-    my_begin = sc.start(blockIdx.x);
-    my_end = sc.start(blockIdx.x + 1);
+    pdl_wait();
+    num_tiles = a.hdr[kHdrNumTiles];
   }
+  if (threadIdx.x == 0) TRACE_POINT(13, 1);
   int* status = a.status;
+  const long long W_total = static_cast<long long>(num_tiles) * a.R * a.KBn;
+  const int G = static_cast<int>(gridDim.x);
+  // Cost-weighted boundaries when the align kernel wrote them (else an even split
+  // of the steps). Every CTA checks the whole table -- it starts at 0, ends at the
+  // step count and never decreases -- and all of them fall back to the even split
+  // (and flag the status word) if it does not: the split units' tickets rely on
+  // every CTA seeing the same boundaries.
+  bool weighted = a.sched != nullptr && ((a.hdr[kHdrSched] >> (kMode - 1)) & 1) != 0;
+  long long* sched_sm = reinterpret_cast<long long*>(gbase + kSmSched);
+  if (weighted) {
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) sched_sm[i] = a.sched[i];
+    __syncthreads();
+    bool ok = true;
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) {
+      const long long v = sched_sm[i];
+      ok = ok && v >= 0 && v <= W_total && (i < G ? v <= sched_sm[i + 1] : v == W_total) &&
+           (i > 0 || v == 0);
+    }
+    weighted = __syncthreads_and(ok) != 0;
+    if (!weighted && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSched);
+  }
+  const Sched sc{W_total, G, weighted ? sched_sm : nullptr};
+  const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
   pdl_launch_dependents();
 
-  // decode this CTA's units in parallel (one round of global loads for all)
+  // decode this CTA's units in parallel (one round of global loads for all); the
+  // widest token tile among them sizes the rings
   Unit* seg_tab = reinterpret_cast<Unit*>(gbase + kSmSeg);
   const long long u_first = my_begin / a.KBn;
   const long long n_units = my_end > my_begin ? (my_end - 1) / a.KBn - u_first + 1 : 0;
   const int n_tab = static_cast<int>(n_units < kMaxSegs ? n_units : kMaxSegs);
-  for (int i = threadIdx.x; i < n_tab; i += blockDim.x)
-    seg_tab[i] = decode_unit(u_first + i, a.R, a.tiles, a.expert_tiles);
-  if (weighted)
-    for (int i = threadIdx.x; i <= static_cast<int>(gridDim.x); i += blockDim.x) sched_sm[i] = a.sched[i];
+  if (n_units > kMaxSegs && threadIdx.x == 0) *ng_max_sm = kBNMax / kRowGroup;
+  for (int i = threadIdx.x; i < n_tab; i += blockDim.x) {
+    const Unit un = small ? decode_unit_small(u_first + i, a.R, small_tiles)
+                          : decode_unit(u_first + i, a.R, a.tiles, a.expert_tiles);
+    seg_tab[i] = un;
+    atomicMax(ng_max_sm, un.ng);
+  }
   __syncthreads();
-  const SegTable segs{seg_tab, u_first, n_tab, a.R, a.tiles, a.expert_tiles};
+  const SegTable segs{seg_tab, u_first, n_tab, a.R, a.tiles, a.expert_tiles, small ? small_tiles : nullptr};
+  // (the four configurations are compile-time constants; pick one without dividing)
+  const int ngm = *ng_max_sm;
+  const RingCfg rc = ngm <= 1 ? ring_cfg(1) : ngm == 2 ? ring_cfg(2) : ngm == 3 ? ring_cfg(3) : ring_cfg(4);
+  const int nws = rc.nws, nb = rc.nb;
+  const uint32_t sW = sRings, sB = sRings + static_cast<uint32_t>(nws) * kWChunkBytes;
 
   if (warp == kWarpW) {
     // ------------------------------------------------ packed-weight producer
@@ -443,10 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       // every row tile of their expert) or the intermediate.
       const uint64_t w_policy = l2_policy_evict_first();
       long long c = 0;
+      int s = 0;
+      uint32_t sph = 0;  // slot of chunk c, and the parity of its phase
       for (; c < n_chunks; ++c) {
-        const int s = static_cast<int>(c % kNWS);
-        if (!mbar_wait(bar(kBarWEmpty + s), ((c / kNWS) & 1) ^ 1, abort_flag, status,
-                       kStatusTimeout))
+        if (!mbar_wait(bar(kBarWEmpty + s), sph ^ 1, abort_flag, status, kStatusTimeout, wait_ns))
           break;
         const long long it0 = c * kWChunk;
         const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
@@ -468,12 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                           bar(kBarWFull + s), w_policy);
           it += run;
         }
+        if (++s == nws) {
+          s = 0;
+          sph ^= 1u;
+        }
       }
       // let the last chunks land before shared memory is released
-      for (long long j = 0; j < kNWS && j < c; ++j) {
+      for (long long j = 0; j < nws && j < c; ++j) {
         const long long idx = c - 1 - j;
-        mbar_wait_drain(bar(kBarWFull + static_cast<int>(idx % kNWS)),
-                        static_cast<uint32_t>((idx / kNWS) & 1));
+        mbar_wait_drain(bar(kBarWFull + static_cast<int>(idx % nws)),
+                        static_cast<uint32_t>((idx / nws) & 1));
       }
     }
   } else if (warp == kWarpB) {
@@ -481,12 +625,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // kProducerLanes lanes walk consecutive k-blocks in step and issue their
     // (2-8 KB) copies in one go: a bulk-copy issue holds its thread
     // for a while, so small copies must leave several at a time.
+    if (small) pdl_wait();  // the activations are the preceding kernel's output
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
       Cursor cur(my_begin, my_end, a.KBn, segs);
       long long last = -1;
       long long issued_hi = 0;  // no lane has issued a step at or beyond this index
       uint32_t mine = 0;
+      int s = lane;      // slot of this lane's step, advanced by kProducerLanes (nb is a multiple)
+      uint32_t sph = 0;  // parity of that slot's phase
       for (long long base_it = 0; base_it < n_it; base_it += kProducerLanes) {
         const long long it = base_it + lane;
         issued_hi = base_it + kProducerLanes < n_it ? base_it + kProducerLanes : n_it;
@@ -494,13 +641,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         if (it < n_it) {
           int kb = 0;
           cur.seek(it, kb);
-          if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 && cur.un.e >= 0 && cur.un.e < a.E &&
+          if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 &&
+                             static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes <= rc.b_plane &&
+                             cur.un.e >= 0 && cur.un.e < a.E &&
                              cur.un.g0 >= 0 && cur.un.g0 + cur.un.ng <= a.tiles_cap && kb >= 0 && kb < a.KBn,
                          a.status, a.dbg, 11, cur.un.ng * 1000 + cur.un.e, cur.un.g0 * 1000 + kb))
             cur.un.ng = 1;
-          const int s = static_cast<int>(it % kNB);
-          const bool ok = mbar_wait(bar(kBarBEmpty + s), ((it / kNB) & 1) ^ 1, abort_flag, status,
-                                    kStatusTimeout);
+          const bool ok = mbar_wait(bar(kBarBEmpty + s), sph ^ 1, abort_flag, status,
+                                    kStatusTimeout, wait_ns);
           __syncwarp(active);
           if (ok) {
             // the step's two 64-element k-blocks are two planes of the blocked layout
@@ -510,27 +658,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             const long long plane = static_cast<long long>(a.Gcap) * kRowGroupBytes;
             TRACE_POINT(1, it);
             mbar_arrive_expect_tx(bar(kBarBFull + s), kSub * bytes);
-            if (MOE_CHECK(boff >= 0 && boff + bytes <= a.bsrc_bytes && bytes <= kBSub && bytes > 0 &&
-                              s >= 0 && s < kNB,
+            if (MOE_CHECK(boff >= 0 && boff + bytes <= a.bsrc_bytes && bytes <= rc.b_plane && bytes > 0 &&
+                              s >= 0 && s < nb,
                           a.status, a.dbg, 2, boff, bytes))
-              bulk_g2s(sB + s * kBStage, a.bsrc + boff, bytes, bar(kBarBFull + s));
+              bulk_g2s(sB + s * rc.b_stage, a.bsrc + boff, bytes, bar(kBarBFull + s));
             if (MOE_CHECK(boff + plane + bytes <= a.bsrc_bytes, a.status, a.dbg, 3, boff + plane,
                           bytes))
-              bulk_g2s(sB + s * kBStage + kBSub, a.bsrc + boff + plane, bytes, bar(kBarBFull + s));
+              bulk_g2s(sB + s * rc.b_stage + rc.b_plane, a.bsrc + boff + plane, bytes,
+                       bar(kBarBFull + s));
             last = it;
             ++mine;
           }
           if (__any_sync(active, !ok)) break;
         }
+        s += kProducerLanes;
+        if (s >= nb) {
+          s -= nb;
+          sph ^= 1u;
+        }
       }
       // bounded wait for this lane's last copies to land before shared memory is
       // released
-      // (exactly the copies of the last kNB steps issued: no later copy reused
+      // (exactly the copies of the last nb steps issued: no later copy reused
       // their slots, so their phases cannot alias; earlier ones were consumed)
-      for (long long idx = last; mine > 0 && idx >= 0 && idx + kNB >= issued_hi;
+      for (long long idx = last; mine > 0 && idx >= 0 && idx + nb >= issued_hi;
            idx -= kProducerLanes) {
-        mbar_wait_drain(bar(kBarBFull + static_cast<int>(idx % kNB)),
-                        static_cast<uint32_t>((idx / kNB) & 1));
+        mbar_wait_drain(bar(kBarBFull + static_cast<int>(idx % nb)),
+                        static_cast<uint32_t>((idx / nb) & 1));
       }
     }
   } else if (warp == kWarpMma0 || warp == kWarpMma1) {
@@ -540,11 +694,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // other's MMAs. Each warp runs its loop uniformly; one elected lane issues.
     const uint32_t par = static_cast<uint32_t>(warp - kWarpMma0);
     uint32_t it_base = 0, acc_it = 0;
-    SegIter si{my_begin, my_end, a.KBn};
+    SegIter si(my_begin, my_end, a.KBn);
     long long u;
     int kb0, kb1;
     bool ok = true;
     const uint64_t b_desc0 = sw128_kmajor_desc(sB);
+    // B slot of this issuer's next step (its steps are 2 apart; nb is even) and
+    // the parity of that slot's phase
+    uint32_t sb = par, bph = 0;
     while (ok && si.next(u, kb0, kb1)) {
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
       const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
@@ -555,26 +712,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
-                                                    kStatusTimeout));
+                                                    kStatusTimeout, wait_ns));
         if (!ok) break;
         const uint32_t d_tmem = tmem + kAccCol0 + (par * 2 + ab) * kBNMax;
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
-          const uint32_t st = it % kNS, sb = it % kNB;
+          const uint32_t st = it % kNS;
           if (lane == 0) TRACE_POINT(2, it);
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarBFull + sb), (it / kNB) & 1,
-                                                      abort_flag, status, kStatusTimeout));
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarBFull + sb), bph, abort_flag, status,
+                                                      kStatusTimeout, wait_ns));
           if (ok)
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
-                                                        abort_flag, status, kStatusTimeout));
+                                                        abort_flag, status, kStatusTimeout, wait_ns));
           if (!ok) break;
           if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
-          // B stage sb is sb * kBStage bytes after stage 0, its second 64-element
-          // half kBSub bytes further (16-byte units in the descriptor); +32 bytes of
+          // B stage sb is sb * b_stage bytes after stage 0, its second 64-element
+          // half b_plane bytes further (16-byte units in the descriptor); +32 bytes of
           // K per MMA inside the 128-byte swizzled rows.
-          const uint64_t b_desc = b_desc0 + ((sb * kBStage) >> 4);
-          const uint64_t b_desc1 = b_desc + (kBSub >> 4);
+          const uint64_t b_desc = b_desc0 + ((sb * rc.b_stage) >> 4);
+          const uint64_t b_desc1 = b_desc + (rc.b_plane >> 4);
           if (elect_one()) {
             tc_fence_after();
             tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
@@ -590,6 +747,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             TRACE_POINT(4, it);
           }
           acc_flag = 1u;
+          sb += 2;
+          if (sb >= static_cast<uint32_t>(nb)) {
+            sb -= static_cast<uint32_t>(nb);
+            bph ^= 1u;
+          }
         }
         if (!ok) break;
         if (elect_one()) {
@@ -618,16 +780,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     const int r = quad * 32 + lane;
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
+    // weight chunk of the step (2 steps per chunk): its ring slot and phase parity,
+    // advanced by 2 chunks per iteration
+    uint32_t ws = static_cast<uint32_t>(phase) >> 1, wpar = 0;
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
-      const uint32_t wc = it >> 1;                 // weight chunk (2 steps per chunk)
-      const uint32_t ws = wc % kNWS;               // its ring slot
       const uint32_t st = it & (kNS - 1);
       // non-blocking test of the stage-free barrier now; its latency overlaps the
       // conversion and the blocking wait below runs only if it was not ready
       const bool e_early = mbar_test_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1);
       if (lane == 0 && quad == 0) TRACE_POINT(12, it);
-      bool w_ok = mbar_wait(bar(kBarWFull + ws), (wc / kNWS) & 1, abort_flag, status,
-                            kStatusTimeout);
+      bool w_ok = mbar_wait(bar(kBarWFull + ws), wpar, abort_flag, status, kStatusTimeout, wait_ns);
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(5, it);
       // the step's weights: slot ws, step (it & 1) of the chunk
@@ -645,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       dequant_group(q1, __byte_perm(sc0, 0, 0x3232), &out[16]);
       if (!__all_sync(0xffffffffu, e_early)) {
         w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                         kStatusTimeout);
+                         kStatusTimeout, wait_ns);
         if (!__all_sync(0xffffffffu, w_ok)) break;
       }
       if (lane == 0 && quad == 0) TRACE_POINT(7, it);
@@ -666,15 +828,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       __syncwarp();
       if (lane == 0) TRACE_POINT(8 + quad, it);
       if (lane == 0) mbar_arrive(bar(kBarFull + st));
+      ws += 2;
+      if (ws >= static_cast<uint32_t>(nws)) {
+        ws -= static_cast<uint32_t>(nws);
+        wpar ^= 1u;
+      }
     }
   } else if (warp >= kWarpEpi0) {
     // ------------------------------------------------ epilogue
+    if (small) pdl_wait();  // routing rows, exponents and the zeroed accumulator / tickets
+    // Test hook: wait on a barrier that nothing arrives on. The wait gives up after
+    // the wait limit, raises the abort flag and records the timeout; every role then
+    // stops at its next wait and the teardown lets in-flight copies and MMAs land.
+    if (a.test_never_wait) mbar_wait(bar(kBarNever), 0, abort_flag, a.status, kStatusTimeout, wait_ns);
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const int epi_tid = threadIdx.x - kWarpEpi0 * 32;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t acc_it = 0, it_base = 0, full_phase = 0;
-    SegIter si{my_begin, my_end, a.KBn};
+    SegIter si(my_begin, my_end, a.KBn);
     long long u;
     int kb0, kb1;
     while (si.next(u, kb0, kb1)) {
@@ -690,27 +862,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       const bool has1 = len >= 2 || (it_base & 1u) == 1;
       it_base += len;
 
-      // routing of the tile's token rows (down GEMM), fetched before the wait
-      int sid_r[kRowRegs], tok_r[kRowRegs];
+      // routing of the tile's token rows, fetched before the wait: every row's
+      // prescale exponent, and for the down GEMM its slot, token and routing
+      // weight (times 2^2e, undoing the prescale of x and of h)
+      int sid_r[kRowRegs], tok_r[kRowRegs], e_r[kRowRegs];
       float w_r[kRowRegs];
-#pragma unroll
-      for (int j = 0; j < kRowRegs; ++j) {
-        sid_r[j] = a.MK;
-        tok_r[j] = 0;
-        w_r[j] = 0.f;
-      }
-      if constexpr (kMode == 2) {
+      {
         const int pbase = un.g0 * kRowGroup;
 #pragma unroll
         for (int j = 0; j < kRowRegs; ++j) {
           const int row = 32 * j + lane;
           const bool in_tile = row < nch * 16 &&
                                MOE_CHECK(pbase + row < a.sorted_cap, a.status, a.dbg, 9, pbase + row, nch);
-          const int sid = in_tile ? a.sorted_ids[pbase + row] : a.MK;
-          sid_r[j] = sid;
-          if (sid < a.MK) {
-            w_r[j] = a.topk_weights[sid];
-            tok_r[j] = sid / a.topk;
+          e_r[j] = in_tile ? a.rowexp[pbase + row] : 0;  // (kPadRowExp for a padding row)
+          sid_r[j] = a.MK;
+          tok_r[j] = 0;
+          w_r[j] = 0.f;
+          if constexpr (kMode == 2) {
+            const int sid = in_tile ? a.sorted_ids[pbase + row] : a.MK;
+            sid_r[j] = sid;
+            if (sid < a.MK) {  // a real row: |e| <= kMaxRowExp
+              const int e = e_r[j] < -kMaxRowExp ? -kMaxRowExp : (e_r[j] > kMaxRowExp ? kMaxRowExp : e_r[j]);
+              w_r[j] = a.topk_weights[sid] * exp2_int(2 * e);
+              tok_r[j] = sid / a.topk;
+            }
           }
         }
       }
@@ -718,12 +893,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       bool w_ok = true;
       if (has0) {
         w_ok = mbar_wait(bar(kBarAccFull + ab), (full_phase >> ab) & 1u, abort_flag, status,
-                         kStatusTimeout);
+                         kStatusTimeout, wait_ns);
         full_phase ^= 1u << ab;
       }
       if (has1 && w_ok) {
         w_ok = mbar_wait(bar(kBarAccFull + 2 + ab), (full_phase >> (2 + ab)) & 1u, abort_flag,
-                         status, kStatusTimeout);
+                         status, kStatusTimeout, wait_ns);
         full_phase ^= 1u << (2 + ab);
       }
       w_ok = __all_sync(0xffffffffu, w_ok);
@@ -759,12 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       if constexpr (kMode == 1) {
         const bool full = (kb0 == 0 && kb1 == a.KBn);
         bool write_tile = full;
+        bool sat = false;
         if (full) {
           for (int c = 0; c < nch; ++c) {
             float v[16];
             load_chunk(c, v);
             if (epi_tid == 0 && c == 0) TRACE_POINT(14, 600 + acc_it * 8 + 0);  // accumulators loaded
-            swiglu_chunk(v, c, quad, lane, sStage);
+            sat |= swiglu_chunk(v, c, quad, lane, sStage, (c >> 1) ? e_r[1] : e_r[0]);
           }
           if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 1);  // SwiGLU staged
           tc_fence_before();
@@ -817,10 +993,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                   for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
                 }
               }
-              swiglu_chunk(v, c, quad, lane, sStage);
+              sat |= swiglu_chunk(v, c, quad, lane, sStage, (c >> 1) ? e_r[1] : e_r[0]);
             }
           }
         }
+        if (__any_sync(0xffffffffu, sat) && lane == 0) atomicOr(status, kStatusHSaturated);
         if (write_tile) {
           if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 2);  // tile ready to store
           fence_proxy_async_smem();

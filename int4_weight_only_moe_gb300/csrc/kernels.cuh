@@ -9,15 +9,23 @@
 
 namespace moe {
 
+// Sets *bad_scale (device) when a scale lies outside the supported range.
 cudaError_t launch_repack(const uint32_t* q, const uint16_t* s, uint8_t* out, int E, int Kred,
-                          int Nout, int R, int KBn, int interleave, cudaStream_t stream);
+                          int Nout, int R, int KBn, int interleave, int32_t* bad_scale,
+                          cudaStream_t stream);
 cudaError_t launch_unpack(const uint8_t* in, uint32_t* q, uint16_t* s, int E, int Kred, int Nout,
                           int R, int KBn, int interleave, cudaStream_t stream);
 
 // Token->expert align (counting sort + padding + token-tile list). With bn_max == 0
 // no tile list is written (the debug entry point); expert_offsets may be null.
 struct AlignArgs {
-  const int32_t* topk_ids;
+  const int32_t* topk_ids;  // device, or the routing kernel's own shared-memory copy
+  // small-batch launch only: route the tokens' router logits [M, E] here first
+  // (null: topk_ids are given), writing ids and weights to ids_out / wts_out
+  const float* logits;
+  int32_t* ids_out;
+  float* wts_out;
+  int M_tokens, topk;
   int MK;             // M * topk (flat slot count; also the padding sentinel)
   int E;
   int block;          // per-expert padding granularity
@@ -52,6 +60,7 @@ struct GatherArgs {
   const int32_t* hdr;
   int MK, topk, K, Gcap;
   uint8_t* xs;        // blocked [K/64][Gcap][16 x 128 B]
+  int32_t* rowexp;    // [padded rows] prescale exponent of each expert-sorted row
   float* acc;         // [M, K] fp32, zeroed
   long long acc_elems;
   long long xs_bytes;  // extents for the self-checking build
@@ -65,12 +74,23 @@ cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cuda
 cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
                                       int num_sms, cudaStream_t stream, bool pdl);
 
+// Router: top-k routing of logits [M, E] into ids / weights [M, k] (k <= 32).
+cudaError_t launch_route(const float* logits, int M, int E, int k, int32_t* ids, float* wts,
+                         int num_sms, cudaStream_t stream, bool pdl);
+
 struct GemmArgs {
   const uint8_t* wpack;    // packed weights of this GEMM
   const uint8_t* bsrc;     // blocked activations (B operand)
   const int32_t* hdr;
   const TokenTile* tiles;
   const int32_t* expert_tiles;
+  const int32_t* rowexp;   // prescale exponent of each expert-sorted row
+  // at most 32 routed slots: the caller's topk_ids [MK], from which the kernel
+  // recomputes the routing tiles itself (so its weight stream need not wait for
+  // the preceding kernel); null: read the tiles the align kernel wrote
+  const int32_t* small_ids;
+  uint32_t wait_kcycles;   // pipeline wait limit in units of 1024 SM cycles (wait_limit_kcycles)
+  int test_never_wait;     // test hook: the epilogue first waits on a barrier nothing arrives on
   int R;                   // row tiles per expert
   int KBn;                 // k-blocks per unit
   int Gcap;                // row groups per k-block plane of bsrc / hout
@@ -99,8 +119,8 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int nu
                             cudaStream_t stream, bool pdl);
 
 cudaError_t launch_read_intermediate(const uint8_t* hbuf, const int32_t* sorted_ids,
-                                     const int32_t* hdr, int MK, int N, int Gcap, int max_rows,
-                                     uint16_t* h_rows, cudaStream_t stream);
+                                     const int32_t* rowexp, const int32_t* hdr, int MK, int N,
+                                     int Gcap, int max_rows, float* h_rows, cudaStream_t stream);
 
 // Self-checking build (-DMOE_CHECKS): every global access is range-checked first;
 // a failed check sets status bit 8, records the first failure (site, two values,

@@ -61,6 +61,33 @@ struct TokenTile {
 // even split of that GEMM's steps.
 enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrSched = 3, kHdrWords = 64 };
 
+// Device status bits (the public values are in the C header).
+enum {
+  kStatusBadId = 1,       // a routed expert id outside [0, E) was skipped
+  kStatusTimeout = 2,     // a pipeline wait gave up
+  kStatusHSaturated = 4,  // an intermediate activation exceeded fp16's range (saturated)
+  kStatusCheck = 8,       // self-checking build: a range check failed
+  kStatusBadSched = 16    // malformed stream-K boundaries: the GEMMs split their steps evenly
+};
+
+// Per-token power-of-two prescale of the hidden states. A token row x is fed to
+// the tensor cores as x * 2^-e (exact), with e chosen from the row's largest
+// magnitude so that it lands in [4, 8): every row then sits in the same, safe
+// part of fp16's range whatever its own scale. The gate/up epilogue multiplies
+// the accumulators back by 2^e before SiLU and stores h * 2^-2e; the down
+// epilogue multiplies by 2^2e. |e| <= kMaxRowExp keeps 2^e and 2^2e normal floats.
+constexpr int kMaxRowExp = 63;
+constexpr int kPadRowExp = -1000;  // the exponent recorded for a padding row
+__host__ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, |e| <= 126
+#ifdef __CUDA_ARCH__
+  return __int_as_float((127 + e) << 23);
+#else
+  union { int i; float f; } u;
+  u.i = (127 + e) << 23;
+  return u.f;
+#endif
+}
+
 // Relative cost of one pipeline step of a unit whose token tile holds ng row
 // groups: a base of 8 plus `per_group` for every row group beyond the second. The
 // weight stream (9 KB a step from HBM) and its conversion are the same for every

@@ -44,6 +44,16 @@ __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t dst) {
 // Scales are kept as fp16 in the packed layout (the tensor-core operand type):
 // exact for bf16 scales inside fp16's normal range, which the dequantisation
 // needs anyway; the inverse conversion restores the bf16 bits exactly there.
+//
+// Supported scales: zero, or a finite magnitude in [2^-14, 8160]. Inside that set
+// the fp16 scale equals the bf16 one and every dequantised weight (u - 8) * s
+// (at most 3 + 8 significant bits, |u - 8| <= 8) is an exact fp16 normal number
+// no larger than 65280; outside it a weight would be rounded, flushed or
+// infinite, so the repack flags the scale instead.
+__device__ __forceinline__ bool scale_supported(uint16_t b) {
+  const uint32_t m = b & 0x7FFFu;             // bf16 magnitude bits
+  return m == 0 || (m >= 0x3880u && m <= 0x45FFu);  // 0, or 2^-14 .. 8160
+}
 __device__ __forceinline__ uint16_t bf16_to_f16_bits(uint16_t b) {
   return __half_as_ushort(__float2half_rn(__uint_as_float(static_cast<uint32_t>(b) << 16)));
 }
@@ -57,7 +67,8 @@ __device__ __forceinline__ uint16_t f16_to_bf16_bits(uint16_t h) {
 __global__ void __launch_bounds__(256) repack_kernel(const uint32_t* __restrict__ q,
                                                      const uint16_t* __restrict__ s,
                                                      uint8_t* __restrict__ out, int Kred,
-                                                     int Nout, int R, int KBn, int interleave) {
+                                                     int Nout, int R, int KBn, int interleave,
+                                                     int32_t* __restrict__ bad_scale) {
   const long long blk = blockIdx.x;
   const int kb = static_cast<int>(blk % KBn);
   const int rt = static_cast<int>((blk / KBn) % R);
@@ -77,7 +88,9 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint32_t* __restrict_
   for (int t = threadIdx.x; t < 256; t += blockDim.x) {
     const int r = t & 127, h = t >> 7;
     const int f = tile_row_source(rt, r, Nout, interleave);
-    ds[r * 2 + h] = bf16_to_f16_bits(s[(e * srows + kb * 2 + h) * Nout + f]);
+    const uint16_t b = s[(e * srows + kb * 2 + h) * Nout + f];
+    if (!scale_supported(b)) *bad_scale = 1;
+    ds[r * 2 + h] = bf16_to_f16_bits(b);
   }
 }
 
@@ -107,11 +120,12 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
 }
 
 cudaError_t launch_repack(const uint32_t* q, const uint16_t* s, uint8_t* out, int E, int Kred,
-                          int Nout, int R, int KBn, int interleave, cudaStream_t stream) {
+                          int Nout, int R, int KBn, int interleave, int32_t* bad_scale,
+                          cudaStream_t stream) {
   const long long blocks = static_cast<long long>(E) * R * KBn;
   if (blocks <= 0) return cudaSuccess;
   repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q, s, out, Kred, Nout, R, KBn,
-                                                                   interleave);
+                                                                   interleave, bad_scale);
   return cudaGetLastError();
 }
 

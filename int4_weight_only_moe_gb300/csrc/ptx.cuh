@@ -29,16 +29,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 // Test the phase; a thread whose phase is not complete is suspended in hardware
-// until it completes or about `kSuspendHintNs` pass, so waiting costs no issue slots.
+// until it completes or about `hint_ns` pass (kSuspendHintNs by default), so
+// waiting costs no issue slots.
 constexpr uint32_t kSuspendHintNs = 100000;
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
+                                              uint32_t hint_ns = kSuspendHintNs) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -73,24 +75,35 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Longest time any single pipeline wait may take before the kernel gives up.
-// Normal waits last micro- to milliseconds; this only ends a broken pipeline.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// Longest time any single pipeline wait may take before the kernel gives up,
+// counted in SM clock cycles (the cycle counter always advances; the global
+// timer may tick coarsely), in units of 1,024 cycles so that one 32-bit register
+// holds it. Default: 2 s at 4 GHz, i.e. about 4 s at this part's 2 GHz. Normal
+// waits last micro- to milliseconds; this only ends a broken pipeline. (A
+// handle option can shorten it, to exercise the give-up path.)
+constexpr uint32_t kWaitLimitKCyclesDefault = 7812500u;  // 8e9 cycles / 1024
+__host__ __device__ constexpr uint32_t wait_limit_kcycles(unsigned long long limit_us) {
+  // 4 cycles a nanosecond: at least the requested time at clocks up to 4 GHz
+  return limit_us == 0 ? kWaitLimitKCyclesDefault
+                       : (limit_us * 4000ull / 1024ull >= 0xFFFFFFFFull
+                              ? 0xFFFFFFFFu
+                              : static_cast<uint32_t>(limit_us * 4000ull / 1024ull + 1));
+}
 
 // Wait for the phase of parity `parity` of `bar` to complete: a non-blocking test
 // first (cheapest when the phase is already complete, the common case), then
 // suspended tries. Returns false if another thread of the CTA has raised
-// `abort_flag`, or if the wait has lasted longer than kWaitTimeoutNs (then it
-// raises the flag and records `status_bit` in the global status word). Never
-// spins without bound.
+// `abort_flag`, or if the wait has lasted longer than `limit_kcycles` * 1024 SM
+// cycles (then it raises the flag and records `status_bit` in the global status
+// word). Never spins without bound.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int status_bit) {
+                                          int* status, int status_bit, uint32_t limit_kcycles) {
   if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long c0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (((clock64() - c0) >> 10) > static_cast<long long>(limit_kcycles)) {
       *abort_flag = 1;
       atomicOr(status, status_bit);
       return false;

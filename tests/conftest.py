@@ -9,6 +9,9 @@ if ROOT not in sys.path:
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
+# Parity margins recorded by the full-size tests, printed at the end of the session.
+MARGINS = []
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
@@ -24,3 +27,10 @@ def read_golden(name):
                 continue
             rows.append(line.split())
     return rows
+
+
+def pytest_terminal_summary(terminalreporter):
+    if MARGINS:
+        terminalreporter.section("parity margins (GPU vs oracle)")
+        for line in MARGINS:
+            terminalreporter.write_line(line)

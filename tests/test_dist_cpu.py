@@ -42,23 +42,53 @@ def test_replica_time_is_max_over_ranks():
     assert [g[2] for g in got] == [(0, 0, 2), (1, 1, 2)]
 
 
+class _FakePool:
+    procs = 4
+
+    def __init__(self, *a, **k):
+        pass
+
+    def close(self):
+        pass
+
+
 def test_reference_arm_runs_on_rank0_only(monkeypatch, capsys):
     import bench
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
     called = []
-    monkeypatch.setattr(bench, "oracle_step", lambda wl, s: called.append(s) or 0.1)
+    monkeypatch.setattr(bench, "OraclePool", _FakePool)
+    monkeypatch.setattr(bench, "oracle_call", lambda pool, wl, s: called.append(s) or (0.1, 8))
     bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"])
     assert called == [] and capsys.readouterr().out == ""
 
 
 def test_reference_arm_line(monkeypatch, capsys):
+    # the reference arm honours --steps and --warmup and reports the GPU arm's config
     import json
     import bench
     monkeypatch.setenv("RANK", "0")
     monkeypatch.setenv("WORLD_SIZE", "1")
-    monkeypatch.setattr(bench, "oracle_step", lambda wl, s: 0.5)
+    called = []
+    monkeypatch.setattr(bench, "OraclePool", _FakePool)
+    monkeypatch.setattr(bench, "oracle_call", lambda pool, wl, s: called.append(s) or (0.5, 8))
     bench.main(["--impl", "reference", "--steps", "4", "--warmup", "3"])
     line = json.loads(capsys.readouterr().out.strip())
+    assert called == list(range(7))
     assert line["impl"] == "reference" and line["value"] == pytest.approx(2.0)
+    assert line["steps"] == 4 and line["warmup"] == 3
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["config"] == bench.headline_config(bench.inputs.WORKLOADS["decode"], 1)
+    assert line["cpu_baseline"]["cores"] == 4
+
+
+def test_oracle_pool_times_expert_shares():
+    # the pooled oracle timing runs real oracle arithmetic on a tiny workload
+    import bench
+    wl = bench.inputs.WORKLOADS["tiny"]
+    pool = bench.OraclePool(procs=2)
+    try:
+        wall, n = bench.oracle_call(pool, wl, 0)
+    finally:
+        pool.close()
+    assert n >= 1 and wall > 0

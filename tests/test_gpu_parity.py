@@ -11,7 +11,7 @@ import torch
 import int4_weight_only_moe_gb300 as pkg
 import oracle
 from int4_weight_only_moe_gb300 import inputs
-from tests.gpu_helpers import Problem, assert_close, bf16_tensor_to_f64, bits16, dev
+from tests.gpu_helpers import Problem, assert_close, bf16_tensor_to_f64, bits16, dev, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -147,7 +147,7 @@ def check_forward(prob, hidden, ids, wts, what):
 def test_tiny_forward_and_intermediate():
     wl = inputs.WORKLOADS["tiny"]
     prob = Problem(wl.E, wl.K, wl.N, wl.topk)
-    hidden, ids, wts = inputs.workload_inputs(wl)
+    hidden, ids, wts = workload_inputs(wl)
     check_forward(prob, hidden, ids, wts, "tiny")
     h_rows = bf16_tensor_to_f64(prob.moe.intermediate(wl.M))
     x = oracle.bf16_to_f64(hidden)
@@ -156,7 +156,7 @@ def test_tiny_forward_and_intermediate():
         for j in range(wl.topk):
             w1, _ = oracle.expert_dense(*prob.w, int(ids[t, j]))
             ref_h[t * wl.topk + j] = oracle.expert_hidden(x[t:t + 1], w1)[0]
-    assert_close(h_rows, ref_h, "tiny intermediate")
+    assert_close(h_rows, ref_h, "tiny intermediate", bf16_output=False)
     prob.close()
 
 
@@ -166,7 +166,7 @@ def test_mid_forward_grid_sizes(M, num_ctas):
     E, K, N, k = 16, 512, 256, 4
     prob = Problem(E, K, N, k, num_ctas=num_ctas)
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
-    hidden, ids, wts = inputs.workload_inputs(wl)
+    hidden, ids, wts = workload_inputs(wl)
     check_forward(prob, hidden, ids, wts, f"mid M={M} ctas={num_ctas}")
     prob.close()
 
@@ -210,7 +210,7 @@ def test_cost_weighted_stream_k_shares(step_cost, num_ctas):
 def test_bad_expert_ids_are_skipped_and_flagged():
     wl = inputs.WORKLOADS["tiny"]
     prob = Problem(wl.E, wl.K, wl.N, wl.topk)
-    hidden, ids, wts = inputs.workload_inputs(wl)
+    hidden, ids, wts = workload_inputs(wl)
     ids = ids.copy()
     ids[1, 0] = -3
     ids[2, 1] = wl.E
@@ -227,7 +227,7 @@ def test_zero_tokens_and_small_workspace():
     empty = torch.zeros((0, wl.K), dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     pkg.moe_w4a16_forward(h, empty, empty, empty, empty, 0, ws)  # M == 0 is a no-op
-    hidden, ids, wts = inputs.workload_inputs(wl)
+    hidden, ids, wts = workload_inputs(wl)
     out = torch.empty((wl.M, wl.K), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(pkg.MoeW4A16Error) as ei:
         pkg.moe_w4a16_forward(h, dev(bits16(hidden)), dev(ids), dev(wts), out, wl.M, ws)
@@ -239,7 +239,7 @@ def test_forward_host_matches_device_forward():
     E, K, N, k, M = 16, 512, 256, 4, 23
     prob = Problem(E, K, N, k)
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
-    hidden, ids, wts = inputs.workload_inputs(wl)
+    hidden, ids, wts = workload_inputs(wl)
     dev_out = prob.run(hidden, ids, wts)
     h_hidden = torch.from_numpy(bits16(hidden)).pin_memory()
     h_ids = torch.from_numpy(ids).pin_memory()
@@ -280,7 +280,7 @@ def test_forward_host_zero_copy_and_staged_paths():
             continue
         M = what
         wl = inputs.Workload("mid", E, K, N, k, M, "normal")
-        hidden, ids, wts = inputs.workload_inputs(wl, step=seed)
+        hidden, ids, wts = workload_inputs(wl, step=seed)
         host_out = _host_forward(prob, hidden, ids, wts, pinned=arg)
         dev_out = prob.run(hidden, ids, wts)
         assert_within_one_ulp(host_out, dev_out)
@@ -296,7 +296,7 @@ def test_forward_replays_from_a_cuda_graph(M):
     E, K, N, k = 16, 512, 256, 4
     prob = Problem(E, K, N, k)
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
-    steps = [inputs.workload_inputs(wl, step=s) for s in range(3)]
+    steps = [workload_inputs(wl, step=s) for s in range(3)]
     static = [dev(bits16(steps[0][0])), dev(steps[0][1]), dev(steps[0][2])]
     out = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     prob.moe.ensure_workspace(M)
@@ -327,10 +327,192 @@ def test_repeated_calls_agree():
     E, K, N, k, M = 16, 512, 256, 4, 64
     prob = Problem(E, K, N, k)
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
-    hidden, ids, wts = inputs.workload_inputs(wl)
+    hidden, ids, wts = workload_inputs(wl)
     a = prob.run(hidden, ids, wts)
     b = prob.run(hidden, ids, wts)
     # the down GEMM adds partial products with float atomics: only the summation
     # order may differ, which can flip the last bit of the bf16 output
     assert_within_one_ulp(a, b)
+    prob.close()
+
+
+# ---------------------------------------------------------------------------- router
+
+
+@pytest.mark.parametrize("M,E,k,routing", [
+    (1, 384, 8, "uniform"), (9, 384, 8, "normal"), (1024, 384, 8, "zipf"), (1024, 384, 8, "normal"),
+    (37, 40, 5, "ties"), (5, 1024, 32, "normal"), (3, 7, 7, "normal"), (64, 33, 1, "ties"),
+])
+def test_router_matches_oracle(M, E, k, routing):
+    # ids bit-exact (ties by ascending expert id), weights to fp32 rounding
+    if routing == "ties":
+        logits = (np.round(np.random.default_rng(M).standard_normal((M, E)) * 2) / 2).astype(np.float32)
+    else:
+        logits = inputs.router_logits(M, E, routing)
+    ref_ids, ref_w = oracle.route(logits, k)
+    d_ids = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+    d_w = torch.full((M, k), -1.0, dtype=torch.float32, device="cuda")
+    pkg.moe_w4a16_route(dev(logits), M, E, k, d_ids, d_w)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(d_ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(d_w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("M", [1, 4, 37])
+def test_forward_logits_routes_then_runs_the_forward(M):
+    # M * k <= 32 routes inside the first launch, larger batches in a router launch
+    E, K, N, k = 16, 512, 256, 8
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, logits = inputs.workload_inputs(wl)
+    ref_ids, ref_w = oracle.route(logits, k)
+    out, d_ids, d_w = prob.moe.forward_logits(dev(bits16(hidden)), dev(logits))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(d_ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(d_w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-9)
+    got = bf16_tensor_to_f64(out)
+    assert prob.moe.status() == 0
+    assert_close(got, prob.reference(hidden, ref_ids, ref_w.astype(np.float32)), f"forward_logits M={M}")
+    assert_within_one_ulp(got, prob.run(hidden, d_ids.cpu().numpy(), d_w.cpu().numpy()))
+    prob.close()
+
+
+# ---------------------------------------------------------------------------- fp16 operand range
+
+
+@pytest.mark.parametrize("bad", [0x4600, 0xC600, 0x3870, 0x0001, 0x7F80, 0x7FC0, 0xFF80])
+def test_pack_rejects_unsupported_scales(bad):
+    # 8192, -8192 (a weight of 8 * 8192 overflows fp16), just below 2^-14 (not exact
+    # in fp16), a subnormal, +inf, NaN, -inf
+    E, K, N = 2, 256, 128
+    q1, s1, q2, s2 = inputs.all_expert_weights(E, K, N)
+    s2 = s2.copy()
+    s2[1, 3, 77] = bad
+    moe = pkg.MoEW4A16(E, K, N, 2)
+    with pytest.raises(pkg.MoeW4A16Error) as ei:
+        moe.pack(dev(q1), dev(bits16(s1)), dev(q2), dev(bits16(s2)))
+    assert ei.value.code == pkg.UNSUPPORTED_SCALE
+    with pytest.raises(pkg.MoeW4A16Error) as ei:  # the handle stays unpacked
+        moe.forward(dev(bits16(inputs.hidden_states(1, K))), dev(np.zeros((1, 2), np.int32)),
+                    dev(np.full((1, 2), 0.5, np.float32)))
+    assert ei.value.code == pkg.NOT_PACKED
+    moe.close()
+
+
+def test_boundary_scales_are_exact():
+    # 0, -0 and 2^-14 (the smallest accepted magnitude) in the gate/up scales, 8160
+    # and -8160 (the largest) in the down scales -- in the gate/up scales those
+    # would only overflow the intermediate, whatever the format -- are accepted,
+    # and the forward stays exact with them
+    E, K, N, k, M = 4, 256, 128, 2, 6
+    q1, s1, q2, s2 = inputs.all_expert_weights(E, K, N)
+    s1, s2 = s1.copy(), s2.copy()
+    rng = np.random.default_rng(9)
+    for arr, vals in ((s1, [0x0000, 0x8000, 0x3880, 0xB880]), (s2, [0x45FF, 0xC5FF, 0x3880, 0x0000])):
+        flat = arr.reshape(-1)
+        idx = rng.choice(flat.size, size=40, replace=False)
+        flat[idx] = np.array(vals * 10, dtype=np.uint16)
+    prob = Problem(E, K, N, k, weights=(q1, s1, q2, s2))
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    got = prob.run(hidden, ids, wts)
+    assert prob.moe.status() == 0
+    assert_close(got, prob.reference(hidden, ids, wts), "boundary scales")
+    prob.close()
+
+
+def per_row_errors(got, ref):
+    out = []
+    for t in range(ref.shape[0]):
+        r, g = ref[t], got[t]
+        nr = np.linalg.norm(r)
+        rms = np.sqrt(np.mean(r ** 2))
+        out.append((np.linalg.norm(g - r) / nr, np.max(np.abs(g - r)) / rms) if nr > 0 else (0.0, 0.0))
+    return out
+
+
+@pytest.mark.parametrize("M", [3, 12])
+def test_hidden_rows_far_outside_fp16_range(M):
+    # every token row is fed in at a power-of-two prescale chosen from its own largest
+    # magnitude: rows from 1e-15 to 1e15 (fp16 covers 6e-5 .. 65504) all match the
+    # oracle row by row; M = 3 (12 slots) takes the small-batch gather, M = 12 the
+    # general one
+    E, K, N, k = 8, 512, 256, 4
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    x = oracle.bf16_to_f64(hidden).astype(np.float32)
+    factors = np.array([1e6, 1e-6, 3e4, 1e15, 1e-15, 0.0, 1.0, 7e10, 2e-9, 65504.0, 1e5, 1e-4])[:M]
+    x = (x * factors[:, None].astype(np.float32)).astype(np.float32)
+    big = inputs.f32_to_bf16_bits(x)
+    got = prob.run(big, ids, wts)
+    ref = prob.reference(big, ids, wts)
+    assert prob.moe.status() == 0
+    assert np.all(np.isfinite(got))
+    for t, (rel, mx) in enumerate(per_row_errors(got, ref)):
+        if factors[t] == 0.0:
+            assert np.all(got[t] == 0.0)
+            continue
+        assert rel <= 5e-3 and mx <= 2e-2, f"row {t} (scale {factors[t]:g}): rel {rel:.3e} max/rms {mx:.3e}"
+    prob.close()
+
+
+def test_intermediate_saturation_sets_status():
+    # gate/up scales of 8160 make SiLU(g) * u far exceed fp16's range even for
+    # prescaled rows: the epilogue saturates and says so; a normal call is clean again
+    E, K, N, k, M = 4, 256, 128, 2, 3
+    q1, s1, q2, s2 = inputs.all_expert_weights(E, K, N)
+    hot = np.full_like(s1, 0x45FF)
+    prob = Problem(E, K, N, k, weights=(q1, hot, q2, s2))
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    prob.run(hidden, ids, wts)
+    assert prob.moe.status() & pkg.STATUS_H_SATURATED
+    prob.close()
+    prob = Problem(E, K, N, k, weights=(q1, s1, q2, s2))
+    check_forward(prob, hidden, ids, wts, "after saturation")
+    prob.close()
+
+
+# ---------------------------------------------------------------------------- give-up path
+
+
+@pytest.mark.parametrize("M", [4, 40])
+def test_wait_limit_gives_up_cleanly(M):
+    # Each GEMM's epilogue is made to wait on a barrier that nothing ever arrives on,
+    # with a 1 ms limit: the wait gives up, the kernels flag MOE_W4A16_STATUS_TIMEOUT,
+    # every role stops at its next wait, in-flight copies and MMAs land, tensor
+    # memory is freed and the call returns. The next call on the same handle, with
+    # the hook off and the default limit, is clean and correct.
+    E, K, N, k = 8, 512, 256, 4
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    h = prob.moe.handle
+    pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 1000)
+    pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 1)
+    prob.run(hidden, ids, wts)  # returns; its output is not meaningful
+    assert prob.moe.status() & pkg.STATUS_TIMEOUT
+    pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 0)
+    pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 0)
+    check_forward(prob, hidden, ids, wts, f"after give-up M={M}")
+    prob.close()
+
+
+# ---------------------------------------------------------------------------- duplicate experts
+
+
+@pytest.mark.parametrize("M", [3, 40])
+def test_forward_with_duplicate_experts_in_a_token(M):
+    # a token may name one expert in several of its slots: each slot is an
+    # independent routed row (its own weight), as the oracle defines
+    E, K, N, k = 6, 512, 256, 4
+    prob = Problem(E, K, N, k)
+    rng = np.random.default_rng(M)
+    ids = rng.integers(0, E, size=(M, k)).astype(np.int32)
+    ids[0] = [2, 2, 2, 5]
+    ids[1] = [1, 1, 4, 4]
+    hidden = inputs.hidden_states(M, K)
+    wts = rng.uniform(0.1, 1.0, size=(M, k)).astype(np.float32)
+    check_forward(prob, hidden, ids, wts, f"duplicates M={M}")
     prob.close()

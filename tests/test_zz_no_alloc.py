@@ -15,7 +15,7 @@ import torch
 
 import int4_weight_only_moe_gb300 as pkg
 from int4_weight_only_moe_gb300 import inputs
-from tests.gpu_helpers import Problem, assert_close, bf16_tensor_to_f64, bits16, dev
+from tests.gpu_helpers import Problem, assert_close, bf16_tensor_to_f64, bits16, dev, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def _built():
 
 
 def run_both(prob, wl, step):
-    hidden, ids, wts = inputs.workload_inputs(wl, step=step)
+    hidden, ids, wts = workload_inputs(wl, step=step)
     d_h, d_ids, d_w = dev(bits16(hidden)), dev(ids), dev(wts)
     ref = prob.moe.forward(d_h, d_ids, d_w)
     out = torch.full((wl.M, wl.K), float("nan"), dtype=torch.bfloat16, device="cuda")
