@@ -105,7 +105,8 @@ size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M);
  *   topk_weights fp32  [M, topk]
  *   out          bf16  [M, K]      written completely (rounded to nearest even)
  *   workspace    >= moe_w4a16_workspace_size(h, M) bytes, 256-byte aligned
- * M == 0 is a no-op. Launches 5 kernels on `stream` (4 when M * topk <= 32),
+ * M == 0 is a no-op. Launches 5 kernels on `stream` (3 when M * topk <= 32:
+ * routing + gather, gate/up GEMM, down GEMM with the bf16 rounding folded in),
  * allocates nothing and makes no host-synchronising call, so it may be captured
  * into a CUDA graph and replayed with new inputs in the same buffers. */
 int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
@@ -188,7 +189,8 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order
  * (align, gather, gemm1, gemm2, finalize); when M * topk <= 32 the routing and
- * the gather run as one kernel, reported as align (gather then reads ~0).
+ * the gather run as one kernel, reported as align (gather then reads ~0), and the
+ * down GEMM rounds the output itself (finalize then reads ~0).
  * Synchronises on the recorded events.
  * `n` is the capacity of `ms`; returns the number written or a negative code. */
 int moe_w4a16_kernel_times(moe_w4a16_t h, float* ms, int n);

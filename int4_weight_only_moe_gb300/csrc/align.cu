@@ -401,10 +401,14 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
   __shared__ int32_t s_ids[32];
   __shared__ int s_red[kGatherWarps + 1];
   pdl_wait();
-  AlignArgs a = a_in;
+  // The GEMM that follows starts its weight stream on its own; where it reads
+  // this kernel's outputs it waits for this grid to complete. Let it launch now.
+  pdl_launch_dependents();
+  const AlignArgs& a = a_in;
   if (a.logits) {
     // route the (at most 32 / k) tokens first: warp w takes tokens w, w + 8, ...;
-    // CTA 0 publishes ids and weights, every CTA keeps the ids for its own use
+    // CTA 0 publishes ids and weights, every CTA keeps the ids in shared memory
+    // for its own use (the published copy is written concurrently by CTA 0)
     const int lane = threadIdx.x & 31;
     for (int t = threadIdx.x >> 5; t < a.M_tokens; t += kGatherWarps) {
       int id;
@@ -419,11 +423,12 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
       }
     }
     __syncthreads();
-    a.topk_ids = s_ids;
   }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    const SmallRoute r = small_route(a, lane);
+    int v = -1;  // this lane's slot id: from shared memory when routed here, else the input
+    if (lane < a.MK) v = a.logits ? s_ids[lane] : a.topk_ids[lane];
+    const SmallRoute r = small_route_ids(v, a.MK, a.E, a.block, a.bn_max, lane);
     const int npad = r.tot_pad < kSmallPadRows ? r.tot_pad : kSmallPadRows;
     for (int p = lane; p < npad; p += 32) s_sorted[p] = a.MK;
     __syncwarp();
@@ -437,7 +442,6 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
   float4* acc4 = reinterpret_cast<float4*>(g.acc);
   for (long long i = gt; i < g.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int p = blockIdx.x; p < s_npad; p += gridDim.x) gather_row(g, p, s_sorted[p], s_red);
-  pdl_launch_dependents();
 }
 
 cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,

@@ -94,8 +94,8 @@ WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   L.hdr = off;
   off += kHdrWords * sizeof(int32_t);
   off = align_up(off, 256);
-  L.tickets = off;
-  off = align_up(off + kMaxCtas * sizeof(int32_t), 256);
+  L.tickets = off;  // gate/up split-unit tickets [kMaxCtas], then the down row-tile tickets [K/128]
+  off = align_up(off + (kMaxCtas + h->K / kBM) * sizeof(int32_t), 256);
   L.sched = off;  // stream-K boundaries of the two GEMMs
   off = align_up(off + 2 * (kMaxCtas + 1) * sizeof(long long), 256);
   L.sorted = off;
@@ -350,7 +350,7 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   aa.expert_tiles = expert_tiles;
   aa.hdr = hdr;
   aa.tickets = tickets;
-  aa.n_tickets = kMaxCtas;
+  aa.n_tickets = kMaxCtas + h->K / kBM;
   aa.sorted_cap = L.Pcap;
   aa.tiles_cap = L.Gcap;
   aa.dbg = hdr + 8;
@@ -441,6 +441,12 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.wait_kcycles = wait_limit_kcycles(h->wait_us);
   g2.test_never_wait = h->test_never_wait ? 1 : 0;
   g2.small_ids = small_ids;
+  // small batches (the routing + gather launch zeroes every ticket): the down GEMM
+  // rounds each finished output row tile to bf16 itself, with no finalize launch
+  const bool fold_finalize = MK <= 32;
+  g2.rt_tickets = fold_finalize ? tickets + kMaxCtas : nullptr;
+  g2.out = out;
+  g2.M = M;
   g2.R = h->K / kBM;
   g2.KBn = h->N / (2 * kBK);
   g2.Gcap = L.Gcap;
@@ -462,7 +468,8 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 
-  MOE_CUDA_TRY(launch_finalize(acc, out, static_cast<long long>(M) * h->K, h->num_sms, s, pdl));
+  if (!fold_finalize)
+    MOE_CUDA_TRY(launch_finalize(acc, out, static_cast<long long>(M) * h->K, h->num_sms, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[5], s));
   return MOE_W4A16_OK;
 }

@@ -55,6 +55,7 @@
 // raises a CTA-wide abort flag, records MOE_W4A16_STATUS_TIMEOUT, and all roles
 // fall through to the teardown, which still waits for in-flight copies and MMAs
 // and frees tensor memory.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
@@ -102,10 +103,17 @@ constexpr int kSub = 2;
 constexpr int kWStepBytes = kSub * kWBlockBytes;  // packed weights of one step (9 KB)
 constexpr int kWChunk = 2;               // steps per weight copy (one 18 KB bulk copy)
 constexpr int kWChunkBytes = kWChunk * kWStepBytes;
-constexpr int kNS = 4;                   // A operand stage ring (tensor memory)
+// A operand stage ring in tensor memory: 6 stages when the CTA's widest token tile
+// has at most two row groups (the accumulators then take at most 4 x 32 columns),
+// else 4. More stages give each dequantisation warp more slack between storing a
+// stage and needing it again.
+constexpr int kNS = 4;                   // stages with tiles of three or four row groups
+constexpr int kNSNarrow = 6;             // stages with tiles of at most two row groups
+constexpr int kNSMax = kNSNarrow;
 constexpr int kTmemCols = 512;
 constexpr int kACols = kSub * 32;        // one step of fp16 A: 128 lanes x 64 columns
-constexpr int kAccCol0 = kNS * kACols;   // accumulators follow the A ring
+// accumulators follow the A ring: 4 of them (2 issuers x 2 buffers), each as wide
+// as the CTA's widest token tile
 constexpr int kProducerLanes = 4;        // copy-issuing threads per producer warp
 
 // The two shared-memory rings (packed weights, activation tiles) divide one
@@ -123,8 +131,8 @@ constexpr int kBRowGroupStep = kSub * kRowGroupBytes;  // B bytes of one row gro
 constexpr int kBarWFull = 0;                     // weight chunk landed (bulk-copy bytes)
 constexpr int kBarWEmpty = kBarWFull + kMaxNWS;  // weight chunk read (4 dequant warps per step)
 constexpr int kBarFull = kBarWEmpty + kMaxNWS;   // A stage ready: stored by its 4 dequant warps
-constexpr int kBarEmpty = kBarFull + kNS;        // A stage consumed by the MMAs (tcgen05.commit)
-constexpr int kBarBFull = kBarEmpty + kNS;       // B stage landed (bulk-copy bytes)
+constexpr int kBarEmpty = kBarFull + kNSMax;     // A stage consumed by the MMAs (tcgen05.commit)
+constexpr int kBarBFull = kBarEmpty + kNSMax;    // B stage landed (bulk-copy bytes)
 constexpr int kBarBEmpty = kBarBFull + kMaxNB;   // B stage consumed by the MMAs (tcgen05.commit)
 constexpr int kBarAccFull = kBarBEmpty + kMaxNB; // [issuer][buffer]: accumulator complete
 constexpr int kBarAccEmpty = kBarAccFull + 4;    // [buffer]: epilogue has read both issuers' sums
@@ -144,9 +152,9 @@ constexpr int kSmRings = ((kSmSmall + kSmallTiles * 16 + 16 + 1023) / 1024) * 10
 constexpr int kSmAlloc = 227 * 1024;     // the whole per-CTA limit (base aligned to 1024 inside)
 constexpr int kRingBytes = kSmAlloc - 1024 - kSmRings;
 static_assert(kSmRings < kSmAlloc - 1024, "shared memory budget");
-static_assert(kAccCol0 + 4 * kBNMax <= kTmemCols, "tensor memory budget");
-static_assert((kNS & (kNS - 1)) == 0 && kWChunk == 2,
-              "stage index arithmetic below assumes a power-of-two A ring and 2-step chunks");
+static_assert(kNS * kACols + 4 * kBNMax <= kTmemCols && kNSNarrow * kACols + 4 * 32 <= kTmemCols,
+              "tensor memory budget");
+static_assert(kWChunk == 2, "the chunk arithmetic below assumes 2-step chunks");
 
 // Ring depths for a CTA whose widest token tile has `ng` row groups: nws weight
 // chunks (an even number: the parity arguments below need even depths) and
@@ -186,7 +194,7 @@ constexpr bool stage_reuse_is_safe(int phases, int stages) {
     if ((stages - j * phases) % 2 == 0) return true;
   return false;
 }
-static_assert(stage_reuse_is_safe(kDeqPhases, kNS),
+static_assert(stage_reuse_is_safe(kDeqPhases, kNS) && stage_reuse_is_safe(kDeqPhases, kNSNarrow),
               "a dequantisation warp could pass a stale Empty phase (parity aliasing)");
 // The MMA issuer that waits on a B (or A) stage for step it consumed the
 // previous phase itself (step it - depth) only if the depth is even; a B
@@ -194,7 +202,8 @@ static_assert(stage_reuse_is_safe(kDeqPhases, kNS),
 // dequantisation warp sees every second weight chunk (its steps are 4 apart, 2
 // steps a chunk), so with an even weight ring it has itself waited for the
 // previous phase of every chunk slot it waits on.
-static_assert(kMaxNB % 2 == 0 && kNS % 2 == 0 && ring_cfg(4).nb >= kProducerLanes &&
+static_assert(kMaxNB % 2 == 0 && kNS % 2 == 0 && kNSNarrow % 2 == 0 &&
+                  kNS >= kDeqPhases && kNSNarrow >= kDeqPhases && ring_cfg(4).nb >= kProducerLanes &&
                   kDeqPhases == 2 * kWChunk,
               "ring depths must be even and the B ring at least as deep as the producer lanes");
 
@@ -454,12 +463,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t wait_ns = a.wait_kcycles;  // (the wait limit, in units of 1024 cycles)
   if (threadIdx.x == 0) TRACE_POINT(13, 0);  // kernel entry
+  // A small batch (at most 32 routed slots, small_ids set) recomputes its routing
+  // tiles from the caller's topk_ids in the activation producer's warp, while
+  // thread 0 initialises the barriers and warp 2 allocates tensor memory.
+  const bool small = a.small_ids != nullptr;
+  TokenTile* small_tiles = reinterpret_cast<TokenTile*>(gbase + kSmSmall);
+  int* small_ntiles = reinterpret_cast<int*>(gbase + kSmSmall + kSmallTiles * 16);
+  if (small && warp == kWarpB) {
+    const SmallRoute r = small_route(a.small_ids, a.MK, a.E, kRowGroup, kBNMax, lane);
+    if (r.leader && r.tile0 < kSmallTiles) {  // one tile per expert present
+      TokenTile tt;
+      tt.expert = r.e;
+      tt.g0 = r.seg / kRowGroup;
+      tt.ngroups = r.pad / kRowGroup;
+      tt.first = r.tile0;
+      small_tiles[r.tile0] = tt;
+    }
+    const int ng = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(r.leader ? r.pad / kRowGroup : 1));
+    if (lane == 0) {
+      *small_ntiles = r.tot_tiles < kSmallTiles ? r.tot_tiles : kSmallTiles;
+      *ng_max_sm = ng;  // the widest tile of the batch (at most 2 row groups)
+    }
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxNWS; ++i) {
       mbar_init(bar(kBarWFull + i), 1);
       mbar_init(bar(kBarWEmpty + i), 4 * kWChunk);  // 4 quadrant warps x steps
     }
-    for (int i = 0; i < kNS; ++i) {
+    for (int i = 0; i < kNSMax; ++i) {
       mbar_init(bar(kBarFull + i), 4);
       mbar_init(bar(kBarEmpty + i), 1);
     }
@@ -475,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     mbar_init(bar(kBarNever), 1);
     *abort_flag = 0;
     *last_flag = 0;
-    *ng_max_sm = 1;
+    if (!small) *ng_max_sm = 1;
     fence_mbar_init();
   }
   if (warp == kWarpMma0) {
@@ -497,25 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   // activation producer and the epilogue read the preceding kernel's outputs, so
   // only they wait; the weight stream starts right away (it has a whole decode
   // step's latency to hide and the preceding kernels are small).
-  const bool small = a.small_ids != nullptr;
-  TokenTile* small_tiles = reinterpret_cast<TokenTile*>(gbase + kSmSmall);
-  int* small_ntiles = reinterpret_cast<int*>(gbase + kSmSmall + kSmallTiles * 16);
   int num_tiles;
   if (small) {
-    if (warp == 0) {
-      const SmallRoute r = small_route(a.small_ids, a.MK, a.E, kRowGroup, kBNMax, lane);
-      if (r.leader && r.tile0 < kSmallTiles) {  // one tile per expert present
-        TokenTile tt;
-        tt.expert = r.e;
-        tt.g0 = r.seg / kRowGroup;
-        tt.ngroups = r.pad / kRowGroup;
-        tt.first = r.tile0;
-        small_tiles[r.tile0] = tt;
-      }
-      if (lane == 0) *small_ntiles = r.tot_tiles < kSmallTiles ? r.tot_tiles : kSmallTiles;
-    }
-    __syncthreads();
-    num_tiles = *small_ntiles;
+    num_tiles = *small_ntiles;  // (written before the barrier above)
   } else {
     pdl_wait();
     num_tiles = a.hdr[kHdrNumTiles];
@@ -546,27 +561,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   const Sched sc{W_total, G, weighted ? sched_sm : nullptr};
   const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
   pdl_launch_dependents();
+  if (threadIdx.x == 0) TRACE_POINT(13, 2);  // range known
 
   // decode this CTA's units in parallel (one round of global loads for all); the
   // widest token tile among them sizes the rings
   Unit* seg_tab = reinterpret_cast<Unit*>(gbase + kSmSeg);
   const long long u_first = my_begin / a.KBn;
   const long long n_units = my_end > my_begin ? (my_end - 1) / a.KBn - u_first + 1 : 0;
-  const int n_tab = static_cast<int>(n_units < kMaxSegs ? n_units : kMaxSegs);
-  if (n_units > kMaxSegs && threadIdx.x == 0) *ng_max_sm = kBNMax / kRowGroup;
-  for (int i = threadIdx.x; i < n_tab; i += blockDim.x) {
-    const Unit un = small ? decode_unit_small(u_first + i, a.R, small_tiles)
-                          : decode_unit(u_first + i, a.R, a.tiles, a.expert_tiles);
-    seg_tab[i] = un;
-    atomicMax(ng_max_sm, un.ng);
+  // (a small batch needs no table: its units decode from the shared tile list)
+  const int n_tab = small ? 0 : static_cast<int>(n_units < kMaxSegs ? n_units : kMaxSegs);
+  if (!small) {
+    if (n_units > kMaxSegs && threadIdx.x == 0) *ng_max_sm = kBNMax / kRowGroup;
+    for (int i = threadIdx.x; i < n_tab; i += blockDim.x) {
+      const Unit un = decode_unit(u_first + i, a.R, a.tiles, a.expert_tiles);
+      seg_tab[i] = un;
+      atomicMax(ng_max_sm, un.ng);
+    }
+    __syncthreads();
   }
-  __syncthreads();
+  if (threadIdx.x == 0) TRACE_POINT(13, 3);  // units decoded
   const SegTable segs{seg_tab, u_first, n_tab, a.R, a.tiles, a.expert_tiles, small ? small_tiles : nullptr};
   // (the four configurations are compile-time constants; pick one without dividing)
   const int ngm = *ng_max_sm;
   const RingCfg rc = ngm <= 1 ? ring_cfg(1) : ngm == 2 ? ring_cfg(2) : ngm == 3 ? ring_cfg(3) : ring_cfg(4);
   const int nws = rc.nws, nb = rc.nb;
   const uint32_t sW = sRings, sB = sRings + static_cast<uint32_t>(nws) * kWChunkBytes;
+  // tensor memory: nst A stages, then 4 accumulators of accw columns (computed
+  // in the roles that use them, from the widest tile's row groups)
+#define MOE_TMEM_NST (ngm <= 2 ? static_cast<uint32_t>(kNSNarrow) : static_cast<uint32_t>(kNS))
+#define MOE_TMEM_ACCW (static_cast<uint32_t>(ngm < 1 ? 1 : (ngm > 4 ? 4 : ngm)) * kRowGroup)
 
   if (warp == kWarpW) {
     // ------------------------------------------------ packed-weight producer
@@ -582,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       // evict-first policy, so they do not displace the activations (re-read by
       // every row tile of their expert) or the intermediate.
       const uint64_t w_policy = l2_policy_evict_first();
+      TRACE_POINT(13, 4);  // weight producer ready
       long long c = 0;
       int s = 0;
       uint32_t sph = 0;  // slot of chunk c, and the parity of its phase
@@ -702,6 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // B slot of this issuer's next step (its steps are 2 apart; nb is even) and
     // the parity of that slot's phase
     uint32_t sb = par, bph = 0;
+    uint32_t sa = par, aph = 0;  // the same for the A stage ring (nst stages, even)
+    const uint32_t nst = MOE_TMEM_NST, accw = MOE_TMEM_ACCW, acc_col0 = nst * kACols;
     while (ok && si.next(u, kb0, kb1)) {
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
       const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
@@ -714,16 +740,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                                                     ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
                                                     kStatusTimeout, wait_ns));
         if (!ok) break;
-        const uint32_t d_tmem = tmem + kAccCol0 + (par * 2 + ab) * kBNMax;
+        const uint32_t d_tmem = tmem + acc_col0 + (par * 2 + ab) * accw;
         uint32_t acc_flag = 0;
         for (uint32_t it = first; it < it_base + len; it += 2) {
-          const uint32_t st = it % kNS;
+          const uint32_t st = sa;
           if (lane == 0) TRACE_POINT(2, it);
           ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarBFull + sb), bph, abort_flag, status,
                                                       kStatusTimeout, wait_ns));
           if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), (it / kNS) & 1,
-                                                        abort_flag, status, kStatusTimeout, wait_ns));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), aph, abort_flag, status,
+                                                        kStatusTimeout, wait_ns));
           if (!ok) break;
           if (lane == 0) TRACE_POINT(3, it);
           const uint32_t a_tmem = tmem + st * kACols;
@@ -751,6 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
           if (sb >= static_cast<uint32_t>(nb)) {
             sb -= static_cast<uint32_t>(nb);
             bph ^= 1u;
+          }
+          sa += 2;
+          if (sa >= nst) {
+            sa -= nst;
+            aph ^= 1u;
           }
         }
         if (!ok) break;
@@ -783,11 +814,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // weight chunk of the step (2 steps per chunk): its ring slot and phase parity,
     // advanced by 2 chunks per iteration
     uint32_t ws = static_cast<uint32_t>(phase) >> 1, wpar = 0;
+    // A stage of the step and the parity of that stage's use, advanced by
+    // kDeqPhases steps per iteration (kDeqPhases <= nst)
+    uint32_t st = static_cast<uint32_t>(phase), sph = 0;
+    const uint32_t nst = MOE_TMEM_NST;
     for (uint32_t it = static_cast<uint32_t>(phase); it < n_it; it += kDeqPhases) {
-      const uint32_t st = it & (kNS - 1);
       // non-blocking test of the stage-free barrier now; its latency overlaps the
       // conversion and the blocking wait below runs only if it was not ready
-      const bool e_early = mbar_test_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1);
+      const bool e_early = mbar_test_wait(bar(kBarEmpty + st), sph ^ 1);
       if (lane == 0 && quad == 0) TRACE_POINT(12, it);
       bool w_ok = mbar_wait(bar(kBarWFull + ws), wpar, abort_flag, status, kStatusTimeout, wait_ns);
       if (!__all_sync(0xffffffffu, w_ok)) break;
@@ -806,8 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       dequant_group(q0, __byte_perm(sc0, 0, 0x1010), &out[0]);
       dequant_group(q1, __byte_perm(sc0, 0, 0x3232), &out[16]);
       if (!__all_sync(0xffffffffu, e_early)) {
-        w_ok = mbar_wait(bar(kBarEmpty + st), ((it / kNS) & 1) ^ 1, abort_flag, status,
-                         kStatusTimeout, wait_ns);
+        w_ok = mbar_wait(bar(kBarEmpty + st), sph ^ 1, abort_flag, status, kStatusTimeout, wait_ns);
         if (!__all_sync(0xffffffffu, w_ok)) break;
       }
       if (lane == 0 && quad == 0) TRACE_POINT(7, it);
@@ -828,6 +861,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       __syncwarp();
       if (lane == 0) TRACE_POINT(8 + quad, it);
       if (lane == 0) mbar_arrive(bar(kBarFull + st));
+      st += kDeqPhases;
+      if (st >= nst) {
+        st -= nst;
+        sph ^= 1u;
+      }
       ws += 2;
       if (ws >= static_cast<uint32_t>(nws)) {
         ws -= static_cast<uint32_t>(nws);
@@ -909,8 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                           epi_ok[(acc_it & 1) * 4 + 2] && epi_ok[(acc_it & 1) * 4 + 3];
       if (!all_ok) break;
       tc_fence_after();
-      const uint32_t tacc0 = tmem + t_lane + kAccCol0 + ab * kBNMax;
-      const uint32_t tacc1 = tmem + t_lane + kAccCol0 + (2 + ab) * kBNMax;
+      const uint32_t accw = MOE_TMEM_ACCW, acc_col0 = MOE_TMEM_NST * kACols;
+      const uint32_t tacc0 = tmem + t_lane + acc_col0 + ab * accw;
+      const uint32_t tacc1 = tmem + t_lane + acc_col0 + (2 + ab) * accw;
       // fp32 sums of 16 token columns of this lane's row, both issuers added
       auto load_chunk = [&](int c, float (&v)[16]) {
         uint32_t rr[16];
@@ -1039,6 +1078,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
+        if (a.rt_tickets) {
+          // Output finalisation (small batches): the contributions to output row
+          // tile rt come from every token tile's unit (tile, rt); the contributor
+          // whose steps complete the tile's count rounds its fp32 sums to bf16.
+          __threadfence();  // this thread's additions are visible before the ticket
+          named_bar_sync(kEpiBar, kEpiThreads);
+          if (epi_tid == 0) {
+            const int add = kb1 - kb0;
+            const int old = atomicAdd(a.rt_tickets + un.rt, add);
+            *last_flag = (old + add == num_tiles * a.KBn) ? 1 : 0;
+          }
+          named_bar_sync(kEpiBar, kEpiThreads);
+          if (*last_flag) {
+            __threadfence();
+            const long long col = static_cast<long long>(un.rt) * kBM + epi_tid;
+            for (int t = 0; t < a.M; ++t) {
+              const float v = __ldcg(a.acc + static_cast<long long>(t) * a.Kout + col);
+              a.out[static_cast<long long>(t) * a.Kout + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            }
+          }
+          named_bar_sync(kEpiBar, kEpiThreads);  // last_flag is reused by the next segment
+        }
       }
       if (epi_tid == 0) TRACE_POINT(15, acc_it);  // epilogue done with a segment
       ++acc_it;
@@ -1056,6 +1117,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#undef MOE_TMEM_NST
+#undef MOE_TMEM_ACCW
 }
 
 }  // namespace

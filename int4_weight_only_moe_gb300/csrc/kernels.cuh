@@ -36,7 +36,7 @@ struct AlignArgs {
   int32_t* expert_tiles;    // [E] token tiles per expert, or null
   int32_t* hdr;             // workspace header (status, num_padded, num_tiles)
   int32_t* tickets;         // zeroed, or null
-  int n_tickets;
+  int n_tickets;            // (tickets holds n_tickets entries, all zeroed)
   int32_t* num_padded_out;  // optional extra copy of num_padded
   int sorted_cap, tiles_cap;  // extents for the self-checking build
   int32_t* dbg;
@@ -91,6 +91,12 @@ struct GemmArgs {
   const int32_t* small_ids;
   uint32_t wait_kcycles;   // pipeline wait limit in units of 1024 SM cycles (wait_limit_kcycles)
   int test_never_wait;     // test hook: the epilogue first waits on a barrier nothing arrives on
+  // down GEMM, small batches: per output row tile, a zeroed ticket counting the
+  // steps added into it; the contributor that completes a tile writes its bf16
+  // output (null: a separate finalize launch rounds the accumulator)
+  int32_t* rt_tickets;
+  uint16_t* out;           // bf16 [M, Kout]
+  int M;
   int R;                   // row tiles per expert
   int KBn;                 // k-blocks per unit
   int Gcap;                // row groups per k-block plane of bsrc / hout

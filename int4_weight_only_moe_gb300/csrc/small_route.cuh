@@ -24,13 +24,14 @@ struct SmallRoute {
   bool any_bad;
 };
 
-__device__ __forceinline__ SmallRoute small_route(const int32_t* ids, int MK, int E, int block,
-                                                  int bn_max, int lane) {
+// `v` is the expert id of flat slot `lane` (read by the caller: global or shared
+// memory), ignored for lanes at or beyond MK.
+__device__ __forceinline__ SmallRoute small_route_ids(int v, int MK, int E, int block, int bn_max,
+                                                      int lane) {
   SmallRoute r;
   r.e = -1;
   bool bad = false;
   if (lane < MK) {
-    const int v = ids[lane];
     if (v >= 0 && v < E)
       r.e = v;
     else
@@ -60,6 +61,12 @@ __device__ __forceinline__ SmallRoute small_route(const int32_t* ids, int MK, in
   }
   r.any_bad = __any_sync(0xffffffffu, bad);
   return r;
+}
+
+// The same, reading slot `lane`'s id from `ids` (global memory).
+__device__ __forceinline__ SmallRoute small_route(const int32_t* ids, int MK, int E, int block,
+                                                  int bn_max, int lane) {
+  return small_route_ids(lane < MK ? ids[lane] : -1, MK, E, block, bn_max, lane);
 }
 
 }  // namespace moe
