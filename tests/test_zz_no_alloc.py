@@ -40,8 +40,12 @@ def run_both(prob, wl, step):
 
 
 def within_one_ulp(a, b):
+    # One bf16 unit of the larger value, plus the term by which two orders of the
+    # down projection's float atomic additions can differ near zero (2^-16 of the
+    # output's largest magnitude), as in the other GPU tests.
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(a), np.abs(b)) + 1e-30)) - 7)
-    return bool(np.all(np.abs(a - b) <= ulp))
+    floor = np.exp2(-16.0) * max(float(np.abs(b).max()), 1e-30)
+    return bool(np.all(np.abs(a - b) <= ulp + floor))
 
 
 @pytest.mark.parametrize("shape", [(16, 512, 256, 4, 37), (48, 7168, 2048, 8, 1), (48, 7168, 2048, 8, 9)])
