@@ -114,6 +114,36 @@ def all_expert_weights(E: int, K: int, N: int, seed: int = WEIGHT_SEED):
     return w1_q, w1_s, w2_q, w2_s
 
 
+def expert_weights_ct(e: int, K: int, N: int, seed: int = WEIGHT_SEED):
+    """Random weights of expert ``e`` in the compressed-tensors packed layout.
+
+    Every output feature's reduction row is contiguous: returns
+    ``(w1_q [2N, K/8] int32, w1_s [2N, K/32] uint16, w2_q [K, N/8] int32,
+    w2_s [K, N/32] uint16)``; code ``i`` of word ``[c, r]`` in bits ``4i..4i+3``
+    is reduction element ``8r+i`` of feature ``c``.
+    """
+    g = _rng(seed, 3000 + e)
+    w1_q = g.integers(0, 2**32, size=(2 * N, K // 8), dtype=np.uint32).view(np.int32)
+    w1_s = f32_to_bf16_bits(g.uniform(0.005, 0.02, size=(2 * N, K // GROUP_SIZE)))
+    w2_q = g.integers(0, 2**32, size=(K, N // 8), dtype=np.uint32).view(np.int32)
+    w2_s = f32_to_bf16_bits(g.uniform(0.005, 0.02, size=(K, N // GROUP_SIZE)))
+    return w1_q, w1_s, w2_q, w2_s
+
+
+def act_order_g_idx(e: int, R: int, which: int, seed: int = WEIGHT_SEED) -> np.ndarray:
+    """Group index ``[R]`` int32 of a matrix quantised in a random activation order.
+
+    A seeded random order of the ``R`` reduction channels is cut into runs of 32;
+    channel ``c`` gets the number of the run it falls in, so every group has
+    exactly 32 members, scattered over the axis. ``which`` tells w1 (0) from
+    w2 (1).
+    """
+    order = _rng(seed, 5000 + e, which).permutation(R)
+    g_idx = np.empty(R, dtype=np.int32)
+    g_idx[order] = np.arange(R, dtype=np.int32) // GROUP_SIZE
+    return g_idx
+
+
 def hidden_states(M: int, K: int, seed: int = HIDDEN_SEED, step: int = 0) -> np.ndarray:
     """bf16 bit patterns of ``M`` standard-normal hidden vectors of length ``K``."""
     g = _rng(seed, 7, step)

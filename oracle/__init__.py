@@ -6,6 +6,8 @@ from .moe_oracle import (  # noqa: F401
     GROUP_SIZE,
     bf16_to_f64,
     dequantize,
+    dequantize_ct,
+    dequantize_g_idx,
     expert_dense,
     expert_ffn,
     expert_hidden,
@@ -15,4 +17,5 @@ from .moe_oracle import (  # noqa: F401
     route,
     silu,
     unpack_codes,
+    unpack_codes_ct,
 )

@@ -78,6 +78,51 @@ def dequantize(qweight: np.ndarray, scales: np.ndarray, group_size: int = GROUP_
     return ((u - 8).astype(np.float64) * s_full).T  # [C, R]
 
 
+def unpack_codes_ct(weight_packed: np.ndarray) -> np.ndarray:
+    """Stored 4-bit codes of a compressed-tensors packed ``[C, R/8]`` int32 matrix -> ``[R, C]`` int64.
+
+    The compressed-tensors INT4 layout ("The Pivot to Real Hardware ...", The
+    Context: Where We Stand -- the model ships in that format) keeps every output
+    feature's row contiguous: word ``[c, r]`` holds elements ``(8r + i, c)`` of
+    the reduction axis, code ``i`` in bits ``4i..4i+3`` (lowest first), with the
+    same symmetric offset (a code ``u`` stands for ``u - 8``).
+    """
+    q = np.asarray(weight_packed).view(np.uint32).astype(np.int64)
+    c, r8 = q.shape
+    u = np.empty((r8 * 8, c), dtype=np.int64)
+    for i in range(8):
+        u[i::8, :] = ((q >> (4 * i)) & 0xF).T
+    return u
+
+
+def dequantize_ct(weight_packed: np.ndarray, weight_scale: np.ndarray,
+                  group_size: int = GROUP_SIZE) -> np.ndarray:
+    """Dequantised weight ``[C, R]`` of a compressed-tensors matrix.
+
+    ``W[c, r] = (u[r, c] - 8) * scale[c, r // group_size]`` with the codes of
+    ``unpack_codes_ct`` and the scales stored feature-major, ``[C, R/G]`` bf16.
+    """
+    u = unpack_codes_ct(weight_packed)                       # [R, C]
+    s = bf16_to_f64(weight_scale)                            # [C, R/G]
+    s_full = np.repeat(s, group_size, axis=1)                # [C, R]
+    return (u.T - 8).astype(np.float64) * s_full             # [C, R]
+
+
+def dequantize_g_idx(qweight: np.ndarray, scales: np.ndarray, g_idx: np.ndarray) -> np.ndarray:
+    """Dequantised weight ``[C, R]`` of a GPTQ matrix quantised in activation order.
+
+    With act-order ("The Pivot to Real Hardware ...", Step 2: the repack's
+    permutation and group-index tensors) reduction element ``r`` belongs to the
+    scale group ``g_idx[r]`` instead of ``r // 32``:
+    ``W[c, r] = (u[r, c] - 8) * scale[g_idx[r], c]``. The codes stay in the
+    natural order of ``r``.
+    """
+    u = unpack_codes(qweight)                                # [R, C]
+    s = bf16_to_f64(scales)                                  # [R/G, C]
+    g = np.asarray(g_idx, dtype=np.int64)
+    return ((u - 8).astype(np.float64) * s[g, :]).T          # [C, R]
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     """SiLU (swish): ``z * sigmoid(z) = z / (1 + exp(-z))``."""
     return z / (1.0 + np.exp(-z))
@@ -109,7 +154,8 @@ def expert_dense(w1_q, w1_s, w2_q, w2_s, e: int, group_size: int = GROUP_SIZE):
 
 
 def moe_forward(hidden_bf16, topk_ids, topk_weights, w1_q, w1_s, w2_q, w2_s,
-                tokens=None, group_size: int = GROUP_SIZE, expert_source=None) -> np.ndarray:
+                tokens=None, group_size: int = GROUP_SIZE, expert_source=None,
+                dense_source=None) -> np.ndarray:
     """Fused MoE feed-forward, float64 ``[len(tokens), K]``.
 
     ``out[t] = sum_j topk_weights[t, j] * FFN_{topk_ids[t, j]}(x_t)``.
@@ -117,8 +163,10 @@ def moe_forward(hidden_bf16, topk_ids, topk_weights, w1_q, w1_s, w2_q, w2_s,
     ``tokens`` restricts the computation to those rows (a sampled check of a
     large batch). ``expert_source(e)`` may supply ``(w1_q, w1_s, w2_q, w2_s)`` of
     one expert instead of indexing the stacked arrays (so that a caller can
-    regenerate only the experts it needs); slot ids outside ``[0, E)`` are
-    skipped. Experts are visited one at a time, each dequantised once.
+    regenerate only the experts it needs); ``dense_source(e)`` may instead
+    supply expert ``e``'s dequantised ``(W1 [2N, K], W2 [K, N])`` (weights held in
+    another packed layout). Slot ids outside ``[0, E)`` are skipped. Experts are
+    visited one at a time, each dequantised once.
     """
     x_all = bf16_to_f64(hidden_bf16)
     ids = np.asarray(topk_ids)
@@ -128,14 +176,16 @@ def moe_forward(hidden_bf16, topk_ids, topk_weights, w1_q, w1_s, w2_q, w2_s,
     K = x_all.shape[1]
     out = np.zeros((len(rows), K), dtype=np.float64)
     sub_ids = ids[rows]
-    if expert_source is None:
+    if expert_source is None and dense_source is None:
         E = w1_q.shape[0]
     else:
         E = None
     for e in np.unique(sub_ids):
         if e < 0 or (E is not None and e >= E):
             continue
-        if expert_source is None:
+        if dense_source is not None:
+            w1, w2 = dense_source(int(e))
+        elif expert_source is None:
             w1, w2 = expert_dense(w1_q, w1_s, w2_q, w2_s, int(e), group_size)
         else:
             q1, s1, q2, s2 = expert_source(int(e))
