@@ -51,7 +51,15 @@ enum {
   MOE_W4A16_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < moe_w4a16_workspace_size(h, M) */
   MOE_W4A16_CUDA_ERROR = -4,          /* a CUDA runtime call failed (message has the CUDA error) */
   MOE_W4A16_NOT_PACKED = -5,          /* forward before moe_w4a16_pack */
-  MOE_W4A16_UNSUPPORTED_SCALE = -6    /* pack: a scale outside {0} U [2^-14, 8160] in magnitude */
+  MOE_W4A16_UNSUPPORTED_SCALE = -6,   /* pack: a scale outside {0} U [2^-14, 8160] in magnitude */
+  MOE_W4A16_BAD_G_IDX = -7            /* pack_ex: a group index out of range, or a group whose
+                                         size is not 32 */
+};
+
+/* Weight layouts accepted by moe_w4a16_pack_ex. */
+enum {
+  MOE_W4A16_LAYOUT_GPTQ = 0,              /* codes [R/8, C] int32, scales [R/32, C] per expert */
+  MOE_W4A16_LAYOUT_COMPRESSED_TENSORS = 1 /* codes [C, R/8] int32, scales [C, R/32] per expert */
 };
 
 /* Device status bits (see moe_w4a16_status). */
@@ -91,6 +99,32 @@ int moe_w4a16_destroy(moe_w4a16_t h);
  * it returns. */
 int moe_w4a16_pack(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s,
                    const int32_t* w2_q, const uint16_t* w2_s, void* stream);
+
+/* moe_w4a16_pack with a choice of input layout and optional act-order group
+ * indices. Sources: "The Pivot to Real Hardware ...", The Context: Where We
+ * Stand (the model's INT4 weights ship in the compressed-tensors format) and
+ * Step 2: The Repack Pipeline (the repack takes GPTQ weights plus a
+ * permutation, empty when the model was quantised without activation order).
+ * Per expert, with R the reduction length and C the output features of a matrix
+ * (w1: R = K, C = 2N, gate features first; w2: R = N, C = K):
+ *   layout MOE_W4A16_LAYOUT_GPTQ: codes [R/8, C], scales [R/32, C] (as pack);
+ *   layout MOE_W4A16_LAYOUT_COMPRESSED_TENSORS: codes [C, R/8] (every output
+ *     feature's row contiguous, code i of word [c, r] = element 8r+i in bits
+ *     4i..4i+3, the stored nibble u standing for u - 8), scales [C, R/32].
+ * w1_g_idx / w2_g_idx (int32 [E, K] / [E, N], device, or NULL for none): the
+ * act-order group of every reduction element -- element r of a matrix uses the
+ * scale of group g_idx[r] instead of r / 32. Every group must hold exactly 32
+ * elements, else MOE_W4A16_BAD_G_IDX. The library packs each matrix's elements
+ * in group order (a stable sort by group); the forward then gathers the hidden
+ * states of w1's experts in that order and w1's output features are stored in
+ * w2's order, so the results are those of the unpermuted weights (to rounding)
+ * at no extra cost in the GEMMs. With act-order the handle keeps the packing
+ * order on the device (4 * E * (K or N) bytes per matrix), and the intermediate
+ * returned by moe_w4a16_read_intermediate is in w2's packing order.
+ * Same checks, synchronisation and ownership as moe_w4a16_pack. */
+int moe_w4a16_pack_ex(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s,
+                      const int32_t* w2_q, const uint16_t* w2_s, int layout,
+                      const int32_t* w1_g_idx, const int32_t* w2_g_idx, void* stream);
 
 /* Bytes of device workspace that moe_w4a16_forward needs for M tokens (and any
  * smaller M). Holds the per-call routing tables, the expert-sorted activations,
@@ -152,6 +186,37 @@ int moe_w4a16_forward_host(moe_w4a16_t h, const uint16_t* hidden, const int32_t*
                            const float* topk_weights, uint16_t* out, int M,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Expert parallelism ("The Weight-Streaming Threshold", Assumptions Embedded in
+ * the Analysis: with TP-8 each GPU holds a subset of the experts and an
+ * AllReduce combines the GPUs' outputs). A layer of E_total experts is split
+ * into contiguous ranges; each part is a handle of its own:
+ *
+ * moe_w4a16_create_ep: a handle holding experts [expert_begin, expert_end) of
+ * E_total (0 <= expert_begin < expert_end <= E_total <= 1024, 1 <= topk <=
+ * E_total; other requirements and allocation as moe_w4a16_create with E =
+ * expert_end - expert_begin). moe_w4a16_pack / pack_ex then take the local
+ * experts' weights only ([expert_end - expert_begin, ...]). The forward calls take
+ * the layer's expert ids: a slot routed to an expert outside the range is
+ * skipped silently (another part holds it); an id outside [0, E_total) still
+ * sets MOE_W4A16_STATUS_BAD_EXPERT_ID. The router variant routes over all
+ * E_total logits ([M, E_total]).
+ *
+ * moe_w4a16_forward_partial: the forward without the output rounding: writes
+ * partial fp32 [M, K] (device, 16-byte aligned, overwritten) = the weighted sum
+ * over this handle's experts only. Launches on `stream` as moe_w4a16_forward,
+ * with no finalize step. Summing the parts' partials (an all-reduce across the
+ * ranks) and rounding the sum with moe_w4a16_finalize gives the full layer's
+ * output, up to the order of the fp32 additions.
+ *
+ * moe_w4a16_finalize: out bf16 [n] = round-to-nearest-even of acc fp32 [n]
+ * (device, 16-byte aligned, n a multiple of 8). One launch on `stream`. */
+int moe_w4a16_create_ep(int E_total, int expert_begin, int expert_end, int K, int N, int topk,
+                        int group_size, moe_w4a16_t* out);
+int moe_w4a16_forward_partial(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                              const float* topk_weights, float* partial, int M,
+                              void* workspace, size_t workspace_bytes, void* stream);
+int moe_w4a16_finalize(const float* acc, uint16_t* out, long long n, void* stream);
+
 /* Read the device status word of the last forward that used `workspace`
  * (bits MOE_W4A16_STATUS_*; 0 = clean). Synchronises `stream`. */
 int moe_w4a16_status(moe_w4a16_t h, const void* workspace, int32_t* status, void* stream);
@@ -209,15 +274,17 @@ int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int b
                           int32_t* sorted_ids, int32_t* expert_offsets, int32_t* num_padded,
                           int capacity, void* stream);
 
-/* Invert the repack: write the handle's packed weights back in the GPTQ-style
- * layout of moe_w4a16_pack (device pointers, same shapes). */
+/* Invert the repack: write the handle's packed weights back in the layout and
+ * order they were packed from (moe_w4a16_pack or moe_w4a16_pack_ex: device
+ * pointers, the same shapes; codes and scales bit for bit). */
 int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s,
                            int32_t* w2_q, uint16_t* w2_s, void* stream);
 
 /* Copy the intermediate activations SiLU(gate)*up of the last forward that used
  * `workspace` into h_rows fp32 [M*topk, N] (device), row = flat slot id
  * t*topk+j: the fp16 tensor-core operand with the row's prescale undone; rows of
- * skipped slots are left untouched. */
+ * skipped slots are left untouched. With act-order on w2 the features come in
+ * w2's packing order (see moe_w4a16_pack_ex). */
 int moe_w4a16_read_intermediate(moe_w4a16_t h, const void* workspace, int M,
                                 float* h_rows, void* stream);
 

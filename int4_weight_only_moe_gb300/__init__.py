@@ -13,6 +13,8 @@ import os
 
 __all__ = [
     "MoeW4A16Error", "lib", "moe_w4a16_create", "moe_w4a16_destroy", "moe_w4a16_pack",
+    "moe_w4a16_pack_ex", "LAYOUT_GPTQ", "LAYOUT_COMPRESSED_TENSORS", "BAD_G_IDX",
+    "moe_w4a16_create_ep", "moe_w4a16_forward_partial", "moe_w4a16_finalize",
     "moe_w4a16_workspace_size", "moe_w4a16_host_staging_size", "moe_w4a16_forward",
     "moe_w4a16_forward_host", "moe_w4a16_status", "moe_w4a16_last_error",
     "moe_w4a16_set_option", "moe_w4a16_kernel_times", "moe_w4a16_packed_bytes",
@@ -26,7 +28,8 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libmoe_w4a16.so")
 
 OK, INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE_TOO_SMALL, CUDA_ERROR, NOT_PACKED = 0, -1, -2, -3, -4, -5
-UNSUPPORTED_SCALE = -6
+UNSUPPORTED_SCALE, BAD_G_IDX = -6, -7
+LAYOUT_GPTQ, LAYOUT_COMPRESSED_TENSORS = 0, 1
 STATUS_BAD_EXPERT_ID, STATUS_TIMEOUT, STATUS_H_SATURATED, STATUS_BAD_SCHEDULE = 1, 2, 4, 16
 OPT_NUM_CTAS, OPT_PROFILE, OPT_PDL = 1, 2, 3
 OPT_STEP_COST_GATEUP, OPT_STEP_COST_DOWN, OPT_WAIT_LIMIT_US = 4, 5, 6
@@ -40,6 +43,10 @@ _SIGNATURES = {
     "moe_w4a16_create": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_vp)]),
     "moe_w4a16_destroy": (_c_int, [_vp]),
     "moe_w4a16_pack": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_w4a16_pack_ex": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _vp]),
+    "moe_w4a16_create_ep": (_c_int, [_c_int] * 7 + [ctypes.POINTER(_vp)]),
+    "moe_w4a16_forward_partial": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_size, _vp]),
+    "moe_w4a16_finalize": (_c_int, [_vp, _vp, ctypes.c_longlong, _vp]),
     "moe_w4a16_workspace_size": (_c_size, [_vp, _c_int]),
     "moe_w4a16_host_staging_size": (_c_size, [_vp, _c_int]),
     "moe_w4a16_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_size, _vp]),
@@ -142,12 +149,35 @@ def moe_w4a16_create(E: int, K: int, N: int, topk: int, group_size: int = 32) ->
     return h.value
 
 
+def moe_w4a16_create_ep(E_total, expert_begin, expert_end, K, N, topk, group_size=32) -> int:
+    h = _vp()
+    _check(lib().moe_w4a16_create_ep(E_total, expert_begin, expert_end, K, N, topk, group_size,
+                                     ctypes.byref(h)))
+    return h.value
+
+
+def moe_w4a16_forward_partial(h, hidden, topk_ids, topk_weights, partial, M, workspace, stream=None):
+    _check(lib().moe_w4a16_forward_partial(h, _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights),
+                                           _ptr(partial), M, _ptr(workspace), workspace.numel(),
+                                           _stream(stream)))
+
+
+def moe_w4a16_finalize(acc, out, stream=None):
+    _check(lib().moe_w4a16_finalize(_ptr(acc), _ptr(out), acc.numel(), _stream(stream)))
+
+
 def moe_w4a16_destroy(h: int):
     _check(lib().moe_w4a16_destroy(h))
 
 
 def moe_w4a16_pack(h, w1_q, w1_s, w2_q, w2_s, stream=None):
     _check(lib().moe_w4a16_pack(h, _ptr(w1_q), _ptr(w1_s), _ptr(w2_q), _ptr(w2_s), _stream(stream)))
+
+
+def moe_w4a16_pack_ex(h, w1_q, w1_s, w2_q, w2_s, layout=LAYOUT_GPTQ, w1_g_idx=None, w2_g_idx=None,
+                      stream=None):
+    _check(lib().moe_w4a16_pack_ex(h, _ptr(w1_q), _ptr(w1_s), _ptr(w2_q), _ptr(w2_s), int(layout),
+                                   _ptr(w1_g_idx), _ptr(w2_g_idx), _stream(stream)))
 
 
 def moe_w4a16_workspace_size(h, M: int) -> int:
@@ -247,9 +277,19 @@ def moe_w4a16_forward_noalloc(h, hidden, topk_ids, topk_weights, out, M, stream=
 class MoEW4A16:
     """Owns a library handle (packed weights) and a reusable device workspace."""
 
-    def __init__(self, E: int, K: int, N: int, topk: int, group_size: int = 32):
-        self.E, self.K, self.N, self.topk = E, K, N, topk
-        self.handle = moe_w4a16_create(E, K, N, topk, group_size)
+    def __init__(self, E: int, K: int, N: int, topk: int, group_size: int = 32, expert_range=None):
+        """``E`` experts of hidden size ``K`` and intermediate size ``N``; with
+        ``expert_range=(begin, end)`` the handle holds only experts [begin, end) of
+        the ``E`` (expert parallelism: pack takes those experts' weights)."""
+        self.E_total = E
+        self.K, self.N, self.topk = K, N, topk
+        if expert_range is None:
+            self.expert_begin, self.E = 0, E
+            self.handle = moe_w4a16_create(E, K, N, topk, group_size)
+        else:
+            b, e = (int(v) for v in expert_range)
+            self.expert_begin, self.E = b, e - b
+            self.handle = moe_w4a16_create_ep(E, b, e, K, N, topk, group_size)
         self.workspace = None
         self._ws_bytes = {}  # (M, host staging) -> workspace bytes
 
@@ -265,13 +305,27 @@ class MoEW4A16:
         except Exception:
             pass
 
-    def pack(self, w1_q, w1_s, w2_q, w2_s, stream=None):
+    def pack(self, w1_q, w1_s, w2_q, w2_s, stream=None, layout=LAYOUT_GPTQ, w1_g_idx=None,
+             w2_g_idx=None):
+        """Repack the weights; ``layout`` GPTQ (codes [E, R/8, C]) or compressed-tensors
+        (codes [E, C, R/8]); optional act-order group indices [E, K] / [E, N]."""
         E, K, N = self.E, self.K, self.N
-        _need(w1_q, ("int32",), (E, K // 8, 2 * N), "w1_q")
-        _need(w1_s, _BITS16, (E, K // 32, 2 * N), "w1_s")
-        _need(w2_q, ("int32",), (E, N // 8, K), "w2_q")
-        _need(w2_s, _BITS16, (E, N // 32, K), "w2_s")
-        moe_w4a16_pack(self.handle, w1_q, w1_s, w2_q, w2_s, stream)
+        if layout == LAYOUT_GPTQ:
+            shapes = [(E, K // 8, 2 * N), (E, K // 32, 2 * N), (E, N // 8, K), (E, N // 32, K)]
+        else:
+            shapes = [(E, 2 * N, K // 8), (E, 2 * N, K // 32), (E, K, N // 8), (E, K, N // 32)]
+        _need(w1_q, ("int32",), shapes[0], "w1_q")
+        _need(w1_s, _BITS16, shapes[1], "w1_s")
+        _need(w2_q, ("int32",), shapes[2], "w2_q")
+        _need(w2_s, _BITS16, shapes[3], "w2_s")
+        if w1_g_idx is not None:
+            _need(w1_g_idx, ("int32",), (E, K), "w1_g_idx")
+        if w2_g_idx is not None:
+            _need(w2_g_idx, ("int32",), (E, N), "w2_g_idx")
+        if layout == LAYOUT_GPTQ and w1_g_idx is None and w2_g_idx is None:
+            moe_w4a16_pack(self.handle, w1_q, w1_s, w2_q, w2_s, stream)
+        else:
+            moe_w4a16_pack_ex(self.handle, w1_q, w1_s, w2_q, w2_s, layout, w1_g_idx, w2_g_idx, stream)
 
     def ensure_workspace(self, M: int, host_staging: bool = False):
         need = self._ws_bytes.get((M, host_staging))
@@ -298,14 +352,28 @@ class MoEW4A16:
         moe_w4a16_forward(self.handle, hidden, topk_ids, topk_weights, out, M, ws, stream)
         return out
 
+    def forward_partial(self, hidden, topk_ids, topk_weights, partial=None, stream=None):
+        """fp32 [M, K] weighted sum over this handle's experts (no bf16 rounding)."""
+        import torch
+        M = hidden.shape[0]
+        _need(hidden, _BITS16, (M, self.K), "hidden")
+        _need(topk_ids, ("int32",), (M, self.topk), "topk_ids")
+        _need(topk_weights, ("float32",), (M, self.topk), "topk_weights")
+        if partial is None:
+            partial = torch.empty((M, self.K), dtype=torch.float32, device=hidden.device)
+        _need(partial, ("float32",), (M, self.K), "partial")
+        ws = self.ensure_workspace(M)
+        moe_w4a16_forward_partial(self.handle, hidden, topk_ids, topk_weights, partial, M, ws, stream)
+        return partial
+
     def route(self, router_logits, stream=None):
         """Top-k routing of ``router_logits`` fp32 [M, E] on the device: (ids, weights)."""
         import torch
         M = router_logits.shape[0]
-        _need(router_logits, ("float32",), (M, self.E), "router_logits")
+        _need(router_logits, ("float32",), (M, self.E_total), "router_logits")
         ids = torch.empty((M, self.topk), dtype=torch.int32, device=router_logits.device)
         w = torch.empty((M, self.topk), dtype=torch.float32, device=router_logits.device)
-        moe_w4a16_route(router_logits, M, self.E, self.topk, ids, w, stream)
+        moe_w4a16_route(router_logits, M, self.E_total, self.topk, ids, w, stream)
         return ids, w
 
     def forward_logits(self, hidden, router_logits, out=None, stream=None):
@@ -313,7 +381,7 @@ class MoEW4A16:
         import torch
         M = hidden.shape[0]
         _need(hidden, _BITS16, (M, self.K), "hidden")
-        _need(router_logits, ("float32",), (M, self.E), "router_logits")
+        _need(router_logits, ("float32",), (M, self.E_total), "router_logits")
         if out is None:
             out = torch.empty((M, self.K), dtype=torch.bfloat16, device=hidden.device)
         _need(out, _BITS16, (M, self.K), "out")

@@ -65,11 +65,10 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
   const int lo = min(a.MK, w * chunk), hi = min(a.MK, lo + chunk);
   int bad = 0;
   for (int i = lo + lane; i < hi; i += 32) {
-    const int e = a.topk_ids[i];
-    if (e >= 0 && e < E)
-      atomicAdd(&hist[w * E + e], 1);
-    else
-      bad = 1;
+    bool b = false;
+    const int e = local_expert(a.topk_ids[i], a.e_begin, E, a.E_total, &b);
+    if (e >= 0) atomicAdd(&hist[w * E + e], 1);
+    bad |= b ? 1 : 0;
   }
   if (bad && a.hdr) atomicOr(&a.hdr[kHdrStatus], 1);
   __syncthreads();
@@ -97,8 +96,8 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
     const int i = base + lane;
     int e = -1;
     if (i < hi) {
-      const int v = a.topk_ids[i];
-      if (v >= 0 && v < E) e = v;
+      bool b = false;
+      e = local_expert(a.topk_ids[i], a.e_begin, E, a.E_total, &b);
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0) {
@@ -215,7 +214,7 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
 }
 
 __device__ SmallRoute small_route(const AlignArgs& a, int lane) {
-  return small_route(a.topk_ids, a.MK, a.E, a.block, a.bn_max, lane);
+  return small_route(a.topk_ids, a.MK, a.E, a.block, a.bn_max, lane, a.e_begin, a.E_total);
 }
 
 // Write the routing outputs of a small batch (one warp): header, counters, sorted
@@ -333,7 +332,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float f) 
 // the gate/up epilogue stores zeros for them).
 constexpr int kGatherThreads = 256;
 constexpr int kGatherChunks = 8;  // chunks of 8 elements per thread and pass: K <= 16384 in one pass
-__device__ void gather_row(const GatherArgs& g, int p, int sid, int* red) {
+// With act-order on w1 (perm1 set) the row is written in the expert's packing
+// order: element j of the copy is hidden element perm1[expert][j] (the largest
+// magnitude, and so the exponent, does not depend on the order).
+__device__ __forceinline__ uint32_t bf16_pair(const uint16_t* xr, int a, int b) {
+  return static_cast<uint32_t>(__ldg(xr + a)) | (static_cast<uint32_t>(__ldg(xr + b)) << 16);
+}
+__device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int expert) {
   const int tid = threadIdx.x;
   const bool real = sid < g.MK && MOE_CHECK(sid >= 0 && sid / g.topk < g.M, const_cast<int32_t*>(g.hdr),
                                             g.dbg, 24, sid, p);
@@ -369,12 +374,22 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red) {
   __syncthreads();  // red is reused by the next row
   if (tid == 0) g.rowexp[p] = e;
   const float f = exp2_int(-e);
+  const uint16_t* xr = g.x + static_cast<long long>(sid / g.topk) * g.K;
+  const int32_t* pr = nullptr;
+  if (g.perm1 && MOE_CHECK(expert >= 0, const_cast<int32_t*>(g.hdr), g.dbg, 26, expert, p))
+    pr = g.perm1 + static_cast<long long>(expert) * g.K;
   for (int c0 = 0; c0 < cpr; c0 += kPass) {
 #pragma unroll
     for (int i = 0; i < kGatherChunks; ++i) {
       const int ch = c0 + i * kGatherThreads + tid;
       if (ch >= cpr) continue;
-      const uint4 x = one_pass ? v[i] : src[ch];
+      uint4 x = one_pass ? v[i] : src[ch];
+      if (pr) {
+        const int4 i0 = *reinterpret_cast<const int4*>(pr + 8 * ch);
+        const int4 i1 = *reinterpret_cast<const int4*>(pr + 8 * ch + 4);
+        x = make_uint4(bf16_pair(xr, i0.x, i0.y), bf16_pair(xr, i0.z, i0.w), bf16_pair(xr, i1.x, i1.y),
+                       bf16_pair(xr, i1.z, i1.w));
+      }
       const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
                                  bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
       const long long off = (static_cast<long long>(ch >> 3) * g.Gcap + grp) * kRowGroupBytes +
@@ -391,16 +406,43 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red) {
 // it after waiting for this kernel). Then every warp gathers its share of the
 // expert-sorted rows, one row at a time, and every thread zeroes its share of the
 // accumulator, as gather_kernel.
+#ifdef MOE_GEMM_TRACE
+// trace builds: global-timer stamps per CTA (entry, dependency resolved, exit)
+__device__ unsigned long long g_rg_trace[512][4];
+extern "C" int moe_rg_trace_read(unsigned long long* host, int reset) {
+  int e = static_cast<int>(cudaMemcpyFromSymbol(host, g_rg_trace, sizeof(g_rg_trace)));
+  if (reset) {
+    static unsigned long long z[512 * 4];
+    cudaMemcpyToSymbol(g_rg_trace, z, sizeof(z));
+  }
+  return e;
+}
+#define RG_STAMP(ev)                                                                  \
+  do {                                                                                \
+    if (threadIdx.x == 0 && blockIdx.x < 512) {                                       \
+      unsigned long long t;                                                           \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));                           \
+      g_rg_trace[blockIdx.x][(ev)] = t;                                               \
+    }                                                                                 \
+  } while (0)
+#else
+#define RG_STAMP(ev) \
+  do {               \
+  } while (0)
+#endif
 constexpr int kSmallPadRows = 32 + 32 * (kRowGroup - 1);  // at most 32 slots, padded to 16 each
 constexpr int kGatherWarps = kGatherThreads / 32;
 
 __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(const AlignArgs a_in,
                                                                            const GatherArgs g) {
   __shared__ int s_sorted[kSmallPadRows];
+  __shared__ int s_expert[kSmallPadRows];  // expert of every real padded row
   __shared__ int s_npad;
   __shared__ int32_t s_ids[32];
   __shared__ int s_red[kGatherWarps + 1];
+  RG_STAMP(0);
   pdl_wait();
+  RG_STAMP(1);
   // The GEMM that follows starts its weight stream on its own; where it reads
   // this kernel's outputs it waits for this grid to complete. Let it launch now.
   pdl_launch_dependents();
@@ -413,7 +455,7 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
     for (int t = threadIdx.x >> 5; t < a.M_tokens; t += kGatherWarps) {
       int id;
       float w;
-      warp_topk(a.logits + static_cast<long long>(t) * a.E, a.E, a.topk, lane, &id, &w);
+      warp_topk(a.logits + static_cast<long long>(t) * a.E_total, a.E_total, a.topk, lane, &id, &w);
       if (lane < a.topk) {
         s_ids[t * a.topk + lane] = id;
         if (blockIdx.x == 0) {
@@ -428,11 +470,14 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
     const int lane = threadIdx.x;
     int v = -1;  // this lane's slot id: from shared memory when routed here, else the input
     if (lane < a.MK) v = a.logits ? s_ids[lane] : a.topk_ids[lane];
-    const SmallRoute r = small_route_ids(v, a.MK, a.E, a.block, a.bn_max, lane);
+    const SmallRoute r = small_route_ids(v, a.MK, a.E, a.block, a.bn_max, lane, a.e_begin, a.E_total);
     const int npad = r.tot_pad < kSmallPadRows ? r.tot_pad : kSmallPadRows;
     for (int p = lane; p < npad; p += 32) s_sorted[p] = a.MK;
     __syncwarp();
-    if (r.e >= 0 && r.seg + r.rank < kSmallPadRows) s_sorted[r.seg + r.rank] = lane;
+    if (r.e >= 0 && r.seg + r.rank < kSmallPadRows) {
+      s_sorted[r.seg + r.rank] = lane;
+      s_expert[r.seg + r.rank] = r.e;
+    }
     if (lane == 0) s_npad = npad;
     if (blockIdx.x == 0) small_route_write(a, r, lane);
   }
@@ -441,7 +486,14 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   float4* acc4 = reinterpret_cast<float4*>(g.acc);
   for (long long i = gt; i < g.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = blockIdx.x; p < s_npad; p += gridDim.x) gather_row(g, p, s_sorted[p], s_red);
+  for (int p = blockIdx.x; p < s_npad; p += gridDim.x) {
+    const int sid = s_sorted[p];
+    gather_row(g, p, sid, s_red, sid < a.MK ? s_expert[p] : -1);
+  }
+#ifdef MOE_GEMM_TRACE
+  __syncthreads();
+  RG_STAMP(2);
+#endif
 }
 
 cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
@@ -466,7 +518,12 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
   float4* acc4 = reinterpret_cast<float4*>(a.acc);
   for (long long i = gt; i < a.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int num_padded = a.hdr[kHdrNumPadded];
-  for (int p = blockIdx.x; p < num_padded; p += gridDim.x) gather_row(a, p, a.sorted_ids[p], s_red);
+  for (int p = blockIdx.x; p < num_padded; p += gridDim.x) {
+    const int sid = a.sorted_ids[p];
+    // (the expert of a real row: align placed it in that expert's segment)
+    const int e = a.perm1 && sid >= 0 && sid < a.MK ? a.topk_ids[sid] - a.e_begin : -1;
+    gather_row(a, p, sid, s_red, e);
+  }
   pdl_launch_dependents();
 }
 

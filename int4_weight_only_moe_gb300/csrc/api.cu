@@ -12,6 +12,7 @@ using namespace moe;
 
 struct moe_w4a16_ctx {
   int E, K, N, topk, group;
+  int e_begin, E_total;  // expert parallelism: the handle holds [e_begin, e_begin + E) of E_total
   int device;
   int num_sms;
   int num_ctas;
@@ -20,11 +21,14 @@ struct moe_w4a16_ctx {
   bool profile;
   unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
-  int32_t* dflag;              // device word: pack's scale check
+  int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
   uint8_t* w2p;
   size_t w1p_bytes, w2p_bytes;
   bool packed;
+  int layout;      // source layout of the last pack (for the inverse)
+  int32_t* perm1;  // act-order packing order of w1's reduction elements [E, K], or null
+  int32_t* perm2;  // the same for w2 [E, N] (also the order of w1's output features)
   cudaEvent_t ev[6];
   bool ev_valid;
   // pinned staging of small host-buffer forwards whose buffers are pageable
@@ -154,6 +158,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   auto* h = new moe_w4a16_ctx();
   std::memset(h, 0, sizeof(*h));
   h->E = E;
+  h->E_total = E;
   h->K = K;
   h->N = N;
   h->topk = topk;
@@ -186,12 +191,33 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   return MOE_W4A16_OK;
 }
 
+int moe_w4a16_create_ep(int E_total, int expert_begin, int expert_end, int K, int N, int topk,
+                        int group_size, moe_w4a16_t* out) {
+  if (!out) return fail(MOE_W4A16_INVALID_ARG, "out is null");
+  *out = nullptr;
+  if (E_total < 1 || E_total > kMaxExperts)
+    return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "E_total must be in [1, 1024]");
+  if (expert_begin < 0 || expert_end <= expert_begin || expert_end > E_total)
+    return fail(MOE_W4A16_INVALID_ARG, "need 0 <= expert_begin < expert_end <= E_total");
+  if (topk < 1 || topk > E_total) return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "topk must be in [1, E_total]");
+  const int E = expert_end - expert_begin;
+  // (the local handle may hold fewer experts than a token's top-k)
+  int rc = moe_w4a16_create(E, K, N, topk <= E ? topk : E, group_size, out);
+  if (rc != MOE_W4A16_OK) return rc;
+  (*out)->topk = topk;
+  (*out)->e_begin = expert_begin;
+  (*out)->E_total = E_total;
+  return MOE_W4A16_OK;
+}
+
 int moe_w4a16_destroy(moe_w4a16_t h) {
   if (!h) return fail(MOE_W4A16_INVALID_ARG, "null handle");
   cudaDeviceSynchronize();
   cudaFree(h->w1p);
   cudaFree(h->w2p);
   cudaFree(h->dflag);
+  cudaFree(h->perm1);
+  cudaFree(h->perm2);
   if (h->hstage) cudaFreeHost(h->hstage);
   if (h->ev_valid)
     for (auto& ev : h->ev) cudaEventDestroy(ev);
@@ -203,19 +229,61 @@ size_t moe_w4a16_packed_bytes(moe_w4a16_t h) { return h ? h->w1p_bytes + h->w2p_
 
 int moe_w4a16_pack(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s, const int32_t* w2_q,
                    const uint16_t* w2_s, void* stream) {
+  return moe_w4a16_pack_ex(h, w1_q, w1_s, w2_q, w2_s, MOE_W4A16_LAYOUT_GPTQ, nullptr, nullptr, stream);
+}
+
+namespace {
+
+// Source description of w1 (gate/up: reduction K, 2N output features, features
+// reordered by w2's act-order permutation) and of w2 (reduction N, K features).
+RepackSource w1_source(moe_w4a16_t h, const int32_t* q, const uint16_t* sc) {
+  return RepackSource{q, sc, h->layout, h->perm1, h->perm2, h->N, h->K, 2 * h->N};
+}
+RepackSource w2_source(moe_w4a16_t h, const int32_t* q, const uint16_t* sc) {
+  return RepackSource{q, sc, h->layout, h->perm2, nullptr, 0, h->N, h->K};
+}
+
+// Act-order packing order of one matrix from its group index, or none.
+int make_perm(moe_w4a16_t h, const int32_t* g_idx, int R, int32_t** perm, cudaStream_t s) {
+  cudaFree(*perm);
+  *perm = nullptr;
+  if (!g_idx) return MOE_W4A16_OK;
+  MOE_CUDA_TRY(cudaMalloc(perm, static_cast<size_t>(h->E) * R * sizeof(int32_t)));
+  MOE_CUDA_TRY(launch_perm_from_g_idx(g_idx, *perm, h->E, R, h->dflag + 1, s));
+  return MOE_W4A16_OK;
+}
+
+}  // namespace
+
+int moe_w4a16_pack_ex(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s, const int32_t* w2_q,
+                      const uint16_t* w2_s, int layout, const int32_t* w1_g_idx,
+                      const int32_t* w2_g_idx, void* stream) {
   if (int rc = check_handle(h)) return rc;
   if (!w1_q || !w1_s || !w2_q || !w2_s) return fail(MOE_W4A16_INVALID_ARG, "null weight pointer");
+  if (layout != MOE_W4A16_LAYOUT_GPTQ && layout != MOE_W4A16_LAYOUT_COMPRESSED_TENSORS)
+    return fail(MOE_W4A16_INVALID_ARG, "unknown weight layout");
   auto s = static_cast<cudaStream_t>(stream);
   h->packed = false;
-  MOE_CUDA_TRY(cudaMemsetAsync(h->dflag, 0, sizeof(int32_t), s));
-  MOE_CUDA_TRY(launch_repack(reinterpret_cast<const uint32_t*>(w1_q), w1_s, h->w1p, h->E, h->K,
-                             2 * h->N, 2 * h->N / kBM, h->K / kBK, 1, h->dflag, s));
-  MOE_CUDA_TRY(launch_repack(reinterpret_cast<const uint32_t*>(w2_q), w2_s, h->w2p, h->E, h->N,
-                             h->K, h->K / kBM, h->N / kBK, 0, h->dflag, s));
-  int32_t bad = 0;
-  MOE_CUDA_TRY(cudaMemcpyAsync(&bad, h->dflag, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  h->layout = layout == MOE_W4A16_LAYOUT_GPTQ ? kLayoutGptq : kLayoutCompressedTensors;
+  MOE_CUDA_TRY(cudaMemsetAsync(h->dflag, 0, 2 * sizeof(int32_t), s));
+  if (int rc = make_perm(h, w1_g_idx, h->K, &h->perm1, s)) return rc;
+  if (int rc = make_perm(h, w2_g_idx, h->N, &h->perm2, s)) return rc;
+  int32_t flags[2] = {0, 0};
+  if (h->perm1 || h->perm2) {  // a bad group index stops here, before any repack reads it
+    MOE_CUDA_TRY(cudaMemcpyAsync(flags, h->dflag, sizeof(flags), cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    if (flags[1])
+      return fail(MOE_W4A16_BAD_G_IDX,
+                  "g_idx: every group index must lie in [0, R/32) and every group hold exactly 32 "
+                  "elements");
+  }
+  MOE_CUDA_TRY(launch_repack(w1_source(h, w1_q, w1_s), h->w1p, h->E, 2 * h->N / kBM, h->K / kBK, 1,
+                             h->dflag, s));
+  MOE_CUDA_TRY(launch_repack(w2_source(h, w2_q, w2_s), h->w2p, h->E, h->K / kBM, h->N / kBK, 0,
+                             h->dflag, s));
+  MOE_CUDA_TRY(cudaMemcpyAsync(flags, h->dflag, sizeof(flags), cudaMemcpyDeviceToHost, s));
   MOE_CUDA_TRY(cudaStreamSynchronize(s));
-  if (bad)
+  if (flags[0])
     return fail(MOE_W4A16_UNSUPPORTED_SCALE,
                 "a scale is outside the supported range (0, or 2^-14 <= |s| <= 8160, finite): "
                 "its fp16 dequantised weights would not be exact");
@@ -229,10 +297,10 @@ int moe_w4a16_unpack_debug(moe_w4a16_t h, int32_t* w1_q, uint16_t* w1_s, int32_t
   if (!w1_q || !w1_s || !w2_q || !w2_s) return fail(MOE_W4A16_INVALID_ARG, "null weight pointer");
   if (!h->packed) return fail(MOE_W4A16_NOT_PACKED, "weights not packed");
   auto s = static_cast<cudaStream_t>(stream);
-  MOE_CUDA_TRY(launch_unpack(h->w1p, reinterpret_cast<uint32_t*>(w1_q), w1_s, h->E, h->K, 2 * h->N,
-                             2 * h->N / kBM, h->K / kBK, 1, s));
-  MOE_CUDA_TRY(launch_unpack(h->w2p, reinterpret_cast<uint32_t*>(w2_q), w2_s, h->E, h->N, h->K,
-                             h->K / kBM, h->N / kBK, 0, s));
+  MOE_CUDA_TRY(launch_unpack(h->w1p, w1_source(h, nullptr, nullptr), w1_q, w1_s, h->E, 2 * h->N / kBM,
+                             h->K / kBK, 1, s));
+  MOE_CUDA_TRY(launch_unpack(h->w2p, w2_source(h, nullptr, nullptr), w2_q, w2_s, h->E, h->K / kBM,
+                             h->N / kBK, 0, s));
   return MOE_W4A16_OK;
 }
 
@@ -297,12 +365,14 @@ namespace {
 // writes topk_ids / topk_weights (outputs then); without, they are inputs.
 int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, const int32_t* topk_ids,
                  const float* topk_weights, uint16_t* out, int M, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+                 size_t workspace_bytes, void* stream, float* partial = nullptr) {
   if (int rc = check_handle(h)) return rc;
   if (M < 0) return fail(MOE_W4A16_INVALID_ARG, "M must be >= 0");
   if (M == 0) return MOE_W4A16_OK;
-  if (!hidden || !topk_ids || !topk_weights || !out || !workspace)
+  if (!hidden || !topk_ids || !topk_weights || (!out && !partial) || !workspace)
     return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  if (partial && reinterpret_cast<uintptr_t>(partial) % 16 != 0)
+    return fail(MOE_W4A16_INVALID_ARG, "partial must be 16-byte aligned");
   if (logits && h->topk > 32)
     return fail(MOE_W4A16_UNSUPPORTED_SHAPE, "the router supports topk <= 32");
   if (!h->packed) return fail(MOE_W4A16_NOT_PACKED, "moe_w4a16_pack has not been called");
@@ -327,7 +397,8 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   uint8_t* xs = ws + L.xs;
   uint8_t* hbuf = ws + L.hbuf;
   float* scratch = reinterpret_cast<float*>(ws + L.scratch);
-  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  // (the partial-sum forward accumulates straight into the caller's buffer)
+  float* acc = partial ? partial : reinterpret_cast<float*>(ws + L.acc);
   const bool prof = h->profile && h->ev_valid;
   const bool pdl = h->pdl && !prof;
 
@@ -343,6 +414,8 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   }
   aa.MK = static_cast<int>(MK);
   aa.E = h->E;
+  aa.e_begin = h->e_begin;
+  aa.E_total = h->E_total;
   aa.block = kRowGroup;
   aa.bn_max = kBNMax;
   aa.sorted_ids = sorted;
@@ -383,13 +456,16 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   ga.xs_bytes = static_cast<long long>(L.Pcap) * h->K * 2;
   ga.M = M;
   ga.dbg = hdr + 8;
+  ga.perm1 = h->perm1;
+  ga.topk_ids = topk_ids;
+  ga.e_begin = h->e_begin;
   if (MK <= 32) {
     // small batch (decode): routing and gather in one launch, timed as "align"
     MOE_CUDA_TRY(launch_route_gather_small(aa, ga, L.Pcap, h->num_sms, s, false));
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
   } else {
     if (logits)  // router kernel first; the align reads what it wrote
-      MOE_CUDA_TRY(launch_route(logits, M, h->E, h->topk, const_cast<int32_t*>(topk_ids),
+      MOE_CUDA_TRY(launch_route(logits, M, h->E_total, h->topk, const_cast<int32_t*>(topk_ids),
                                 const_cast<float*>(topk_weights), h->num_sms, s, false));
     MOE_CUDA_TRY(launch_align(aa, s, logits != nullptr && pdl));
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
@@ -410,6 +486,8 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   // start their weight streams without waiting for the routing + gather launch
   const int32_t* small_ids = (MK <= 32 && !logits) ? topk_ids : nullptr;
   g1.small_ids = small_ids;
+  g1.e_begin = h->e_begin;
+  g1.E_total = h->E_total;
   g1.R = 2 * h->N / kBM;
   g1.KBn = h->K / (2 * kBK);  // GEMM pipeline steps of 128 reduction elements
   g1.Gcap = L.Gcap;
@@ -441,9 +519,12 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.wait_kcycles = wait_limit_kcycles(h->wait_us);
   g2.test_never_wait = h->test_never_wait ? 1 : 0;
   g2.small_ids = small_ids;
+  g2.e_begin = h->e_begin;
+  g2.E_total = h->E_total;
   // small batches (the routing + gather launch zeroes every ticket): the down GEMM
-  // rounds each finished output row tile to bf16 itself, with no finalize launch
-  const bool fold_finalize = MK <= 32;
+  // rounds each finished output row tile to bf16 itself, with no finalize launch;
+  // the partial-sum forward rounds nothing
+  const bool fold_finalize = MK <= 32 && !partial;
   g2.rt_tickets = fold_finalize ? tickets + kMaxCtas : nullptr;
   g2.out = out;
   g2.M = M;
@@ -468,7 +549,7 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 
-  if (!fold_finalize)
+  if (!fold_finalize && !partial)
     MOE_CUDA_TRY(launch_finalize(acc, out, static_cast<long long>(M) * h->K, h->num_sms, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[5], s));
   return MOE_W4A16_OK;
@@ -491,6 +572,27 @@ int moe_w4a16_forward_logits(moe_w4a16_t h, const uint16_t* hidden, const float*
   if (!router_logits && M > 0) return fail(MOE_W4A16_INVALID_ARG, "null router_logits");
   return forward_impl(h, hidden, router_logits, topk_ids, topk_weights, out, M, workspace,
                       workspace_bytes, stream);
+}
+
+int moe_w4a16_forward_partial(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
+                              const float* topk_weights, float* partial, int M, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!partial && M > 0) return fail(MOE_W4A16_INVALID_ARG, "null partial");
+  return forward_impl(h, hidden, nullptr, topk_ids, topk_weights, nullptr, M, workspace,
+                      workspace_bytes, stream, partial);
+}
+
+int moe_w4a16_finalize(const float* acc, uint16_t* out, long long n, void* stream) {
+  if (n < 0) return fail(MOE_W4A16_INVALID_ARG, "n must be >= 0");
+  if (n == 0) return MOE_W4A16_OK;
+  if (!acc || !out) return fail(MOE_W4A16_INVALID_ARG, "null pointer argument");
+  if ((reinterpret_cast<uintptr_t>(acc) | reinterpret_cast<uintptr_t>(out)) % 16 != 0 || n % 8 != 0)
+    return fail(MOE_W4A16_INVALID_ARG, "acc and out must be 16-byte aligned and n a multiple of 8");
+  int dev = 0, sms = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  MOE_CUDA_TRY(launch_finalize(acc, out, n, sms, static_cast<cudaStream_t>(stream), false));
+  return MOE_W4A16_OK;
 }
 
 int moe_w4a16_route(const float* router_logits, int M, int E, int topk, int32_t* topk_ids,
@@ -649,6 +751,7 @@ int moe_w4a16_align_debug(const int32_t* topk_ids, int M, int topk, int E, int b
   aa.topk_ids = topk_ids;
   aa.MK = static_cast<int>(MK);
   aa.E = E;
+  aa.E_total = E;
   aa.block = block;
   aa.bn_max = 0;
   aa.sorted_ids = sorted_ids;

@@ -71,6 +71,14 @@ __device__ long long g_gemm_trace[16][2048];
 extern "C" int moe_gemm_trace_read(long long* host) {
   return static_cast<int>(cudaMemcpyFromSymbol(host, g_gemm_trace, sizeof(g_gemm_trace)));
 }
+extern "C" int moe_gemm_wait_iters(unsigned long long* host, int reset) {
+  int e = static_cast<int>(cudaMemcpyFromSymbol(host, g_wait_iters, sizeof(g_wait_iters)));
+  if (reset) {
+    unsigned long long z[32] = {};
+    cudaMemcpyToSymbol(g_wait_iters, z, sizeof(z));
+  }
+  return e;
+}
 #ifndef MOE_GEMM_TRACE_MODE
 #define MOE_GEMM_TRACE_MODE 1
 #endif
@@ -79,7 +87,29 @@ extern "C" int moe_gemm_trace_read(long long* host) {
     if (blockIdx.x == 0 && kMode == MOE_GEMM_TRACE_MODE && (idx) < 2048)            \
       g_gemm_trace[(slot)][(idx)] = clock64();                                      \
   } while (0)
+// every CTA of both GEMMs: global-timer stamps of a few events (latest wins)
+__device__ unsigned long long g_cta_trace[2][256][8];
+extern "C" int moe_gemm_cta_trace_read(unsigned long long* host, int reset) {
+  int e = static_cast<int>(cudaMemcpyFromSymbol(host, g_cta_trace, sizeof(g_cta_trace)));
+  if (reset) {
+    static unsigned long long z[2 * 256 * 8];
+    cudaMemcpyToSymbol(g_cta_trace, z, sizeof(z));
+  }
+  return e;
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define CTA_STAMP(ev)                                                               \
+  do {                                                                              \
+    if (blockIdx.x < 256) atomicMax(&g_cta_trace[kMode - 1][blockIdx.x][(ev)], gtimer()); \
+  } while (0)
 #else
+#define CTA_STAMP(ev) \
+  do {                \
+  } while (0)
 #define TRACE_POINT(slot, idx) \
   do {                         \
   } while (0)
@@ -463,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t wait_ns = a.wait_kcycles;  // (the wait limit, in units of 1024 cycles)
   if (threadIdx.x == 0) TRACE_POINT(13, 0);  // kernel entry
+  if (threadIdx.x == 0) CTA_STAMP(0);
   // A small batch (at most 32 routed slots, small_ids set) recomputes its routing
   // tiles from the caller's topk_ids in the activation producer's warp, while
   // thread 0 initialises the barriers and warp 2 allocates tensor memory.
@@ -470,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   TokenTile* small_tiles = reinterpret_cast<TokenTile*>(gbase + kSmSmall);
   int* small_ntiles = reinterpret_cast<int*>(gbase + kSmSmall + kSmallTiles * 16);
   if (small && warp == kWarpB) {
-    const SmallRoute r = small_route(a.small_ids, a.MK, a.E, kRowGroup, kBNMax, lane);
+    const SmallRoute r = small_route(a.small_ids, a.MK, a.E, kRowGroup, kBNMax, lane, a.e_begin, a.E_total);
     if (r.leader && r.tile0 < kSmallTiles) {  // one tile per expert present
       TokenTile tt;
       tt.expert = r.e;
@@ -536,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     num_tiles = a.hdr[kHdrNumTiles];
   }
   if (threadIdx.x == 0) TRACE_POINT(13, 1);
+  if (threadIdx.x == 0) CTA_STAMP(1);
   int* status = a.status;
   const long long W_total = static_cast<long long>(num_tiles) * a.R * a.KBn;
   const int G = static_cast<int>(gridDim.x);
@@ -650,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // (2-8 KB) copies in one go: a bulk-copy issue holds its thread
     // for a while, so small copies must leave several at a time.
     if (small) pdl_wait();  // the activations are the preceding kernel's output
+    if (lane == 0) CTA_STAMP(2);
     const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
       Cursor cur(my_begin, my_end, a.KBn, segs);
@@ -752,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                                                         kStatusTimeout, wait_ns));
           if (!ok) break;
           if (lane == 0) TRACE_POINT(3, it);
+          if (lane == 0 && it < 2) CTA_STAMP(4);
           const uint32_t a_tmem = tmem + st * kACols;
           // B stage sb is sb * b_stage bytes after stage 0, its second 64-element
           // half b_plane bytes further (16-byte units in the descriptor); +32 bytes of
@@ -771,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             tc_commit(bar(kBarEmpty + st));
             tc_commit(bar(kBarBEmpty + sb));
             TRACE_POINT(4, it);
+            CTA_STAMP(5);
           }
           acc_flag = 1u;
           sb += 2;
@@ -826,6 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
       bool w_ok = mbar_wait(bar(kBarWFull + ws), wpar, abort_flag, status, kStatusTimeout, wait_ns);
       if (!__all_sync(0xffffffffu, w_ok)) break;
       if (lane == 0 && quad == 0) TRACE_POINT(5, it);
+      if (lane == 0 && it == 0) CTA_STAMP(3);
       // the step's weights: slot ws, step (it & 1) of the chunk
       const uint32_t wstep = ws * kWChunk + (it & 1);
       const uint32_t wb = sW + wstep * kWStepBytes + r * 16;
@@ -1102,6 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
         }
       }
       if (epi_tid == 0) TRACE_POINT(15, acc_it);  // epilogue done with a segment
+      if (epi_tid == 0) CTA_STAMP(6);
       ++acc_it;
     }
     if (epi_tid == 0) bulk_wait_all();
@@ -1112,6 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   __syncwarp();  // lanes that skipped a single-lane role wait for it here
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) CTA_STAMP(7);
   if (warp == kWarpMma0) {
     __syncwarp();
     tc_fence_after();

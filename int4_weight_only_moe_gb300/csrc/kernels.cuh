@@ -10,11 +10,26 @@
 namespace moe {
 
 // Sets *bad_scale (device) when a scale lies outside the supported range.
-cudaError_t launch_repack(const uint32_t* q, const uint16_t* s, uint8_t* out, int E, int Kred,
-                          int Nout, int R, int KBn, int interleave, int32_t* bad_scale,
-                          cudaStream_t stream);
-cudaError_t launch_unpack(const uint8_t* in, uint32_t* q, uint16_t* s, int E, int Kred, int Nout,
+// Source layouts of the repack (see pack.cu).
+constexpr int kLayoutGptq = 0;
+constexpr int kLayoutCompressedTensors = 1;
+struct RepackSource {
+  const int32_t* q;         // codes (null for the unpack direction)
+  const uint16_t* s;        // bf16 scales
+  int layout;               // kLayoutGptq or kLayoutCompressedTensors
+  const int32_t* red_perm;  // [E, Kred] packed -> source reduction element (act-order), or null
+  const int32_t* out_perm;  // [E, out_period] packed -> source output feature, or null
+  int out_period;
+  int Kred, Nout;
+};
+cudaError_t launch_repack(const RepackSource& src, uint8_t* out, int E, int R, int KBn,
+                          int interleave, int32_t* bad_scale, cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t* in, const RepackSource& dst, int32_t* q, uint16_t* s, int E,
                           int R, int KBn, int interleave, cudaStream_t stream);
+// Act-order packing order [E, R] from the group index [E, R]; *bad set on an
+// index out of range or a group without exactly 32 elements.
+cudaError_t launch_perm_from_g_idx(const int32_t* g_idx, int32_t* perm, int E, int R, int32_t* bad,
+                                   cudaStream_t stream);
 
 // Token->expert align (counting sort + padding + token-tile list). With bn_max == 0
 // no tile list is written (the debug entry point); expert_offsets may be null.
@@ -27,7 +42,8 @@ struct AlignArgs {
   float* wts_out;
   int M_tokens, topk;
   int MK;             // M * topk (flat slot count; also the padding sentinel)
-  int E;
+  int E;              // experts held (local experts under expert parallelism)
+  int e_begin, E_total;  // the held experts are [e_begin, e_begin + E) of E_total
   int block;          // per-expert padding granularity
   int bn_max;         // token-tile size (multiple of 16) or 0
   int32_t* sorted_ids;
@@ -66,6 +82,11 @@ struct GatherArgs {
   long long xs_bytes;  // extents for the self-checking build
   int M;
   int32_t* dbg;
+  // act-order on w1: packed reduction element j of expert e is hidden element
+  // perm1[e][j]; the gather writes the row in that order (null: natural order)
+  const int32_t* perm1;
+  const int32_t* topk_ids;  // expert of a slot (read only when perm1 is set)
+  int e_begin;              // first expert held (the ids are the layer's)
 };
 cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
                           bool pdl);
@@ -89,6 +110,7 @@ struct GemmArgs {
   // recomputes the routing tiles itself (so its weight stream need not wait for
   // the preceding kernel); null: read the tiles the align kernel wrote
   const int32_t* small_ids;
+  int e_begin, E_total;    // the held experts are [e_begin, e_begin + E) of E_total (small_ids)
   uint32_t wait_kcycles;   // pipeline wait limit in units of 1024 SM cycles (wait_limit_kcycles)
   int test_never_wait;     // test hook: the epilogue first waits on a barrier nothing arrives on
   // down GEMM, small batches: per output row tile, a zeroed ticket counting the

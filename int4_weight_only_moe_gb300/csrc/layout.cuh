@@ -88,6 +88,20 @@ __host__ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, |e| <= 126
 #endif
 }
 
+// Expert parallelism: a handle may hold only experts [e_begin, e_begin + E) of a
+// layer with E_total experts (E_total == E, e_begin == 0 otherwise). A routed
+// slot's expert id v maps to the local expert v - e_begin, or to -1 (skipped)
+// when another part of the layer holds it; an id outside [0, E_total) is no
+// expert of the layer at all: skipped too, and *bad is set.
+__host__ __device__ __forceinline__ int local_expert(int v, int e_begin, int E, int E_total, bool* bad) {
+  if (v < 0 || v >= E_total) {
+    *bad = true;
+    return -1;
+  }
+  const int l = v - e_begin;
+  return (l >= 0 && l < E) ? l : -1;
+}
+
 // Relative cost of one pipeline step of a unit whose token tile holds ng row
 // groups: a base of 8 plus `per_group` for every row group beyond the second. The
 // weight stream (9 KB a step from HBM) and its conversion are the same for every

@@ -1,8 +1,9 @@
-// Weight repack: GPTQ-style int32-packed INT4 codes + bf16 group scales ->
-// the tiled layout described in layout.cuh (and its inverse, for round-trip
-// checks). Counterpart of the repack step of "The Pivot to Real Hardware ...",
-// Step 2 (GPTQ in, hardware-friendly layout out, no act-order permutation);
-// the byte count is unchanged.
+// Weight repack: int32-packed INT4 codes + bf16 group scales (GPTQ or
+// compressed-tensors layout, optionally quantised in activation order) -> the
+// tiled layout described in layout.cuh (and its inverse, for round-trip checks).
+// Counterpart of the repack step of "The Pivot to Real Hardware ...", Step 2
+// (GPTQ in, with an act-order permutation or without, hardware-friendly layout
+// out); the byte count is unchanged.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -62,12 +63,57 @@ __device__ __forceinline__ uint16_t f16_to_bf16_bits(uint16_t h) {
   return *reinterpret_cast<const uint16_t*>(&v);
 }
 
-// One CTA per (expert, row tile, k-block) block. `q` is [E, Kred/8, Nout] int32,
-// `s` is [E, Kred/32, Nout] bf16; `R` row tiles of 128 rows, `KBn` k-blocks.
-__global__ void __launch_bounds__(256) repack_kernel(const uint32_t* __restrict__ q,
-                                                     const uint16_t* __restrict__ s,
-                                                     uint8_t* __restrict__ out, int Kred,
-                                                     int Nout, int R, int KBn, int interleave,
+// Where a packed element comes from. The codes and scales arrive in one of two
+// layouts (`layout`):
+//   kLayoutGptq: q [E, Kred/8, Nout] int32, s [E, Kred/32, Nout] -- eight codes of
+//     one output feature along the reduction axis per word;
+//   kLayoutCompressedTensors: q [E, Nout, Kred/8], s [E, Nout, Kred/32] -- every
+//     output feature's row contiguous, the same eight-codes-per-word order.
+// With act-order the packed reduction element j of expert e is source element
+// red_perm[e][j] (the elements sorted by scale group, so that packed group j/32 is
+// source group j/32), and an output-feature permutation (out_perm, period P:
+// feature f -> P * (f / P) + out_perm[e][f % P]) may reorder the features.
+struct PackSrc {
+  const uint32_t* q;
+  const uint16_t* s;
+  int layout;
+  const int32_t* red_perm;  // [E, Kred] or null
+  const int32_t* out_perm;  // [E, P] or null
+  int out_period;
+  int Kred, Nout;
+};
+
+__device__ __forceinline__ long long q_index(const PackSrc& p, long long e, int r8, int f) {
+  return p.layout == kLayoutGptq ? (e * (p.Kred / 8) + r8) * p.Nout + f
+                                 : (e * p.Nout + f) * (p.Kred / 8) + r8;
+}
+__device__ __forceinline__ long long s_index(const PackSrc& p, long long e, int g, int f) {
+  return p.layout == kLayoutGptq ? (e * (p.Kred / kGroup) + g) * p.Nout + f
+                                 : (e * p.Nout + f) * (p.Kred / kGroup) + g;
+}
+__device__ __forceinline__ int source_feature(const PackSrc& p, long long e, int f) {
+  if (!p.out_perm) return f;
+  const int P = p.out_period;
+  return (f / P) * P + p.out_perm[e * P + f % P];
+}
+
+// Codes of packed reduction elements 8*r8 .. 8*r8+7 of source feature f (GPTQ
+// word order: element 8*r8+i in bits 4i..).
+__device__ __forceinline__ uint32_t gather_word(const PackSrc& p, long long e, int r8, int f) {
+  if (!p.red_perm) return p.q[q_index(p, e, r8, f)];
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int k = p.red_perm[e * p.Kred + 8 * r8 + i];
+    w |= ((p.q[q_index(p, e, k >> 3, f)] >> (4 * (k & 7))) & 0xFu) << (4 * i);
+  }
+  return w;
+}
+
+// One CTA per (expert, row tile, k-block) block; `R` row tiles of 128 rows,
+// `KBn` k-blocks of 64 reduction elements.
+__global__ void __launch_bounds__(256) repack_kernel(const PackSrc p, uint8_t* __restrict__ out,
+                                                     int R, int KBn, int interleave,
                                                      int32_t* __restrict__ bad_scale) {
   const long long blk = blockIdx.x;
   const int kb = static_cast<int>(blk % KBn);
@@ -76,27 +122,27 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint32_t* __restrict_
   uint8_t* dst = out + blk * kWBlockBytes;
   uint32_t* dw = reinterpret_cast<uint32_t*>(dst);
   uint16_t* ds = reinterpret_cast<uint16_t*>(dst + kWCodeBytes);
-  const long long qrows = Kred / 8, srows = Kred / kGroup;
   // codes: thread t -> row r = t % 128 (consecutive threads read neighbouring columns)
   for (int t = threadIdx.x; t < 1024; t += blockDim.x) {
     const int r = t & 127, j = (t >> 7) & 3, h = t >> 9;
-    const int f = tile_row_source(rt, r, Nout, interleave);
-    const long long row8 = static_cast<long long>(kb) * 8 + h * 4 + j;
-    const uint32_t src = q[(e * qrows + row8) * Nout + f];
-    dw[h * 512 + r * 4 + j] = interleave_codes(src);
+    const int f = source_feature(p, e, tile_row_source(rt, r, p.Nout, interleave));
+    dw[h * 512 + r * 4 + j] = interleave_codes(gather_word(p, e, kb * 8 + h * 4 + j, f));
   }
+  // scales: packed group kb*2 + h is source group kb*2 + h (act-order sorts the
+  // elements by group)
   for (int t = threadIdx.x; t < 256; t += blockDim.x) {
     const int r = t & 127, h = t >> 7;
-    const int f = tile_row_source(rt, r, Nout, interleave);
-    const uint16_t b = s[(e * srows + kb * 2 + h) * Nout + f];
+    const int f = source_feature(p, e, tile_row_source(rt, r, p.Nout, interleave));
+    const uint16_t b = p.s[s_index(p, e, kb * 2 + h, f)];
     if (!scale_supported(b)) *bad_scale = 1;
     ds[r * 2 + h] = bf16_to_f16_bits(b);
   }
 }
 
-__global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__ in,
-                                                     uint32_t* __restrict__ q,
-                                                     uint16_t* __restrict__ s, int Kred, int Nout,
+// Inverse of repack_kernel into the source layout (q must be zeroed first when a
+// reduction permutation scatters single codes: they are OR-ed into place).
+__global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__ in, PackSrc p,
+                                                     uint32_t* __restrict__ q, uint16_t* __restrict__ s,
                                                      int R, int KBn, int interleave) {
   const long long blk = blockIdx.x;
   const int kb = static_cast<int>(blk % KBn);
@@ -105,36 +151,95 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
   const uint8_t* src = in + blk * kWBlockBytes;
   const uint32_t* sw = reinterpret_cast<const uint32_t*>(src);
   const uint16_t* ss = reinterpret_cast<const uint16_t*>(src + kWCodeBytes);
-  const long long qrows = Kred / 8, srows = Kred / kGroup;
   for (int t = threadIdx.x; t < 1024; t += blockDim.x) {
     const int r = t & 127, j = (t >> 7) & 3, h = t >> 9;
-    const int f = tile_row_source(rt, r, Nout, interleave);
-    const long long row8 = static_cast<long long>(kb) * 8 + h * 4 + j;
-    q[(e * qrows + row8) * Nout + f] = deinterleave_codes(sw[h * 512 + r * 4 + j]);
+    const int f = source_feature(p, e, tile_row_source(rt, r, p.Nout, interleave));
+    const int r8 = kb * 8 + h * 4 + j;
+    const uint32_t w = deinterleave_codes(sw[h * 512 + r * 4 + j]);
+    if (!p.red_perm) {
+      q[q_index(p, e, r8, f)] = w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = p.red_perm[e * p.Kred + 8 * r8 + i];
+        atomicOr(q + q_index(p, e, k >> 3, f), ((w >> (4 * i)) & 0xFu) << (4 * (k & 7)));
+      }
+    }
   }
   for (int t = threadIdx.x; t < 256; t += blockDim.x) {
     const int r = t & 127, h = t >> 7;
-    const int f = tile_row_source(rt, r, Nout, interleave);
-    s[(e * srows + kb * 2 + h) * Nout + f] = f16_to_bf16_bits(ss[r * 2 + h]);
+    const int f = source_feature(p, e, tile_row_source(rt, r, p.Nout, interleave));
+    s[s_index(p, e, kb * 2 + h, f)] = f16_to_bf16_bits(ss[r * 2 + h]);
   }
 }
 
-cudaError_t launch_repack(const uint32_t* q, const uint16_t* s, uint8_t* out, int E, int Kred,
-                          int Nout, int R, int KBn, int interleave, int32_t* bad_scale,
-                          cudaStream_t stream) {
+// Act-order: the packing order of each expert's reduction elements from its group
+// index g_idx [E, R] -- the elements of group 0 in ascending index, then those of
+// group 1, ... (a stable sort by group). Every group must hold exactly 32
+// elements (the layout keeps one scale per 32 consecutive packed elements); an
+// index outside [0, R/32) or a group of another size sets *bad. One warp per
+// expert; the running count of every group lives in shared memory.
+__global__ void __launch_bounds__(32) perm_from_g_idx_kernel(const int32_t* __restrict__ g_idx,
+                                                             int32_t* __restrict__ perm, int R,
+                                                             int32_t* __restrict__ bad) {
+  extern __shared__ int cnt[];
+  const int G = R / kGroup;
+  const long long e = blockIdx.x;
+  const int lane = threadIdx.x;
+  for (int i = lane; i < G; i += 32) cnt[i] = 0;
+  __syncwarp();
+  for (int base = 0; base < R; base += 32) {
+    const int k = base + lane;  // R is a multiple of 32
+    const int g = g_idx[e * R + k];
+    const bool ok = g >= 0 && g < G;
+    if (!ok) *bad = 1;
+    // lanes of the same group, in lane (= element) order; a bad lane stands alone
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? g : -1 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int c = ok ? cnt[g] : 0;
+    __syncwarp();
+    if (ok && rank == 0) cnt[g] = c + __popc(peers);
+    __syncwarp();
+    if (ok) {
+      const int pos = c + rank;
+      if (pos < kGroup)
+        perm[e * R + g * kGroup + pos] = k;
+      else
+        *bad = 1;
+    }
+  }
+}
+
+cudaError_t launch_repack(const RepackSource& src, uint8_t* out, int E, int R, int KBn,
+                          int interleave, int32_t* bad_scale, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(E) * R * KBn;
   if (blocks <= 0) return cudaSuccess;
-  repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(q, s, out, Kred, Nout, R, KBn,
-                                                                   interleave, bad_scale);
+  const PackSrc p{reinterpret_cast<const uint32_t*>(src.q), src.s, src.layout, src.red_perm,
+                  src.out_perm, src.out_period, src.Kred, src.Nout};
+  repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p, out, R, KBn, interleave,
+                                                                   bad_scale);
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpack(const uint8_t* in, uint32_t* q, uint16_t* s, int E, int Kred, int Nout,
+cudaError_t launch_unpack(const uint8_t* in, const RepackSource& dst, int32_t* q, uint16_t* s, int E,
                           int R, int KBn, int interleave, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(E) * R * KBn;
   if (blocks <= 0) return cudaSuccess;
-  unpack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(in, q, s, Kred, Nout, R, KBn,
-                                                                   interleave);
+  if (dst.red_perm) {
+    cudaError_t e = cudaMemsetAsync(q, 0, static_cast<size_t>(E) * dst.Kred / 8 * dst.Nout * 4, stream);
+    if (e != cudaSuccess) return e;
+  }
+  const PackSrc p{nullptr, nullptr, dst.layout, dst.red_perm, dst.out_perm, dst.out_period,
+                  dst.Kred, dst.Nout};
+  unpack_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      in, p, reinterpret_cast<uint32_t*>(q), s, R, KBn, interleave);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_from_g_idx(const int32_t* g_idx, int32_t* perm, int E, int R, int32_t* bad,
+                                   cudaStream_t stream) {
+  if (E <= 0) return cudaSuccess;
+  perm_from_g_idx_kernel<<<E, 32, (R / kGroup) * sizeof(int), stream>>>(g_idx, perm, R, bad);
   return cudaGetLastError();
 }
 

@@ -96,11 +96,20 @@ __host__ __device__ constexpr uint32_t wait_limit_kcycles(unsigned long long lim
 // `abort_flag`, or if the wait has lasted longer than `limit_kcycles` * 1024 SM
 // cycles (then it raises the flag and records `status_bit` in the global status
 // word). Never spins without bound.
+#ifdef MOE_GEMM_TRACE
+// trace builds: try-wait iterations per warp of CTA 0 (read with the trace)
+__device__ unsigned long long g_wait_iters[32];
+#define MOE_WAIT_ITER() \
+  do { if (blockIdx.x == 0 && (threadIdx.x & 31) == 0) atomicAdd(&g_wait_iters[threadIdx.x >> 5], 1ull); } while (0)
+#else
+#define MOE_WAIT_ITER() do { } while (0)
+#endif
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, int status_bit, uint32_t limit_kcycles) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long c0 = clock64();
   for (;;) {
+    MOE_WAIT_ITER();
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (((clock64() - c0) >> 10) > static_cast<long long>(limit_kcycles)) {

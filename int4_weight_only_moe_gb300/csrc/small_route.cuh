@@ -5,6 +5,8 @@
 #pragma once
 #include <cstdint>
 
+#include "layout.cuh"
+
 namespace moe {
 
 // Small batches (at most 32 routed slots, e.g. decode) take one warp, with no
@@ -25,18 +27,15 @@ struct SmallRoute {
 };
 
 // `v` is the expert id of flat slot `lane` (read by the caller: global or shared
-// memory), ignored for lanes at or beyond MK.
+// memory), ignored for lanes at or beyond MK. The handle holds experts
+// [e_begin, e_begin + E) of a layer of E_total: a slot of another expert of the
+// layer is skipped, an id outside [0, E_total) is skipped and flagged.
 __device__ __forceinline__ SmallRoute small_route_ids(int v, int MK, int E, int block, int bn_max,
-                                                      int lane) {
+                                                      int lane, int e_begin, int E_total) {
   SmallRoute r;
   r.e = -1;
   bool bad = false;
-  if (lane < MK) {
-    if (v >= 0 && v < E)
-      r.e = v;
-    else
-      bad = true;
-  }
+  if (lane < MK) r.e = local_expert(v, e_begin, E, E_total, &bad);
   const unsigned peers = __match_any_sync(0xffffffffu, r.e);
   const bool valid = r.e >= 0;
   r.rank = __popc(peers & ((1u << lane) - 1u));
@@ -65,8 +64,8 @@ __device__ __forceinline__ SmallRoute small_route_ids(int v, int MK, int E, int 
 
 // The same, reading slot `lane`'s id from `ids` (global memory).
 __device__ __forceinline__ SmallRoute small_route(const int32_t* ids, int MK, int E, int block,
-                                                  int bn_max, int lane) {
-  return small_route_ids(lane < MK ? ids[lane] : -1, MK, E, block, bn_max, lane);
+                                                  int bn_max, int lane, int e_begin, int E_total) {
+  return small_route_ids(lane < MK ? ids[lane] : -1, MK, E, block, bn_max, lane, e_begin, E_total);
 }
 
 }  // namespace moe
