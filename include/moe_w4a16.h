@@ -140,7 +140,8 @@ size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M);
  *   out          bf16  [M, K]      written completely (rounded to nearest even)
  *   workspace    >= moe_w4a16_workspace_size(h, M) bytes, 256-byte aligned
  * M == 0 is a no-op. Launches 5 kernels on `stream` (3 when M * topk <= 32:
- * routing + gather, gate/up GEMM, down GEMM with the bf16 rounding folded in),
+ * routing + gather, gate/up GEMM, down GEMM with the bf16 rounding folded in;
+ * or 2, see MOE_W4A16_OPT_FUSED_SMALL_BATCH),
  * allocates nothing and makes no host-synchronising call, so it may be captured
  * into a CUDA graph and replayed with new inputs in the same buffers. */
 int moe_w4a16_forward(moe_w4a16_t h, const uint16_t* hidden, const int32_t* topk_ids,
@@ -246,10 +247,17 @@ const char* moe_w4a16_last_error(void);
  *   MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES
  *                            test hook: 1 makes each GEMM's epilogue first wait on
  *                            a barrier nothing arrives on, so that the give-up path
- *                            above runs (use with a short wait limit). 0 = off. */
+ *                            above runs (use with a short wait limit). 0 = off.
+ *   MOE_W4A16_OPT_FUSED_SMALL_BATCH
+ *                            1 = a forward with M * topk <= 32 whose ids are given
+ *                            runs both GEMMs in one cooperative launch (the down
+ *                            GEMM's weights stream while the gate/up GEMM
+ *                            finishes); 0 (default) = two launches. Either way the
+ *                            same arithmetic. */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
        MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5,
-       MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7 };
+       MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7,
+       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8 };
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order

@@ -21,6 +21,7 @@ struct moe_w4a16_ctx {
   bool profile;
   unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
+  bool fused_small;            // MOE_W4A16_OPT_FUSED_SMALL_BATCH
   int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
   uint8_t* w2p;
@@ -86,6 +87,8 @@ struct WsLayout {
 
 // Workspace carve-up for M tokens. Pcap bounds the padded routed-row count:
 // M*k rows plus at most 15 padding rows for each expert that receives any.
+int n_tickets(const moe_w4a16_ctx* h) { return kMaxCtas + h->K / kBM + kSmallTiles * (h->N / kBM); }
+
 WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   WsLayout L{};
   const long long MK = static_cast<long long>(M) * h->topk;
@@ -98,8 +101,10 @@ WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   L.hdr = off;
   off += kHdrWords * sizeof(int32_t);
   off = align_up(off, 256);
-  L.tickets = off;  // gate/up split-unit tickets [kMaxCtas], then the down row-tile tickets [K/128]
-  off = align_up(off + (kMaxCtas + h->K / kBM) * sizeof(int32_t), 256);
+  // gate/up split-unit tickets [kMaxCtas], the down row-tile tickets [K/128], then
+  // the fused launch's intermediate counters [32 token tiles][N/128]
+  L.tickets = off;
+  off = align_up(off + n_tickets(h) * sizeof(int32_t), 256);
   L.sched = off;  // stream-K boundaries of the two GEMMs
   off = align_up(off + 2 * (kMaxCtas + 1) * sizeof(long long), 256);
   L.sorted = off;
@@ -164,6 +169,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->topk = topk;
   h->group = group_size;
   h->pdl = true;
+  h->fused_small = false;
   h->step_cost[0] = kDefaultStepCostGateUp;
   h->step_cost[1] = kDefaultStepCostDown;
   cudaError_t e = cudaGetDevice(&h->device);
@@ -335,6 +341,9 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
       if (value < 0) return fail(MOE_W4A16_INVALID_ARG, "wait limit must be >= 0");
       h->wait_us = static_cast<unsigned long long>(value);
       return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_FUSED_SMALL_BATCH:
+      h->fused_small = value != 0;
+      return MOE_W4A16_OK;
     case MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES:
       h->test_never_wait = value != 0;
       return MOE_W4A16_OK;
@@ -423,7 +432,7 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   aa.expert_tiles = expert_tiles;
   aa.hdr = hdr;
   aa.tickets = tickets;
-  aa.n_tickets = kMaxCtas + h->K / kBM;
+  aa.n_tickets = n_tickets(h);
   aa.sorted_cap = L.Pcap;
   aa.tiles_cap = L.Gcap;
   aa.dbg = hdr + 8;
@@ -506,7 +515,13 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g1.E = h->E;
   g1.dbg = hdr + 8;
   g1.sched = (sched && h->step_cost[0] > 0) ? sched : nullptr;
-  MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
+  // small batch with given ids: both GEMMs in one cooperative launch (the shares
+  // of its gate/up phase start at multiples of 4 steps, so the step count per
+  // unit must allow that)
+  // (cooperative: at most one CTA per SM)
+  const bool fused = h->fused_small && small_ids != nullptr && h->num_ctas <= h->num_sms &&
+                     (static_cast<long long>(g1.R) * g1.KBn) % 4 == 0;
+  if (!fused) MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
   GemmArgs g2{};
@@ -546,7 +561,12 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.E = h->E;
   g2.dbg = hdr + 8;
   g2.sched = (sched && h->step_cost[1] > 0) ? sched + (h->num_ctas + 1) : nullptr;
-  MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
+  int32_t* h_ready = tickets + kMaxCtas + h->K / kBM;
+  g1.h_ready = g2.h_ready = h_ready;
+  if (fused)
+    MOE_CUDA_TRY(launch_gemm_fused(g1, g2, h->num_ctas, s, pdl));
+  else
+    MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 
   if (!fold_finalize && !partial)

@@ -88,11 +88,11 @@ extern "C" int moe_gemm_wait_iters(unsigned long long* host, int reset) {
       g_gemm_trace[(slot)][(idx)] = clock64();                                      \
   } while (0)
 // every CTA of both GEMMs: global-timer stamps of a few events (latest wins)
-__device__ unsigned long long g_cta_trace[2][256][8];
+__device__ unsigned long long g_cta_trace[3][256][16];
 extern "C" int moe_gemm_cta_trace_read(unsigned long long* host, int reset) {
   int e = static_cast<int>(cudaMemcpyFromSymbol(host, g_cta_trace, sizeof(g_cta_trace)));
   if (reset) {
-    static unsigned long long z[2 * 256 * 8];
+    static unsigned long long z[3 * 256 * 16];
     cudaMemcpyToSymbol(g_cta_trace, z, sizeof(z));
   }
   return e;
@@ -176,7 +176,6 @@ constexpr int kSmMisc = kSmBar + kNumBars * 8;
 constexpr int kMaxSegs = 256;            // units decoded into shared memory up front
 constexpr int kSmSeg = kSmMisc + 64;
 constexpr int kSmSched = kSmSeg + kMaxSegs * 16;  // [kMaxCtas + 1] stream-K boundaries
-constexpr int kSmallTiles = 32;          // token tiles of a batch of at most 32 routed slots
 constexpr int kSmSmall = kSmSched + (kMaxCtas + 1) * 8 + 8;  // [kSmallTiles] TokenTile + count
 constexpr int kSmRings = ((kSmSmall + kSmallTiles * 16 + 16 + 1023) / 1024) * 1024;
 constexpr int kSmAlloc = 227 * 1024;     // the whole per-CTA limit (base aligned to 1024 inside)
@@ -251,12 +250,36 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Bounded wait until the n counters at p (raised by other CTAs of the grid with
+// a fence then an atomic add) all reach `target`; then this thread's later bulk
+// copies see the data written before those releases. Gives up like mbar_wait.
+__device__ __noinline__ bool wait_counters(const int32_t* p, int n, int target, volatile int* abort_flag,
+                                           int* status, uint32_t limit_kcycles) {
+  const long long c0 = clock64();
+  for (;;) {
+    int below = 0;
+    for (int k = 0; k < n; ++k) below += ld_relaxed_gpu(p + k) < target ? 1 : 0;
+    if (below == 0) break;
+    if (*abort_flag) return false;
+    if (((clock64() - c0) >> 10) > static_cast<long long>(limit_kcycles)) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(256);
+  }
+  __threadfence();             // acquire: pairs with the writers' fence before their add
+  fence_proxy_async_global();  // and orders the bulk copies (async proxy) after it
+  return true;
+}
+
 struct Sched {
   long long W;           // total steps
   int G;                 // CTAs
   const long long* tab;  // [G + 1] cost-weighted first steps (shared memory), or null: even split
+  int gran;              // even split: shares start at multiples of gran (W is a multiple)
   __device__ __forceinline__ long long start(int c) const {
-    return tab ? tab[c] : static_cast<long long>(c) * W / G;
+    return tab ? tab[c] : gran * (static_cast<long long>(c) * (W / gran) / G);
   }
   // CTA whose share contains step g.
   __device__ int cta_of(long long g) const {
@@ -475,8 +498,10 @@ __device__ __forceinline__ bool swiglu_chunk(const float (&v)[16], int chunk, in
   return sat;
 }
 
-template <int kMode>  // 1: gate/up + SwiGLU, 2: down + weighted scatter-add
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
+// kMode 1: gate/up + SwiGLU; 2: down + weighted scatter-add; 3: both in one
+// launch for a small batch (phase 1 with `a`, then phase 2 with `a2`; see below).
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, const GemmArgs a2) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -492,6 +517,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t wait_ns = a.wait_kcycles;  // (the wait limit, in units of 1024 cycles)
+  // Phases of this launch. The fused launch (small batches only) runs every
+  // role's gate/up share and then its down share with the rings, stage counters
+  // and accumulator buffers carried across: a CTA's down-projection weights
+  // stream in as soon as its gate/up weights are issued, and its down
+  // activations (the intermediate h) are waited for per token tile, on counters
+  // the gate/up epilogues raise as they store h -- the CTAs of the grid are all
+  // resident (cooperative launch), and no gate/up work ever waits on down work.
+  constexpr int kPh0 = kMode == 2 ? 2 : 1, kPh1 = kMode == 1 ? 1 : 2;
+  auto args = [&](int ph) -> const GemmArgs& { return (kMode == 3 && ph == 2) ? a2 : a; };
   if (threadIdx.x == 0) TRACE_POINT(13, 0);  // kernel entry
   if (threadIdx.x == 0) CTA_STAMP(0);
   // A small batch (at most 32 routed slots, small_ids set) recomputes its routing
@@ -569,16 +603,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
   if (threadIdx.x == 0) TRACE_POINT(13, 1);
   if (threadIdx.x == 0) CTA_STAMP(1);
   int* status = a.status;
-  const long long W_total = static_cast<long long>(num_tiles) * a.R * a.KBn;
   const int G = static_cast<int>(gridDim.x);
   // Cost-weighted boundaries when the align kernel wrote them (else an even split
   // of the steps). Every CTA checks the whole table -- it starts at 0, ends at the
   // step count and never decreases -- and all of them fall back to the even split
   // (and flag the status word) if it does not: the split units' tickets rely on
-  // every CTA seeing the same boundaries.
-  bool weighted = a.sched != nullptr && ((a.hdr[kHdrSched] >> (kMode - 1)) & 1) != 0;
+  // every CTA seeing the same boundaries. (Separate launches only: a small batch
+  // has no table.)
+  bool weighted = kMode != 3 && a.sched != nullptr && ((a.hdr[kHdrSched] >> ((kMode & 3) - 1)) & 1) != 0;
   long long* sched_sm = reinterpret_cast<long long*>(gbase + kSmSched);
   if (weighted) {
+    const long long W_total = static_cast<long long>(num_tiles) * a.R * a.KBn;
     for (int i = threadIdx.x; i <= G; i += blockDim.x) sched_sm[i] = a.sched[i];
     __syncthreads();
     bool ok = true;
@@ -590,8 +625,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     weighted = __syncthreads_and(ok) != 0;
     if (!weighted && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, kStatusBadSched);
   }
-  const Sched sc{W_total, G, weighted ? sched_sm : nullptr};
-  const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
+  // The split of phase ph's steps. In the fused launch the gate/up shares start
+  // at multiples of 4 steps, so that every CTA's gate/up share is a whole number
+  // of 2-step weight chunks (its down share starts a chunk of its own) and of
+  // activation-producer rounds (each producer lane keeps its slots).
+  auto phase_sched = [&](int ph) -> Sched {
+    const GemmArgs& A = args(ph);
+    return Sched{static_cast<long long>(num_tiles) * A.R * A.KBn, G, weighted ? sched_sm : nullptr,
+                 (kMode == 3 && ph == 1) ? 4 : 1};
+  };
+  // this CTA's share of each phase, and where the down share starts in the CTA's
+  // step sequence (every ring slot and stage follows that sequence)
+  long long my_begin = 0, my_end = 0, n_first = 0;
+  {
+    const Sched s0 = phase_sched(kPh0);
+    my_begin = s0.start(blockIdx.x);
+    my_end = s0.start(blockIdx.x + 1);
+    n_first = my_end - my_begin;
+  }
+  long long my_begin2 = 0, my_end2 = 0;
+  if (kMode == 3) {
+    const Sched s1 = phase_sched(2);
+    my_begin2 = s1.start(blockIdx.x);
+    my_end2 = s1.start(blockIdx.x + 1);
+  }
+  const long long n_total = n_first + (my_end2 - my_begin2);
   pdl_launch_dependents();
   if (threadIdx.x == 0) TRACE_POINT(13, 2);  // range known
 
@@ -612,7 +670,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     __syncthreads();
   }
   if (threadIdx.x == 0) TRACE_POINT(13, 3);  // units decoded
-  const SegTable segs{seg_tab, u_first, n_tab, a.R, a.tiles, a.expert_tiles, small ? small_tiles : nullptr};
+  // unit tables of the phases (the second only in the fused launch, always small)
+  auto phase_segs = [&](int ph) -> SegTable {
+    const GemmArgs& A = args(ph);
+    return SegTable{seg_tab, u_first, (kMode == 3 && ph == 2) ? 0 : n_tab, A.R, A.tiles, A.expert_tiles,
+                    small ? small_tiles : nullptr};
+  };
+  // phase ph's share [begin, end) and its first index in the CTA's step sequence
+  auto phase_range = [&](int ph, long long& b, long long& e, long long& off) {
+    if (kMode == 3 && ph == 2) {
+      b = my_begin2;
+      e = my_end2;
+      off = n_first;
+    } else {
+      b = my_begin;
+      e = my_end;
+      off = 0;
+    }
+  };
   // (the four configurations are compile-time constants; pick one without dividing)
   const int ngm = *ng_max_sm;
   const RingCfg rc = ngm <= 1 ? ring_cfg(1) : ngm == 2 ? ring_cfg(2) : ngm == 3 ? ring_cfg(3) : ring_cfg(4);
@@ -630,48 +705,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // per contiguous run where a chunk crosses units). Copies this large keep HBM
     // busy from a single issuing thread; 4.5 KB ones do not.
     if (lane == 0) {
-      const long long n_it = my_end - my_begin;
-      const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
-      Cursor cur(my_begin, my_end, a.KBn, segs);
       // The weights are read exactly once: stream them through L2 with an
       // evict-first policy, so they do not displace the activations (re-read by
       // every row tile of their expert) or the intermediate.
       const uint64_t w_policy = l2_policy_evict_first();
       TRACE_POINT(13, 4);  // weight producer ready
-      long long c = 0;
+      long long c_all = 0;  // chunks issued, over the phases
       int s = 0;
-      uint32_t sph = 0;  // slot of chunk c, and the parity of its phase
-      for (; c < n_chunks; ++c) {
-        if (!mbar_wait(bar(kBarWEmpty + s), sph ^ 1, abort_flag, status, kStatusTimeout, wait_ns))
-          break;
-        const long long it0 = c * kWChunk;
-        const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
-        TRACE_POINT(0, it0);
-        mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWStepBytes);
-        for (long long it = it0; it < it1;) {
-          int kb = 0;
-          cur.seek(it, kb);
-          const long long left_in_unit = cur.kb1 - kb;
-          const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
-          const long long woff =
-              ((static_cast<long long>(cur.un.e) * a.R + cur.un.rt) * a.KBn + kb) * kWStepBytes;
-          if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kWStepBytes <= a.wpack_bytes &&
-                            cur.un.e >= 0 && cur.un.e < a.E && cur.un.rt < a.R && kb + run <= a.KBn &&
-                            run >= 1 && (it - it0) + run <= kWChunk,
-                        a.status, a.dbg, 1, woff, run * 100 + (it - it0)))
-            bulk_g2s_hint(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
-                          a.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes,
-                          bar(kBarWFull + s), w_policy);
-          it += run;
-        }
-        if (++s == nws) {
-          s = 0;
-          sph ^= 1u;
+      uint32_t sph = 0;  // slot of the next chunk, and the parity of its phase
+      bool ok = true;
+#pragma unroll
+      for (int ph = kPh0; ph <= kPh1; ++ph) {
+        if (!ok) break;
+        const GemmArgs& A = args(ph);
+        long long pb, pe, off;
+        phase_range(ph, pb, pe, off);
+        const long long n_it = pe - pb;
+        const long long n_chunks = (n_it + kWChunk - 1) / kWChunk;
+        Cursor cur(pb, pe, A.KBn, phase_segs(ph));
+        for (long long c = 0; c < n_chunks; ++c) {
+          if (!mbar_wait(bar(kBarWEmpty + s), sph ^ 1, abort_flag, status, kStatusTimeout, wait_ns)) {
+            ok = false;
+            break;
+          }
+          const long long it0 = c * kWChunk;
+          const long long it1 = it0 + kWChunk < n_it ? it0 + kWChunk : n_it;
+          TRACE_POINT(0, off + it0);
+          mbar_arrive_expect_tx(bar(kBarWFull + s), static_cast<uint32_t>(it1 - it0) * kWStepBytes);
+          for (long long it = it0; it < it1;) {
+            int kb = 0;
+            cur.seek(it, kb);
+            const long long left_in_unit = cur.kb1 - kb;
+            const int run = static_cast<int>(it1 - it < left_in_unit ? it1 - it : left_in_unit);
+            const long long woff =
+                ((static_cast<long long>(cur.un.e) * A.R + cur.un.rt) * A.KBn + kb) * kWStepBytes;
+            if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kWStepBytes <= A.wpack_bytes &&
+                              cur.un.e >= 0 && cur.un.e < A.E && cur.un.rt < A.R && kb + run <= A.KBn &&
+                              run >= 1 && (it - it0) + run <= kWChunk,
+                          A.status, A.dbg, 1, woff, run * 100 + (it - it0)))
+              bulk_g2s_hint(sW + s * kWChunkBytes + static_cast<uint32_t>(it - it0) * kWStepBytes,
+                            A.wpack + woff, static_cast<uint32_t>(run) * kWStepBytes,
+                            bar(kBarWFull + s), w_policy);
+            it += run;
+          }
+          ++c_all;
+          if (++s == nws) {
+            s = 0;
+            sph ^= 1u;
+          }
         }
       }
       // let the last chunks land before shared memory is released
-      for (long long j = 0; j < nws && j < c; ++j) {
-        const long long idx = c - 1 - j;
+      for (long long j = 0; j < nws && j < c_all; ++j) {
+        const long long idx = c_all - 1 - j;
         mbar_wait_drain(bar(kBarWFull + static_cast<int>(idx % nws)),
                         static_cast<uint32_t>((idx / nws) & 1));
       }
@@ -683,55 +769,82 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // for a while, so small copies must leave several at a time.
     if (small) pdl_wait();  // the activations are the preceding kernel's output
     if (lane == 0) CTA_STAMP(2);
-    const long long n_it = my_end - my_begin;
     if (lane < kProducerLanes) {
-      Cursor cur(my_begin, my_end, a.KBn, segs);
+      // (indices below are in the CTA's step sequence over the phases; a down
+      // share starts at a multiple of kProducerLanes, so lane l keeps the steps
+      // l, l + 4, ... and its slot keeps advancing by 4 across the phases)
       long long last = -1;
       long long issued_hi = 0;  // no lane has issued a step at or beyond this index
       uint32_t mine = 0;
       int s = lane;      // slot of this lane's step, advanced by kProducerLanes (nb is a multiple)
       uint32_t sph = 0;  // parity of that slot's phase
-      for (long long base_it = 0; base_it < n_it; base_it += kProducerLanes) {
-        const long long it = base_it + lane;
-        issued_hi = base_it + kProducerLanes < n_it ? base_it + kProducerLanes : n_it;
-        const unsigned active = __ballot_sync(0x0000000fu, it < n_it) & 0xFu;
-        if (it < n_it) {
-          int kb = 0;
-          cur.seek(it, kb);
-          if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 &&
-                             static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes <= rc.b_plane &&
-                             cur.un.e >= 0 && cur.un.e < a.E &&
-                             cur.un.g0 >= 0 && cur.un.g0 + cur.un.ng <= a.tiles_cap && kb >= 0 && kb < a.KBn,
-                         a.status, a.dbg, 11, cur.un.ng * 1000 + cur.un.e, cur.un.g0 * 1000 + kb))
-            cur.un.ng = 1;
-          const bool ok = mbar_wait(bar(kBarBEmpty + s), sph ^ 1, abort_flag, status,
-                                    kStatusTimeout, wait_ns);
-          __syncwarp(active);
-          if (ok) {
-            // the step's two 64-element k-blocks are two planes of the blocked layout
-            const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
-            const long long boff =
-                (static_cast<long long>(kb) * kSub * a.Gcap + cur.un.g0) * kRowGroupBytes;
-            const long long plane = static_cast<long long>(a.Gcap) * kRowGroupBytes;
-            TRACE_POINT(1, it);
-            mbar_arrive_expect_tx(bar(kBarBFull + s), kSub * bytes);
-            if (MOE_CHECK(boff >= 0 && boff + bytes <= a.bsrc_bytes && bytes <= rc.b_plane && bytes > 0 &&
-                              s >= 0 && s < nb,
-                          a.status, a.dbg, 2, boff, bytes))
-              bulk_g2s(sB + s * rc.b_stage, a.bsrc + boff, bytes, bar(kBarBFull + s));
-            if (MOE_CHECK(boff + plane + bytes <= a.bsrc_bytes, a.status, a.dbg, 3, boff + plane,
-                          bytes))
-              bulk_g2s(sB + s * rc.b_stage + rc.b_plane, a.bsrc + boff + plane, bytes,
-                       bar(kBarBFull + s));
-            last = it;
-            ++mine;
+      bool ok_all = true;
+      int ready_tile = -1;  // fused down phase: the token tile whose intermediate was seen complete
+#pragma unroll
+      for (int ph = kPh0; ph <= kPh1; ++ph) {
+        if (!ok_all) break;
+        const GemmArgs& A = args(ph);
+        long long pb, pe, off;
+        phase_range(ph, pb, pe, off);
+        const long long n_it = pe - pb;
+        Cursor cur(pb, pe, A.KBn, phase_segs(ph));
+        for (long long base_it = 0; base_it < n_it; base_it += kProducerLanes) {
+          const long long it = base_it + lane;
+          issued_hi = off + (base_it + kProducerLanes < n_it ? base_it + kProducerLanes : n_it);
+          const unsigned active = __ballot_sync(0x0000000fu, it < n_it) & 0xFu;
+          if (it < n_it) {
+            int kb = 0;
+            cur.seek(it, kb);
+            if (!MOE_CHECK(cur.un.ng >= 1 && cur.un.ng <= kBNMax / 16 &&
+                               static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes <= rc.b_plane &&
+                               cur.un.e >= 0 && cur.un.e < A.E &&
+                               cur.un.g0 >= 0 && cur.un.g0 + cur.un.ng <= A.tiles_cap && kb >= 0 && kb < A.KBn,
+                           A.status, A.dbg, 11, cur.un.ng * 1000 + cur.un.e, cur.un.g0 * 1000 + kb))
+              cur.un.ng = 1;
+            bool ok = true;
+            if (kMode == 3 && ph == 2) {
+              // the down GEMM's activations are the gate/up GEMM's intermediate:
+              // wait (once per token tile) until every row tile of it is stored
+              const int t = static_cast<int>(cur.u / A.R);
+              if (t != ready_tile) {
+                if (ready_tile < 0) CTA_STAMP(8);
+                ok = wait_counters(a.h_ready + static_cast<long long>(t) * A.KBn, A.KBn, 2, abort_flag,
+                                   status, wait_ns);
+                if (ready_tile < 0) CTA_STAMP(9);
+                ready_tile = t;
+              }
+            }
+            ok = ok && mbar_wait(bar(kBarBEmpty + s), sph ^ 1, abort_flag, status, kStatusTimeout, wait_ns);
+            __syncwarp(active);
+            if (ok) {
+              // the step's two 64-element k-blocks are two planes of the blocked layout
+              const uint32_t bytes = static_cast<uint32_t>(cur.un.ng) * kRowGroupBytes;
+              const long long boff =
+                  (static_cast<long long>(kb) * kSub * A.Gcap + cur.un.g0) * kRowGroupBytes;
+              const long long plane = static_cast<long long>(A.Gcap) * kRowGroupBytes;
+              TRACE_POINT(1, off + it);
+              mbar_arrive_expect_tx(bar(kBarBFull + s), kSub * bytes);
+              if (MOE_CHECK(boff >= 0 && boff + bytes <= A.bsrc_bytes && bytes <= rc.b_plane && bytes > 0 &&
+                                s >= 0 && s < nb,
+                            A.status, A.dbg, 2, boff, bytes))
+                bulk_g2s(sB + s * rc.b_stage, A.bsrc + boff, bytes, bar(kBarBFull + s));
+              if (MOE_CHECK(boff + plane + bytes <= A.bsrc_bytes, A.status, A.dbg, 3, boff + plane,
+                            bytes))
+                bulk_g2s(sB + s * rc.b_stage + rc.b_plane, A.bsrc + boff + plane, bytes,
+                         bar(kBarBFull + s));
+              last = off + it;
+              ++mine;
+            }
+            if (__any_sync(active, !ok)) {
+              ok_all = false;
+              break;
+            }
           }
-          if (__any_sync(active, !ok)) break;
-        }
-        s += kProducerLanes;
-        if (s >= nb) {
-          s -= nb;
-          sph ^= 1u;
+          s += kProducerLanes;
+          if (s >= nb) {
+            s -= nb;
+            sph ^= 1u;
+          }
         }
       }
       // bounded wait for this lane's last copies to land before shared memory is
@@ -751,9 +864,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // other's MMAs. Each warp runs its loop uniformly; one elected lane issues.
     const uint32_t par = static_cast<uint32_t>(warp - kWarpMma0);
     uint32_t it_base = 0, acc_it = 0;
-    SegIter si(my_begin, my_end, a.KBn);
-    long long u;
-    int kb0, kb1;
     bool ok = true;
     const uint64_t b_desc0 = sw128_kmajor_desc(sB);
     // B slot of this issuer's next step (its steps are 2 apart; nb is even) and
@@ -761,73 +871,86 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     uint32_t sb = par, bph = 0;
     uint32_t sa = par, aph = 0;  // the same for the A stage ring (nst stages, even)
     const uint32_t nst = MOE_TMEM_NST, accw = MOE_TMEM_ACCW, acc_col0 = nst * kACols;
-    while (ok && si.next(u, kb0, kb1)) {
-      const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
-      const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
-      const int ab = acc_it & 1;
-      if (first < it_base + len) {
-        Unit un = segs.get(u);
-        if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16, a.status, a.dbg, 12, un.ng, u)) un.ng = 1;
-        const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
-                                                    ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
-                                                    kStatusTimeout, wait_ns));
-        if (!ok) break;
-        const uint32_t d_tmem = tmem + acc_col0 + (par * 2 + ab) * accw;
-        uint32_t acc_flag = 0;
-        for (uint32_t it = first; it < it_base + len; it += 2) {
-          const uint32_t st = sa;
-          if (lane == 0) TRACE_POINT(2, it);
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarBFull + sb), bph, abort_flag, status,
+#pragma unroll
+    for (int ph = kPh0; ph <= kPh1; ++ph) {
+      if (!ok) break;
+      const GemmArgs& A = args(ph);
+      long long pb, pe, off;
+      phase_range(ph, pb, pe, off);
+      SegIter si(pb, pe, A.KBn);
+      const SegTable segs = phase_segs(ph);
+      long long u;
+      int kb0, kb1;
+      while (ok && si.next(u, kb0, kb1)) {
+        const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
+        const uint32_t first = it_base + (((it_base & 1u) != par) ? 1u : 0u);
+        const int ab = acc_it & 1;
+        if (first < it_base + len) {
+          Unit un = segs.get(u);
+          if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16, A.status, A.dbg, 12, un.ng, u)) un.ng = 1;
+          const uint32_t idesc = idesc_f16_f32(kBM, un.ng * kRowGroup);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccEmpty + ab),
+                                                      ((acc_it >> 1) & 1) ^ 1, abort_flag, status,
                                                       kStatusTimeout, wait_ns));
-          if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), aph, abort_flag, status,
-                                                        kStatusTimeout, wait_ns));
           if (!ok) break;
-          if (lane == 0) TRACE_POINT(3, it);
-          if (lane == 0 && it < 2) CTA_STAMP(4);
-          const uint32_t a_tmem = tmem + st * kACols;
-          // B stage sb is sb * b_stage bytes after stage 0, its second 64-element
-          // half b_plane bytes further (16-byte units in the descriptor); +32 bytes of
-          // K per MMA inside the 128-byte swizzled rows.
-          const uint64_t b_desc = b_desc0 + ((sb * rc.b_stage) >> 4);
-          const uint64_t b_desc1 = b_desc + (rc.b_plane >> 4);
+          const uint32_t d_tmem = tmem + acc_col0 + (par * 2 + ab) * accw;
+          uint32_t acc_flag = 0;
+          for (uint32_t it = first; it < it_base + len; it += 2) {
+            const uint32_t st = sa;
+            if (lane == 0) TRACE_POINT(2, it);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarBFull + sb), bph, abort_flag, status,
+                                                        kStatusTimeout, wait_ns));
+            if (ok)
+              ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarFull + st), aph, abort_flag, status,
+                                                          kStatusTimeout, wait_ns));
+            if (!ok) break;
+            if (lane == 0) TRACE_POINT(3, it);
+            if (lane == 0 && it < 2) CTA_STAMP(4);
+            if (lane == 0 && ph == 2 && kMode == 3 && it < n_first + 2) CTA_STAMP(11);
+            const uint32_t a_tmem = tmem + st * kACols;
+            // B stage sb is sb * b_stage bytes after stage 0, its second 64-element
+            // half b_plane bytes further (16-byte units in the descriptor); +32 bytes of
+            // K per MMA inside the 128-byte swizzled rows.
+            const uint64_t b_desc = b_desc0 + ((sb * rc.b_stage) >> 4);
+            const uint64_t b_desc1 = b_desc + (rc.b_plane >> 4);
+            if (elect_one()) {
+              tc_fence_after();
+              tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
+              tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
+              tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
+              tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
+              tc_mma_ts(d_tmem, a_tmem + 32, b_desc1, idesc, 1u);
+              tc_mma_ts(d_tmem, a_tmem + 40, b_desc1 + 2, idesc, 1u);
+              tc_mma_ts(d_tmem, a_tmem + 48, b_desc1 + 4, idesc, 1u);
+              tc_mma_ts(d_tmem, a_tmem + 56, b_desc1 + 6, idesc, 1u);
+              tc_commit(bar(kBarEmpty + st));
+              tc_commit(bar(kBarBEmpty + sb));
+              TRACE_POINT(4, it);
+              CTA_STAMP(5);
+              if (ph == 1) CTA_STAMP(10);
+            }
+            acc_flag = 1u;
+            sb += 2;
+            if (sb >= static_cast<uint32_t>(nb)) {
+              sb -= static_cast<uint32_t>(nb);
+              bph ^= 1u;
+            }
+            sa += 2;
+            if (sa >= nst) {
+              sa -= nst;
+              aph ^= 1u;
+            }
+          }
+          if (!ok) break;
           if (elect_one()) {
-            tc_fence_after();
-            tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, acc_flag);
-            tc_mma_ts(d_tmem, a_tmem + 8, b_desc + 2, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 16, b_desc + 4, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 24, b_desc + 6, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 32, b_desc1, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 40, b_desc1 + 2, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 48, b_desc1 + 4, idesc, 1u);
-            tc_mma_ts(d_tmem, a_tmem + 56, b_desc1 + 6, idesc, 1u);
-            tc_commit(bar(kBarEmpty + st));
-            tc_commit(bar(kBarBEmpty + sb));
-            TRACE_POINT(4, it);
-            CTA_STAMP(5);
+            tc_commit(bar(kBarAccFull + par * 2 + ab));
+            TRACE_POINT(14, 32 + acc_it * 2 + par);  // issuer done with a segment
           }
-          acc_flag = 1u;
-          sb += 2;
-          if (sb >= static_cast<uint32_t>(nb)) {
-            sb -= static_cast<uint32_t>(nb);
-            bph ^= 1u;
-          }
-          sa += 2;
-          if (sa >= nst) {
-            sa -= nst;
-            aph ^= 1u;
-          }
+          __syncwarp();
         }
-        if (!ok) break;
-        if (elect_one()) {
-          tc_commit(bar(kBarAccFull + par * 2 + ab));
-          TRACE_POINT(14, 32 + acc_it * 2 + par);  // issuer done with a segment
-        }
-        __syncwarp();
+        it_base += len;
+        ++acc_it;
       }
-      it_base += len;
-      ++acc_it;
     }
     if (elect_one()) {
       tc_commit(bar(kBarDrain + par));
@@ -845,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     const int phase = (warp - kWarpDeq0) >> 2;
     const int r = quad * 32 + lane;
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t n_it = static_cast<uint32_t>(my_end - my_begin);
+    const uint32_t n_it = static_cast<uint32_t>(n_total);  // (the phases' steps, in sequence)
     // weight chunk of the step (2 steps per chunk): its ring slot and phase parity,
     // advanced by 2 chunks per iteration
     uint32_t ws = static_cast<uint32_t>(phase) >> 1, wpar = 0;
@@ -920,226 +1043,255 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     const int epi_tid = threadIdx.x - kWarpEpi0 * 32;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t acc_it = 0, it_base = 0, full_phase = 0;
-    SegIter si(my_begin, my_end, a.KBn);
-    long long u;
-    int kb0, kb1;
-    while (si.next(u, kb0, kb1)) {
-      Unit un = segs.get(u);
-      if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16 && un.rt >= 0 && un.rt < a.R, a.status, a.dbg,
-                     13, un.ng, un.rt))
-        un.ng = 1;
-      const int nch = un.ng;  // 16-column chunks
-      const int ab = acc_it & 1;
-      const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
-      // which MMA issuer (even / odd k-blocks of this CTA's sequence) has a sum
-      const bool has0 = len >= 2 || (it_base & 1u) == 0;
-      const bool has1 = len >= 2 || (it_base & 1u) == 1;
-      it_base += len;
-
-      // routing of the tile's token rows, fetched before the wait: every row's
-      // prescale exponent, and for the down GEMM its slot, token and routing
-      // weight (times 2^2e, undoing the prescale of x and of h)
-      int sid_r[kRowRegs], tok_r[kRowRegs], e_r[kRowRegs];
-      float w_r[kRowRegs];
-      {
-        const int pbase = un.g0 * kRowGroup;
 #pragma unroll
-        for (int j = 0; j < kRowRegs; ++j) {
-          const int row = 32 * j + lane;
-          const bool in_tile = row < nch * 16 &&
-                               MOE_CHECK(pbase + row < a.sorted_cap, a.status, a.dbg, 9, pbase + row, nch);
-          e_r[j] = in_tile ? a.rowexp[pbase + row] : 0;  // (kPadRowExp for a padding row)
-          sid_r[j] = a.MK;
-          tok_r[j] = 0;
-          w_r[j] = 0.f;
-          if constexpr (kMode == 2) {
-            const int sid = in_tile ? a.sorted_ids[pbase + row] : a.MK;
-            sid_r[j] = sid;
-            if (sid < a.MK) {  // a real row: |e| <= kMaxRowExp
-              const int e = e_r[j] < -kMaxRowExp ? -kMaxRowExp : (e_r[j] > kMaxRowExp ? kMaxRowExp : e_r[j]);
-              w_r[j] = a.topk_weights[sid] * exp2_int(2 * e);
-              tok_r[j] = sid / a.topk;
+    for (int ph = kPh0; ph <= kPh1; ++ph) {
+      const GemmArgs& A = args(ph);
+      const int mode = kMode == 3 ? ph : kMode;
+      const Sched sc = phase_sched(ph);
+      const SegTable segs = phase_segs(ph);
+      long long pb, pe, off;
+      phase_range(ph, pb, pe, off);
+      SegIter si(pb, pe, A.KBn);
+      long long u;
+      int kb0, kb1;
+      bool stop = false;
+      while (si.next(u, kb0, kb1)) {
+        Unit un = segs.get(u);
+        if (!MOE_CHECK(un.ng >= 1 && un.ng <= kBNMax / 16 && un.rt >= 0 && un.rt < A.R, A.status, A.dbg,
+                       13, un.ng, un.rt))
+          un.ng = 1;
+        const int nch = un.ng;  // 16-column chunks
+        const int ab = acc_it & 1;
+        const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
+        // which MMA issuer (even / odd k-blocks of this CTA's sequence) has a sum
+        const bool has0 = len >= 2 || (it_base & 1u) == 0;
+        const bool has1 = len >= 2 || (it_base & 1u) == 1;
+        it_base += len;
+
+        // routing of the tile's token rows, fetched before the wait: every row's
+        // prescale exponent, and for the down GEMM its slot, token and routing
+        // weight (times 2^2e, undoing the prescale of x and of h)
+        int sid_r[kRowRegs], tok_r[kRowRegs], e_r[kRowRegs];
+        float w_r[kRowRegs];
+        {
+          const int pbase = un.g0 * kRowGroup;
+  #pragma unroll
+          for (int j = 0; j < kRowRegs; ++j) {
+            const int row = 32 * j + lane;
+            const bool in_tile = row < nch * 16 &&
+                                 MOE_CHECK(pbase + row < A.sorted_cap, A.status, A.dbg, 9, pbase + row, nch);
+            e_r[j] = in_tile ? A.rowexp[pbase + row] : 0;  // (kPadRowExp for a padding row)
+            sid_r[j] = A.MK;
+            tok_r[j] = 0;
+            w_r[j] = 0.f;
+            if (mode == 2) {
+              const int sid = in_tile ? A.sorted_ids[pbase + row] : A.MK;
+              sid_r[j] = sid;
+              if (sid < A.MK) {  // a real row: |e| <= kMaxRowExp
+                const int e = e_r[j] < -kMaxRowExp ? -kMaxRowExp : (e_r[j] > kMaxRowExp ? kMaxRowExp : e_r[j]);
+                w_r[j] = A.topk_weights[sid] * exp2_int(2 * e);
+                tok_r[j] = sid / A.topk;
+              }
             }
           }
         }
-      }
 
-      bool w_ok = true;
-      if (has0) {
-        w_ok = mbar_wait(bar(kBarAccFull + ab), (full_phase >> ab) & 1u, abort_flag, status,
-                         kStatusTimeout, wait_ns);
-        full_phase ^= 1u << ab;
-      }
-      if (has1 && w_ok) {
-        w_ok = mbar_wait(bar(kBarAccFull + 2 + ab), (full_phase >> (2 + ab)) & 1u, abort_flag,
-                         status, kStatusTimeout, wait_ns);
-        full_phase ^= 1u << (2 + ab);
-      }
-      w_ok = __all_sync(0xffffffffu, w_ok);
-      if (epi_tid == 0) TRACE_POINT(14, 512 + acc_it);  // epilogue's accumulator wait done
-      if (lane == 0) epi_ok[(acc_it & 1) * 4 + quad] = w_ok ? 1 : 0;
-      named_bar_sync(kEpiBar, kEpiThreads);
-      const bool all_ok = epi_ok[(acc_it & 1) * 4 + 0] && epi_ok[(acc_it & 1) * 4 + 1] &&
-                          epi_ok[(acc_it & 1) * 4 + 2] && epi_ok[(acc_it & 1) * 4 + 3];
-      if (!all_ok) break;
-      tc_fence_after();
-      const uint32_t accw = MOE_TMEM_ACCW, acc_col0 = MOE_TMEM_NST * kACols;
-      const uint32_t tacc0 = tmem + t_lane + acc_col0 + ab * accw;
-      const uint32_t tacc1 = tmem + t_lane + acc_col0 + (2 + ab) * accw;
-      // fp32 sums of 16 token columns of this lane's row, both issuers added
-      auto load_chunk = [&](int c, float (&v)[16]) {
-        uint32_t rr[16];
-        __syncwarp();  // tcgen05.ld is warp-collective: converge after per-lane code
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        bool w_ok = true;
         if (has0) {
-          tmem_ld16(tacc0 + c * 16, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rr[i]);
+          w_ok = mbar_wait(bar(kBarAccFull + ab), (full_phase >> ab) & 1u, abort_flag, status,
+                           kStatusTimeout, wait_ns);
+          full_phase ^= 1u << ab;
         }
-        if (has1) {
-          tmem_ld16(tacc1 + c * 16, rr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(rr[i]);
+        if (has1 && w_ok) {
+          w_ok = mbar_wait(bar(kBarAccFull + 2 + ab), (full_phase >> (2 + ab)) & 1u, abort_flag,
+                           status, kStatusTimeout, wait_ns);
+          full_phase ^= 1u << (2 + ab);
         }
-      };
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        if (epi_tid == 0) TRACE_POINT(14, 512 + acc_it);  // epilogue's accumulator wait done
+        if (lane == 0) epi_ok[(acc_it & 1) * 4 + quad] = w_ok ? 1 : 0;
+        named_bar_sync(kEpiBar, kEpiThreads);
+        const bool all_ok = epi_ok[(acc_it & 1) * 4 + 0] && epi_ok[(acc_it & 1) * 4 + 1] &&
+                            epi_ok[(acc_it & 1) * 4 + 2] && epi_ok[(acc_it & 1) * 4 + 3];
+        if (!all_ok) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t accw = MOE_TMEM_ACCW, acc_col0 = MOE_TMEM_NST * kACols;
+        const uint32_t tacc0 = tmem + t_lane + acc_col0 + ab * accw;
+        const uint32_t tacc1 = tmem + t_lane + acc_col0 + (2 + ab) * accw;
+        // fp32 sums of 16 token columns of this lane's row, both issuers added
+        auto load_chunk = [&](int c, float (&v)[16]) {
+          uint32_t rr[16];
+          __syncwarp();  // tcgen05.ld is warp-collective: converge after per-lane code
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          if (has0) {
+            tmem_ld16(tacc0 + c * 16, rr);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rr[i]);
+          }
+          if (has1) {
+            tmem_ld16(tacc1 + c * 16, rr);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += __uint_as_float(rr[i]);
+          }
+        };
 
-      if constexpr (kMode == 1) {
-        const bool full = (kb0 == 0 && kb1 == a.KBn);
-        bool write_tile = full;
-        bool sat = false;
-        if (full) {
-          for (int c = 0; c < nch; ++c) {
-            float v[16];
-            load_chunk(c, v);
-            if (epi_tid == 0 && c == 0) TRACE_POINT(14, 600 + acc_it * 8 + 0);  // accumulators loaded
-            sat |= swiglu_chunk(v, c, quad, lane, sStage, (c >> 1) ? e_r[1] : e_r[0]);
-          }
-          if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 1);  // SwiGLU staged
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
-        } else {
-          // split unit: park this CTA's partial sums, take a ticket
-          const long long ustart = u * a.KBn;
-          const int part = (sc.start(blockIdx.x) < ustart) ? 1 : 0;
-          float* slot = a.scratch + (static_cast<long long>(blockIdx.x) * 2 + part) * kBNMax * kBM;
-          for (int c = 0; c < nch; ++c) {
-            float v[16];
-            load_chunk(c, v);
-            const long long so = (slot - a.scratch) + (c * 16) * kBM + r;
-            (void)so;  // read only by the self-checking build
-            if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 6, so, c)) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
-          __threadfence();
-          named_bar_sync(kEpiBar, kEpiThreads);
-          const int c0 = sc.cta_of(ustart), c1 = sc.cta_of(ustart + a.KBn - 1);
-          if (epi_tid == 0) {
-            const int add = kb1 - kb0;
-            const int old = atomicAdd(a.tickets + c0, add);
-            *last_flag = (old + add == a.KBn) ? 1 : 0;
-          }
-          named_bar_sync(kEpiBar, kEpiThreads);
-          if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 5);  // ticket taken
-          write_tile = *last_flag != 0;
-          if (write_tile) {
-            __threadfence();
+        if (mode == 1) {
+          const bool full = (kb0 == 0 && kb1 == A.KBn);
+          bool write_tile = full;
+          bool sat = false;
+          if (full) {
             for (int c = 0; c < nch; ++c) {
               float v[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              for (int cc = c0; cc <= c1; ++cc) {
-                if (sc.start(cc) == sc.start(cc + 1)) continue;  // empty share: no partial
-                const int pc = (sc.start(cc) < ustart) ? 1 : 0;
-                const float* sl =
-                    a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
-                const long long so = (sl - a.scratch) + (c * 16) * kBM + r;
-                (void)so;  // read only by the self-checking build
-                if (MOE_CHECK(so >= 0 && so + 15 * kBM < a.scratch_elems, a.status, a.dbg, 7, so, cc)) {
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
-                }
-              }
+              load_chunk(c, v);
+              if (epi_tid == 0 && c == 0) TRACE_POINT(14, 600 + acc_it * 8 + 0);  // accumulators loaded
               sat |= swiglu_chunk(v, c, quad, lane, sStage, (c >> 1) ? e_r[1] : e_r[0]);
             }
-          }
-        }
-        if (__any_sync(0xffffffffu, sat) && lane == 0) atomicOr(status, kStatusHSaturated);
-        if (write_tile) {
-          if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 2);  // tile ready to store
-          fence_proxy_async_smem();
-          named_bar_sync(kEpiBar, kEpiThreads);
-          if (epi_tid == 0) {
-            const long long hoff = (static_cast<long long>(un.rt) * a.Gcap + un.g0) * kRowGroupBytes;
-            if (MOE_CHECK(hoff >= 0 && hoff + nch * kRowGroupBytes <= a.hout_bytes && nch > 0 &&
-                              nch <= kBNMax / 16,
-                          a.status, a.dbg, 5, hoff, nch))
-              bulk_s2g(a.hout + hoff, sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
-            bulk_commit();
-            TRACE_POINT(14, 600 + acc_it * 8 + 3);  // bulk store issued
-            bulk_wait_read_all();
-            TRACE_POINT(14, 600 + acc_it * 8 + 4);  // staging tile read by the store
-          }
-          named_bar_sync(kEpiBar, kEpiThreads);
-        }
-      } else {
-        float* acc_col = a.acc + static_cast<long long>(un.rt) * kBM + r;
-#pragma unroll
-        for (int c = 0; c < kBNMax / 16; ++c) {
-          if (c < nch) {
-            float v[16];
-            load_chunk(c, v);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int row = c * 16 + i;
-              const int sid = __shfl_sync(0xffffffffu, sid_r[row >> 5], row & 31);
-              if (sid < a.MK) {
-                const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
-                const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
-                const long long ai = (acc_col - a.acc) + static_cast<long long>(tok) * a.Kout;
-                if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 8, ai, sid))
-                  atomicAdd(a.acc + ai, wt * v[i]);
+            if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 1);  // SwiGLU staged
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
+          } else {
+            // split unit: park this CTA's partial sums, take a ticket
+            const long long ustart = u * A.KBn;
+            const int part = (sc.start(blockIdx.x) < ustart) ? 1 : 0;
+            float* slot = A.scratch + (static_cast<long long>(blockIdx.x) * 2 + part) * kBNMax * kBM;
+            for (int c = 0; c < nch; ++c) {
+              float v[16];
+              load_chunk(c, v);
+              const long long so = (slot - A.scratch) + (c * 16) * kBM + r;
+              (void)so;  // read only by the self-checking build
+              if (MOE_CHECK(so >= 0 && so + 15 * kBM < A.scratch_elems, A.status, A.dbg, 6, so, c)) {
+  #pragma unroll
+                for (int i = 0; i < 16; ++i) __stcg(slot + (c * 16 + i) * kBM + r, v[i]);
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
+            __threadfence();
+            named_bar_sync(kEpiBar, kEpiThreads);
+            const int c0 = sc.cta_of(ustart), c1 = sc.cta_of(ustart + A.KBn - 1);
+            if (epi_tid == 0) {
+              const int add = kb1 - kb0;
+              const int old = atomicAdd(A.tickets + c0, add);
+              *last_flag = (old + add == A.KBn) ? 1 : 0;
+            }
+            named_bar_sync(kEpiBar, kEpiThreads);
+            if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 5);  // ticket taken
+            write_tile = *last_flag != 0;
+            if (write_tile) {
+              __threadfence();
+              for (int c = 0; c < nch; ++c) {
+                float v[16];
+  #pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                for (int cc = c0; cc <= c1; ++cc) {
+                  if (sc.start(cc) == sc.start(cc + 1)) continue;  // empty share: no partial
+                  const int pc = (sc.start(cc) < ustart) ? 1 : 0;
+                  const float* sl =
+                      A.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
+                  const long long so = (sl - A.scratch) + (c * 16) * kBM + r;
+                  (void)so;  // read only by the self-checking build
+                  if (MOE_CHECK(so >= 0 && so + 15 * kBM < A.scratch_elems, A.status, A.dbg, 7, so, cc)) {
+  #pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] += __ldcg(sl + (c * 16 + i) * kBM + r);
+                  }
+                }
+                sat |= swiglu_chunk(v, c, quad, lane, sStage, (c >> 1) ? e_r[1] : e_r[0]);
               }
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
-        if (a.rt_tickets) {
-          // Output finalisation (small batches): the contributions to output row
-          // tile rt come from every token tile's unit (tile, rt); the contributor
-          // whose steps complete the tile's count rounds its fp32 sums to bf16.
-          __threadfence();  // this thread's additions are visible before the ticket
-          named_bar_sync(kEpiBar, kEpiThreads);
-          if (epi_tid == 0) {
-            const int add = kb1 - kb0;
-            const int old = atomicAdd(a.rt_tickets + un.rt, add);
-            *last_flag = (old + add == num_tiles * a.KBn) ? 1 : 0;
-          }
-          named_bar_sync(kEpiBar, kEpiThreads);
-          if (*last_flag) {
-            __threadfence();
-            const long long col = static_cast<long long>(un.rt) * kBM + epi_tid;
-            for (int t = 0; t < a.M; ++t) {
-              const float v = __ldcg(a.acc + static_cast<long long>(t) * a.Kout + col);
-              a.out[static_cast<long long>(t) * a.Kout + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          if (__any_sync(0xffffffffu, sat) && lane == 0) atomicOr(status, kStatusHSaturated);
+          if (write_tile) {
+            if (epi_tid == 0) TRACE_POINT(14, 600 + acc_it * 8 + 2);  // tile ready to store
+            const long long hoff = (static_cast<long long>(un.rt) * A.Gcap + un.g0) * kRowGroupBytes;
+            const bool hoff_ok = MOE_CHECK(hoff >= 0 && hoff + nch * kRowGroupBytes <= A.hout_bytes &&
+                                               nch > 0 && nch <= kBNMax / 16,
+                                           A.status, A.dbg, 5, hoff, nch);
+            if (kMode == 3) {
+              // The fused launch's down phase reads h from other CTAs: plain
+              // stores, a fence, then the tile's counter for the k-block it
+              // feeds (its two gate/up row tiles make one down k-block)
+              named_bar_sync(kEpiBar, kEpiThreads);  // the staging tile is complete
+              for (int i = epi_tid; i < nch * (kRowGroupBytes / 16); i += kEpiThreads)
+                if (hoff_ok)
+                  *reinterpret_cast<uint4*>(A.hout + hoff + i * 16) = ld_shared_v4(sStage + i * 16);
+              __threadfence();
+              named_bar_sync(kEpiBar, kEpiThreads);
+              if (epi_tid == 0)
+                atomicAdd(A.h_ready + (u / A.R) * a2.KBn + un.rt / 2, 1);
+            } else {
+              fence_proxy_async_smem();
+              named_bar_sync(kEpiBar, kEpiThreads);
+              if (epi_tid == 0) {
+                if (hoff_ok) bulk_s2g(A.hout + hoff, sStage, static_cast<uint32_t>(nch) * kRowGroupBytes);
+                bulk_commit();
+                TRACE_POINT(14, 600 + acc_it * 8 + 3);  // bulk store issued
+                bulk_wait_read_all();
+                TRACE_POINT(14, 600 + acc_it * 8 + 4);  // staging tile read by the store
+              }
+              named_bar_sync(kEpiBar, kEpiThreads);
             }
           }
-          named_bar_sync(kEpiBar, kEpiThreads);  // last_flag is reused by the next segment
+        } else {
+          float* acc_col = A.acc + static_cast<long long>(un.rt) * kBM + r;
+  #pragma unroll
+          for (int c = 0; c < kBNMax / 16; ++c) {
+            if (c < nch) {
+              float v[16];
+              load_chunk(c, v);
+  #pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int row = c * 16 + i;
+                const int sid = __shfl_sync(0xffffffffu, sid_r[row >> 5], row & 31);
+                if (sid < A.MK) {
+                  const int tok = __shfl_sync(0xffffffffu, tok_r[row >> 5], row & 31);
+                  const float wt = __shfl_sync(0xffffffffu, w_r[row >> 5], row & 31);
+                  const long long ai = (acc_col - A.acc) + static_cast<long long>(tok) * A.Kout;
+                  if (MOE_CHECK(ai >= 0 && ai < A.acc_elems, A.status, A.dbg, 8, ai, sid))
+                    atomicAdd(A.acc + ai, wt * v[i]);
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
+          if (A.rt_tickets) {
+            // Output finalisation (small batches): the contributions to output row
+            // tile rt come from every token tile's unit (tile, rt); the contributor
+            // whose steps complete the tile's count rounds its fp32 sums to bf16.
+            __threadfence();  // this thread's additions are visible before the ticket
+            named_bar_sync(kEpiBar, kEpiThreads);
+            if (epi_tid == 0) {
+              const int add = kb1 - kb0;
+              const int old = atomicAdd(A.rt_tickets + un.rt, add);
+              *last_flag = (old + add == num_tiles * A.KBn) ? 1 : 0;
+            }
+            named_bar_sync(kEpiBar, kEpiThreads);
+            if (*last_flag) {
+              __threadfence();
+              const long long col = static_cast<long long>(un.rt) * kBM + epi_tid;
+              for (int t = 0; t < A.M; ++t) {
+                const float v = __ldcg(A.acc + static_cast<long long>(t) * A.Kout + col);
+                A.out[static_cast<long long>(t) * A.Kout + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+              }
+            }
+            named_bar_sync(kEpiBar, kEpiThreads);  // last_flag is reused by the next segment
+          }
         }
+        if (epi_tid == 0) TRACE_POINT(15, acc_it);  // epilogue done with a segment
+        if (epi_tid == 0) CTA_STAMP(6);
+        if (epi_tid == 0 && ph == 1) CTA_STAMP(12);
+        ++acc_it;
       }
-      if (epi_tid == 0) TRACE_POINT(15, acc_it);  // epilogue done with a segment
-      if (epi_tid == 0) CTA_STAMP(6);
-      ++acc_it;
+      if (stop) break;
     }
     if (epi_tid == 0) bulk_wait_all();
   }
@@ -1164,17 +1316,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 cudaError_t gemm_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmAlloc);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+  return e;
 }
 
 cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
-  return launch_k(gemm_kernel<1>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a);
+  return launch_k(gemm_kernel<1>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a, a);
 }
 
 cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
-  return launch_k(gemm_kernel<2>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a);
+  return launch_k(gemm_kernel<2>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a, a);
+}
+
+cudaError_t launch_gemm_fused(const GemmArgs& a1, const GemmArgs& a2, int num_ctas, cudaStream_t stream,
+                              bool pdl) {
+  return launch_k_coop(gemm_kernel<3>, dim3(num_ctas), dim3(kThreads), kSmAlloc, stream, pdl, a1, a2);
 }
 
 }  // namespace moe

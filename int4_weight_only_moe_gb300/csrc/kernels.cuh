@@ -117,6 +117,9 @@ struct GemmArgs {
   // steps added into it; the contributor that completes a tile writes its bf16
   // output (null: a separate finalize launch rounds the accumulator)
   int32_t* rt_tickets;
+  // fused small-batch launch: per token tile and down-GEMM k-block, a zeroed
+  // counter of the gate/up row tiles whose intermediate is stored ([32][N/128])
+  int32_t* h_ready;
   uint16_t* out;           // bf16 [M, Kout]
   int M;
   int R;                   // row tiles per expert
@@ -141,6 +144,9 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
+// Both GEMMs in one cooperative launch (small batches: small_ids set in both).
+cudaError_t launch_gemm_fused(const GemmArgs& a1, const GemmArgs& a2, int num_ctas, cudaStream_t stream,
+                              bool pdl);
 cudaError_t gemm_set_attributes();
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
@@ -188,6 +194,25 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+// The same as a cooperative launch: every CTA of the grid is resident at once
+// (or the launch fails), as kernels whose CTAs wait on one another need.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -171,6 +171,25 @@ def test_mid_forward_grid_sizes(M, num_ctas):
     prob.close()
 
 
+@pytest.mark.parametrize("num_ctas", [None, 1, 3, 64])
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_fused_small_batch_matches_two_launches(M, num_ctas):
+    # at most 32 routed slots: both GEMMs in one cooperative launch (the down
+    # phase waits per token tile for the intermediate) against the two-launch path
+    # and the oracle; 1 and 3 CTAs put many gate/up and down units in one CTA's
+    # sequence, 64 leaves some CTAs a share of only a few steps
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl, step=M)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_FUSED_SMALL_BATCH, 1)
+    fused = check_forward(prob, hidden, ids, wts, f"fused M={M} ctas={num_ctas}")
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_FUSED_SMALL_BATCH, 0)
+    two = check_forward(prob, hidden, ids, wts, f"two launches M={M} ctas={num_ctas}")
+    assert_within_one_ulp(fused, two)
+    prob.close()
+
+
 def test_hot_expert_spans_several_token_tiles():
     # one expert receives every token (> 128 rows: several token tiles of one expert)
     E, K, N, k, M = 8, 768, 384, 2, 300
@@ -493,6 +512,11 @@ def test_wait_limit_gives_up_cleanly(M):
     pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 1)
     prob.run(hidden, ids, wts)  # returns; its output is not meaningful
     assert prob.moe.status() & pkg.STATUS_TIMEOUT
+    if M * k <= 32:  # and the same through the fused small-batch launch
+        pkg.moe_w4a16_set_option(h, pkg.OPT_FUSED_SMALL_BATCH, 1)
+        prob.run(hidden, ids, wts)
+        assert prob.moe.status() & pkg.STATUS_TIMEOUT
+        pkg.moe_w4a16_set_option(h, pkg.OPT_FUSED_SMALL_BATCH, 0)
     pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 0)
     pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 0)
     check_forward(prob, hidden, ids, wts, f"after give-up M={M}")
