@@ -51,7 +51,7 @@ enum {
   MOE_W4A16_WORKSPACE_TOO_SMALL = -3, /* workspace_bytes < moe_w4a16_workspace_size(h, M) */
   MOE_W4A16_CUDA_ERROR = -4,          /* a CUDA runtime call failed (message has the CUDA error) */
   MOE_W4A16_NOT_PACKED = -5,          /* forward before moe_w4a16_pack */
-  MOE_W4A16_UNSUPPORTED_SCALE = -6,   /* pack: a scale outside {0} U [2^-14, 8160] in magnitude */
+  MOE_W4A16_UNSUPPORTED_SCALE = -6,   /* pack: a scale outside {0} U [2^-14, 2720] in magnitude */
   MOE_W4A16_BAD_G_IDX = -7            /* pack_ex: a group index out of range, or a group whose
                                          size is not 32 */
 };
@@ -92,8 +92,10 @@ int moe_w4a16_destroy(moe_w4a16_t h);
  *   w1_s bf16  [E, K/32, 2N]
  *   w2_q int32 [E, N/8, K]
  *   w2_s bf16  [E, N/32, K]
- * Every scale must be 0 or have a finite magnitude in [2^-14, 8160], the range in
- * which each dequantised weight (u - 8) * s is an exact fp16 number; otherwise
+ * Every scale must be 0 or have a finite magnitude in [2^-14, 2720], the range in
+ * which each dequantised weight (u - 8) * s, and the dequantisation's offset
+ * term -24 * s, are exact fp16 numbers (a practical GPTQ scale is far below the
+ * ceiling: |w| <= 8 * s); otherwise
  * the call returns MOE_W4A16_UNSUPPORTED_SCALE and the handle stays unpacked.
  * Synchronises `stream` (to read the scale check); the inputs may be freed once
  * it returns. */

@@ -291,7 +291,7 @@ int moe_w4a16_pack_ex(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s, 
   MOE_CUDA_TRY(cudaStreamSynchronize(s));
   if (flags[0])
     return fail(MOE_W4A16_UNSUPPORTED_SCALE,
-                "a scale is outside the supported range (0, or 2^-14 <= |s| <= 8160, finite): "
+                "a scale is outside the supported range (0, or 2^-14 <= |s| <= 2720, finite): "
                 "its fp16 dequantised weights would not be exact");
   h->packed = true;
   return MOE_W4A16_OK;

@@ -432,26 +432,31 @@ struct Cursor {
 };
 
 // 32 INT4 codes (one scale group) -> 16 f16x2 words, columns of the A operand.
-// OR-ing a code u into the mantissa of fp16 1024 gives exactly 1024 + u (code at
-// bits 0..3 of a half) or 1024 + 16u (code at bits 4..7); subtracting 1032, or
-// scaling by 1/16 and subtracting 72, gives u - 8 exactly. The product with the
-// scale, (u - 8) * s, has at most 3 + 8 significant bits and is exact in fp16
-// (for scales in fp16's normal range), so the dequantised weight carries no
-// rounding error. One shift and four masks unpack a word of eight codes; `s2` is
-// the fp16 scale in both halves.
+// The repack places each pair of codes (u_lo, u_hi) of a word at bits 6..9 and
+// 22..25 (directly, after a shift left or right by 4, or after a rotation by 8):
+// OR-ing them below the exponent of fp16 16.0 gives the pair 16 + u exactly, and
+// one fused multiply-add with the scale s and -24 s gives (16 + u) s - 24 s =
+// (u - 8) s, rounded once. It is exact: -24 s = -3 * 8 s has at most 10
+// significant bits for a bf16 scale (8), and (u - 8) s at most 3 + 8, so both are
+// fp16 numbers for scales in [2^-14, 2720] (the repack rejects others). Per word
+// of eight codes: 3 shifts, 4 three-input logic ops, 4 fma. `s2` is the fp16 scale
+// in both halves.
+__device__ __forceinline__ uint32_t or_masked(uint32_t a, uint32_t mask, uint32_t bits) {
+  uint32_t d;  // (a & mask) | bits in one three-input logic op
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+  return d;
+}
 __device__ __forceinline__ void dequant_group(const uint4 qv, const uint32_t s2, uint32_t* out) {
   const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+  const uint32_t c2 = f16x2_mul(s2, 0xCE00CE00u);  // -24 s in both halves (exact)
+  constexpr uint32_t kMask = 0x03C003C0u, kSixteen = 0x4C004C00u;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t q = w[j], q8 = w[j] >> 8;
-    const uint32_t v0 = (q & 0x000F000Fu) | 0x64006400u;   // elements 0, 1: 1024 + u
-    const uint32_t v1 = (q & 0x00F000F0u) | 0x64006400u;   // elements 2, 3: 1024 + 16u
-    const uint32_t v2 = (q8 & 0x000F000Fu) | 0x64006400u;  // elements 4, 5
-    const uint32_t v3 = (q8 & 0x00F000F0u) | 0x64006400u;  // elements 6, 7
-    out[4 * j + 0] = f16x2_mul(f16x2_sub(v0, 0x64086408u), s2);
-    out[4 * j + 1] = f16x2_mul(f16x2_fma(v1, 0x2C002C00u, 0xD480D480u), s2);
-    out[4 * j + 2] = f16x2_mul(f16x2_sub(v2, 0x64086408u), s2);
-    out[4 * j + 3] = f16x2_mul(f16x2_fma(v3, 0x2C002C00u, 0xD480D480u), s2);
+    const uint32_t q = w[j];
+    out[4 * j + 0] = f16x2_fma(or_masked(q, kMask, kSixteen), s2, c2);        // codes 0, 1
+    out[4 * j + 1] = f16x2_fma(or_masked(q << 4, kMask, kSixteen), s2, c2);   // codes 2, 3
+    out[4 * j + 2] = f16x2_fma(or_masked(q >> 4, kMask, kSixteen), s2, c2);   // codes 4, 5
+    out[4 * j + 3] = f16x2_fma(or_masked(__funnelshift_l(q, q, 8), kMask, kSixteen), s2, c2);  // 6, 7
   }
 }
 

@@ -20,25 +20,29 @@ __device__ __forceinline__ int tile_row_source(int rt, int r, int Nout, int inte
   return rt * kBM + r;
 }
 
-// GPTQ word (code i = element 8*row + i at bits 4i..) -> interleaved word
-// (element 2p at bits 4p, element 2p+1 at bits 16 + 4p).
+// Bit position of code i (element 8*row + i of a GPTQ word) in a packed word:
+// the codes of pair p = i / 2 (fp16 pair p of the A operand) sit where the
+// dequantisation finds them at bits 6..9 (low half) and 22..25 (high half) of
+// the word itself (p = 0), shifted left by 4 (p = 1), shifted right by 4 (p = 2)
+// or rotated left by 8 (p = 3: bits 30, 31, 0, 1 and 14..17).
+__device__ __forceinline__ int code_pos(int i) {
+  const int p = i >> 1, h = i & 1;
+  return p == 0 ? (h ? 22 : 6) : p == 1 ? (h ? 18 : 2) : p == 2 ? (h ? 26 : 10) : (h ? 14 : 30);
+}
+// GPTQ word (code i at bits 4i..4i+3) -> packed word, and back.
 __device__ __forceinline__ uint32_t interleave_codes(uint32_t src) {
   uint32_t dst = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint32_t nib = (src >> (4 * i)) & 0xFu;
-    int pos = (i & 1) ? 16 + 4 * (i >> 1) : 4 * (i >> 1);
-    dst |= nib << pos;
+    const uint32_t nib = (src >> (4 * i)) & 0xFu;
+    dst |= __funnelshift_l(nib, nib, code_pos(i));  // a rotation: code 6 wraps past bit 31
   }
   return dst;
 }
 __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t dst) {
   uint32_t src = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    int pos = (i & 1) ? 16 + 4 * (i >> 1) : 4 * (i >> 1);
-    src |= ((dst >> pos) & 0xFu) << (4 * i);
-  }
+  for (int i = 0; i < 8; ++i) src |= (__funnelshift_r(dst, dst, code_pos(i)) & 0xFu) << (4 * i);
   return src;
 }
 
@@ -46,14 +50,15 @@ __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t dst) {
 // exact for bf16 scales inside fp16's normal range, which the dequantisation
 // needs anyway; the inverse conversion restores the bf16 bits exactly there.
 //
-// Supported scales: zero, or a finite magnitude in [2^-14, 8160]. Inside that set
-// the fp16 scale equals the bf16 one and every dequantised weight (u - 8) * s
-// (at most 3 + 8 significant bits, |u - 8| <= 8) is an exact fp16 normal number
-// no larger than 65280; outside it a weight would be rounded, flushed or
-// infinite, so the repack flags the scale instead.
+// Supported scales: zero, or a finite magnitude in [2^-14, 2720]. Inside that set
+// the fp16 scale equals the bf16 one, -24 s (the dequantisation's offset term) is
+// an exact fp16 number, and every dequantised weight (u - 8) * s (at most 3 + 8
+// significant bits, |u - 8| <= 8) is an exact fp16 normal number no larger than
+// 21760; outside it a weight would be rounded, flushed or infinite, so the repack
+// flags the scale instead.
 __device__ __forceinline__ bool scale_supported(uint16_t b) {
   const uint32_t m = b & 0x7FFFu;             // bf16 magnitude bits
-  return m == 0 || (m >= 0x3880u && m <= 0x45FFu);  // 0, or 2^-14 .. 8160
+  return m == 0 || (m >= 0x3880u && m <= 0x452Au);  // 0, or 2^-14 .. 2720
 }
 __device__ __forceinline__ uint16_t bf16_to_f16_bits(uint16_t b) {
   return __half_as_ushort(__float2half_rn(__uint_as_float(static_cast<uint32_t>(b) << 16)));

@@ -399,10 +399,11 @@ def test_forward_logits_routes_then_runs_the_forward(M):
 # ---------------------------------------------------------------------------- fp16 operand range
 
 
-@pytest.mark.parametrize("bad", [0x4600, 0xC600, 0x3870, 0x0001, 0x7F80, 0x7FC0, 0xFF80])
+@pytest.mark.parametrize("bad", [0x452B, 0xC52B, 0x4600, 0x3870, 0x0001, 0x7F80, 0x7FC0, 0xFF80])
 def test_pack_rejects_unsupported_scales(bad):
-    # 8192, -8192 (a weight of 8 * 8192 overflows fp16), just below 2^-14 (not exact
-    # in fp16), a subnormal, +inf, NaN, -inf
+    # 2736 and -2736 (just above the largest accepted magnitude: -24 * s leaves
+    # fp16's range), 8192, just below 2^-14 (not exact in fp16), a subnormal, +inf,
+    # NaN, -inf
     E, K, N = 2, 256, 128
     q1, s1, q2, s2 = inputs.all_expert_weights(E, K, N)
     s2 = s2.copy()
@@ -419,15 +420,15 @@ def test_pack_rejects_unsupported_scales(bad):
 
 
 def test_boundary_scales_are_exact():
-    # 0, -0 and 2^-14 (the smallest accepted magnitude) in the gate/up scales, 8160
-    # and -8160 (the largest) in the down scales -- in the gate/up scales those
+    # 0, -0 and 2^-14 (the smallest accepted magnitude) in the gate/up scales, 2720
+    # and -2720 (the largest) in the down scales -- in the gate/up scales those
     # would only overflow the intermediate, whatever the format -- are accepted,
     # and the forward stays exact with them
     E, K, N, k, M = 4, 256, 128, 2, 6
     q1, s1, q2, s2 = inputs.all_expert_weights(E, K, N)
     s1, s2 = s1.copy(), s2.copy()
     rng = np.random.default_rng(9)
-    for arr, vals in ((s1, [0x0000, 0x8000, 0x3880, 0xB880]), (s2, [0x45FF, 0xC5FF, 0x3880, 0x0000])):
+    for arr, vals in ((s1, [0x0000, 0x8000, 0x3880, 0xB880]), (s2, [0x452A, 0xC52A, 0x3880, 0x0000])):
         flat = arr.reshape(-1)
         idx = rng.choice(flat.size, size=40, replace=False)
         flat[idx] = np.array(vals * 10, dtype=np.uint16)
@@ -477,11 +478,11 @@ def test_hidden_rows_far_outside_fp16_range(M):
 
 
 def test_intermediate_saturation_sets_status():
-    # gate/up scales of 8160 make SiLU(g) * u far exceed fp16's range even for
+    # gate/up scales of 2720 make SiLU(g) * u far exceed fp16's range even for
     # prescaled rows: the epilogue saturates and says so; a normal call is clean again
     E, K, N, k, M = 4, 256, 128, 2, 3
     q1, s1, q2, s2 = inputs.all_expert_weights(E, K, N)
-    hot = np.full_like(s1, 0x45FF)
+    hot = np.full_like(s1, 0x452A)
     prob = Problem(E, K, N, k, weights=(q1, hot, q2, s2))
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
     hidden, ids, wts = workload_inputs(wl)
