@@ -6,6 +6,7 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "rowcopy.cuh"
 #include "route.cuh"
 #include "small_route.cuh"
 
@@ -290,39 +291,6 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl) {
   return launch_k(align_kernel, dim3(1), dim3(1024), smem, stream, pdl, a);
 }
 
-// Largest magnitude among eight bf16 values, as bf16 magnitude bits: for finite
-// values the order of |x| is the order of the low 15 bits.
-__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-  return m;
-}
-
-// Prescale exponent of a token row whose largest magnitude has bf16 bits `m`:
-// the e for which that magnitude times 2^-e lies in [4, 8) (clamped to
-// +-kMaxRowExp); 0 for an all-zero row, and for a row holding an infinity or a
-// NaN (outside the supported input range: such values saturate).
-__device__ __forceinline__ int row_exponent(uint32_t m) {
-  if (m == 0 || m >= 0x7F80u) return 0;
-  const int biased = static_cast<int>(m >> 7);
-  // floor(log2 |x|): from the exponent field, or for a subnormal (m * 2^-133) from
-  // the leading mantissa bit
-  const int lg = biased > 0 ? biased - 127 : (31 - __clz(static_cast<int>(m))) - 133;
-  const int e = lg - 2;
-  return e < -kMaxRowExp ? -kMaxRowExp : (e > kMaxRowExp ? kMaxRowExp : e);
-}
-
-// bf16 pair times f -> fp16 pair (f = 2^-e is exact; values stay below 8 for a
-// finite row, the clamp only bounds non-finite ones).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float f) {
-  const float lo = fminf(fmaxf(__uint_as_float(w << 16) * f, -65504.0f), 65504.0f);
-  const float hi = fminf(fmaxf(__uint_as_float(w & 0xFFFF0000u) * f, -65504.0f), 65504.0f);
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // One CTA copies expert-sorted row p (flat slot `sid`, or padding when sid is the
 // sentinel) into the blocked fp16 B-operand layout: every thread loads its
 // 16-byte chunks of the token's row at once (up to kGatherChunks each), the CTA
@@ -335,9 +303,6 @@ constexpr int kGatherChunks = 8;  // chunks of 8 elements per thread and pass: K
 // With act-order on w1 (perm1 set) the row is written in the expert's packing
 // order: element j of the copy is hidden element perm1[expert][j] (the largest
 // magnitude, and so the exponent, does not depend on the order).
-__device__ __forceinline__ uint32_t bf16_pair(const uint16_t* xr, int a, int b) {
-  return static_cast<uint32_t>(__ldg(xr + a)) | (static_cast<uint32_t>(__ldg(xr + b)) << 16);
-}
 __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int expert) {
   const int tid = threadIdx.x;
   const bool real = sid < g.MK && MOE_CHECK(sid >= 0 && sid / g.topk < g.M, const_cast<int32_t*>(g.hdr),
@@ -392,8 +357,7 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
       }
       const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
                                  bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
-      const long long off = (static_cast<long long>(ch >> 3) * g.Gcap + grp) * kRowGroupBytes +
-                            row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+      const long long off = b_operand_offset(ch, p, g.Gcap);
       if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 25, off, p))
         *reinterpret_cast<uint4*>(g.xs + off) = o;
     }
@@ -430,7 +394,6 @@ extern "C" int moe_rg_trace_read(unsigned long long* host, int reset) {
   do {               \
   } while (0)
 #endif
-constexpr int kSmallPadRows = 32 + 32 * (kRowGroup - 1);  // at most 32 slots, padded to 16 each
 constexpr int kGatherWarps = kGatherThreads / 32;
 
 __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(const AlignArgs a_in,

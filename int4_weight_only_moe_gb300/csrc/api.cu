@@ -30,6 +30,8 @@ struct moe_w4a16_ctx {
   int layout;      // source layout of the last pack (for the inverse)
   int32_t* perm1;  // act-order packing order of w1's reduction elements [E, K], or null
   int32_t* perm2;  // the same for w2 [E, N] (also the order of w1's output features)
+  int32_t* fsync;  // the fused small-batch launch's counters (zero between calls)
+  int fsync_words;
   cudaEvent_t ev[6];
   bool ev_valid;
   // pinned staging of small host-buffer forwards whose buffers are pageable
@@ -187,6 +189,10 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   e = cudaMalloc(&h->w1p, h->w1p_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->w2p, h->w2p_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&h->dflag, 256);
+  h->fsync_words = kFsTickets + kMaxCtas + K / kBM + kSmallTiles * (N / kBM);
+  if (e == cudaSuccess) e = cudaMalloc(&h->fsync, static_cast<size_t>(h->fsync_words) * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->fsync, 0, static_cast<size_t>(h->fsync_words) * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(h->w1p);
     cudaFree(h->w2p);
@@ -222,6 +228,7 @@ int moe_w4a16_destroy(moe_w4a16_t h) {
   cudaFree(h->w1p);
   cudaFree(h->w2p);
   cudaFree(h->dflag);
+  cudaFree(h->fsync);
   cudaFree(h->perm1);
   cudaFree(h->perm2);
   if (h->hstage) cudaFreeHost(h->hstage);
@@ -468,7 +475,14 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   ga.perm1 = h->perm1;
   ga.topk_ids = topk_ids;
   ga.e_begin = h->e_begin;
-  if (MK <= 32) {
+  // Small batch with given ids: both GEMMs in one cooperative launch that also
+  // routes and gathers for itself (its gate/up shares start at multiples of 4
+  // steps, so the steps per unit must allow that; at most one CTA per SM).
+  const bool fused = h->fused_small && MK <= 32 && !logits && h->num_ctas <= h->num_sms &&
+                     (static_cast<long long>(2 * h->N / kBM) * (h->K / (2 * kBK))) % 4 == 0;
+  if (fused) {
+    if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
+  } else if (MK <= 32) {
     // small batch (decode): routing and gather in one launch, timed as "align"
     MOE_CUDA_TRY(launch_route_gather_small(aa, ga, L.Pcap, h->num_sms, s, false));
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
@@ -515,12 +529,6 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g1.E = h->E;
   g1.dbg = hdr + 8;
   g1.sched = (sched && h->step_cost[0] > 0) ? sched : nullptr;
-  // small batch with given ids: both GEMMs in one cooperative launch (the shares
-  // of its gate/up phase start at multiples of 4 steps, so the step count per
-  // unit must allow that)
-  // (cooperative: at most one CTA per SM)
-  const bool fused = h->fused_small && small_ids != nullptr && h->num_ctas <= h->num_sms &&
-                     (static_cast<long long>(g1.R) * g1.KBn) % 4 == 0;
   if (!fused) MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
@@ -561,12 +569,32 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.E = h->E;
   g2.dbg = hdr + 8;
   g2.sched = (sched && h->step_cost[1] > 0) ? sched + (h->num_ctas + 1) : nullptr;
-  int32_t* h_ready = tickets + kMaxCtas + h->K / kBM;
-  g1.h_ready = g2.h_ready = h_ready;
-  if (fused)
-    MOE_CUDA_TRY(launch_gemm_fused(g1, g2, h->num_ctas, s, pdl));
-  else
+  if (fused) {
+    // the counters live in the handle (zero between calls); the kernel writes the
+    // workspace header itself at the end
+    int32_t* fs = h->fsync;
+    g1.status = g2.status = fs + kFsStatus;
+    g1.tickets = fs + kFsTickets;
+    if (g2.rt_tickets) g2.rt_tickets = fs + kFsTickets + kMaxCtas;  // (none for a partial sum)
+    g1.h_ready = g2.h_ready = fs + kFsTickets + kMaxCtas + h->K / kBM;
+    FusedPrep& P = g1.prep;
+    P.x = hidden;
+    P.xs = xs;
+    P.sorted_ids = sorted;
+    P.rowexp = rowexp;
+    P.acc = acc;
+    P.acc_elems = static_cast<long long>(M) * h->K;
+    P.perm1 = h->perm1;
+    P.fsync = fs;
+    P.fsync_words = h->fsync_words;
+    P.ws_hdr = hdr;
+    P.K = h->K;
+    P.topk = h->topk;
+    g2.prep = P;
+    MOE_CUDA_TRY(launch_gemm_fused(g1, g2, h->num_ctas, s, false));
+  } else {
     MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
+  }
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 
   if (!fold_finalize && !partial)

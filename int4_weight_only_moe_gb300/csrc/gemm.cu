@@ -59,6 +59,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
+#include "rowcopy.cuh"
 #include "small_route.cuh"
 
 namespace moe {
@@ -181,6 +182,8 @@ constexpr int kSmRings = ((kSmSmall + kSmallTiles * 16 + 16 + 1023) / 1024) * 10
 constexpr int kSmAlloc = 227 * 1024;     // the whole per-CTA limit (base aligned to 1024 inside)
 constexpr int kRingBytes = kSmAlloc - 1024 - kSmRings;
 static_assert(kSmRings < kSmAlloc - 1024, "shared memory budget");
+static_assert(2 * kSmallPadRows * 4 <= kMaxSegs * 16,
+              "the fused launch's padded row list takes the segment table's place");
 static_assert(kNS * kACols + 4 * kBNMax <= kTmemCols && kNSNarrow * kACols + 4 * 32 <= kTmemCols,
               "tensor memory budget");
 static_assert(kWChunk == 2, "the chunk arithmetic below assumes 2-step chunks");
@@ -503,6 +506,75 @@ __device__ __forceinline__ bool swiglu_chunk(const float (&v)[16], int chunk, in
   return sat;
 }
 
+// The fused launch's preparation, by the 128 epilogue threads of every CTA before
+// their first segment: CTA c takes padded rows c, c + G, ...: records the row's
+// slot, and for a real row its prescale exponent and its copy as scaled fp16 in
+// the blocked B layout (the expert's packing order under act-order), as the
+// routing + gather kernel does for the separate launches; then zeroes its slice of
+// the output accumulator.
+__device__ void fused_prep(const GemmArgs& a, const int* s_sorted, const int* s_expert, int npad,
+                           int epi_tid, volatile int* red) {
+  const FusedPrep& P = a.prep;
+  const int G = static_cast<int>(gridDim.x);
+  const int cpr = P.K / 8;  // 16-byte chunks per row
+  for (int p = blockIdx.x; p < npad; p += G) {
+    const int sid = s_sorted[p];
+    if (epi_tid == 0) P.sorted_ids[p] = sid;
+    if (sid >= a.MK) {  // padding: only the sentinel exponent (uniform branch)
+      if (epi_tid == 0) P.rowexp[p] = kPadRowExp;
+      continue;
+    }
+    const uint16_t* xr = P.x + static_cast<long long>(sid / P.topk) * P.K;
+    const uint4* src = reinterpret_cast<const uint4*>(xr);
+    // every load of the row issued at once (rows up to kPrepChunks * 128 * 8
+    // elements stay in registers; longer ones are read again below)
+    constexpr int kPrepChunks = 8;
+    uint4 v[kPrepChunks];
+#pragma unroll
+    for (int i = 0; i < kPrepChunks; ++i) {
+      const int ch = epi_tid + i * kEpiThreads;
+      v[i] = ch < cpr ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kPrepChunks; ++i) m = max(m, bf16x8_absmax_bits(v[i]));
+    for (int ch = epi_tid + kPrepChunks * kEpiThreads; ch < cpr; ch += kEpiThreads)
+      m = max(m, bf16x8_absmax_bits(src[ch]));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((epi_tid & 31) == 0) red[epi_tid >> 5] = static_cast<int>(m);
+    named_bar_sync(kEpiBar, kEpiThreads);
+    const uint32_t mm = max(max(static_cast<uint32_t>(red[0]), static_cast<uint32_t>(red[1])),
+                            max(static_cast<uint32_t>(red[2]), static_cast<uint32_t>(red[3])));
+    named_bar_sync(kEpiBar, kEpiThreads);  // (red is reused by the next row)
+    const int e = row_exponent(mm);
+    if (epi_tid == 0) P.rowexp[p] = e;
+    const float f = exp2_int(-e);
+    const int32_t* pr = P.perm1 ? P.perm1 + static_cast<long long>(s_expert[p]) * P.K : nullptr;
+    // chunk ch of the copy (in the packing order under act-order), as scaled fp16
+    auto put = [&](int ch, uint4 x) {
+      if (pr) {
+        const int4 i0 = *reinterpret_cast<const int4*>(pr + 8 * ch);
+        const int4 i1 = *reinterpret_cast<const int4*>(pr + 8 * ch + 4);
+        x = make_uint4(bf16_pair(xr, i0.x, i0.y), bf16_pair(xr, i0.z, i0.w), bf16_pair(xr, i1.x, i1.y),
+                       bf16_pair(xr, i1.z, i1.w));
+      }
+      const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
+                                 bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
+      *reinterpret_cast<uint4*>(P.xs + b_operand_offset(ch, p, a.Gcap)) = o;
+    };
+#pragma unroll
+    for (int i = 0; i < kPrepChunks; ++i) {
+      const int ch = epi_tid + i * kEpiThreads;
+      if (ch < cpr) put(ch, v[i]);
+    }
+    for (int ch = epi_tid + kPrepChunks * kEpiThreads; ch < cpr; ch += kEpiThreads) put(ch, src[ch]);
+  }
+  float4* acc4 = reinterpret_cast<float4*>(P.acc);
+  for (long long i = static_cast<long long>(blockIdx.x) * kEpiThreads + epi_tid; i < P.acc_elems / 4;
+       i += static_cast<long long>(G) * kEpiThreads)
+    acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // kMode 1: gate/up + SwiGLU; 2: down + weighted scatter-add; 3: both in one
 // launch for a small batch (phase 1 with `a`, then phase 2 with `a2`; see below).
 template <int kMode>
@@ -553,6 +625,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
     if (lane == 0) {
       *small_ntiles = r.tot_tiles < kSmallTiles ? r.tot_tiles : kSmallTiles;
       *ng_max_sm = ng;  // the widest tile of the batch (at most 2 row groups)
+    }
+    if (kMode == 3) {
+      // the fused launch prepares its own operand rows: the padded row list (slot
+      // of every expert-sorted row, or the sentinel) and each real row's expert
+      int* s_sorted = reinterpret_cast<int*>(gbase + kSmSeg);
+      int* s_expert = s_sorted + kSmallPadRows;
+      const int npad = r.tot_pad < kSmallPadRows ? r.tot_pad : kSmallPadRows;
+      for (int p = lane; p < npad; p += 32) s_sorted[p] = a.MK;
+      __syncwarp();
+      if (r.e >= 0 && r.seg + r.rank < kSmallPadRows) {
+        s_sorted[r.seg + r.rank] = lane;
+        s_expert[r.seg + r.rank] = r.e;
+      }
+      if (lane == 0) {
+        small_ntiles[1] = npad;
+        if (r.any_bad && blockIdx.x == 0) atomicOr(a.status, kStatusBadId);
+      }
     }
   }
   if (threadIdx.x == 0) {
@@ -772,7 +861,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
     // kProducerLanes lanes walk consecutive k-blocks in step and issue their
     // (2-8 KB) copies in one go: a bulk-copy issue holds its thread
     // for a while, so small copies must leave several at a time.
-    if (small) pdl_wait();  // the activations are the preceding kernel's output
+    // the activations are the preceding kernel's output, or, in the fused launch,
+    // the rows every CTA prepares (counted on the handle's prep counter)
+    bool prep_ok = true;
+    if (kMode == 3) {
+      if (lane < kProducerLanes)
+        prep_ok = wait_counters(a.prep.fsync + kFsPrep, 1, G, abort_flag, status, wait_ns);
+    } else if (small) {
+      pdl_wait();
+    }
     if (lane == 0) CTA_STAMP(2);
     if (lane < kProducerLanes) {
       // (indices below are in the CTA's step sequence over the phases; a down
@@ -783,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
       uint32_t mine = 0;
       int s = lane;      // slot of this lane's step, advanced by kProducerLanes (nb is a multiple)
       uint32_t sph = 0;  // parity of that slot's phase
-      bool ok_all = true;
+      bool ok_all = prep_ok;
       int ready_tile = -1;  // fused down phase: the token tile whose intermediate was seen complete
 #pragma unroll
       for (int ph = kPh0; ph <= kPh1; ++ph) {
@@ -1038,7 +1135,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
     }
   } else if (warp >= kWarpEpi0) {
     // ------------------------------------------------ epilogue
-    if (small) pdl_wait();  // routing rows, exponents and the zeroed accumulator / tickets
+    if (kMode == 3) {
+      // prepare this CTA's rows, count it, and wait until every CTA has
+      const int* s_sorted = reinterpret_cast<const int*>(gbase + kSmSeg);
+      fused_prep(a, s_sorted, s_sorted + kSmallPadRows, small_ntiles[1], threadIdx.x - kWarpEpi0 * 32,
+                 epi_ok + 8);
+      __threadfence();
+      named_bar_sync(kEpiBar, kEpiThreads);
+      if (threadIdx.x == kWarpEpi0 * 32) {
+        atomicAdd(a.prep.fsync + kFsPrep, 1);
+        wait_counters(a.prep.fsync + kFsPrep, 1, G, abort_flag, status, wait_ns);
+      }
+      named_bar_sync(kEpiBar, kEpiThreads);
+      __threadfence();
+    } else if (small) {
+      pdl_wait();  // routing rows, exponents and the zeroed accumulator / tickets
+    }
     // Test hook: wait on a barrier that nothing arrives on. The wait gives up after
     // the wait limit, raises the abort flag and records the timeout; every role then
     // stops at its next wait and the teardown lets in-flight copies and MMAs land.
@@ -1311,6 +1423,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (kMode == 3) {
+    // The last CTA to finish publishes the status and row counts in the workspace
+    // header and clears the handle's counters for the next call.
+    if (threadIdx.x == 0) {
+      __threadfence();
+      *last_flag = atomicAdd(a.prep.fsync + kFsExit, 1) == G - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_flag) {
+      __threadfence();
+      if (threadIdx.x == 0) {
+        a.prep.ws_hdr[kHdrStatus] = ld_relaxed_gpu(a.prep.fsync + kFsStatus);
+        a.prep.ws_hdr[kHdrNumPadded] = small_ntiles[1];
+        a.prep.ws_hdr[kHdrNumTiles] = num_tiles;
+        a.prep.ws_hdr[kHdrSched] = 0;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < a.prep.fsync_words; i += blockDim.x) a.prep.fsync[i] = 0;
+    }
   }
 #undef MOE_TMEM_NST
 #undef MOE_TMEM_ACCW

@@ -99,6 +99,27 @@ cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, i
 cudaError_t launch_route(const float* logits, int M, int E, int k, int32_t* ids, float* wts,
                          int num_sms, cudaStream_t stream, bool pdl);
 
+// The fused small-batch launch's own preparation (what the routing + gather
+// kernel does otherwise) and its cross-CTA counters, kept in the handle: fsync
+// holds [kFsStatus] the status word, [kFsPrep] CTAs done preparing, [kFsExit]
+// CTAs done, then the split-unit tickets, the output row-tile tickets and the
+// intermediate counters; all zero between calls (the last CTA to finish clears
+// them). The workspace header receives the status and the row counts at the end.
+enum { kFsStatus = 0, kFsPrep = 1, kFsExit = 2, kFsTickets = 8 };
+struct FusedPrep {
+  const uint16_t* x;         // hidden bf16 [M, K]
+  uint8_t* xs;               // blocked B operand of the gate/up GEMM
+  int32_t* sorted_ids;       // [padded rows] flat slot of each expert-sorted row
+  int32_t* rowexp;           // [padded rows] prescale exponent
+  float* acc;                // [M, K] fp32 output accumulator, zeroed here
+  long long acc_elems;
+  const int32_t* perm1;      // act-order packing order of w1 [E, K], or null
+  int32_t* fsync;            // handle's counters (see above)
+  int fsync_words;
+  int32_t* ws_hdr;           // workspace header
+  int K, topk;
+};
+
 struct GemmArgs {
   const uint8_t* wpack;    // packed weights of this GEMM
   const uint8_t* bsrc;     // blocked activations (B operand)
@@ -120,6 +141,7 @@ struct GemmArgs {
   // fused small-batch launch: per token tile and down-GEMM k-block, a zeroed
   // counter of the gate/up row tiles whose intermediate is stored ([32][N/128])
   int32_t* h_ready;
+  FusedPrep prep;          // fused launch only
   uint16_t* out;           // bf16 [M, Kout]
   int M;
   int R;                   // row tiles per expert

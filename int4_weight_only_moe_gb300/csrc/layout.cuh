@@ -39,6 +39,7 @@ constexpr int kBNMax = 64;          // largest token tile (MMA N)
 constexpr int kRowGroup = 16;       // token rows per blocked row group
 constexpr int kRowGroupBytes = kRowGroup * 128;
 constexpr int kSmallTiles = 32;     // token tiles of a batch of at most 32 routed slots (one per expert)
+constexpr int kSmallPadRows = 32 + 32 * (kRowGroup - 1);  // their padded rows (16 per expert at most)
 constexpr int kMaxCtas = 256;       // persistent grid limit (tickets / scratch slots)
 constexpr int kMaxExperts = 1024;
 

@@ -56,11 +56,13 @@ def ep_run(hs, hidden, ids, wts):
 
 
 @pytest.mark.parametrize("world", [2, 3])
-@pytest.mark.parametrize("M", [37, 3])
-def test_partials_sum_to_the_layer(world, M):
+@pytest.mark.parametrize("M,fused", [(37, 0), (3, 0), (3, 1)])
+def test_partials_sum_to_the_layer(world, M, fused):
     need_gpu()
     wl = MID
     hs = rank_handles(wl, world)
+    for moe in hs:
+        pkg.moe_w4a16_set_option(moe.handle, pkg.OPT_FUSED_SMALL_BATCH, fused)
     try:
         hidden, ids, wts = workload_inputs(wl, M=M, step=world)
         total, out = ep_run(hs, hidden, ids, wts)
@@ -71,7 +73,8 @@ def test_partials_sum_to_the_layer(world, M):
         rel, mx = assert_close(got, ref, f"EP world {world}, M={M}")
         check_accumulator(total.cpu().numpy().astype(np.float64), out.view(torch.int16).cpu().numpy(), ref,
                           f"EP world {world}, M={M}")
-        MARGINS.append(f"expert-parallel world {world}, M={M}: rel L2 {rel:.3e}, max|d|/rms {mx:.3e}")
+        MARGINS.append(f"expert-parallel world {world}, M={M}{' fused' if fused else ''}: rel L2 {rel:.3e}, "
+                       f"max|d|/rms {mx:.3e}")
     finally:
         for moe in hs:
             moe.close()

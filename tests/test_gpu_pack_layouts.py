@@ -92,13 +92,15 @@ def test_inverse_repack_is_bit_exact(name, ct, act1, act2):
 
 
 @pytest.mark.parametrize("name,ct,act1,act2", CASES)
-@pytest.mark.parametrize("M", [37, 3])
-def test_forward_matches_oracle_decoder(name, ct, act1, act2, M):
+@pytest.mark.parametrize("M,fused", [(37, 0), (3, 0), (3, 1)])
+def test_forward_matches_oracle_decoder(name, ct, act1, act2, M, fused):
     # M = 37: the batched path (align, gather, split token tiles); M = 3: the
-    # small-batch path (routing and gather in one launch)
+    # small-batch path (routing and gather in one launch), or the fused launch
+    # that gathers (in w1's packing order) for itself
     need_gpu()
     wl = MID
     p = LayoutProblem(wl.E, wl.K, wl.N, wl.topk, ct, act1, act2)
+    pkg.moe_w4a16_set_option(p.moe.handle, pkg.OPT_FUSED_SMALL_BATCH, fused)
     try:
         hidden, ids, wts = workload_inputs(wl, M=M, step=M)
         out = p.moe.forward(dev(bits16(hidden)), dev(ids), dev(wts))
@@ -109,7 +111,8 @@ def test_forward_matches_oracle_decoder(name, ct, act1, act2, M):
         rel, mx = assert_close(got, ref, f"{name}, M={M}")
         acc = p.moe.accumulator(M).cpu().numpy().astype(np.float64)
         check_accumulator(acc, out.view(torch.int16).cpu().numpy(), ref, f"{name}, M={M}")
-        MARGINS.append(f"pack layout {name}, M={M}: rel L2 {rel:.3e}, max|d|/rms {mx:.3e}")
+        MARGINS.append(f"pack layout {name}, M={M}{' fused' if fused else ''}: rel L2 {rel:.3e}, "
+                       f"max|d|/rms {mx:.3e}")
     finally:
         p.close()
 

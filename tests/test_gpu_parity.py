@@ -190,6 +190,43 @@ def test_fused_small_batch_matches_two_launches(M, num_ctas):
     prob.close()
 
 
+def test_fused_small_batch_prepares_its_own_rows():
+    # the fused launch routes, gathers and zeroes for itself and keeps its counters
+    # in the handle: repeated calls (the counters cleared by each call's last CTA),
+    # a bad expert id (the status bit, published in the workspace header), the
+    # intermediate and accumulator read-back, and act-order weights (the gather in
+    # the packing order) all behave as on the two-launch path
+    E, K, N, k, M = 16, 512, 256, 4, 3
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    prob = Problem(E, K, N, k)
+    h = prob.moe.handle
+    pkg.moe_w4a16_set_option(h, pkg.OPT_FUSED_SMALL_BATCH, 1)
+    try:
+        for step in range(3):
+            hidden, ids, wts = workload_inputs(wl, step=step)
+            got = check_forward(prob, hidden, ids, wts, f"fused call {step}")
+        inter = prob.moe.intermediate(M).cpu().numpy()
+        acc = prob.moe.accumulator(M).cpu().numpy()
+        pkg.moe_w4a16_set_option(h, pkg.OPT_FUSED_SMALL_BATCH, 0)
+        two = check_forward(prob, hidden, ids, wts, "two launches")
+        assert_within_one_ulp(got, two)
+        # (the fused launch splits the gate/up steps at multiples of 4, so a split
+        # unit's fp32 partial sums may add in another order: h to one fp16 unit)
+        np.testing.assert_allclose(prob.moe.intermediate(M).cpu().numpy(), inter, rtol=2.0 ** -10,
+                                   atol=2.0 ** -24 * float(np.abs(inter).max()))
+        np.testing.assert_allclose(prob.moe.accumulator(M).cpu().numpy(), acc, rtol=1e-5,
+                                   atol=1e-5 * float(np.abs(acc).max()))
+        pkg.moe_w4a16_set_option(h, pkg.OPT_FUSED_SMALL_BATCH, 1)
+        bad = ids.copy()
+        bad[1, 2] = E + 5
+        got = prob.run(hidden, bad, wts)
+        assert prob.moe.status() == pkg.STATUS_BAD_EXPERT_ID
+        assert_close(got, prob.reference(hidden, np.where(bad >= E, -1, bad), wts), "fused, bad id")
+        check_forward(prob, hidden, ids, wts, "fused after a bad id")  # status clean again
+    finally:
+        prob.close()
+
+
 def test_hot_expert_spans_several_token_tiles():
     # one expert receives every token (> 128 rows: several token tiles of one expert)
     E, K, N, k, M = 8, 768, 384, 2, 300
