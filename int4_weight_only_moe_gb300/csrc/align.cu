@@ -367,9 +367,10 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
 // Small batches in one launch: routing and gather. Every CTA's first warp
 // recomputes the one-warp routing (cheap) and lays the padded sorted-slot list
 // into shared memory; CTA 0 also publishes the routing for the GEMMs (they read
-// it after waiting for this kernel). Then every warp gathers its share of the
-// expert-sorted rows, one row at a time, and every thread zeroes its share of the
-// accumulator, as gather_kernel.
+// it after waiting for this kernel). Then CTA c copies the row of routed slot c
+// (the grid is only as large as the slots, or the accumulator to zero, need:
+// every other SM is free for the GEMM launched behind it), the padding rows get
+// their sentinel exponent, and every thread zeroes its share of the accumulator.
 #ifdef MOE_GEMM_TRACE
 // trace builds: global-timer stamps per CTA (entry, dependency resolved, exit)
 __device__ unsigned long long g_rg_trace[512][4];
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
                                                                            const GatherArgs g) {
   __shared__ int s_sorted[kSmallPadRows];
   __shared__ int s_expert[kSmallPadRows];  // expert of every real padded row
+  __shared__ int s_pos[32];                // padded row of every routed slot, or -1
   __shared__ int s_npad;
   __shared__ int32_t s_ids[32];
   __shared__ int s_red[kGatherWarps + 1];
@@ -437,10 +439,12 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
     const int npad = r.tot_pad < kSmallPadRows ? r.tot_pad : kSmallPadRows;
     for (int p = lane; p < npad; p += 32) s_sorted[p] = a.MK;
     __syncwarp();
-    if (r.e >= 0 && r.seg + r.rank < kSmallPadRows) {
+    const bool placed = r.e >= 0 && r.seg + r.rank < kSmallPadRows;
+    if (placed) {
       s_sorted[r.seg + r.rank] = lane;
       s_expert[r.seg + r.rank] = r.e;
     }
+    s_pos[lane] = placed ? r.seg + r.rank : -1;
     if (lane == 0) s_npad = npad;
     if (blockIdx.x == 0) small_route_write(a, r, lane);
   }
@@ -449,10 +453,14 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   float4* acc4 = reinterpret_cast<float4*>(g.acc);
   for (long long i = gt; i < g.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int p = blockIdx.x; p < s_npad; p += gridDim.x) {
-    const int sid = s_sorted[p];
-    gather_row(g, p, sid, s_red, sid < a.MK ? s_expert[p] : -1);
+  // one CTA per routed slot copies its row (a small grid: the GEMM that follows
+  // starts on every other SM at once); the padding rows only get their sentinel
+  for (int sl = blockIdx.x; sl < a.MK; sl += gridDim.x) {
+    const int p = s_pos[sl];
+    if (p >= 0) gather_row(g, p, sl, s_red, s_expert[p]);
   }
+  for (long long p = gt; p < s_npad; p += nthr)
+    if (s_sorted[p] >= a.MK) g.rowexp[p] = kPadRowExp;
 #ifdef MOE_GEMM_TRACE
   __syncthreads();
   RG_STAMP(2);
@@ -461,8 +469,8 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
 
 cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
                                       int num_sms, cudaStream_t stream, bool pdl) {
-  const long long rows = max_rows < kSmallPadRows ? max_rows : kSmallPadRows;
-  const long long ctas = std::max<long long>(rows, (g.acc_elems / 4 + kGatherThreads - 1) / kGatherThreads);
+  (void)max_rows;
+  const long long ctas = std::max<long long>(a.MK, (g.acc_elems / 4 + kGatherThreads - 1) / kGatherThreads);
   long long grid = ctas;
   const long long cap = 4LL * num_sms;
   if (grid > cap) grid = cap;
