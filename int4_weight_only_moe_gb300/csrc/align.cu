@@ -313,7 +313,6 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
   }
   const int cpr = g.K / 8;  // 16-byte chunks per row
   const uint4* src = reinterpret_cast<const uint4*>(g.x + static_cast<long long>(sid / g.topk) * g.K);
-  const int grp = p / kRowGroup, row = p % kRowGroup;
   constexpr int kPass = kGatherThreads * kGatherChunks;
   const bool one_pass = cpr <= kPass;  // the whole row stays in registers (K <= 16384)
   uint4 v[kGatherChunks];
