@@ -366,10 +366,11 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
 // Small batches in one launch: routing and gather. Every CTA's first warp
 // recomputes the one-warp routing (cheap) and lays the padded sorted-slot list
 // into shared memory; CTA 0 also publishes the routing for the GEMMs (they read
-// it after waiting for this kernel). Then CTA c copies the row of routed slot c
-// (the grid is only as large as the slots, or the accumulator to zero, need:
-// every other SM is free for the GEMM launched behind it), the padding rows get
-// their sentinel exponent, and every thread zeroes its share of the accumulator.
+// it after waiting for this kernel). Then CTA c >= 1 copies the row of routed slot
+// c - 1 (the grid is only as large as the slots, or the accumulator to zero, need:
+// every other SM is free for the GEMM launched behind it; CTA 0, which publishes,
+// copies none), the padding rows get their sentinel exponent, and every thread
+// zeroes its share of the accumulator.
 #ifdef MOE_GEMM_TRACE
 // trace builds: global-timer stamps per CTA (entry, dependency resolved, exit)
 __device__ unsigned long long g_rg_trace[512][4];
@@ -453,8 +454,10 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
   float4* acc4 = reinterpret_cast<float4*>(g.acc);
   for (long long i = gt; i < g.acc_elems / 4; i += nthr) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   // one CTA per routed slot copies its row (a small grid: the GEMM that follows
-  // starts on every other SM at once); the padding rows only get their sentinel
-  for (int sl = blockIdx.x; sl < a.MK; sl += gridDim.x) {
+  // starts on every other SM at once), leaving CTA 0, which publishes the routing,
+  // none when there are others; the padding rows only get their sentinel
+  const int g0 = gridDim.x > 1 ? 1 : 0;
+  for (int sl = static_cast<int>(blockIdx.x) - g0; sl >= 0 && sl < a.MK; sl += gridDim.x - g0) {
     const int p = s_pos[sl];
     if (p >= 0) gather_row(g, p, sl, s_red, s_expert[p]);
   }
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(kGatherThreads) route_gather_small_kernel(cons
 cudaError_t launch_route_gather_small(const AlignArgs& a, const GatherArgs& g, int max_rows,
                                       int num_sms, cudaStream_t stream, bool pdl) {
   (void)max_rows;
-  const long long ctas = std::max<long long>(a.MK, (g.acc_elems / 4 + kGatherThreads - 1) / kGatherThreads);
+  const long long ctas = std::max<long long>(a.MK + 1, (g.acc_elems / 4 + kGatherThreads - 1) / kGatherThreads);
   long long grid = ctas;
   const long long cap = 4LL * num_sms;
   if (grid > cap) grid = cap;

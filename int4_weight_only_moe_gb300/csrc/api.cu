@@ -564,13 +564,6 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.small_ids = small_ids;
   g2.e_begin = h->e_begin;
   g2.E_total = h->E_total;
-  // small batches (the routing + gather launch zeroes every ticket): the down GEMM
-  // rounds each finished output row tile to bf16 itself, with no finalize launch;
-  // the partial-sum forward rounds nothing
-  const bool fold_finalize = MK <= 32 && !partial;
-  g2.rt_tickets = fold_finalize ? tickets + kMaxCtas : nullptr;
-  g2.out = out;
-  g2.M = M;
   g2.R = h->K / kBM;
   g2.KBn = h->N / (2 * kBK);
   g2.Gcap = L.Gcap;
@@ -595,7 +588,6 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
     int32_t* fs = h->fsync;
     g1.status = g2.status = fs + kFsStatus;
     g1.tickets = fs + kFsTickets;
-    if (g2.rt_tickets) g2.rt_tickets = fs + kFsTickets + kMaxCtas;  // (none for a partial sum)
     g1.h_ready = g2.h_ready = fs + kFsTickets + kMaxCtas + h->K / kBM;
     FusedPrep& P = g1.prep;
     P.x = hidden;
@@ -617,7 +609,7 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   }
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[4], s));
 
-  if (!fold_finalize && !partial)
+  if (!partial)
     MOE_CUDA_TRY(launch_finalize(acc, out, static_cast<long long>(M) * h->K, h->num_sms, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[5], s));
   return MOE_W4A16_OK;

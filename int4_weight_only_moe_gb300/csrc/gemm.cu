@@ -139,7 +139,7 @@ constexpr int kWChunkBytes = kWChunk * kWStepBytes;
 // else 4. More stages give each dequantisation warp more slack between storing a
 // stage and needing it again.
 constexpr int kNS = 4;                   // stages with tiles of three or four row groups
-constexpr int kNSNarrow = 6;             // stages with tiles of at most two row groups
+constexpr int kNSNarrow = 4;             // stages with tiles of at most two row groups
 constexpr int kNSMax = kNSNarrow;
 constexpr int kTmemCols = 512;
 constexpr int kACols = kSub * 32;        // one step of fp16 A: 128 lanes x 64 columns
@@ -1409,28 +1409,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarAccEmpty + ab));
-          if (A.rt_tickets) {
-            // Output finalisation (small batches): the contributions to output row
-            // tile rt come from every token tile's unit (tile, rt); the contributor
-            // whose steps complete the tile's count rounds its fp32 sums to bf16.
-            __threadfence();  // this thread's additions are visible before the ticket
-            named_bar_sync(kEpiBar, kEpiThreads);
-            if (epi_tid == 0) {
-              const int add = kb1 - kb0;
-              const int old = atomicAdd(A.rt_tickets + un.rt, add);
-              *last_flag = (old + add == num_tiles * A.KBn) ? 1 : 0;
-            }
-            named_bar_sync(kEpiBar, kEpiThreads);
-            if (*last_flag) {
-              __threadfence();
-              const long long col = static_cast<long long>(un.rt) * kBM + epi_tid;
-              for (int t = 0; t < A.M; ++t) {
-                const float v = __ldcg(A.acc + static_cast<long long>(t) * A.Kout + col);
-                A.out[static_cast<long long>(t) * A.Kout + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-              }
-            }
-            named_bar_sync(kEpiBar, kEpiThreads);  // last_flag is reused by the next segment
-          }
         }
         if (epi_tid == 0) TRACE_POINT(15, acc_it);  // epilogue done with a segment
         if (epi_tid == 0) CTA_STAMP(6);

@@ -102,7 +102,7 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, int32_t* ids,
 // The fused small-batch launch's own preparation (what the routing + gather
 // kernel does otherwise) and its cross-CTA counters, kept in the handle: fsync
 // holds [kFsStatus] the status word, [kFsPrep] CTAs done preparing, [kFsExit]
-// CTAs done, then the split-unit tickets, the output row-tile tickets and the
+// CTAs done, then the split-unit tickets, K/128 reserved words and the
 // intermediate counters; all zero between calls (the last CTA to finish clears
 // them). The workspace header receives the status and the row counts at the end.
 enum { kFsStatus = 0, kFsPrep = 1, kFsExit = 2, kFsTickets = 8 };
@@ -134,10 +134,6 @@ struct GemmArgs {
   int e_begin, E_total;    // the held experts are [e_begin, e_begin + E) of E_total (small_ids)
   uint32_t wait_kcycles;   // pipeline wait limit in units of 1024 SM cycles (wait_limit_kcycles)
   int test_never_wait;     // test hook: the epilogue first waits on a barrier nothing arrives on
-  // down GEMM, small batches: per output row tile, a zeroed ticket counting the
-  // steps added into it; the contributor that completes a tile writes its bf16
-  // output (null: a separate finalize launch rounds the accumulator)
-  int32_t* rt_tickets;
   // fused small-batch launch: per token tile and down-GEMM k-block, a zeroed
   // counter of the gate/up row tiles whose intermediate is stored ([32][N/128])
   int32_t* h_ready;
@@ -148,8 +144,6 @@ struct GemmArgs {
   long long pf_wpack_bytes;
   int pf_R, pf_KBn, pf_max_steps;
   FusedPrep prep;          // fused launch only
-  uint16_t* out;           // bf16 [M, Kout]
-  int M;
   int R;                   // row tiles per expert
   int KBn;                 // k-blocks per unit
   int Gcap;                // row groups per k-block plane of bsrc / hout
