@@ -254,18 +254,11 @@ const char* moe_w4a16_last_error(void);
  *                            runs both GEMMs in one cooperative launch (the down
  *                            GEMM's weights stream while the gate/up GEMM
  *                            finishes); 0 (default) = two launches. Either way the
- *                            same arithmetic.
- *   MOE_W4A16_OPT_L2_PREFETCH_MB
- *                            MB of the down GEMM's packed weights that the gate/up
- *                            GEMM's CTAs bring into L2 once they have issued their
- *                            own weight stream (each the start of the down GEMM's
- *                            even share of its index), so that HBM keeps streaming
- *                            across the boundary between the two (0 = off, the
- *                            default: it measured slower). */
+ *                            same arithmetic. */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
        MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5,
        MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7,
-       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8, MOE_W4A16_OPT_L2_PREFETCH_MB = 9 };
+       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8 };
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order

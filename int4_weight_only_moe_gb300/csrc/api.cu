@@ -22,7 +22,6 @@ struct moe_w4a16_ctx {
   unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
   bool fused_small;            // MOE_W4A16_OPT_FUSED_SMALL_BATCH
-  int l2_prefetch_mb;          // MOE_W4A16_OPT_L2_PREFETCH_MB
   int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
   uint8_t* w2p;
@@ -63,12 +62,6 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // (zero-copy); larger ones move them with the copy engines, which stream large
 // transfers faster than the gather and finalize kernels' loads and stores would.
 constexpr size_t kZeroCopyMaxBytes = 1u << 20;
-
-// L2 prefetch of the down GEMM's weights by the gate/up GEMM, in MB over the grid
-// (a decode step's routed down-projection weights take 66 MB of the 126 MB L2).
-// Off by default: measured on GB300 it made every batch size slightly slower
-// (decode 78.5 -> 81.6 us with 40..120 MB).
-constexpr int kDefaultL2PrefetchMB = 0;
 
 // Default stream-K cost of a pipeline step per row group of its token tile beyond
 // the second, in eighths of a one-group step, per GEMM. Measured on GB300 with
@@ -179,7 +172,6 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->group = group_size;
   h->pdl = true;
   h->fused_small = false;
-  h->l2_prefetch_mb = kDefaultL2PrefetchMB;
   h->step_cost[0] = kDefaultStepCostGateUp;
   h->step_cost[1] = kDefaultStepCostDown;
   cudaError_t e = cudaGetDevice(&h->device);
@@ -355,10 +347,6 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
     case MOE_W4A16_OPT_WAIT_LIMIT_US:
       if (value < 0) return fail(MOE_W4A16_INVALID_ARG, "wait limit must be >= 0");
       h->wait_us = static_cast<unsigned long long>(value);
-      return MOE_W4A16_OK;
-    case MOE_W4A16_OPT_L2_PREFETCH_MB:
-      if (value < 0 || value > 1024) return fail(MOE_W4A16_INVALID_ARG, "L2 prefetch must be in [0, 1024] MB");
-      h->l2_prefetch_mb = value;
       return MOE_W4A16_OK;
     case MOE_W4A16_OPT_FUSED_SMALL_BATCH:
       h->fused_small = value != 0;
@@ -541,14 +529,6 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g1.E = h->E;
   g1.dbg = hdr + 8;
   g1.sched = (sched && h->step_cost[0] > 0) ? sched : nullptr;
-  if (h->l2_prefetch_mb > 0) {
-    g1.pf_wpack = h->w2p;
-    g1.pf_wpack_bytes = static_cast<long long>(h->w2p_bytes);
-    g1.pf_R = h->K / kBM;
-    g1.pf_KBn = h->N / (2 * kBK);
-    g1.pf_max_steps = static_cast<int>((static_cast<long long>(h->l2_prefetch_mb) << 20) /
-                                       (static_cast<long long>(h->num_ctas) * 2 * kWBlockBytes));
-  }
   if (!fused) MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 

@@ -850,33 +850,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a, con
         }
       }
     }
-    if (kMode == 1 && a.pf_wpack != nullptr) {
-      // The down GEMM that follows streams its weights only once this grid has
-      // finished; meanwhile (this CTA's tail and the launch between) HBM would sit
-      // idle. So the warp brings into L2 the first steps of the down GEMM's share
-      // of this CTA index, 128-byte lines split over its lanes, through the
-      // load/store path (not the bulk-copy engine, which the epilogue's stores
-      // still need). Lane 0 arrives here after issuing its last weight chunk.
-      __syncwarp();
-      const long long W2 = static_cast<long long>(num_tiles) * a.pf_R * a.pf_KBn;
-      const long long b2 = W2 * blockIdx.x / G;
-      long long e2 = W2 * (blockIdx.x + 1) / G;
-      if (e2 > b2 + a.pf_max_steps) e2 = b2 + a.pf_max_steps;
-      for (long long g = b2; g < e2;) {
-        const long long u2 = g / a.pf_KBn;
-        const int kb = static_cast<int>(g - u2 * a.pf_KBn);
-        const int run = static_cast<int>(e2 - g < a.pf_KBn - kb ? e2 - g : a.pf_KBn - kb);
-        const Unit un = small ? decode_unit_small(u2, a.pf_R, small_tiles)
-                              : decode_unit(u2, a.pf_R, a.tiles, a.expert_tiles);
-        const long long off = ((static_cast<long long>(un.e) * a.pf_R + un.rt) * a.pf_KBn + kb) * kWStepBytes;
-        const long long len = static_cast<long long>(run) * kWStepBytes;
-        if (un.e >= 0 && un.e < a.E && un.rt >= 0 && un.rt < a.pf_R && off >= 0 &&
-            off + len <= a.pf_wpack_bytes)
-          for (long long o = static_cast<long long>(lane) * 128; o < len; o += 32 * 128)
-            prefetch_l2(a.pf_wpack + off + o);
-        g += run;
-      }
-    }
     if (lane == 0) {
       // let the last chunks land before shared memory is released
       for (long long j = 0; j < nws && j < c_all; ++j) {

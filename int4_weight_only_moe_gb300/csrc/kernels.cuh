@@ -137,12 +137,6 @@ struct GemmArgs {
   // fused small-batch launch: per token tile and down-GEMM k-block, a zeroed
   // counter of the gate/up row tiles whose intermediate is stored ([32][N/128])
   int32_t* h_ready;
-  // gate/up GEMM: the down GEMM's packed weights, prefetched into L2 once this
-  // CTA has issued its own weight stream -- the first pf_max_steps steps of the
-  // down GEMM's even share of the same CTA index (null: no prefetch)
-  const uint8_t* pf_wpack;
-  long long pf_wpack_bytes;
-  int pf_R, pf_KBn, pf_max_steps;
   FusedPrep prep;          // fused launch only
   int R;                   // row tiles per expert
   int KBn;                 // k-blocks per unit
