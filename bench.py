@@ -78,18 +78,22 @@ def file_hash(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def kernel_sources_hash():
-    """Hash of the GEMM kernel's sources (the kernel file and the headers it includes)."""
+GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "layout.cuh", "kernels.cuh", "small_route.cuh", "stream_k.cuh")
+GEMV_SOURCES = ("gemv.cu", "ptx.cuh", "layout.cuh", "kernels.cuh", "small_route.cuh", "stream_k.cuh")
+
+
+def kernel_sources_hash(files=GEMM_SOURCES):
+    """Hash of a kernel's sources (the kernel file and the headers it includes)."""
     csrc = os.path.join(ROOT, "int4_weight_only_moe_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh", "layout.cuh", "kernels.cuh", "small_route.cuh"):
+    for f in files:
         path = os.path.join(csrc, f)
         if os.path.exists(path):
             h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(record="gemm_fused_decode_ncu.json"):
+def recorded_traffic(record="gemm_gateup_decode_ncu.json", files=GEMM_SOURCES):
     """DRAM bytes per launch of the dominant kernel at the headline workload, from the
     committed ncu record under profiles/, valid only while the kernel's sources are
     unchanged since the capture."""
@@ -98,9 +102,9 @@ def recorded_traffic(record="gemm_fused_decode_ncu.json"):
         return None
     try:
         rec = json.load(open(path))
-    except ValueError:
+    except (OSError, ValueError):
         return None
-    if rec.get("kernel_sources_sha256_16") != kernel_sources_hash():
+    if rec.get("kernel_sources_sha256_16") != kernel_sources_hash(files):
         return None
     v = rec.get("dram_bytes_per_launch_full_size")
     return float(v) if v is not None else None
@@ -341,17 +345,29 @@ def run_ours(args):
     # weights and scales, the activation rows read, the intermediate written (and,
     # fused, read back) and the output accumulator.
     fused = False  # (the fused small-batch launch is off by default)
+    gemv = wl.M == 1  # (by default a single-token batch runs its products on the CUDA cores)
     if fused:
         dom_name = "gemm_fused (gate/up + down, one cooperative launch)"
         dom_bytes = (active * (w1b + w2b) + wl.M * wl.K * 2 + 2 * wl.M * wl.topk * wl.N * 2
                      + wl.M * wl.K * 4 + wl.M * wl.K * 2)
         dom_ms = kmean[2] + kmean[3]
+    elif gemv:
+        # the CUDA-core gate/up kernel: weights and scales, the activation step rows
+        # (272 bytes per row and step: 128 fp16 values and 4 group sums) read, h
+        # written twice (step rows for the down kernel, blocked for read-back)
+        dom_name = "gemv_gateup (CUDA cores)"
+        dom_bytes = (active * w1b + wl.M * wl.topk * (wl.K // 128) * 272
+                     + wl.M * wl.topk * (wl.N * 2 + (wl.N // 128) * 272))
+        dom_ms = kmean[2]
     else:
         dom_name = "gemm_gateup"
         dom_bytes = active * w1b + wl.M * wl.K * 2 + wl.M * wl.topk * wl.N * 2
         dom_ms = kmean[2]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = recorded_traffic("gemm_fused_decode_ncu.json" if fused else "gemm_gateup_decode_ncu.json")
+    if gemv:
+        traffic = recorded_traffic("gemv_gateup_decode_ncu.json", GEMV_SOURCES)
+    else:
+        traffic = recorded_traffic("gemm_fused_decode_ncu.json" if fused else "gemm_gateup_decode_ncu.json")
 
     # timing detail of the headline workload: spread, hot L2, graph-captured launches
     hot_ms, _, _ = gb.time_forward(wl, args.steps, args.warmup, flush=False)
@@ -381,8 +397,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "dtype_detail": "INT4 weights dequantised exactly to f16 tensor-core operands, f32 accumulate, "
-                        "bf16 in/out",
+        "dtype_detail": "INT4 weights dequantised exactly to f16 (tensor-core operands; for a single token "
+                        "CUDA-core fma of the exact f16 products), f32 accumulate, bf16 in/out",
         "data": "synthetic (seeded random INT4 weights for all 384 experts, N(0,1) bf16 hidden, "
                 "uniform router logits -> top-8 renormalised by the library's router)",
         "config": headline_config(wl, world),

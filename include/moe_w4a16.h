@@ -254,11 +254,25 @@ const char* moe_w4a16_last_error(void);
  *                            runs both GEMMs in one cooperative launch (the down
  *                            GEMM's weights stream while the gate/up GEMM
  *                            finishes); 0 (default) = two launches. Either way the
- *                            same arithmetic. */
+ *                            same arithmetic.
+ *   MOE_W4A16_OPT_GEMV_SMALL_BATCH
+ *                            how a forward with M * topk <= 32 (the fused launch
+ *                            off) computes its two expert products: 2 (default) =
+ *                            on the CUDA cores for a single token (M == 1), on the
+ *                            tensor cores otherwise; 1 = on the CUDA cores for
+ *                            every such batch; 0 = always on the tensor cores.
+ *                            The CUDA-core kernels compute matrix-vector products
+ *                            over tiles of at most 4 token rows per expert: the
+ *                            weights are dequantised to fp16 (16 + u, exact),
+ *                            multiplied with the fp16 activations into fp32, and
+ *                            the -8 offset applied per scale group through the
+ *                            group's activation sum. The two paths agree to fp32
+ *                            rounding (about 2^-19 of a group's magnitude), not
+ *                            bit for bit. */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
        MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5,
        MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7,
-       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8 };
+       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8, MOE_W4A16_OPT_GEMV_SMALL_BATCH = 9 };
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order

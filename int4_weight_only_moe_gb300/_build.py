@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmoe_w4a16.so")
-SOURCES = ["pack.cu", "align.cu", "route.cu", "gemm.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["pack.cu", "align.cu", "route.cu", "gemm.cu", "gemv.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I", INCLUDE, "-I", CSRC]

@@ -346,19 +346,40 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
 #pragma unroll
     for (int i = 0; i < kGatherChunks; ++i) {
       const int ch = c0 + i * kGatherThreads + tid;
-      if (ch >= cpr) continue;
-      uint4 x = one_pass ? v[i] : src[ch];
-      if (pr) {
-        const int4 i0 = *reinterpret_cast<const int4*>(pr + 8 * ch);
-        const int4 i1 = *reinterpret_cast<const int4*>(pr + 8 * ch + 4);
-        x = make_uint4(bf16_pair(xr, i0.x, i0.y), bf16_pair(xr, i0.z, i0.w), bf16_pair(xr, i1.x, i1.y),
-                       bf16_pair(xr, i1.z, i1.w));
+      const bool in_row = ch < cpr;  // (K is a multiple of 128: whole groups of 4 lanes agree)
+      float gsum = 0.f;
+      uint8_t* xv_step = g.xv ? g.xv + (static_cast<long long>(p) * g.xv_steps + (ch >> 4)) * kXvStepBytes : nullptr;
+      if (in_row) {
+        uint4 x = one_pass ? v[i] : src[ch];
+        if (pr) {
+          const int4 i0 = *reinterpret_cast<const int4*>(pr + 8 * ch);
+          const int4 i1 = *reinterpret_cast<const int4*>(pr + 8 * ch + 4);
+          x = make_uint4(bf16_pair(xr, i0.x, i0.y), bf16_pair(xr, i0.z, i0.w), bf16_pair(xr, i1.x, i1.y),
+                         bf16_pair(xr, i1.z, i1.w));
+        }
+        const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
+                                   bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
+        if (xv_step) {
+          // step rows: the chunk in order within its step, and its group's sum
+          if (MOE_CHECK((xv_step - g.xv) + kXvStepBytes <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 28,
+                        xv_step - g.xv, p))
+            *reinterpret_cast<uint4*>(xv_step + (ch & 15) * 16) = o;
+          gsum = f16x8_sum(o);
+        } else {
+          const long long off = b_operand_offset(ch, p, g.Gcap);
+          if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 25, off, p))
+            *reinterpret_cast<uint4*>(g.xs + off) = o;
+        }
       }
-      const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
-                                 bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
-      const long long off = b_operand_offset(ch, p, g.Gcap);
-      if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 25, off, p))
-        *reinterpret_cast<uint4*>(g.xs + off) = o;
+      if (xv_step) {
+        // the scale group's sum (4 consecutive chunks = 4 consecutive lanes)
+        gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
+        gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
+        if (in_row && (ch & 3) == 0 &&
+            MOE_CHECK((xv_step - g.xv) + kXvStepBytes <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 29,
+                      xv_step - g.xv, p))
+          reinterpret_cast<float*>(xv_step + 256)[(ch >> 2) & 3] = gsum;
+      }
     }
   }
 }

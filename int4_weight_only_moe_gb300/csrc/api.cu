@@ -22,6 +22,7 @@ struct moe_w4a16_ctx {
   unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
   bool fused_small;            // MOE_W4A16_OPT_FUSED_SMALL_BATCH
+  int gemv_small;              // MOE_W4A16_OPT_GEMV_SMALL_BATCH (0 never, 1 small batches, 2 one token)
   int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
   uint8_t* w2p;
@@ -83,7 +84,7 @@ const void* pinned_device_pointer(const void* p) {
 }
 
 struct WsLayout {
-  size_t hdr, tickets, sched, sorted, rowexp, tiles, expert_tiles, xs, hbuf, scratch, acc, total;
+  size_t hdr, tickets, sched, sorted, rowexp, tiles, expert_tiles, xs, hbuf, scratch, acc, xv1, xv2, total;
   int Pcap, Gcap;
 };
 
@@ -125,6 +126,13 @@ WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   off = align_up(off + static_cast<size_t>(kMaxCtas) * 2 * kBNMax * kBM * sizeof(float), 1024);
   L.acc = off;
   off = align_up(off + static_cast<size_t>(M) * h->K * sizeof(float), 1024);
+  // small batches (at most 32 routed slots, the CUDA-core path): the gathered
+  // hidden rows and the intermediate as step rows (layout.cuh)
+  const size_t xv_rows = MK <= 32 ? static_cast<size_t>(L.Pcap) : 0;
+  L.xv1 = off;
+  off = align_up(off + xv_rows * (h->K / 128) * kXvStepBytes, 1024);
+  L.xv2 = off;
+  off = align_up(off + xv_rows * (h->N / 128) * kXvStepBytes, 1024);
   L.total = off;
   return L;
 }
@@ -172,11 +180,13 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->group = group_size;
   h->pdl = true;
   h->fused_small = false;
+  h->gemv_small = 2;
   h->step_cost[0] = kDefaultStepCostGateUp;
   h->step_cost[1] = kDefaultStepCostDown;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
   if (e == cudaSuccess) e = gemm_set_attributes();
+  if (e == cudaSuccess) e = gemv_set_attributes();
   if (e == cudaSuccess) e = align_set_attributes(E);
   if (e != cudaSuccess) {
     delete h;
@@ -351,6 +361,10 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
     case MOE_W4A16_OPT_FUSED_SMALL_BATCH:
       h->fused_small = value != 0;
       return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_GEMV_SMALL_BATCH:
+      if (value < 0 || value > 2) return fail(MOE_W4A16_INVALID_ARG, "GEMV option must be 0, 1 or 2");
+      h->gemv_small = value;
+      return MOE_W4A16_OK;
     case MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES:
       h->test_never_wait = value != 0;
       return MOE_W4A16_OK;
@@ -480,6 +494,20 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   // steps, so the steps per unit must allow that; at most one CTA per SM).
   const bool fused = h->fused_small && MK <= 32 && !logits && h->num_ctas <= h->num_sms &&
                      (static_cast<long long>(2 * h->N / kBM) * (h->K / (2 * kBK))) % 4 == 0;
+  // Small batch otherwise: both products as CUDA-core matrix-vector products
+  // (tiles of at most 4 token rows per expert) -- by default for a single token,
+  // where they were measured faster than the tensor-core kernels -- else on the
+  // tensor cores.
+  const bool gemv = !fused && MK <= 32 && (h->gemv_small == 1 || (h->gemv_small == 2 && M == 1));
+  uint8_t* xv1 = ws + L.xv1;
+  uint8_t* xv2 = ws + L.xv2;
+  const long long xv1_bytes = static_cast<long long>(L.Pcap) * (h->K / 128) * kXvStepBytes;
+  const long long xv2_bytes = static_cast<long long>(L.Pcap) * (h->N / 128) * kXvStepBytes;
+  if (gemv) {
+    ga.xv = xv1;
+    ga.xv_steps = h->K / 128;
+    ga.xs_bytes = xv1_bytes;  // (the extent the rows are written into)
+  }
   if (fused) {
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
   } else if (MK <= 32) {
@@ -509,6 +537,17 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   // start their weight streams without waiting for the routing + gather launch
   const int32_t* small_ids = (MK <= 32 && !logits) ? topk_ids : nullptr;
   g1.small_ids = small_ids;
+  if (gemv) {
+    // the GEMV kernels route from the ids themselves; routed in-launch, they are
+    // the preceding kernel's output
+    g1.small_ids = topk_ids;
+    g1.ids_after_pdl = logits ? 1 : 0;
+    g1.xv_in = xv1;
+    g1.xv_bytes = xv1_bytes;
+    g1.xv_out = xv2;
+    g1.xv_out_bytes = xv2_bytes;
+    g1.Pcap = L.Pcap;
+  }
   g1.e_begin = h->e_begin;
   g1.E_total = h->E_total;
   g1.R = 2 * h->N / kBM;
@@ -529,7 +568,10 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g1.E = h->E;
   g1.dbg = hdr + 8;
   g1.sched = (sched && h->step_cost[0] > 0) ? sched : nullptr;
-  if (!fused) MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
+  if (gemv)
+    MOE_CUDA_TRY(launch_gemv_gateup(g1, h->num_ctas, s, pdl));
+  else if (!fused)
+    MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
   GemmArgs g2{};
@@ -562,6 +604,13 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.E = h->E;
   g2.dbg = hdr + 8;
   g2.sched = (sched && h->step_cost[1] > 0) ? sched + (h->num_ctas + 1) : nullptr;
+  if (gemv) {
+    g2.small_ids = topk_ids;
+    g2.ids_after_pdl = logits ? 1 : 0;
+    g2.xv_in = xv2;
+    g2.xv_bytes = xv2_bytes;
+    g2.Pcap = L.Pcap;
+  }
   if (fused) {
     // the counters live in the handle (zero between calls); the kernel writes the
     // workspace header itself at the end
@@ -584,6 +633,8 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
     P.topk = h->topk;
     g2.prep = P;
     MOE_CUDA_TRY(launch_gemm_fused(g1, g2, h->num_ctas, s, false));
+  } else if (gemv) {
+    MOE_CUDA_TRY(launch_gemv_down(g2, h->num_ctas, s, pdl));
   } else {
     MOE_CUDA_TRY(launch_gemm_down(g2, h->num_ctas, s, pdl));
   }

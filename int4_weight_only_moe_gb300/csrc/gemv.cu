@@ -1,0 +1,700 @@
+// The two expert products of a small batch (at most 32 routed slots) on the CUDA
+// cores: with one to four tokens per expert each product is a matrix-vector
+// product, bound by the packed weight stream, so the weights are dequantised and
+// multiplied in registers instead of being written to tensor memory for an MMA
+// whose 16-column token tile would be mostly padding.
+//
+//   gate/up:  [g; u] = W1[e] . x_t, epilogue h = SiLU(g) * u -> fp16 intermediate
+//             (blocked layout) and the per-group sums of h the down product needs
+//   down:     y = W2[e] . h_r, epilogue acc[t] += topk_weight * y (fp32 red.add)
+//
+// Arithmetic. A packed word holds eight 4-bit codes u of consecutive reduction
+// elements; one three-input logic op (after a shift for three of the four pairs)
+// turns a pair into the fp16 pair 16 + u, exactly. The products (16 + u) * x are
+// exact in fp32 (5 x 11 significant bits) and summed over the scale group of 32
+// elements in fp32 with mixed-precision fma (f16 operands, f32 addend). The
+// group's contribution is then
+//     sum_k (u_k - 8) s x_k  =  s * (sum_k (16 + u_k) x_k  -  24 * X),
+// with X = sum_k x_k over the group (written alongside the operand rows by the
+// kernel that produces them: the routing + gather kernel for the hidden states,
+// the gate/up epilogue for h). The subtraction cancels about 5 of fp32's 24
+// bits, far below the fp16 rounding of the operands and the bf16 output.
+//
+// Per CTA (one per SM), 24 warps, the same work on every SM sub-partition (warp
+// w runs on sub-partition w % 4):
+//   warps 0..15  multiply: warp (quad = w % 4, phase = w / 4) takes weight rows
+//                32*quad .. +31 of the steps phase, phase + 4, ... of this CTA's
+//                share, from two shared-memory rings: packed weights (10 chunks
+//                of 2 steps, 18 KB bulk copies) and activation step rows with
+//                their group sums (3 chunks of 8 steps, one copy per token row).
+//                At the end of a unit each warp leaves its partial sums in a
+//                reduction slot.
+//   warps 16..19 copy producers, one per sub-partition: producer q issues the
+//                activation copies of chunks q, q + 4, ... and the weight copies
+//                of chunks q, q + 4, ... (the ring's first 10 weight chunks are
+//                issued at the start by multiply warps 0..9, one each: they wait
+//                for nothing, not even the preceding kernel), in the order of the
+//                step each copy feeds. A warp that issues bulk copies slows the
+//                multiply warps of its sub-partition (each copy instruction costs
+//                it about 135 issue cycles, whatever its size), and the slowest
+//                sub-partition sets the rings' pace: so the copies are few (a
+//                chunk of 8 activation steps is one copy per row) and spread over
+//                all four sub-partitions.
+//   warps 20..23 epilogue: sums the 4 phases' partials in a fixed order, finishes
+//                split units (gate/up: per-CTA scratch slot + ticket, summed in
+//                CTA order by the last contributor), applies SiLU*up or the
+//                weighted scatter-add
+//
+// Work split: the same stream-K split as the tensor-core kernel (units (tile,
+// 128-row weight tile) of K/128 steps laid end to end, an equal contiguous share
+// per CTA). Every wait is bounded; a wait that gives up raises the CTA's abort
+// flag and records MOE_W4A16_STATUS_TIMEOUT, and every role falls through to the
+// teardown, which lets the copies in flight land.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.cuh"
+#include "small_route.cuh"
+#include "stream_k.cuh"
+
+namespace moe {
+
+// Optional timeline for performance work (built with -DMOE_GEMM_TRACE): every CTA
+// records global-timer stamps of a few events (latest wins), and CTA 0 per-step
+// stamps of one multiply warp and of the weight producer; read back with
+// moe_gemv_trace_read(). Compiled out otherwise.
+#ifdef MOE_GEMM_TRACE
+__device__ unsigned long long g_gv_cta[2][256][16];
+__device__ unsigned long long g_gv_steps[2][8][1024];
+extern "C" int moe_gemv_trace_read(unsigned long long* cta, unsigned long long* steps, int reset) {
+  int e = static_cast<int>(cudaMemcpyFromSymbol(cta, g_gv_cta, sizeof(g_gv_cta)));
+  if (e == 0) e = static_cast<int>(cudaMemcpyFromSymbol(steps, g_gv_steps, sizeof(g_gv_steps)));
+  if (reset) {
+    static unsigned long long z[2 * 8 * 1024];
+    cudaMemcpyToSymbol(g_gv_cta, z, sizeof(g_gv_cta));
+    cudaMemcpyToSymbol(g_gv_steps, z, sizeof(g_gv_steps));
+  }
+  return e;
+}
+__device__ __forceinline__ unsigned long long gv_timer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define GV_STAMP(ev) \
+  do { if (blockIdx.x < 256) atomicMax(&g_gv_cta[kMode - 1][blockIdx.x][(ev)], gv_timer()); } while (0)
+#define GV_POINT(slot, idx) \
+  do { if (blockIdx.x == 0 && (idx) < 1024) g_gv_steps[kMode - 1][(slot)][(idx)] = gv_timer(); } while (0)
+#else
+#define GV_STAMP(ev) do { } while (0)
+#define GV_POINT(slot, idx) do { } while (0)
+#endif
+
+namespace {
+
+constexpr int kGvPhases = 4;                              // steps in flight (one per phase)
+constexpr int kGvWarpP0 = 4 * kGvPhases;                  // 16 multiply warps, then 4 producers
+constexpr int kGvWarpEpi0 = kGvWarpP0 + 4;                // then 4 epilogue warps
+constexpr int kGvThreads = (kGvWarpEpi0 + 4) * 32;        // 768
+constexpr int kGvEpiThreads = 128;
+constexpr int kGvEpiBar = 1;                              // named barrier of the epilogue warps
+constexpr int kGvRows = 4;                                // token rows of a tile
+constexpr int kGvSub = 2;                                 // 64-element k-blocks per step
+constexpr int kGvStepBytes = kGvSub * kWBlockBytes;       // 9 KB of packed weights
+constexpr int kGvChunk = 2;                               // steps per weight copy
+constexpr int kGvChunkBytes = kGvChunk * kGvStepBytes;
+constexpr int kGvNWS = 10;                                // weight ring (chunks)
+constexpr int kGvBSteps = 8;                              // steps per activation chunk
+constexpr int kGvNB = 3;                                  // activation ring (chunks)
+constexpr int kGvBRow = kGvBSteps * kXvStepBytes;         // one token row of a chunk
+constexpr int kGvBStage = kGvRows * kGvBRow;              // [row][step][272 B]
+// barriers
+constexpr int kGbWFull = 0;                      // weight chunk landed (bulk-copy bytes)
+constexpr int kGbWEmpty = kGbWFull + kGvNWS;     // weight chunk read (4 warps x 2 steps)
+constexpr int kGbBFull = kGbWEmpty + kGvNWS;     // activation chunk landed
+constexpr int kGbBEmpty = kGbBFull + kGvNB;      // activation chunk read (4 warps x 8 steps)
+constexpr int kGbRedFull = kGbBEmpty + kGvNB;    // [2] reduction slot written (16 warps)
+constexpr int kGbRedEmpty = kGbRedFull + 2;      // [2] reduction slot read (4 epilogue warps)
+constexpr int kGbNever = kGbRedEmpty + 2;        // nothing arrives (the give-up test hook)
+constexpr int kGvNumBars = kGbNever + 1;
+
+// A tile: up to 4 consecutive padded rows of one expert (the rows the routing +
+// gather kernel wrote for its slots) and the slot of each.
+struct GvTile {
+  int e, p0, n, pad;
+  int slot[kGvRows];
+};
+static_assert(sizeof(GvTile) == 32, "tile table entry size");
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int kGsBar = 0;
+constexpr int kGsMisc = kGsBar + ((kGvNumBars * 8 + 63) / 64) * 64;
+// the last chunk / step copied into each ring slot (for the teardown's drain)
+constexpr int kGsLast = kGsMisc + 64;  // int wlast[kGvNWS], blast[kGvNB]
+constexpr int kGsTiles = kGsLast + (((kGvNWS + kGvNB) * 4 + 63) / 64) * 64;
+constexpr int kGsRed = kGsTiles + kSmallTiles * static_cast<int>(sizeof(GvTile));  // [2][phase][t][128] f32
+constexpr int kGsFin = kGsRed + 2 * kGvPhases * kGvRows * kBM * 4;                  // [t][128] f32
+constexpr int kGsW = ((kGsFin + kGvRows * kBM * 4 + 1023) / 1024) * 1024;
+constexpr int kGsB = kGsW + kGvNWS * kGvChunkBytes;
+constexpr int kGsEnd = kGsB + kGvNB * kGvBStage;
+constexpr int kGsAlloc = kGsEnd + 1024;  // (the base is aligned to 1024 inside)
+static_assert(kGsAlloc <= 227 * 1024, "shared memory budget");
+static_assert(kGvStepBytes % 16 == 0 && kGvBStage % 16 == 0 && kGsB % 16 == 0, "16-byte alignment");
+// Parity safety: a multiply warp sees every second weight chunk (its steps are 4
+// apart, 2 steps a chunk) and, with an even ring, only slots it has itself waited
+// on in their previous phase. An activation chunk is read by every multiply warp
+// (each phase has 2 of its 8 steps), so none can be refilled while a warp still
+// waits for it. The activation ring covers the weight ring's steps.
+static_assert(kGvNWS % 2 == 0 && kGvPhases == 2 * kGvChunk && kGvPhases == 4 && kGvBSteps % kGvPhases == 0 &&
+                  kGvNB * kGvBSteps >= kGvNWS * kGvChunk,
+              "ring depths");
+
+// acc += lo(v) * lo(x) + hi(v) * hi(x): two fp32 fma of fp16 operands (exact products).
+__device__ __forceinline__ void fma2_f16_f32(float& acc, uint32_t v, uint32_t x) {
+  asm("{\n\t.reg .f16 vl, vh, xl, xh;\n\t"
+      "mov.b32 {vl, vh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, vl, xl, %0;\n\t"
+      "fma.rn.f32.f16 %0, vh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(v), "r"(x));
+}
+__device__ __forceinline__ uint32_t pair16(uint32_t a) {  // (a & codes) | fp16 16.0 in both halves
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(0x03C003C0u), "r"(0x4C004C00u));
+  return d;
+}
+
+// One step (128 reduction elements) of weight row r for token rows T0 .. T0+T-1
+// of the tile: the four scale groups of the step, each summed over its 32
+// elements, then scaled. (At most two rows per call: more would not fit the 80
+// registers a thread of this CTA has without spilling; three and four rows take
+// two calls.) w: the step's packed weights; x: the step's row 0 in the activation
+// stage (row t at + t * kGvBRow: 128 fp16 values, then 4 fp32 group sums). Plain
+// loads (not volatile asm), so the compiler can issue a group's loads together;
+// the barrier waits before a step carry memory clobbers, so no load moves across
+// them. The groups run one after another (not unrolled): unrolled, the compiler
+// hoists every group's loads past the register budget.
+template <int T, int T0>
+__device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int r, float (&acc)[kGvRows]) {
+  static_assert(T >= 1 && T <= 2 && T0 + T <= kGvRows, "rows per call");
+#pragma unroll 1
+  for (int gi = 0; gi < 4; ++gi) {
+    // group gi: half gi % 2 of the step's k-block gi / 2
+    const uint8_t* blk = w + (gi >> 1) * kWBlockBytes;
+    const uint4 qv = *reinterpret_cast<const uint4*>(blk + (gi & 1) * 2048 + r * 16);
+    const uint32_t sw = *reinterpret_cast<const uint32_t*>(blk + kWCodeBytes + r * 4);
+    const float s = __half2float(__ushort_as_half(static_cast<uint16_t>((gi & 1) ? (sw >> 16) : (sw & 0xFFFFu))));
+    const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+    float part[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) part[t] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t q = w4[j];
+      const uint32_t v0 = pair16(q), v1 = pair16(q << 4), v2 = pair16(q >> 4),
+                     v3 = pair16(__funnelshift_l(q, q, 8));  // code pairs (0,1) (2,3) (4,5) (6,7)
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + (T0 + t) * kGvBRow + gi * 64 + j * 16);
+        fma2_f16_f32(part[t], v0, xv.x);
+        fma2_f16_f32(part[t], v1, xv.y);
+        fma2_f16_f32(part[t], v2, xv.z);
+        fma2_f16_f32(part[t], v3, xv.w);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const float X = *reinterpret_cast<const float*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
+      acc[T0 + t] = fmaf(s, fmaf(-24.0f, X, part[t]), acc[T0 + t]);
+    }
+  }
+}
+
+// The same with the step's codes and scales already in registers (q0..q3 = group
+// g's 4 words, sc01 / sc23 the scale words of the two k-blocks). The groups run
+// one after another, the registers rotating, so that no array is indexed by the
+// loop counter.
+template <int T, int T0>
+__device__ __forceinline__ void gv_step_regs(uint4 q0, uint4 q1, uint4 q2, uint4 q3, uint32_t sc01, uint32_t sc23,
+                                             const uint8_t* x, float (&acc)[kGvRows]) {
+  static_assert(T >= 1 && T <= 2 && T0 + T <= kGvRows, "rows per call");
+  uint32_t sw = sc01;
+#pragma unroll 1
+  for (int gi = 0; gi < 4; ++gi) {
+    const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(sw & 0xFFFFu)));
+    const uint32_t w4[4] = {q0.x, q0.y, q0.z, q0.w};
+    float part[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) part[t] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w = w4[j];
+      const uint32_t v0 = pair16(w), v1 = pair16(w << 4), v2 = pair16(w >> 4), v3 = pair16(__funnelshift_l(w, w, 8));
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + (T0 + t) * kGvBRow + gi * 64 + j * 16);
+        fma2_f16_f32(part[t], v0, xv.x);
+        fma2_f16_f32(part[t], v1, xv.y);
+        fma2_f16_f32(part[t], v2, xv.z);
+        fma2_f16_f32(part[t], v3, xv.w);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const float X = *reinterpret_cast<const float*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
+      acc[T0 + t] = fmaf(s, fmaf(-24.0f, X, part[t]), acc[T0 + t]);
+    }
+    q0 = q1;
+    q1 = q2;
+    q2 = q3;
+    sw = (gi == 1) ? sc23 : (sw >> 16);
+  }
+}
+
+// The CTA's step sequence in closed form: sequence index `it` -> (unit, step of
+// the unit), in SegIter's order (the unit the share starts inside, the unit it
+// ends inside, then the whole units), plus the end of that unit's steps within
+// the share. Any thread can map any step without walking the sequence.
+struct GvSeq {
+  long long u0, u1, uw, len0, len1;
+  int KBn, kb00;
+  __device__ GvSeq(long long begin, long long end, int kbn) : KBn(kbn) {
+    u0 = begin / KBn;
+    u1 = end > begin ? (end - 1) / KBn : u0;
+    const bool p0 = end > begin && (begin > u0 * KBn || end < (u0 + 1) * KBn);
+    const bool p1 = end > begin && u1 != u0 && end < (u1 + 1) * KBn;
+    kb00 = static_cast<int>(begin - u0 * KBn);
+    len0 = p0 ? ((end < (u0 + 1) * KBn ? end : (u0 + 1) * KBn) - begin) : 0;
+    len1 = p1 ? end - u1 * KBn : 0;
+    uw = p0 ? u0 + 1 : u0;
+  }
+  __device__ __forceinline__ void at(long long it, long long& u, int& kb, int& kb_end) const {
+    if (it < len0) {
+      u = u0;
+      kb = kb00 + static_cast<int>(it);
+      kb_end = kb00 + static_cast<int>(len0);
+    } else if (it < len0 + len1) {
+      u = u1;
+      kb = static_cast<int>(it - len0);
+      kb_end = static_cast<int>(len1);
+    } else {
+      const long long j = it - len0 - len1;
+      u = uw + j / KBn;
+      kb = static_cast<int>(j % KBn);
+      kb_end = KBn;
+    }
+  }
+};
+
+// kMode 1: gate/up + SwiGLU; 2: down + weighted scatter-add.
+template <int kMode>
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  auto bar = [&](int i) -> uint32_t { return base + kGsBar + static_cast<uint32_t>(i) * 8u; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kGsMisc);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(gbase + kGsMisc + 4);
+  int* ntiles_sm = reinterpret_cast<int*>(gbase + kGsMisc + 8);
+  volatile int* epi_ok = reinterpret_cast<volatile int*>(gbase + kGsMisc + 16);  // [2][4]
+  GvTile* tiles = reinterpret_cast<GvTile*>(gbase + kGsTiles);
+  float* red = reinterpret_cast<float*>(gbase + kGsRed);
+  float* fin = reinterpret_cast<float*>(gbase + kGsFin);
+  const uint32_t sW = base + kGsW, sB = base + kGsB;
+  int* wlast = reinterpret_cast<int*>(gbase + kGsLast);
+  int* blast = wlast + kGvNWS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t wait_ns = a.wait_kcycles;
+  int* status = a.status;
+  if (threadIdx.x == 0) GV_STAMP(0);
+
+  // Tiles of the batch from the caller's topk_ids (warp 0): every expert's slots,
+  // in the padded rows the routing + gather kernel placed them in (16 per expert
+  // and row group), cut into tiles of at most 4 rows, experts in id order.
+  if (warp == 0) {
+    if (a.ids_after_pdl) pdl_wait();  // the ids are the preceding kernel's output
+    const int v = lane < a.MK ? a.small_ids[lane] : -1;
+    const SmallRoute r = small_route_ids(v, a.MK, a.E, kRowGroup, kBNMax, lane, a.e_begin, a.E_total);
+    const int nt = r.leader ? (r.cnt + kGvRows - 1) / kGvRows : 0;
+    const int lead_e = r.leader ? r.e : -1;
+    int t0 = 0, tot = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, lead_e, j);
+      const int nj = __shfl_sync(0xffffffffu, nt, j);
+      if (ej >= 0) {
+        tot += nj;
+        if (ej < r.e) t0 += nj;
+      }
+    }
+    if (r.e >= 0 && r.seg + r.rank < kSmallPadRows) {
+      const int ti = t0 + r.rank / kGvRows;
+      if (ti < kSmallTiles) {
+        GvTile& tl = tiles[ti];
+        if (r.rank % kGvRows == 0) {
+          tl.e = r.e;
+          tl.p0 = r.seg + r.rank;
+          tl.n = r.cnt - r.rank < kGvRows ? r.cnt - r.rank : kGvRows;
+        }
+        tl.slot[r.rank % kGvRows] = lane;
+      }
+    }
+    if (lane == 0) *ntiles_sm = tot < kSmallTiles ? tot : kSmallTiles;
+    if (lane == 0) GV_STAMP(9);
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < kGvNWS; ++i) {
+      mbar_init(bar(kGbWFull + i), 1);
+      mbar_init(bar(kGbWEmpty + i), 4 * kGvChunk);
+      wlast[i] = -1;
+    }
+    for (int i = 0; i < kGvNB; ++i) {
+      mbar_init(bar(kGbBFull + i), 1);
+      mbar_init(bar(kGbBEmpty + i), 4 * kGvBSteps);
+      blast[i] = -1;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kGbRedFull + i), 4 * kGvPhases);
+      mbar_init(bar(kGbRedEmpty + i), 4);
+    }
+    mbar_init(bar(kGbNever), 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+    GV_STAMP(10);
+  }
+  if (threadIdx.x == 64) GV_STAMP(11);
+  __syncthreads();
+
+  const int ntiles = *ntiles_sm;
+  const int G = static_cast<int>(gridDim.x);
+  const Sched sc{static_cast<long long>(ntiles) * a.R * a.KBn, G, nullptr, 1};
+  const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
+  const long long n_it = my_end - my_begin;
+  const GvSeq seq(my_begin, my_end, a.KBn);
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) GV_STAMP(1);
+
+  const long long n_chunks = (n_it + kGvChunk - 1) / kGvChunk;
+  // Copy weight chunk c (steps 2c, 2c + 1 of the sequence) into its ring slot.
+  auto issue_w = [&](long long c) {
+    const int s = static_cast<int>(c % kGvNWS);
+    const long long it0 = c * kGvChunk;
+    const long long it1 = it0 + kGvChunk < n_it ? it0 + kGvChunk : n_it;
+    wlast[s] = static_cast<int>(c);
+    mbar_arrive_expect_tx(bar(kGbWFull + s), static_cast<uint32_t>(it1 - it0) * kGvStepBytes);
+    GV_POINT(0, c);
+    if (c == 0) GV_STAMP(8);
+    const uint64_t w_policy = l2_policy_evict_first();  // read once: keep L2 for the operands
+    for (long long it = it0; it < it1;) {
+      long long u;
+      int kb, kbe;
+      seq.at(it, u, kb, kbe);
+      const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
+      const int e = tiles[u / a.R].e;
+      const int rt = static_cast<int>(u % a.R);
+      const long long woff = ((static_cast<long long>(e) * a.R + rt) * a.KBn + kb) * kGvStepBytes;
+      if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kGvStepBytes <= a.wpack_bytes && e >= 0 &&
+                        e < a.E && run >= 1,
+                    a.status, a.dbg, 41, woff, run))
+        bulk_g2s_hint(sW + s * kGvChunkBytes + static_cast<uint32_t>(it - it0) * kGvStepBytes, a.wpack + woff,
+                      static_cast<uint32_t>(run) * kGvStepBytes, bar(kGbWFull + s), w_policy);
+      it += run;
+    }
+  };
+
+  if (warp >= kGvWarpP0 && warp < kGvWarpEpi0) {
+    // ------------------------------------------------ copy producers
+    if (lane == 0) {
+      const int q = warp - kGvWarpP0;  // (= this warp's sub-partition)
+      // activation rows: the preceding kernel's output
+      bool b_ready = false;
+      const long long n_bchunks = (n_it + kGvBSteps - 1) / kGvBSteps;
+      long long nb = q, nw = q;  // next activation chunk, next weight chunk of this producer
+      while (nw < kGvNWS) nw += 4;  // (the multiply warps copy the ring's first chunks)
+      while (nb < n_bchunks || nw < n_chunks) {
+        // the copy feeding the earlier step first: a wait then only depends on
+        // steps whose copies were issued before it
+        if (nb < n_bchunks && (nw >= n_chunks || nb * kGvBSteps <= nw * kGvChunk)) {
+          if (!b_ready) {
+            if (!a.ids_after_pdl) pdl_wait();
+            if (q == 0) GV_STAMP(2);
+            b_ready = true;
+          }
+          const int s = static_cast<int>(nb % kGvNB);
+          if (!mbar_wait(bar(kGbBEmpty + s), static_cast<uint32_t>((nb / kGvNB) & 1) ^ 1u, abort_flag, status,
+                         kStatusTimeout, wait_ns))
+            break;
+          const long long it0 = nb * kGvBSteps;
+          const long long it1 = it0 + kGvBSteps < n_it ? it0 + kGvBSteps : n_it;
+          // the chunk's pieces (one per unit it touches): their bytes, then the copies
+          uint32_t bytes = 0;
+          for (long long it = it0; it < it1;) {
+            long long u;
+            int kb, kbe;
+            seq.at(it, u, kb, kbe);
+            const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
+            bytes += static_cast<uint32_t>(tiles[u / a.R].n * run * kXvStepBytes);
+            it += run;
+          }
+          blast[s] = static_cast<int>(nb);
+          mbar_arrive_expect_tx(bar(kGbBFull + s), bytes);
+          for (long long it = it0; it < it1;) {
+            long long u;
+            int kb, kbe;
+            seq.at(it, u, kb, kbe);
+            const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
+            const GvTile& tl = tiles[u / a.R];
+            for (int t = 0; t < tl.n; ++t) {
+              const long long xoff = (static_cast<long long>(tl.p0 + t) * a.KBn + kb) * kXvStepBytes;
+              if (MOE_CHECK(xoff >= 0 && xoff + static_cast<long long>(run) * kXvStepBytes <= a.xv_bytes &&
+                                tl.n <= kGvRows,
+                            a.status, a.dbg, 42, xoff, run))
+                bulk_g2s(sB + static_cast<uint32_t>(s) * kGvBStage + t * kGvBRow +
+                             static_cast<uint32_t>(it - it0) * kXvStepBytes,
+                         a.xv_in + xoff, static_cast<uint32_t>(run) * kXvStepBytes, bar(kGbBFull + s));
+            }
+            it += run;
+          }
+          nb += 4;
+        } else {
+          const int s = static_cast<int>(nw % kGvNWS);
+          if (!mbar_wait(bar(kGbWEmpty + s), static_cast<uint32_t>((nw / kGvNWS) & 1) ^ 1u, abort_flag, status,
+                         kStatusTimeout, wait_ns))
+            break;
+          issue_w(nw);
+          nw += 4;
+        }
+      }
+    }
+  } else if (warp < kGvWarpP0) {
+    // ------------------------------------------------ multiply
+    // the weight ring's first chunks: one copy per warp, nothing to wait for
+    if (lane == 0 && warp < kGvNWS && warp < n_chunks) issue_w(warp);
+    __syncwarp();
+    const int quad = warp & 3;
+    const int phase = warp >> 2;
+    const int r = quad * 32 + lane;
+    SegIter si(my_begin, my_end, a.KBn);
+    long long u;
+    int kb0, kb1;
+    uint32_t it_base = 0, ru = 0;
+    bool ok = true;
+    while (ok && si.next(u, kb0, kb1)) {
+      const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
+      const GvTile& tl = tiles[u / a.R];
+      const int T = tl.n;
+      float acc[kGvRows] = {0.f, 0.f, 0.f, 0.f};
+      for (uint32_t it = it_base + ((static_cast<uint32_t>(phase) - it_base) & 3u); it < it_base + len;
+           it += kGvPhases) {
+        const uint32_t c = it >> 1;
+        const uint32_t ws = c % kGvNWS, wpar = (c / kGvNWS) & 1u;
+        const uint32_t cb = it / kGvBSteps;
+        const uint32_t sb = cb % kGvNB, bpar = (cb / kGvNB) & 1u;
+        bool w_ok = mbar_wait(bar(kGbWFull + ws), wpar, abort_flag, status, kStatusTimeout, wait_ns);
+        if (warp == 0 && lane == 0) {
+          GV_POINT(1, it >> 2);
+          if (it < 4) GV_STAMP(3);
+        }
+        w_ok = w_ok && mbar_wait(bar(kGbBFull + sb), bpar, abort_flag, status, kStatusTimeout, wait_ns);
+        if (warp == 0 && lane == 0) {
+          GV_POINT(2, it >> 2);
+          if (it < 4) GV_STAMP(4);
+        }
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* wstep = gbase + kGsW + ws * kGvChunkBytes + (it & 1u) * kGvStepBytes;
+        const uint8_t* xst = gbase + kGsB + sb * kGvBStage + (it % kGvBSteps) * kXvStepBytes;
+        if (T == 1) {
+          gv_step<1, 0>(wstep, xst, r, acc);
+        } else {
+          gv_step<2, 0>(wstep, xst, r, acc);
+          if (T == 3) gv_step<1, 2>(wstep, xst, r, acc);
+          if (T == 4) gv_step<2, 2>(wstep, xst, r, acc);
+        }
+        __syncwarp();  // every lane has read the step's shared memory
+        if (lane == 0) {
+          mbar_arrive(bar(kGbWEmpty + ws));
+          mbar_arrive(bar(kGbBEmpty + sb));
+        }
+        if (warp == 0 && lane == 0) {
+          GV_POINT(3, it >> 2);
+          GV_STAMP(5);
+        }
+        if (warp > 0 && warp < 4 && lane == 0) GV_POINT(3 + warp, it >> 2);
+      }
+      if (!ok) break;
+      it_base += len;
+      // this warp's share of the unit's sums (zero where it had no step)
+      const uint32_t rs = ru & 1u, rpar = (ru >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kGbRedEmpty + rs), rpar ^ 1, abort_flag, status,
+                                               kStatusTimeout, wait_ns)))
+        break;
+      float* dst = red + ((rs * kGvPhases + phase) * kGvRows) * kBM + r;
+#pragma unroll
+      for (int t = 0; t < kGvRows; ++t) dst[t * kBM] = acc[t];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kGbRedFull + rs));
+      ++ru;
+    }
+  } else {
+    // ------------------------------------------------ epilogue
+    pdl_wait();  // exponents, zeroed accumulator and tickets, routing weights
+    // Test hook: wait on a barrier that nothing arrives on (gives up, raises the
+    // abort flag and records the timeout).
+    if (a.test_never_wait) mbar_wait(bar(kGbNever), 0, abort_flag, a.status, kStatusTimeout, wait_ns);
+    const int tid = threadIdx.x - kGvWarpEpi0 * 32;  // = the weight row this thread sums
+    const int ew = tid >> 5;
+    SegIter si(my_begin, my_end, a.KBn);
+    long long u;
+    int kb0, kb1;
+    uint32_t ru = 0;
+    bool sat = false;
+    while (si.next(u, kb0, kb1)) {
+      const GvTile tl = tiles[u / a.R];
+      const int T = tl.n;
+      const int rt = static_cast<int>(u % a.R);
+      const uint32_t rs = ru & 1u, rpar = (ru >> 1) & 1u;
+      const bool w_ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbRedFull + rs), rpar, abort_flag, status,
+                                                          kStatusTimeout, wait_ns));
+      if (lane == 0) epi_ok[(ru & 1u) * 4 + ew] = w_ok ? 1 : 0;
+      named_bar_sync(kGvEpiBar, kGvEpiThreads);
+      const bool all_ok = epi_ok[(ru & 1u) * 4 + 0] && epi_ok[(ru & 1u) * 4 + 1] &&
+                          epi_ok[(ru & 1u) * 4 + 2] && epi_ok[(ru & 1u) * 4 + 3];
+      if (!all_ok) break;
+      // the unit's sums over this CTA's steps: the four phases in order
+      float v[kGvRows];
+#pragma unroll
+      for (int t = 0; t < kGvRows; ++t) {
+        const float* src = red + ((rs * kGvPhases) * kGvRows + t) * kBM + tid;
+        v[t] = ((src[0] + src[kGvRows * kBM]) + src[2 * kGvRows * kBM]) + src[3 * kGvRows * kBM];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kGbRedEmpty + rs));
+      ++ru;
+      if (tid == 0) GV_STAMP(6);
+
+      if (kMode == 2) {
+#pragma unroll
+        for (int t = 0; t < kGvRows; ++t) {
+          if (t >= T) break;
+          const int slot = tl.slot[t];
+          int e = a.rowexp[tl.p0 + t];
+          e = e < -kMaxRowExp ? -kMaxRowExp : (e > kMaxRowExp ? kMaxRowExp : e);
+          const float wt = a.topk_weights[slot] * exp2_int(2 * e);
+          const long long ai = static_cast<long long>(slot / a.topk) * a.Kout + static_cast<long long>(rt) * kBM + tid;
+          if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 43, ai, slot)) atomicAdd(a.acc + ai, wt * v[t]);
+        }
+        continue;
+      }
+      // gate/up: a unit cut between CTAs is finished by its last contributor
+      bool write_tile = kb0 == 0 && kb1 == a.KBn;
+      if (!write_tile) {
+        const long long ustart = u * a.KBn;
+        const int part = (sc.start(blockIdx.x) < ustart) ? 1 : 0;
+        float* slot = a.scratch + (static_cast<long long>(blockIdx.x) * 2 + part) * kBNMax * kBM;
+#pragma unroll
+        for (int t = 0; t < kGvRows; ++t)
+          if (t < T && MOE_CHECK((slot - a.scratch) + t * kBM + tid < a.scratch_elems, a.status, a.dbg, 44,
+                                 blockIdx.x, t))
+            __stcg(slot + t * kBM + tid, v[t]);
+        __threadfence();
+        named_bar_sync(kGvEpiBar, kGvEpiThreads);
+        const int c0 = sc.cta_of(ustart), c1 = sc.cta_of(ustart + a.KBn - 1);
+        if (tid == 0) {
+          const int add = kb1 - kb0;
+          const int old = atomicAdd(a.tickets + c0, add);
+          *last_flag = (old + add == a.KBn) ? 1 : 0;
+        }
+        named_bar_sync(kGvEpiBar, kGvEpiThreads);
+        write_tile = *last_flag != 0;
+        if (write_tile) {
+          __threadfence();
+#pragma unroll
+          for (int t = 0; t < kGvRows; ++t) v[t] = 0.f;
+          for (int cc = c0; cc <= c1; ++cc) {
+            if (sc.start(cc) == sc.start(cc + 1)) continue;  // empty share: no partial
+            const int pc = (sc.start(cc) < ustart) ? 1 : 0;
+            const float* sl = a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
+#pragma unroll
+            for (int t = 0; t < kGvRows; ++t)
+              if (t < T) v[t] += __ldcg(sl + t * kBM + tid);
+          }
+        }
+      }
+      if (write_tile) {
+        // h = SiLU(g) * u for the tile's 64 features: rows 2i (gate) and 2i + 1 (up)
+#pragma unroll
+        for (int t = 0; t < kGvRows; ++t) fin[t * kBM + tid] = v[t];
+        named_bar_sync(kGvEpiBar, kGvEpiThreads);
+        const int f = tid & 63;  // feature within the tile; a warp holds 32 of one token
+        for (int t = tid >> 6; t < T; t += 2) {
+          const int p = tl.p0 + t;
+          const int e_raw = a.rowexp[p];
+          const int e = e_raw < -kMaxRowExp ? -kMaxRowExp : (e_raw > kMaxRowExp ? kMaxRowExp : e_raw);
+          const float sc_e = exp2_int(e);
+          const float g = fin[t * kBM + 2 * f] * sc_e;
+          const float uu = fin[t * kBM + 2 * f + 1] * sc_e;
+          const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
+          float hv = g * sig * uu * exp2_int(-2 * e);
+          sat = sat || fabsf(hv) > 65504.0f;
+          hv = fminf(fmaxf(hv, -65504.0f), 65504.0f);
+          const __half hh = __float2half_rn(hv);
+          const long long hoff = (static_cast<long long>(rt) * a.Gcap + p / kRowGroup) * kRowGroupBytes +
+                                 blocked_offset(p % kRowGroup, f);
+          if (MOE_CHECK(hoff >= 0 && hoff + 2 <= a.hout_bytes, a.status, a.dbg, 45, hoff, p))
+            *reinterpret_cast<__half*>(a.hout + hoff) = hh;
+          // h as a step row of the down product (its step rt / 2 holds this tile's
+          // 64 features at (rt % 2) * 64), and the sum of each group of 32 (as stored)
+          uint8_t* xs = a.xv_out + (static_cast<long long>(p) * (a.R / 2) + (rt >> 1)) * kXvStepBytes;
+          const bool xs_ok = MOE_CHECK((xs - a.xv_out) + kXvStepBytes <= a.xv_out_bytes, a.status, a.dbg, 46,
+                                       xs - a.xv_out, p);
+          if (xs_ok) *reinterpret_cast<__half*>(xs + ((rt & 1) * 64 + f) * 2) = hh;
+          float gs = __half2float(hh);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+          if (lane == 0 && xs_ok) reinterpret_cast<float*>(xs + 256)[2 * (rt & 1) + (f >> 5)] = gs;
+        }
+        named_bar_sync(kGvEpiBar, kGvEpiThreads);  // fin is reused by the next tile
+      }
+    }
+    if (__any_sync(0xffffffffu, sat) && lane == 0) atomicOr(status, kStatusHSaturated);
+  }
+
+  // ------------------------------------------------ teardown
+  // Every copy issued is waited for by its readers unless a wait gave up: let the
+  // latest copy into every slot land before shared memory is released.
+  __syncwarp();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGvNWS; ++i)
+      if (wlast[i] >= 0) mbar_wait_drain(bar(kGbWFull + i), static_cast<uint32_t>((wlast[i] / kGvNWS) & 1));
+    for (int i = 0; i < kGvNB; ++i)
+      if (blast[i] >= 0) mbar_wait_drain(bar(kGbBFull + i), static_cast<uint32_t>((blast[i] / kGvNB) & 1));
+    GV_STAMP(7);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+static cudaError_t launch_gemv(void (*kernel)(GemmArgs), const GemmArgs& a, int num_ctas, cudaStream_t stream,
+                               bool pdl) {
+  return launch_k(kernel, dim3(static_cast<unsigned>(num_ctas)), dim3(kGvThreads), kGsAlloc, stream, pdl, a);
+}
+cudaError_t launch_gemv_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
+  return launch_gemv(gemv_kernel<1>, a, num_ctas, stream, pdl);
+}
+cudaError_t launch_gemv_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
+  return launch_gemv(gemv_kernel<2>, a, num_ctas, stream, pdl);
+}
+cudaError_t gemv_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGsAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGsAlloc);
+}
+
+}  // namespace moe

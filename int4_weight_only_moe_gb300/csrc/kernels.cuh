@@ -87,6 +87,10 @@ struct GatherArgs {
   const int32_t* perm1;
   const int32_t* topk_ids;  // expert of a slot (read only when perm1 is set)
   int e_begin;              // first expert held (the ids are the layer's)
+  // small-batch CUDA-core path: write the rows as step rows (layout.cuh, with
+  // xv_steps = K / 128 steps a row) instead of the blocked layout (null: blocked)
+  uint8_t* xv;
+  int xv_steps;
 };
 cudaError_t launch_gather(const GatherArgs& a, int max_groups, int num_sms, cudaStream_t stream,
                           bool pdl);
@@ -157,6 +161,13 @@ struct GemmArgs {
   int32_t* dbg;  // first failed check: site, values, block, thread
   const long long* sched;  // [gridDim.x + 1] weighted boundaries, used when this GEMM's
                            // bit of hdr[kHdrSched] is set (bit 0 gate/up, bit 1 down)
+  // small-batch CUDA-core kernels: the activation rows as step rows (xv_in; the
+  // gate/up kernel also writes h as step rows of the down product, xv_out)
+  const uint8_t* xv_in;
+  uint8_t* xv_out;
+  long long xv_bytes, xv_out_bytes;
+  int Pcap;
+  int ids_after_pdl;       // small_ids is the preceding kernel's output (routed in-launch)
 };
 cudaError_t launch_gemm_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
@@ -164,6 +175,11 @@ cudaError_t launch_gemm_down(const GemmArgs& a, int num_ctas, cudaStream_t strea
 cudaError_t launch_gemm_fused(const GemmArgs& a1, const GemmArgs& a2, int num_ctas, cudaStream_t stream,
                               bool pdl);
 cudaError_t gemm_set_attributes();
+// The same two products for a batch of at most 32 routed slots on the CUDA cores
+// (small_ids set; xv_in / xv_out set): tiles of at most 4 token rows per expert.
+cudaError_t launch_gemv_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
+cudaError_t launch_gemv_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
+cudaError_t gemv_set_attributes();
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
                             cudaStream_t stream, bool pdl);

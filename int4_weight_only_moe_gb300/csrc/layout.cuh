@@ -43,6 +43,13 @@ constexpr int kSmallPadRows = 32 + 32 * (kRowGroup - 1);  // their padded rows (
 constexpr int kMaxCtas = 256;       // persistent grid limit (tickets / scratch slots)
 constexpr int kMaxExperts = 1024;
 
+// Activation rows of the small-batch CUDA-core products ("step rows"): per padded
+// row p and pipeline step kb (128 reduction elements) of an operand with KBn
+// steps, 272 bytes at (p * KBn + kb) * 272: the step's 128 fp16 values in order,
+// then the fp32 sums of its four scale groups of 32. A row's steps are
+// contiguous, so one copy brings several steps of a row.
+constexpr int kXvStepBytes = 272;
+
 // Byte offset of 16-bit element (row, k) inside one 16-row group of a k-block
 // (row in [0, 16), k in [0, 64)).
 __host__ __device__ __forceinline__ uint32_t blocked_offset(int row, int k) {

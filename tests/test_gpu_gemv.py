@@ -1,0 +1,161 @@
+"""The small-batch CUDA-core path (at most 32 routed slots: tiles of at most 4
+token rows per expert, both products as matrix-vector products) against the
+oracle and against the tensor-core kernels on the same inputs, through the C-ABI.
+
+Covered: every grid size from one CTA (every unit in one CTA's sequence) to more
+CTAs than steps; experts with 1..16 rows (several 4-row tiles of one expert);
+skipped ids; a batch with no valid slot; the give-up path of both paths; and the
+intermediate activations. The two paths compute the same products; they differ
+in the order of the fp32 sums, so the intermediate may differ by one fp16 unit
+and the output accumulators by a few fp32 units of their largest magnitude."""
+import numpy as np
+import pytest
+import torch
+
+import int4_weight_only_moe_gb300 as pkg
+import oracle
+from int4_weight_only_moe_gb300 import inputs
+from tests.gpu_helpers import (Problem, assert_close, bf16_tensor_to_f64, check_accumulator, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+GEMV_DEFAULT = 2  # the CUDA-core path for single-token batches only
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def run_path(prob, hidden, ids, wts, gemv):
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, 1 if gemv else 0)
+    try:
+        got = prob.run(hidden, ids, wts)
+        status = prob.moe.status()
+        M = hidden.shape[0]
+        acc = prob.moe.accumulator(M).cpu().numpy().astype(np.float64)
+        inter = prob.moe.intermediate(M).cpu().numpy().astype(np.float64)
+        bits = inputs.f32_to_bf16_bits(got.astype(np.float32))  # (exact: got holds bf16 values)
+    finally:
+        pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, GEMV_DEFAULT)
+    return got, status, acc, inter, bits
+
+
+def compare_paths(prob, hidden, ids, wts, what, ref_ids=None):
+    ref = prob.reference(hidden, ids if ref_ids is None else ref_ids, wts)
+    g_out, g_st, g_acc, g_h, g_bits = run_path(prob, hidden, ids, wts, gemv=True)
+    t_out, t_st, t_acc, t_h, _ = run_path(prob, hidden, ids, wts, gemv=False)
+    assert g_st == t_st, (g_st, t_st)
+    if np.any(ref != 0):
+        assert_close(g_out, ref, f"{what} (CUDA cores)")
+        assert_close(t_out, ref, f"{what} (tensor cores)")
+        check_accumulator(g_acc, g_bits, ref, f"{what} (CUDA cores)")
+    else:
+        assert np.all(g_out == 0) and np.all(t_out == 0)
+    scale = float(np.abs(t_acc).max()) or 1.0
+    np.testing.assert_allclose(g_acc, t_acc, rtol=2.0 ** -10, atol=2.0 ** -12 * scale, err_msg=what)
+    hs = float(np.abs(t_h).max()) or 1.0
+    np.testing.assert_allclose(g_h, t_h, rtol=2.0 ** -10, atol=2.0 ** -24 * hs, err_msg=what + " intermediate")
+    return g_st
+
+
+@pytest.mark.parametrize("num_ctas", [None, 1, 3, 7, 64, 256])
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+def test_gemv_matches_oracle_and_tensor_cores(M, num_ctas):
+    # E=16, K=512, N=256, top-4: 4 steps per gate/up unit, 2 per down unit; 3 and 7
+    # CTAs cut units between CTAs at odd places, 256 leaves most CTAs no step
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl, step=M)
+    assert compare_paths(prob, hidden, ids, wts, f"M={M} ctas={num_ctas}") == 0
+    prob.close()
+
+
+def test_gemv_option_values():
+    # 2 (default): single-token batches only; 1: every batch of <= 32 slots; 0: never;
+    # anything else is rejected
+    prob = Problem(8, 256, 128, 2)
+    h = prob.moe.handle
+    for v in (0, 1, 2):
+        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, v)
+    with pytest.raises(pkg.MoeW4A16Error):
+        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, 3)
+    prob.close()
+
+
+@pytest.mark.parametrize("rows", [4, 5, 9, 16])
+def test_gemv_expert_with_many_rows(rows):
+    # one expert receives `rows` of the batch's slots: ceil(rows / 4) tiles of it,
+    # each streaming the expert's weights (topk 2, 16 tokens: 32 slots)
+    E, K, N, k, M = 8, 768, 384, 2, 16
+    prob = Problem(E, K, N, k, num_ctas=5)
+    rng = np.random.default_rng(rows)
+    ids = np.zeros((M, k), dtype=np.int32)
+    for t in range(M):
+        ids[t] = rng.choice(np.arange(1, E), size=k, replace=False)
+    ids[:rows, 0] = 0  # expert 0 (never drawn above) in `rows` tokens' first slot
+    hidden = inputs.hidden_states(M, K)
+    wts = rng.uniform(0.1, 1.0, size=(M, k)).astype(np.float32)
+    compare_paths(prob, hidden, ids, wts, f"{rows} rows on one expert")
+    prob.close()
+
+
+def test_gemv_skipped_ids_and_empty_batch():
+    E, K, N, k, M = 8, 512, 256, 4, 3
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    bad = ids.copy()
+    bad[0, 1] = E + 3
+    bad[2, 3] = -1
+    st = compare_paths(prob, hidden, bad, wts, "skipped ids", ref_ids=np.where(bad >= E, -1, bad))
+    assert st == pkg.STATUS_BAD_EXPERT_ID
+    none = np.full_like(ids, E + 1)
+    st = compare_paths(prob, hidden, none, wts, "no valid slot", ref_ids=np.full_like(ids, -1))
+    assert st == pkg.STATUS_BAD_EXPERT_ID
+    prob.close()
+
+
+def test_gemv_intermediate_matches_oracle():
+    # h = SiLU(gate) * up of every routed row, element by element
+    E, K, N, k, M = 8, 1024, 512, 4, 2
+    prob = Problem(E, K, N, k, num_ctas=11)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, 1)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    prob.run(hidden, ids, wts)
+    assert prob.moe.status() == 0
+    h_rows = bf16_tensor_to_f64(prob.moe.intermediate(M))
+    x = oracle.bf16_to_f64(hidden)
+    ref = np.zeros_like(h_rows)
+    for t in range(M):
+        for j in range(k):
+            w1, _ = oracle.expert_dense(*prob.w, int(ids[t, j]))
+            ref[t * k + j] = oracle.expert_hidden(x[t:t + 1], w1)[0]
+    assert_close(h_rows, ref, "intermediate (CUDA cores)", bf16_output=False)
+    prob.close()
+
+
+def test_both_small_batch_paths_give_up_cleanly():
+    # the give-up hook on each small-batch path in turn; the next call is clean
+    E, K, N, k, M = 8, 512, 256, 4, 2
+    prob = Problem(E, K, N, k)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    h = prob.moe.handle
+    for gemv in (1, 0):
+        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, gemv)
+        pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 1000)
+        pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 1)
+        prob.run(hidden, ids, wts)
+        assert prob.moe.status() & pkg.STATUS_TIMEOUT
+        pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 0)
+        pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 0)
+        got = prob.run(hidden, ids, wts)
+        assert prob.moe.status() == 0
+        assert_close(got, prob.reference(hidden, ids, wts), f"after give-up, gemv={gemv}")
+    pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, GEMV_DEFAULT)
+    prob.close()
