@@ -345,7 +345,7 @@ def run_ours(args):
     # weights and scales, the activation rows read, the intermediate written (and,
     # fused, read back) and the output accumulator.
     fused = False  # (the fused small-batch launch is off by default)
-    gemv = wl.M == 1  # (by default a single-token batch runs its products on the CUDA cores)
+    gemv = wl.M * wl.topk <= 32  # (by default such a batch runs its products on the CUDA cores)
     if fused:
         dom_name = "gemm_fused (gate/up + down, one cooperative launch)"
         dom_bytes = (active * (w1b + w2b) + wl.M * wl.K * 2 + 2 * wl.M * wl.topk * wl.N * 2
@@ -353,8 +353,8 @@ def run_ours(args):
         dom_ms = kmean[2] + kmean[3]
     elif gemv:
         # the CUDA-core gate/up kernel: weights and scales, the activation step rows
-        # (272 bytes per row and step: 128 fp16 values and 4 group sums) read, h
-        # written twice (step rows for the down kernel, blocked for read-back)
+        # (272 bytes per row and step: 128 16-bit values and 4 group headers) read,
+        # h written twice (step rows for the down kernel, blocked fp16 for read-back)
         dom_name = "gemv_gateup (CUDA cores)"
         dom_bytes = (active * w1b + wl.M * wl.topk * (wl.K // 128) * 272
                      + wl.M * wl.topk * (wl.N * 2 + (wl.N // 128) * 272))
@@ -396,9 +396,11 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "dtype_detail": "INT4 weights dequantised exactly to f16 (tensor-core operands; for a single token "
-                        "CUDA-core fma of the exact f16 products), f32 accumulate, bf16 in/out",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int32+f32" if wl.M * wl.topk <= 32 else "f16",
+        "dtype_detail": "INT4 weights: at most 32 routed slots (decode) exact int32 dot products of the codes "
+                        "with 16-bit block-fixed-point activations (CUDA cores, dp2a), one f32 rounding per "
+                        "group of 32; larger batches f16 tensor-core operands, f32 accumulate; bf16 in/out",
         "data": "synthetic (seeded random INT4 weights for all 384 experts, N(0,1) bf16 hidden, "
                 "uniform router logits -> top-8 renormalised by the library's router)",
         "config": headline_config(wl, world),

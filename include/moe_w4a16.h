@@ -129,9 +129,10 @@ int moe_w4a16_pack_ex(moe_w4a16_t h, const int32_t* w1_q, const uint16_t* w1_s,
                       const int32_t* w1_g_idx, const int32_t* w2_g_idx, void* stream);
 
 /* Bytes of device workspace that moe_w4a16_forward needs for M tokens (and any
- * smaller M). Holds the per-call routing tables, the expert-sorted activations,
- * the intermediate activations, split-K partial tiles and the fp32 output
- * accumulator. No state persists in it between calls. */
+ * smaller M) with the handle's current grid size (MOE_W4A16_OPT_NUM_CTAS: a pair
+ * of split-K partial tiles per CTA). Holds the per-call routing tables, the
+ * expert-sorted activations, the intermediate activations, split-K partial
+ * tiles and the fp32 output accumulator. No state persists in it between calls. */
 size_t moe_w4a16_workspace_size(moe_w4a16_t h, int M);
 
 /* The fused forward. Device pointers:
@@ -256,19 +257,21 @@ const char* moe_w4a16_last_error(void);
  *                            finishes); 0 (default) = two launches. Either way the
  *                            same arithmetic.
  *   MOE_W4A16_OPT_GEMV_SMALL_BATCH
- *                            how a forward with M * topk <= 32 (the fused launch
- *                            off) computes its two expert products: 2 (default) =
- *                            on the CUDA cores for a single token (M == 1), on the
- *                            tensor cores otherwise; 1 = on the CUDA cores for
- *                            every such batch; 0 = always on the tensor cores.
- *                            The CUDA-core kernels compute matrix-vector products
- *                            over tiles of at most 4 token rows per expert: the
- *                            weights are dequantised to fp16 (16 + u, exact),
- *                            multiplied with the fp16 activations into fp32, and
- *                            the -8 offset applied per scale group through the
- *                            group's activation sum. The two paths agree to fp32
- *                            rounding (about 2^-19 of a group's magnitude), not
- *                            bit for bit. */
+ *                            where a forward (the fused launch off) computes its two
+ *                            expert products on the CUDA cores instead of the
+ *                            tensor cores: 1 (default) = batches of M * topk <= 32
+ *                            routed slots; 2 = single tokens (M == 1) only; 3 =
+ *                            batches of up to 256 routed slots (on GB300 slower
+ *                            than the tensor cores beyond 32); 0 = never. The
+ *                            CUDA-core kernels compute matrix-vector products over
+ *                            tiles of at most 4 token rows per expert: activations
+ *                            as 16-bit block fixed point per scale group of 32
+ *                            (a power-of-two exponent each), products with the
+ *                            4-bit codes summed exactly in int32 (dp2a), the -8
+ *                            offset applied through the group's exact value sum,
+ *                            one fp32 rounding per group. The tensor-core kernels
+ *                            round the activations to fp16 instead; the two agree
+ *                            to about 2^-12 of the output's magnitude. */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
        MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5,
        MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7,
@@ -340,7 +343,8 @@ int moe_w4a16_schedule_debug(moe_w4a16_t h, const void* workspace, int M, int64_
  * image (MOE_W4A16_NOALLOC_WORKSPACE_BYTES), present on every GPU that loads the
  * library until the process exits. Calls whose moe_w4a16_workspace_size(h, M)
  * exceeds it are rejected with MOE_W4A16_WORKSPACE_TOO_SMALL and a message giving
- * both sizes (at E=384, K=7168, N=2048, top-8 this admits M <= 14 tokens).
+ * both sizes (at E=384, K=7168, N=2048, top-8 and the default grid this admits
+ * M <= 16 tokens).
  * The first call on a device looks up the array's device address (a one-time
  * set-up per device, repeated automatically if the device's context has been
  * re-created since, e.g. after cudaDeviceReset); make that first call before any

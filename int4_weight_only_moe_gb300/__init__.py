@@ -293,7 +293,6 @@ class MoEW4A16:
             self.expert_begin, self.E = b, e - b
             self.handle = moe_w4a16_create_ep(E, b, e, K, N, topk, group_size)
         self.workspace = None
-        self._ws_bytes = {}  # (M, host staging) -> workspace bytes
 
     def close(self):
         if self.handle:
@@ -330,12 +329,11 @@ class MoEW4A16:
             moe_w4a16_pack_ex(self.handle, w1_q, w1_s, w2_q, w2_s, layout, w1_g_idx, w2_g_idx, stream)
 
     def ensure_workspace(self, M: int, host_staging: bool = False):
-        need = self._ws_bytes.get((M, host_staging))
-        if need is None:
-            need = moe_w4a16_workspace_size(self.handle, M)
-            if host_staging:
-                need += moe_w4a16_host_staging_size(self.handle, M)
-            self._ws_bytes[(M, host_staging)] = need
+        # (asked every call: the size depends on the handle's options, which the
+        # caller may change between calls)
+        need = moe_w4a16_workspace_size(self.handle, M)
+        if host_staging:
+            need += moe_w4a16_host_staging_size(self.handle, M)
         if self.workspace is None or self.workspace.numel() < need:
             import torch
             self.workspace = torch.empty(need, dtype=torch.uint8, device="cuda")

@@ -86,9 +86,11 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
     my_pad = (run + a.block - 1) / a.block * a.block;
     my_tiles = a.bn_max > 0 ? (my_pad + a.bn_max - 1) / a.bn_max : 0;
   }
-  int tot_pad = 0, tot_tiles = 0;
+  int tot_pad = 0, tot_tiles = 0, tot_gv = 0;
   const int seg = block_exclusive_scan(my_pad, warp_tmp, &tot_pad);
   const int tstart = block_exclusive_scan(my_tiles, warp_tmp, &tot_tiles);
+  const int my_gv = (my_cnt + kGemvRows - 1) / kGemvRows;  // (0 for threads beyond E)
+  const int gstart = a.gv_tiles ? block_exclusive_scan(my_gv, warp_tmp, &tot_gv) : 0;
   int* seg_sm = hist + 32 * E;  // [E]
   if (tid < E) seg_sm[tid] = seg;
   __syncthreads();
@@ -133,10 +135,27 @@ __global__ void __launch_bounds__(1024) align_kernel(const AlignArgs a) {
       a.expert_tiles[tid] = my_tiles;
     }
   }
+  if (a.gv_tiles) {
+    // the CUDA-core tiles: each expert's rows (now in sorted_ids) four at a time
+    __syncthreads();
+    if (tid < E) {
+      for (int j = 0; j < my_gv; ++j) {
+        GemvTile gt;
+        gt.e = tid;
+        gt.p0 = seg + j * kGemvRows;
+        gt.n = min(kGemvRows, my_cnt - j * kGemvRows);
+        gt.pad = 0;
+#pragma unroll
+        for (int t = 0; t < kGemvRows; ++t) gt.slot[t] = t < gt.n ? a.sorted_ids[gt.p0 + t] : a.MK;
+        if (MOE_CHECK(gstart + j < a.gv_tiles_cap, a.hdr, a.dbg, 30, gstart + j, tid)) a.gv_tiles[gstart + j] = gt;
+      }
+    }
+  }
   if (tid == 0) {
     if (a.hdr) {
       a.hdr[kHdrNumPadded] = tot_pad;
       a.hdr[kHdrNumTiles] = tot_tiles;
+      a.hdr[kHdrNumGemvTiles] = tot_gv;
     }
     if (a.num_padded_out) *a.num_padded_out = tot_pad;
   }
@@ -347,38 +366,55 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
     for (int i = 0; i < kGatherChunks; ++i) {
       const int ch = c0 + i * kGatherThreads + tid;
       const bool in_row = ch < cpr;  // (K is a multiple of 128: whole groups of 4 lanes agree)
-      float gsum = 0.f;
-      uint8_t* xv_step = g.xv ? g.xv + (static_cast<long long>(p) * g.xv_steps + (ch >> 4)) * kXvStepBytes : nullptr;
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
       if (in_row) {
-        uint4 x = one_pass ? v[i] : src[ch];
+        x = one_pass ? v[i] : src[ch];
         if (pr) {
           const int4 i0 = *reinterpret_cast<const int4*>(pr + 8 * ch);
           const int4 i1 = *reinterpret_cast<const int4*>(pr + 8 * ch + 4);
           x = make_uint4(bf16_pair(xr, i0.x, i0.y), bf16_pair(xr, i0.z, i0.w), bf16_pair(xr, i1.x, i1.y),
                          bf16_pair(xr, i1.z, i1.w));
         }
+      }
+      if (g.xv) {
+        // step rows (layout.cuh): the chunk is one word of its scale group, whose
+        // 4 words sit in 4 consecutive lanes; 16-bit block fixed point per group
+        float xf[8];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xf[2 * k] = fminf(fmaxf(__uint_as_float(w[k] << 16) * f, -65504.0f), 65504.0f);
+          xf[2 * k + 1] = fminf(fmaxf(__uint_as_float(w[k] & 0xFFFF0000u) * f, -65504.0f), 65504.0f);
+          m = fmaxf(m, fmaxf(fabsf(xf[2 * k]), fabsf(xf[2 * k + 1])));
+        }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const int eg = xv_group_exp(m);
+        uint16_t q[8];
+        int sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int v16 = xv_quantize(xf[k], eg);
+          q[xv_slot(k)] = static_cast<uint16_t>(v16);
+          sum += v16;
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        uint8_t* xv_step = g.xv + (static_cast<long long>(sid) * g.xv_steps + (ch >> 4)) * kXvStepBytes;
+        if (in_row && MOE_CHECK((xv_step - g.xv) + kXvStepBytes <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg,
+                                28, xv_step - g.xv, p)) {
+          *reinterpret_cast<uint4*>(xv_step + (ch & 15) * 16) =
+              make_uint4(q[0] | (static_cast<uint32_t>(q[1]) << 16), q[2] | (static_cast<uint32_t>(q[3]) << 16),
+                         q[4] | (static_cast<uint32_t>(q[5]) << 16), q[6] | (static_cast<uint32_t>(q[7]) << 16));
+          if ((ch & 3) == 0) reinterpret_cast<int32_t*>(xv_step + 256)[(ch >> 2) & 3] = xv_header(sum, eg);
+        }
+      } else if (in_row) {
         const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),
                                    bf16x2_to_f16x2_scaled(x.z, f), bf16x2_to_f16x2_scaled(x.w, f));
-        if (xv_step) {
-          // step rows: the chunk in order within its step, and its group's sum
-          if (MOE_CHECK((xv_step - g.xv) + kXvStepBytes <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 28,
-                        xv_step - g.xv, p))
-            *reinterpret_cast<uint4*>(xv_step + (ch & 15) * 16) = o;
-          gsum = f16x8_sum(o);
-        } else {
-          const long long off = b_operand_offset(ch, p, g.Gcap);
-          if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 25, off, p))
-            *reinterpret_cast<uint4*>(g.xs + off) = o;
-        }
-      }
-      if (xv_step) {
-        // the scale group's sum (4 consecutive chunks = 4 consecutive lanes)
-        gsum += __shfl_xor_sync(0xffffffffu, gsum, 1);
-        gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
-        if (in_row && (ch & 3) == 0 &&
-            MOE_CHECK((xv_step - g.xv) + kXvStepBytes <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 29,
-                      xv_step - g.xv, p))
-          reinterpret_cast<float*>(xv_step + 256)[(ch >> 2) & 3] = gsum;
+        const long long off = b_operand_offset(ch, p, g.Gcap);
+        if (MOE_CHECK(off + 16 <= g.xs_bytes, const_cast<int32_t*>(g.hdr), g.dbg, 25, off, p))
+          *reinterpret_cast<uint4*>(g.xs + off) = o;
       }
     }
   }

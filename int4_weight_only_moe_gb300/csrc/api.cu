@@ -22,7 +22,7 @@ struct moe_w4a16_ctx {
   unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
   bool fused_small;            // MOE_W4A16_OPT_FUSED_SMALL_BATCH
-  int gemv_small;              // MOE_W4A16_OPT_GEMV_SMALL_BATCH (0 never, 1 small batches, 2 one token)
+  int gemv_small;              // MOE_W4A16_OPT_GEMV_SMALL_BATCH (0, 1: <= 32 slots, 2: one token, 3: <= 256 slots)
   int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
   uint8_t* w2p;
@@ -84,7 +84,8 @@ const void* pinned_device_pointer(const void* p) {
 }
 
 struct WsLayout {
-  size_t hdr, tickets, sched, sorted, rowexp, tiles, expert_tiles, xs, hbuf, scratch, acc, xv1, xv2, total;
+  size_t hdr, tickets, sched, sorted, rowexp, tiles, expert_tiles, xs, hbuf, scratch, acc, xv1, xv2, gv_tiles,
+      total;
   int Pcap, Gcap;
 };
 
@@ -118,21 +119,29 @@ WsLayout ws_layout(const moe_w4a16_ctx* h, int M) {
   off = align_up(off + static_cast<size_t>(L.Gcap) * sizeof(TokenTile), 256);
   L.expert_tiles = off;
   off = align_up(off + static_cast<size_t>(h->E) * sizeof(int32_t), 1024);
+  // (the blocked hidden rows, or for the CUDA-core products their step rows)
+  // (sized for min(M * topk, kGemvMaxSlots) rows whatever the path, so that the
+  // size never shrinks as M grows)
+  const size_t xv_rows = static_cast<size_t>(MK < kGemvMaxSlots ? MK : kGemvMaxSlots);
   L.xs = off;
-  off = align_up(off + static_cast<size_t>(L.Pcap) * h->K * 2, 1024);
+  const size_t xs_blocked = static_cast<size_t>(L.Pcap) * h->K * 2;
+  const size_t xs_rows = xv_rows * (h->K / 128) * kXvStepBytes;
+  off = align_up(off + (xs_blocked > xs_rows ? xs_blocked : xs_rows), 1024);
   L.hbuf = off;
   off = align_up(off + static_cast<size_t>(L.Pcap) * h->N * 2, 1024);
-  L.scratch = off;
-  off = align_up(off + static_cast<size_t>(kMaxCtas) * 2 * kBNMax * kBM * sizeof(float), 1024);
+  L.scratch = off;  // (a pair of split-unit slots per CTA of the handle's grid)
+  off = align_up(off + static_cast<size_t>(h->num_ctas) * 2 * kBNMax * kBM * sizeof(float), 1024);
   L.acc = off;
   off = align_up(off + static_cast<size_t>(M) * h->K * sizeof(float), 1024);
-  // small batches (at most 32 routed slots, the CUDA-core path): the gathered
-  // hidden rows and the intermediate as step rows (layout.cuh)
-  const size_t xv_rows = MK <= 32 ? static_cast<size_t>(L.Pcap) : 0;
-  L.xv1 = off;
-  off = align_up(off + xv_rows * (h->K / 128) * kXvStepBytes, 1024);
+  // batches the CUDA-core products can take (at most kGemvMaxSlots routed slots):
+  // the gathered hidden rows as step rows (layout.cuh; one row per routed slot, in
+  // the region of the blocked rows, which those products do not read), the
+  // intermediate as step rows, and the tile list
+  L.xv1 = L.xs;
   L.xv2 = off;
   off = align_up(off + xv_rows * (h->N / 128) * kXvStepBytes, 1024);
+  L.gv_tiles = off;
+  off = align_up(off + xv_rows * sizeof(GemvTile), 1024);
   L.total = off;
   return L;
 }
@@ -180,7 +189,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->group = group_size;
   h->pdl = true;
   h->fused_small = false;
-  h->gemv_small = 2;
+  h->gemv_small = 1;
   h->step_cost[0] = kDefaultStepCostGateUp;
   h->step_cost[1] = kDefaultStepCostDown;
   cudaError_t e = cudaGetDevice(&h->device);
@@ -362,7 +371,7 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
       h->fused_small = value != 0;
       return MOE_W4A16_OK;
     case MOE_W4A16_OPT_GEMV_SMALL_BATCH:
-      if (value < 0 || value > 2) return fail(MOE_W4A16_INVALID_ARG, "GEMV option must be 0, 1 or 2");
+      if (value < 0 || value > 3) return fail(MOE_W4A16_INVALID_ARG, "GEMV option must be 0, 1, 2 or 3");
       h->gemv_small = value;
       return MOE_W4A16_OK;
     case MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES:
@@ -494,19 +503,28 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   // steps, so the steps per unit must allow that; at most one CTA per SM).
   const bool fused = h->fused_small && MK <= 32 && !logits && h->num_ctas <= h->num_sms &&
                      (static_cast<long long>(2 * h->N / kBM) * (h->K / (2 * kBK))) % 4 == 0;
-  // Small batch otherwise: both products as CUDA-core matrix-vector products
-  // (tiles of at most 4 token rows per expert) -- by default for a single token,
-  // where they were measured faster than the tensor-core kernels -- else on the
-  // tensor cores.
-  const bool gemv = !fused && MK <= 32 && (h->gemv_small == 1 || (h->gemv_small == 2 && M == 1));
+  // Otherwise both products as CUDA-core matrix-vector products (tiles of at most
+  // 4 token rows per expert): by default for batches of at most 32 routed slots
+  // (measured faster there than the tensor-core kernels; slower at 72 and 256
+  // slots, which the option's value 3 still allows), else on the tensor cores.
+  // (their split tables hold step indices as int: at most MK tiles x 2N/128 row tiles x K/128 steps)
+  const bool gemv_wanted = h->gemv_small == 1 ? MK <= 32
+                           : h->gemv_small == 2 ? M == 1
+                           : h->gemv_small == 3 ? MK <= kGemvMaxSlots : false;
+  const bool gemv = !fused && gemv_wanted && MK * static_cast<long long>(2 * h->N / kBM) * (h->K / 128) < (1LL << 31);
   uint8_t* xv1 = ws + L.xv1;
   uint8_t* xv2 = ws + L.xv2;
-  const long long xv1_bytes = static_cast<long long>(L.Pcap) * (h->K / 128) * kXvStepBytes;
-  const long long xv2_bytes = static_cast<long long>(L.Pcap) * (h->N / 128) * kXvStepBytes;
+  GemvTile* gv_tiles = reinterpret_cast<GemvTile*>(ws + L.gv_tiles);
+  const long long xv1_bytes = MK * static_cast<long long>(h->K / 128) * kXvStepBytes;
+  const long long xv2_bytes = MK * static_cast<long long>(h->N / 128) * kXvStepBytes;
   if (gemv) {
     ga.xv = xv1;
     ga.xv_steps = h->K / 128;
     ga.xs_bytes = xv1_bytes;  // (the extent the rows are written into)
+    if (MK > 32) {            // the align kernel writes the tile list
+      aa.gv_tiles = gv_tiles;
+      aa.gv_tiles_cap = static_cast<int>(MK);
+    }
   }
   if (fused) {
     if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[1], s));
@@ -537,11 +555,18 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   // start their weight streams without waiting for the routing + gather launch
   const int32_t* small_ids = (MK <= 32 && !logits) ? topk_ids : nullptr;
   g1.small_ids = small_ids;
+  if (gemv && MK > 32) {
+    g1.small_ids = nullptr;
+    g1.gv_tiles = gv_tiles;
+  }
   if (gemv) {
-    // the GEMV kernels route from the ids themselves; routed in-launch, they are
-    // the preceding kernel's output
-    g1.small_ids = topk_ids;
-    g1.ids_after_pdl = logits ? 1 : 0;
+    // a small batch: the CUDA-core kernels route from the ids themselves (routed
+    // in-launch, they are the preceding kernel's output); a larger one reads the
+    // align kernel's tile list
+    if (MK <= 32) {
+      g1.small_ids = topk_ids;
+      g1.ids_after_pdl = logits ? 1 : 0;
+    }
     g1.xv_in = xv1;
     g1.xv_bytes = xv1_bytes;
     g1.xv_out = xv2;
@@ -562,7 +587,7 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g1.wpack_bytes = static_cast<long long>(h->w1p_bytes);
   g1.bsrc_bytes = static_cast<long long>(L.Pcap) * h->K * 2;
   g1.hout_bytes = static_cast<long long>(L.Pcap) * h->N * 2;
-  g1.scratch_elems = static_cast<long long>(kMaxCtas) * 2 * kBNMax * kBM;
+  g1.scratch_elems = static_cast<long long>(h->num_ctas) * 2 * kBNMax * kBM;
   g1.sorted_cap = L.Pcap;
   g1.tiles_cap = L.Gcap;
   g1.E = h->E;
@@ -605,8 +630,9 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g2.dbg = hdr + 8;
   g2.sched = (sched && h->step_cost[1] > 0) ? sched + (h->num_ctas + 1) : nullptr;
   if (gemv) {
-    g2.small_ids = topk_ids;
-    g2.ids_after_pdl = logits ? 1 : 0;
+    g2.small_ids = MK <= 32 ? topk_ids : nullptr;
+    g2.ids_after_pdl = (MK <= 32 && logits) ? 1 : 0;
+    g2.gv_tiles = MK <= 32 ? nullptr : gv_tiles;
     g2.xv_in = xv2;
     g2.xv_bytes = xv2_bytes;
     g2.Pcap = L.Pcap;

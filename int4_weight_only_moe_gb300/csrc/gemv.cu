@@ -98,7 +98,7 @@ constexpr int kGvWarpEpi0 = kGvWarpP0 + 4;                // then 4 epilogue war
 constexpr int kGvThreads = (kGvWarpEpi0 + 4) * 32;        // 768
 constexpr int kGvEpiThreads = 128;
 constexpr int kGvEpiBar = 1;                              // named barrier of the epilogue warps
-constexpr int kGvRows = 4;                                // token rows of a tile
+constexpr int kGvRows = kGemvRows;                        // token rows of a tile
 constexpr int kGvSub = 2;                                 // 64-element k-blocks per step
 constexpr int kGvStepBytes = kGvSub * kWBlockBytes;       // 9 KB of packed weights
 constexpr int kGvChunk = 2;                               // steps per weight copy
@@ -118,23 +118,21 @@ constexpr int kGbRedEmpty = kGbRedFull + 2;      // [2] reduction slot read (4 e
 constexpr int kGbNever = kGbRedEmpty + 2;        // nothing arrives (the give-up test hook)
 constexpr int kGvNumBars = kGbNever + 1;
 
-// A tile: up to 4 consecutive padded rows of one expert (the rows the routing +
-// gather kernel wrote for its slots) and the slot of each.
-struct GvTile {
-  int e, p0, n, pad;
-  int slot[kGvRows];
-};
+using GvTile = GemvTile;  // (layout.cuh)
 static_assert(sizeof(GvTile) == 32, "tile table entry size");
+constexpr int kGvTileCache = kSmallTiles;  // tiles kept in shared memory (a batch's all, up to 32 slots)
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kGsBar = 0;
 constexpr int kGsMisc = kGsBar + ((kGvNumBars * 8 + 63) / 64) * 64;
 // the last chunk / step copied into each ring slot (for the teardown's drain)
 constexpr int kGsLast = kGsMisc + 64;  // int wlast[kGvNWS], blast[kGvNB]
-constexpr int kGsTiles = kGsLast + (((kGvNWS + kGvNB) * 4 + 63) / 64) * 64;
+// the small batch's cumulative tile costs, for the cost-weighted split
+constexpr int kGsCum = kGsLast + (((kGvNWS + kGvNB) * 4 + 63) / 64) * 64;  // long long [kSmallTiles + 1]
+constexpr int kGsTiles = kGsCum + (((kSmallTiles + 1) * 8 + 63) / 64) * 64;
 constexpr int kGsRed = kGsTiles + kSmallTiles * static_cast<int>(sizeof(GvTile));  // [2][phase][t][128] f32
-constexpr int kGsFin = kGsRed + 2 * kGvPhases * kGvRows * kBM * 4;                  // [t][128] f32
-constexpr int kGsW = ((kGsFin + kGvRows * kBM * 4 + 1023) / 1024) * 1024;
+constexpr int kGsBounds = kGsRed + 2 * kGvPhases * kGvRows * kBM * 4;  // int [kMaxCtas + 1]: shares
+constexpr int kGsW = ((kGsBounds + (kMaxCtas + 1) * 4 + 1023) / 1024) * 1024;
 constexpr int kGsB = kGsW + kGvNWS * kGvChunkBytes;
 constexpr int kGsEnd = kGsB + kGvNB * kGvBStage;
 constexpr int kGsAlloc = kGsEnd + 1024;  // (the base is aligned to 1024 inside)
@@ -149,36 +147,30 @@ static_assert(kGvNWS % 2 == 0 && kGvPhases == 2 * kGvChunk && kGvPhases == 4 && 
                   kGvNB * kGvBSteps >= kGvNWS * kGvChunk,
               "ring depths");
 
-// acc += lo(v) * lo(x) + hi(v) * hi(x): two fp32 fma of fp16 operands (exact products).
-__device__ __forceinline__ void fma2_f16_f32(float& acc, uint32_t v, uint32_t x) {
-  asm("{\n\t.reg .f16 vl, vh, xl, xh;\n\t"
-      "mov.b32 {vl, vh}, %1;\n\t"
-      "mov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.f16 %0, vl, xl, %0;\n\t"
-      "fma.rn.f32.f16 %0, vh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(v), "r"(x));
+// acc + x.lo * code byte 2h + x.hi * code byte 2h + 1 (h = 0: .lo, 1: .hi): two
+// exact integer products of a 16-bit activation and an unsigned 4-bit code.
+__device__ __forceinline__ int dp2a_lo(uint32_t x, uint32_t codes, int acc) {
+  int d;
+  asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(codes), "r"(acc));
+  return d;
 }
-__device__ __forceinline__ uint32_t pair16(uint32_t a) {  // (a & codes) | fp16 16.0 in both halves
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(0x03C003C0u), "r"(0x4C004C00u));
+__device__ __forceinline__ int dp2a_hi(uint32_t x, uint32_t codes, int acc) {
+  int d;
+  asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(codes), "r"(acc));
   return d;
 }
 
 // One step (128 reduction elements) of weight row r for token rows T0 .. T0+T-1
-// of the tile: the four scale groups of the step, each summed over its 32
-// elements, then scaled. (At most two rows per call: more would not fit the 80
-// registers a thread of this CTA has without spilling; three and four rows take
-// two calls.) w: the step's packed weights; x: the step's row 0 in the activation
-// stage (row t at + t * kGvBRow: 128 fp16 values, then 4 fp32 group sums). Plain
-// loads (not volatile asm), so the compiler can issue a group's loads together;
-// the barrier waits before a step carry memory clobbers, so no load moves across
-// them. The groups run one after another (not unrolled): unrolled, the compiler
-// hoists every group's loads past the register budget.
+// of the tile: per scale group, the exact integer sum of code x value over its 32
+// elements (dp2a), minus 8 times the group's value sum, times the weight scale
+// and the group's 2^-e. w: the step's packed weights; x: the step's row 0 in the
+// activation stage (row t at + t * kGvBRow). At most two rows per call (more do
+// not fit the 80 registers a thread of this CTA has; three and four rows take two
+// calls); the groups are unrolled for a single row only, for the same reason.
 template <int T, int T0>
 __device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int r, float (&acc)[kGvRows]) {
   static_assert(T >= 1 && T <= 2 && T0 + T <= kGvRows, "rows per call");
-#pragma unroll 1
+#pragma unroll(T == 1 ? 4 : 1)
   for (int gi = 0; gi < 4; ++gi) {
     // group gi: half gi % 2 of the step's k-block gi / 2
     const uint8_t* blk = w + (gi >> 1) * kWBlockBytes;
@@ -186,69 +178,31 @@ __device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int 
     const uint32_t sw = *reinterpret_cast<const uint32_t*>(blk + kWCodeBytes + r * 4);
     const float s = __half2float(__ushort_as_half(static_cast<uint16_t>((gi & 1) ? (sw >> 16) : (sw & 0xFFFFu))));
     const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
-    float part[T];
+    int part[T];
 #pragma unroll
-    for (int t = 0; t < T; ++t) part[t] = 0.f;
+    for (int t = 0; t < T; ++t) part[t] = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t q = w4[j];
-      const uint32_t v0 = pair16(q), v1 = pair16(q << 4), v2 = pair16(q >> 4),
-                     v3 = pair16(__funnelshift_l(q, q, 8));  // code pairs (0,1) (2,3) (4,5) (6,7)
+      // codes of elements 2, 4, 3, 5 and 0, 7, 1, 6 as bytes (layout.cuh)
+      const uint32_t c0 = __funnelshift_r(w4[j], w4[j], 2) & 0x0F0F0F0Fu;
+      const uint32_t c1 = __funnelshift_r(w4[j], w4[j], 6) & 0x0F0F0F0Fu;
 #pragma unroll
       for (int t = 0; t < T; ++t) {
         const uint4 xv = *reinterpret_cast<const uint4*>(x + (T0 + t) * kGvBRow + gi * 64 + j * 16);
-        fma2_f16_f32(part[t], v0, xv.x);
-        fma2_f16_f32(part[t], v1, xv.y);
-        fma2_f16_f32(part[t], v2, xv.z);
-        fma2_f16_f32(part[t], v3, xv.w);
+        part[t] = dp2a_lo(xv.x, c0, part[t]);
+        part[t] = dp2a_hi(xv.y, c0, part[t]);
+        part[t] = dp2a_lo(xv.z, c1, part[t]);
+        part[t] = dp2a_hi(xv.w, c1, part[t]);
       }
     }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-      const float X = *reinterpret_cast<const float*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
-      acc[T0 + t] = fmaf(s, fmaf(-24.0f, X, part[t]), acc[T0 + t]);
+      const int hdr = *reinterpret_cast<const int*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
+      const int e = static_cast<int8_t>(hdr & 0xFF);
+      // sum (u - 8) v: exact in int32 and in fp32 (|.| < 2^23)
+      const float dot = static_cast<float>(part[t] - 8 * (hdr >> 8));
+      acc[T0 + t] = fmaf(s * __int_as_float((127 - e) << 23), dot, acc[T0 + t]);
     }
-  }
-}
-
-// The same with the step's codes and scales already in registers (q0..q3 = group
-// g's 4 words, sc01 / sc23 the scale words of the two k-blocks). The groups run
-// one after another, the registers rotating, so that no array is indexed by the
-// loop counter.
-template <int T, int T0>
-__device__ __forceinline__ void gv_step_regs(uint4 q0, uint4 q1, uint4 q2, uint4 q3, uint32_t sc01, uint32_t sc23,
-                                             const uint8_t* x, float (&acc)[kGvRows]) {
-  static_assert(T >= 1 && T <= 2 && T0 + T <= kGvRows, "rows per call");
-  uint32_t sw = sc01;
-#pragma unroll 1
-  for (int gi = 0; gi < 4; ++gi) {
-    const float s = __half2float(__ushort_as_half(static_cast<uint16_t>(sw & 0xFFFFu)));
-    const uint32_t w4[4] = {q0.x, q0.y, q0.z, q0.w};
-    float part[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) part[t] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w = w4[j];
-      const uint32_t v0 = pair16(w), v1 = pair16(w << 4), v2 = pair16(w >> 4), v3 = pair16(__funnelshift_l(w, w, 8));
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(x + (T0 + t) * kGvBRow + gi * 64 + j * 16);
-        fma2_f16_f32(part[t], v0, xv.x);
-        fma2_f16_f32(part[t], v1, xv.y);
-        fma2_f16_f32(part[t], v2, xv.z);
-        fma2_f16_f32(part[t], v3, xv.w);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const float X = *reinterpret_cast<const float*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
-      acc[T0 + t] = fmaf(s, fmaf(-24.0f, X, part[t]), acc[T0 + t]);
-    }
-    q0 = q1;
-    q1 = q2;
-    q2 = q3;
-    sw = (gi == 1) ? sc23 : (sw >> 16);
   }
 }
 
@@ -287,6 +241,41 @@ struct GvSeq {
   }
 };
 
+// Relative cost of one step of a tile with T token rows (T = 1..4): the multiply
+// warps' time per step, measured at full size -- one row is bound by the weight
+// stream, two and more rows by the arithmetic (the rows after the first are
+// neither unrolled nor free).
+__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 8 : T == 2 ? 18 : T == 3 ? 26 : 37; }
+
+// The stream-K split weighted by tile cost: every unit of tile i costs
+// gv_step_cost(rows of tile i) per step, and CTA c starts at the first step at or
+// after which c / G of the total cost has gone before (so shares start anywhere,
+// like the even split's). cum[i] = cost of tiles 0 .. i-1 (cum[0] = 0), per step
+// of a unit; a tile has unit_steps = R * KBn steps.
+struct GvSched {
+  const long long* cum;  // [ntiles + 1], shared memory
+  int ntiles, G;
+  long long unit_steps;
+  __device__ __forceinline__ long long total_steps() const { return ntiles * unit_steps; }
+  __device__ long long start(int c) const {
+    if (c <= 0) return 0;
+    if (c >= G) return total_steps();
+    const long long total = cum[ntiles] * unit_steps;
+    const long long target = (static_cast<long long>(c) * total + G - 1) / G;  // ceil(c * total / G)
+    // the tile in which the cumulative cost reaches target
+    int lo = 0, hi = ntiles - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] * unit_steps <= target) lo = mid; else hi = mid - 1;
+    }
+    const long long base = cum[lo] * unit_steps;
+    const long long per = cum[lo + 1] - cum[lo];  // this tile's cost per step
+    const long long k = per > 0 ? (target - base + per - 1) / per : 0;
+    const long long s = lo * unit_steps + (k < unit_steps ? k : unit_steps);
+    return s < total_steps() ? s : total_steps();
+  }
+};
+
 // kMode 1: gate/up + SwiGLU; 2: down + weighted scatter-add.
 template <int kMode>
 __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
@@ -301,7 +290,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
   volatile int* epi_ok = reinterpret_cast<volatile int*>(gbase + kGsMisc + 16);  // [2][4]
   GvTile* tiles = reinterpret_cast<GvTile*>(gbase + kGsTiles);
   float* red = reinterpret_cast<float*>(gbase + kGsRed);
-  float* fin = reinterpret_cast<float*>(gbase + kGsFin);
+  int* bounds = reinterpret_cast<int*>(gbase + kGsBounds);
   const uint32_t sW = base + kGsW, sB = base + kGsB;
   int* wlast = reinterpret_cast<int*>(gbase + kGsLast);
   int* blast = wlast + kGvNWS;
@@ -312,8 +301,16 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
 
   // Tiles of the batch from the caller's topk_ids (warp 0): every expert's slots,
   // in the padded rows the routing + gather kernel placed them in (16 per expert
-  // and row group), cut into tiles of at most 4 rows, experts in id order.
-  if (warp == 0) {
+  // and row group), cut into tiles of at most 4 rows, experts in id order. A
+  // larger batch reads the align kernel's tile list instead (its count now; the
+  // tiles below, once the share is known): the whole kernel then waits for the
+  // preceding kernels.
+  const bool small = a.small_ids != nullptr;
+  if (warp == 0 && !small) {
+    pdl_wait();
+    if (lane == 0) *ntiles_sm = a.hdr[kHdrNumGemvTiles];
+  }
+  if (warp == 0 && small) {
     if (a.ids_after_pdl) pdl_wait();  // the ids are the preceding kernel's output
     const int v = lane < a.MK ? a.small_ids[lane] : -1;
     const SmallRoute r = small_route_ids(v, a.MK, a.E, kRowGroup, kBNMax, lane, a.e_begin, a.E_total);
@@ -369,10 +366,64 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
 
   const int ntiles = *ntiles_sm;
   const int G = static_cast<int>(gridDim.x);
-  const Sched sc{static_cast<long long>(ntiles) * a.R * a.KBn, G, nullptr, 1};
-  const long long my_begin = sc.start(blockIdx.x), my_end = sc.start(blockIdx.x + 1);
+  // Shares: a small batch's weighted by the tiles' costs (its tiles are all in
+  // shared memory); the align kernel's list split evenly.
+  // (tiles of one cost, as at decode, take the even split's simpler arithmetic)
+  long long* cum = reinterpret_cast<long long*>(gbase + kGsCum);
+  int* weighted_sm = reinterpret_cast<int*>(gbase + kGsMisc + 12);
+  if (threadIdx.x == 0) {
+    bool uneven = false;
+    if (small) {
+      long long c = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        cum[i] = c;
+        c += gv_step_cost(tiles[i].n);
+        uneven = uneven || tiles[i].n != tiles[0].n;
+      }
+      cum[ntiles] = c;
+    }
+    if (!uneven) {
+      cum[0] = 0;  // an even split: one cost unit per step of one tile spanning all
+      cum[1] = 1;
+    }
+    *weighted_sm = uneven ? 1 : 0;
+  }
+  __syncthreads();
+  const bool weighted = *weighted_sm != 0;
+  // every CTA's first step (the host keeps the step count below 2^31), computed
+  // in parallel into shared memory: the shares, and the epilogue's lookups of the
+  // CTAs that share a unit, then cost nothing
+  const int sc_tiles = weighted ? ntiles : 1;
+  const long long sc_unit = weighted ? static_cast<long long>(a.R) * a.KBn : static_cast<long long>(ntiles) * a.R * a.KBn;
+  {
+    const GvSched s0{cum, sc_tiles, G, sc_unit};
+    for (int c = threadIdx.x; c <= G; c += blockDim.x) bounds[c] = static_cast<int>(s0.start(c));
+  }
+  __syncthreads();
+  const long long my_begin = bounds[blockIdx.x], my_end = bounds[blockIdx.x + 1];
+  // the CTA whose share contains step g
+  auto cta_of = [&](long long g) -> int {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (bounds[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
   const long long n_it = my_end - my_begin;
   const GvSeq seq(my_begin, my_end, a.KBn);
+  // Tiles in shared memory: all of a small batch's; for the align kernel's list
+  // the window of this CTA's share (tiles beyond it, only when a CTA spans more
+  // than kGvTileCache tiles, are read from global memory).
+  const int t_lo = small ? 0 : static_cast<int>(my_begin / (static_cast<long long>(a.R) * a.KBn));
+  if (!small) {
+    for (int i = threadIdx.x; i < kGvTileCache && t_lo + i < ntiles; i += blockDim.x) tiles[i] = a.gv_tiles[t_lo + i];
+    __syncthreads();
+  }
+  auto tile_at = [&](long long ti) -> const GvTile* {
+    const long long k = ti - t_lo;
+    return (k >= 0 && k < kGvTileCache) ? tiles + k : a.gv_tiles + ti;
+  };
   pdl_launch_dependents();
   if (threadIdx.x == 0) GV_STAMP(1);
 
@@ -392,7 +443,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
       int kb, kbe;
       seq.at(it, u, kb, kbe);
       const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
-      const int e = tiles[u / a.R].e;
+      const int e = tile_at(u / a.R)->e;
       const int rt = static_cast<int>(u % a.R);
       const long long woff = ((static_cast<long long>(e) * a.R + rt) * a.KBn + kb) * kGvStepBytes;
       if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kGvStepBytes <= a.wpack_bytes && e >= 0 &&
@@ -435,7 +486,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
             int kb, kbe;
             seq.at(it, u, kb, kbe);
             const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
-            bytes += static_cast<uint32_t>(tiles[u / a.R].n * run * kXvStepBytes);
+            bytes += static_cast<uint32_t>(tile_at(u / a.R)->n * run * kXvStepBytes);
             it += run;
           }
           blast[s] = static_cast<int>(nb);
@@ -445,9 +496,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
             int kb, kbe;
             seq.at(it, u, kb, kbe);
             const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
-            const GvTile& tl = tiles[u / a.R];
+            const GvTile& tl = *tile_at(u / a.R);
             for (int t = 0; t < tl.n; ++t) {
-              const long long xoff = (static_cast<long long>(tl.p0 + t) * a.KBn + kb) * kXvStepBytes;
+              // (step rows are indexed by the routed slot)
+              const long long xoff = (static_cast<long long>(tl.slot[t]) * a.KBn + kb) * kXvStepBytes;
               if (MOE_CHECK(xoff >= 0 && xoff + static_cast<long long>(run) * kXvStepBytes <= a.xv_bytes &&
                                 tl.n <= kGvRows,
                             a.status, a.dbg, 42, xoff, run))
@@ -483,8 +535,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     bool ok = true;
     while (ok && si.next(u, kb0, kb1)) {
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
-      const GvTile& tl = tiles[u / a.R];
-      const int T = tl.n;
+      const int T = tile_at(u / a.R)->n;
       float acc[kGvRows] = {0.f, 0.f, 0.f, 0.f};
       for (uint32_t it = it_base + ((static_cast<uint32_t>(phase) - it_base) & 3u); it < it_base + len;
            it += kGvPhases) {
@@ -554,7 +605,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     uint32_t ru = 0;
     bool sat = false;
     while (si.next(u, kb0, kb1)) {
-      const GvTile tl = tiles[u / a.R];
+      const GvTile& tl = *tile_at(u / a.R);
       const int T = tl.n;
       const int rt = static_cast<int>(u % a.R);
       const uint32_t rs = ru & 1u, rpar = (ru >> 1) & 1u;
@@ -572,8 +623,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
         const float* src = red + ((rs * kGvPhases) * kGvRows + t) * kBM + tid;
         v[t] = ((src[0] + src[kGvRows * kBM]) + src[2 * kGvRows * kBM]) + src[3 * kGvRows * kBM];
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kGbRedEmpty + rs));
+      // (the slot is released at the end of this unit's epilogue: the SwiGLU
+      // stages the sums in its first phase's part, where each thread has just
+      // read its own row)
+      float* fin = red + (rs * kGvPhases * kGvRows) * kBM;
       ++ru;
       if (tid == 0) GV_STAMP(6);
 
@@ -588,13 +641,15 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
           const long long ai = static_cast<long long>(slot / a.topk) * a.Kout + static_cast<long long>(rt) * kBM + tid;
           if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 43, ai, slot)) atomicAdd(a.acc + ai, wt * v[t]);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kGbRedEmpty + rs));
         continue;
       }
       // gate/up: a unit cut between CTAs is finished by its last contributor
       bool write_tile = kb0 == 0 && kb1 == a.KBn;
       if (!write_tile) {
         const long long ustart = u * a.KBn;
-        const int part = (sc.start(blockIdx.x) < ustart) ? 1 : 0;
+        const int part = (my_begin < ustart) ? 1 : 0;
         float* slot = a.scratch + (static_cast<long long>(blockIdx.x) * 2 + part) * kBNMax * kBM;
 #pragma unroll
         for (int t = 0; t < kGvRows; ++t)
@@ -603,7 +658,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
             __stcg(slot + t * kBM + tid, v[t]);
         __threadfence();
         named_bar_sync(kGvEpiBar, kGvEpiThreads);
-        const int c0 = sc.cta_of(ustart), c1 = sc.cta_of(ustart + a.KBn - 1);
+        const int c0 = cta_of(ustart), c1 = cta_of(ustart + a.KBn - 1);
         if (tid == 0) {
           const int add = kb1 - kb0;
           const int old = atomicAdd(a.tickets + c0, add);
@@ -616,8 +671,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
 #pragma unroll
           for (int t = 0; t < kGvRows; ++t) v[t] = 0.f;
           for (int cc = c0; cc <= c1; ++cc) {
-            if (sc.start(cc) == sc.start(cc + 1)) continue;  // empty share: no partial
-            const int pc = (sc.start(cc) < ustart) ? 1 : 0;
+            if (bounds[cc] == bounds[cc + 1]) continue;  // empty share: no partial
+            const int pc = (bounds[cc] < ustart) ? 1 : 0;
             const float* sl = a.scratch + (static_cast<long long>(cc) * 2 + pc) * kBNMax * kBM;
 #pragma unroll
             for (int t = 0; t < kGvRows; ++t)
@@ -647,19 +702,31 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
                                  blocked_offset(p % kRowGroup, f);
           if (MOE_CHECK(hoff >= 0 && hoff + 2 <= a.hout_bytes, a.status, a.dbg, 45, hoff, p))
             *reinterpret_cast<__half*>(a.hout + hoff) = hh;
-          // h as a step row of the down product (its step rt / 2 holds this tile's
-          // 64 features at (rt % 2) * 64), and the sum of each group of 32 (as stored)
-          uint8_t* xs = a.xv_out + (static_cast<long long>(p) * (a.R / 2) + (rt >> 1)) * kXvStepBytes;
+          // h as a step row of the down product (its step rt / 2 holds this
+          // tile's 64 features at (rt % 2) * 64): this warp's 32 features are one
+          // scale group of it, in 16-bit block fixed point (layout.cuh)
+          uint8_t* xs = a.xv_out + (static_cast<long long>(tl.slot[t]) * (a.R / 2) + (rt >> 1)) * kXvStepBytes;
           const bool xs_ok = MOE_CHECK((xs - a.xv_out) + kXvStepBytes <= a.xv_out_bytes, a.status, a.dbg, 46,
                                        xs - a.xv_out, p);
-          if (xs_ok) *reinterpret_cast<__half*>(xs + ((rt & 1) * 64 + f) * 2) = hh;
-          float gs = __half2float(hh);
+          float m = fabsf(hv);
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
-          if (lane == 0 && xs_ok) reinterpret_cast<float*>(xs + 256)[2 * (rt & 1) + (f >> 5)] = gs;
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          const int eg = xv_group_exp(m);
+          const int v16 = xv_quantize(hv, eg);
+          int sum = v16;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          const int gi = 2 * (rt & 1) + (f >> 5);
+          if (xs_ok) {
+            *reinterpret_cast<int16_t*>(xs + gi * 64 + ((f & 31) >> 3) * 16 + xv_slot(f & 7) * 2) =
+                static_cast<int16_t>(v16);
+            if (lane == 0) reinterpret_cast<int32_t*>(xs + 256)[gi] = xv_header(sum, eg);
+          }
         }
-        named_bar_sync(kGvEpiBar, kGvEpiThreads);  // fin is reused by the next tile
+        named_bar_sync(kGvEpiBar, kGvEpiThreads);  // every thread is done with the staged sums
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kGbRedEmpty + rs));
     }
     if (__any_sync(0xffffffffu, sat) && lane == 0) atomicOr(status, kStatusHSaturated);
   }

@@ -63,6 +63,10 @@ struct AlignArgs {
   int sched_ctas;
   int sched_R[2], sched_KBn[2];
   int step_cost_per_group[2];  // per GEMM; 0 = even split for that GEMM
+  // the CUDA-core products' tile list (every expert's rows in tiles of at most
+  // kGemvRows, experts in id order; count in hdr[kHdrNumGemvTiles]), or null
+  GemvTile* gv_tiles;
+  int gv_tiles_cap;
 };
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t stream, bool pdl);
 // At handle creation: the general align kernel's dynamic shared memory limit,
@@ -166,6 +170,8 @@ struct GemmArgs {
   const uint8_t* xv_in;
   uint8_t* xv_out;
   long long xv_bytes, xv_out_bytes;
+  // more than 32 routed slots: the align kernel's CUDA-core tile list (small_ids null)
+  const GemvTile* gv_tiles;
   int Pcap;
   int ids_after_pdl;       // small_ids is the preceding kernel's output (routed in-launch)
 };

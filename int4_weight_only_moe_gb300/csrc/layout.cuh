@@ -45,10 +45,38 @@ constexpr int kMaxExperts = 1024;
 
 // Activation rows of the small-batch CUDA-core products ("step rows"): per padded
 // row p and pipeline step kb (128 reduction elements) of an operand with KBn
-// steps, 272 bytes at (p * KBn + kb) * 272: the step's 128 fp16 values in order,
-// then the fp32 sums of its four scale groups of 32. A row's steps are
-// contiguous, so one copy brings several steps of a row.
+// steps, 272 bytes at (p * KBn + kb) * 272. A row's steps are contiguous, so one
+// copy brings several steps of a row. Each scale group g (32 elements) of the
+// step is stored as 16-bit block fixed point: v = round(x * 2^e_g) with e_g
+// chosen so that the group's largest |x| times 2^e_g lies in [2^13, 2^14)
+// (xv_group_exp; 0 for an all-zero group):
+//   bytes [64 g, 64 g + 64):  the group's four words of 8 elements, 16 bytes each,
+//                             element i of a word in 16-bit slot kXvSlot[i]
+//   bytes [256 + 4 g, +4):    (sum of the group's 32 values) << 8 | (e_g & 0xFF)
+// The slot order pairs the values with the packed codes for dp2a: rotating a
+// packed word right by 2 (by 6) and masking every fourth nibble gives the codes
+// of elements 2, 4, 3, 5 (0, 7, 1, 6) as bytes, which meet slots 0..3 (4..7).
 constexpr int kXvStepBytes = 272;
+__host__ __device__ constexpr int xv_slot(int i) {
+  return i == 0 ? 4 : i == 1 ? 6 : i == 2 ? 0 : i == 3 ? 2 : i == 4 ? 1 : i == 5 ? 3 : i == 6 ? 7 : 5;
+}
+constexpr int kXvMaxExp = 100;  // |e_g| bound (2^-e_g stays a normal float)
+#ifdef __CUDACC__
+// e_g of a group whose largest magnitude is m (finite, >= 0).
+__device__ __forceinline__ int xv_group_exp(float m) {
+  if (!(m > 0.0f)) return 0;
+  const int lg = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127;  // floor(log2 m) (normal m)
+  const int e = 13 - lg;
+  return e < -kXvMaxExp ? -kXvMaxExp : (e > kXvMaxExp ? kXvMaxExp : e);
+}
+// 16-bit value of x in a group with exponent e.
+__device__ __forceinline__ int xv_quantize(float x, int e) {
+  return __float2int_rn(x * __int_as_float((127 + e) << 23));
+}
+__device__ __forceinline__ int32_t xv_header(int sum, int e) {
+  return static_cast<int32_t>((static_cast<uint32_t>(sum) << 8) | (static_cast<uint32_t>(e) & 0xFFu));
+}
+#endif
 
 // Byte offset of 16-bit element (row, k) inside one 16-row group of a k-block
 // (row in [0, 16), k in [0, 64)).
@@ -64,11 +92,23 @@ struct TokenTile {
   int first;    // index of this expert's first token tile
 };
 
+// One tile of the CUDA-core (matrix-vector) products: up to kGemvRows routed rows
+// of one expert -- padded rows p0 .. p0+n-1 of the expert-sorted order -- and the
+// flat slot of each.
+constexpr int kGemvRows = 4;
+constexpr int kGemvMaxSlots = 256;  // routed slots up to which a forward may use them
+struct GemvTile {
+  int e, p0, n, pad;
+  int slot[kGemvRows];
+};
+
 // Header words at the start of the workspace.
 // kHdrSched: bit w set when the align kernel wrote cost-weighted stream-K
 // boundaries for GEMM w (0 gate/up, 1 down; the general path only), clear for an
 // even split of that GEMM's steps.
-enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrSched = 3, kHdrWords = 64 };
+// kHdrNumGemvTiles: tiles in the CUDA-core tile list (written by the align kernel
+// when the forward runs its products on the CUDA cores).
+enum { kHdrStatus = 0, kHdrNumPadded = 1, kHdrNumTiles = 2, kHdrSched = 3, kHdrNumGemvTiles = 4, kHdrWords = 64 };
 
 // Device status bits (the public values are in the C header).
 enum {

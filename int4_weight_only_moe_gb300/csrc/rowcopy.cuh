@@ -43,18 +43,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float f) 
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// fp32 sum of eight fp16 values (a 16-byte chunk of an operand row).
-__device__ __forceinline__ float f16x8_sum(uint4 o) {
-  const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-    s += __low2float(h) + __high2float(h);
-  }
-  return s;
-}
-
 __device__ __forceinline__ uint32_t bf16_pair(const uint16_t* xr, int a, int b) {
   return static_cast<uint32_t>(__ldg(xr + a)) | (static_cast<uint32_t>(__ldg(xr + b)) << 16);
 }

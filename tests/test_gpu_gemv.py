@@ -5,9 +5,11 @@ oracle and against the tensor-core kernels on the same inputs, through the C-ABI
 Covered: every grid size from one CTA (every unit in one CTA's sequence) to more
 CTAs than steps; experts with 1..16 rows (several 4-row tiles of one expert);
 skipped ids; a batch with no valid slot; the give-up path of both paths; and the
-intermediate activations. The two paths compute the same products; they differ
-in the order of the fp32 sums, so the intermediate may differ by one fp16 unit
-and the output accumulators by a few fp32 units of their largest magnitude."""
+intermediate activations. The two paths compute the same products from
+differently rounded activations (the tensor cores read them as fp16, the CUDA
+cores as 16-bit block fixed point per scale group), so the intermediate may
+differ by about one fp16 unit and the output accumulators by about 2^-12 of
+their magnitude (the oracle comparison is the parity check proper)."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,7 @@ from int4_weight_only_moe_gb300 import inputs
 from tests.gpu_helpers import (Problem, assert_close, bf16_tensor_to_f64, check_accumulator, workload_inputs)
 
 pytestmark = pytest.mark.gpu
-GEMV_DEFAULT = 2  # the CUDA-core path for single-token batches only
+GEMV_DEFAULT = 1  # the CUDA-core path for every batch of at most 32 routed slots
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,7 +32,7 @@ def _built():
 
 
 def run_path(prob, hidden, ids, wts, gemv):
-    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, 1 if gemv else 0)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, gemv)
     try:
         got = prob.run(hidden, ids, wts)
         status = prob.moe.status()
@@ -43,10 +45,10 @@ def run_path(prob, hidden, ids, wts, gemv):
     return got, status, acc, inter, bits
 
 
-def compare_paths(prob, hidden, ids, wts, what, ref_ids=None):
+def compare_paths(prob, hidden, ids, wts, what, ref_ids=None, gemv=1):
     ref = prob.reference(hidden, ids if ref_ids is None else ref_ids, wts)
-    g_out, g_st, g_acc, g_h, g_bits = run_path(prob, hidden, ids, wts, gemv=True)
-    t_out, t_st, t_acc, t_h, _ = run_path(prob, hidden, ids, wts, gemv=False)
+    g_out, g_st, g_acc, g_h, g_bits = run_path(prob, hidden, ids, wts, gemv=gemv)
+    t_out, t_st, t_acc, t_h, _ = run_path(prob, hidden, ids, wts, gemv=0)
     assert g_st == t_st, (g_st, t_st)
     if np.any(ref != 0):
         assert_close(g_out, ref, f"{what} (CUDA cores)")
@@ -55,9 +57,9 @@ def compare_paths(prob, hidden, ids, wts, what, ref_ids=None):
     else:
         assert np.all(g_out == 0) and np.all(t_out == 0)
     scale = float(np.abs(t_acc).max()) or 1.0
-    np.testing.assert_allclose(g_acc, t_acc, rtol=2.0 ** -10, atol=2.0 ** -12 * scale, err_msg=what)
+    np.testing.assert_allclose(g_acc, t_acc, rtol=2.0 ** -9, atol=2.0 ** -10 * scale, err_msg=what)
     hs = float(np.abs(t_h).max()) or 1.0
-    np.testing.assert_allclose(g_h, t_h, rtol=2.0 ** -10, atol=2.0 ** -24 * hs, err_msg=what + " intermediate")
+    np.testing.assert_allclose(g_h, t_h, rtol=2.0 ** -9, atol=2.0 ** -12 * hs, err_msg=what + " intermediate")
     return g_st
 
 
@@ -75,14 +77,28 @@ def test_gemv_matches_oracle_and_tensor_cores(M, num_ctas):
 
 
 def test_gemv_option_values():
-    # 2 (default): single-token batches only; 1: every batch of <= 32 slots; 0: never;
-    # anything else is rejected
+    # 1 (default): batches of <= 32 slots; 2: single-token batches only; 3: up to
+    # 256 slots; 0: never; anything else is rejected
     prob = Problem(8, 256, 128, 2)
     h = prob.moe.handle
-    for v in (0, 1, 2):
+    for v in (0, 1, 2, 3):
         pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, v)
     with pytest.raises(pkg.MoeW4A16Error):
-        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, 3)
+        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, 4)
+    prob.close()
+
+
+@pytest.mark.parametrize("num_ctas", [None, 1, 5, 256])
+@pytest.mark.parametrize("M", [9, 37, 64])
+def test_gemv_align_tile_list(M, num_ctas):
+    # more than 32 routed slots (option 3): the align kernel writes the tile list
+    # and the CUDA-core kernels read it (1 CTA: every tile through the global-memory
+    # fallback of the kernel's tile window)
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl, step=M)
+    assert compare_paths(prob, hidden, ids, wts, f"tile list M={M} ctas={num_ctas}", gemv=3) == 0
     prob.close()
 
 

@@ -185,7 +185,10 @@ def test_fused_small_batch_matches_two_launches(M, num_ctas):
     pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_FUSED_SMALL_BATCH, 1)
     fused = check_forward(prob, hidden, ids, wts, f"fused M={M} ctas={num_ctas}")
     pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_FUSED_SMALL_BATCH, 0)
+    # (against the two tensor-core launches: the same arithmetic)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, 0)
     two = check_forward(prob, hidden, ids, wts, f"two launches M={M} ctas={num_ctas}")
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, 1)
     assert_within_one_ulp(fused, two)
     prob.close()
 
@@ -208,6 +211,7 @@ def test_fused_small_batch_prepares_its_own_rows():
         inter = prob.moe.intermediate(M).cpu().numpy()
         acc = prob.moe.accumulator(M).cpu().numpy()
         pkg.moe_w4a16_set_option(h, pkg.OPT_FUSED_SMALL_BATCH, 0)
+        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, 0)  # (the tensor-core launches)
         two = check_forward(prob, hidden, ids, wts, "two launches")
         assert_within_one_ulp(got, two)
         # (the fused launch splits the gate/up steps at multiples of 4, so a split
