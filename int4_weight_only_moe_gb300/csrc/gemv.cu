@@ -127,9 +127,9 @@ constexpr int kGsBar = 0;
 constexpr int kGsMisc = kGsBar + ((kGvNumBars * 8 + 63) / 64) * 64;
 // the last chunk / step copied into each ring slot (for the teardown's drain)
 constexpr int kGsLast = kGsMisc + 64;  // int wlast[kGvNWS], blast[kGvNB]
-// the small batch's cumulative tile costs, for the cost-weighted split
-constexpr int kGsCum = kGsLast + (((kGvNWS + kGvNB) * 4 + 63) / 64) * 64;  // long long [kSmallTiles + 1]
-constexpr int kGsTiles = kGsCum + (((kSmallTiles + 1) * 8 + 63) / 64) * 64;
+// the tiles' cumulative costs, for the cost-weighted split
+constexpr int kGsCum = kGsLast + (((kGvNWS + kGvNB) * 4 + 63) / 64) * 64;  // int [kGemvMaxSlots + 1]
+constexpr int kGsTiles = kGsCum + (((kGemvMaxSlots + 1) * 4 + 63) / 64) * 64;
 constexpr int kGsRed = kGsTiles + kSmallTiles * static_cast<int>(sizeof(GvTile));  // [2][phase][t][128] f32
 constexpr int kGsBounds = kGsRed + 2 * kGvPhases * kGvRows * kBM * 4;  // int [kMaxCtas + 1]: shares
 constexpr int kGsW = ((kGsBounds + (kMaxCtas + 1) * 4 + 1023) / 1024) * 1024;
@@ -253,7 +253,7 @@ __host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 8 : T ==
 // like the even split's). cum[i] = cost of tiles 0 .. i-1 (cum[0] = 0), per step
 // of a unit; a tile has unit_steps = R * KBn steps.
 struct GvSched {
-  const long long* cum;  // [ntiles + 1], shared memory
+  const int* cum;  // [ntiles + 1], shared memory
   int ntiles, G;
   long long unit_steps;
   __device__ __forceinline__ long long total_steps() const { return ntiles * unit_steps; }
@@ -368,25 +368,49 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
   const int G = static_cast<int>(gridDim.x);
   // Shares: a small batch's weighted by the tiles' costs (its tiles are all in
   // shared memory); the align kernel's list split evenly.
-  // (tiles of one cost, as at decode, take the even split's simpler arithmetic)
-  long long* cum = reinterpret_cast<long long*>(gbase + kGsCum);
+  // (tiles of one cost, as at decode, take the even split's simpler arithmetic).
+  // Costs per tile into cum[1..], then a prefix sum by warp 0.
+  int* cum = reinterpret_cast<int*>(gbase + kGsCum);
   int* weighted_sm = reinterpret_cast<int*>(gbase + kGsMisc + 12);
-  if (threadIdx.x == 0) {
+  for (int i = threadIdx.x; i < ntiles; i += blockDim.x)
+    cum[i + 1] = gv_step_cost(small ? tiles[i].n : a.gv_tiles[i].n);
+  __syncthreads();
+  if (warp == 0) {
+    // lane l sums tiles 8l .. 8l + 7 (ntiles <= 256), then a warp scan of the lane sums
+    constexpr int kPer = (kGemvMaxSlots + 31) / 32;
+    int v[kPer];
+    int lane_sum = 0;
     bool uneven = false;
-    if (small) {
-      long long c = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        cum[i] = c;
-        c += gv_step_cost(tiles[i].n);
-        uneven = uneven || tiles[i].n != tiles[0].n;
-      }
-      cum[ntiles] = c;
+    const int c0 = ntiles > 0 ? cum[1] : 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = lane * kPer + j;
+      v[j] = i < ntiles ? cum[i + 1] : 0;
+      lane_sum += v[j];
+      uneven = uneven || (i < ntiles && v[j] != c0);
     }
-    if (!uneven) {
+    int incl = lane_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uneven = __any_sync(0xffffffffu, uneven);
+    __syncwarp();  // (every lane has read its costs before any lane overwrites)
+    if (uneven) {
+      int run = incl - lane_sum;  // cost of the tiles before this lane's
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = lane * kPer + j;
+        if (i < ntiles) cum[i] = run;
+        run += v[j];
+      }
+      if (lane == 31) cum[ntiles] = incl;
+    } else if (lane == 0) {
       cum[0] = 0;  // an even split: one cost unit per step of one tile spanning all
       cum[1] = 1;
     }
-    *weighted_sm = uneven ? 1 : 0;
+    if (lane == 0) *weighted_sm = uneven ? 1 : 0;
   }
   __syncthreads();
   const bool weighted = *weighted_sm != 0;

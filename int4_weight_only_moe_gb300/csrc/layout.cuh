@@ -96,7 +96,8 @@ struct TokenTile {
 // of one expert -- padded rows p0 .. p0+n-1 of the expert-sorted order -- and the
 // flat slot of each.
 constexpr int kGemvRows = 4;
-constexpr int kGemvMaxSlots = 256;  // routed slots up to which a forward may use them
+constexpr int kGemvMaxSlots = 256;      // routed slots up to which a forward may use them
+constexpr int kGemvDefaultSlots = 128;  // ... and by default (measured faster up to there)
 struct GemvTile {
   int e, p0, n, pad;
   int slot[kGemvRows];

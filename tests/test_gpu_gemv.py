@@ -20,7 +20,7 @@ from int4_weight_only_moe_gb300 import inputs
 from tests.gpu_helpers import (Problem, assert_close, bf16_tensor_to_f64, check_accumulator, workload_inputs)
 
 pytestmark = pytest.mark.gpu
-GEMV_DEFAULT = 1  # the CUDA-core path for every batch of at most 32 routed slots
+GEMV_DEFAULT = 1  # the CUDA-core path for batches of at most 128 routed slots
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -77,7 +77,7 @@ def test_gemv_matches_oracle_and_tensor_cores(M, num_ctas):
 
 
 def test_gemv_option_values():
-    # 1 (default): batches of <= 32 slots; 2: single-token batches only; 3: up to
+    # 1 (default): batches of <= 128 slots; 2: single-token batches only; 3: up to
     # 256 slots; 0: never; anything else is rejected
     prob = Problem(8, 256, 128, 2)
     h = prob.moe.handle
@@ -91,9 +91,9 @@ def test_gemv_option_values():
 @pytest.mark.parametrize("num_ctas", [None, 1, 5, 256])
 @pytest.mark.parametrize("M", [9, 37, 64])
 def test_gemv_align_tile_list(M, num_ctas):
-    # more than 32 routed slots (option 3): the align kernel writes the tile list
-    # and the CUDA-core kernels read it (1 CTA: every tile through the global-memory
-    # fallback of the kernel's tile window)
+    # more than 32 routed slots (up to 256 with option 3): the align kernel writes
+    # the tile list and the CUDA-core kernels read it (1 CTA: every tile through
+    # the global-memory fallback of the kernel's tile window)
     E, K, N, k = 16, 512, 256, 4
     prob = Problem(E, K, N, k, num_ctas=num_ctas)
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
