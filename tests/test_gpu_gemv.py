@@ -17,7 +17,8 @@ import torch
 import int4_weight_only_moe_gb300 as pkg
 import oracle
 from int4_weight_only_moe_gb300 import inputs
-from tests.gpu_helpers import (Problem, assert_close, bf16_tensor_to_f64, check_accumulator, workload_inputs)
+from tests.gpu_helpers import (Problem, assert_close, bf16_tensor_to_f64, bits16, check_accumulator, dev,
+                               workload_inputs)
 
 pytestmark = pytest.mark.gpu
 GEMV_DEFAULT = 1  # the CUDA-core path for batches of at most 128 routed slots
@@ -174,4 +175,36 @@ def test_both_small_batch_paths_give_up_cleanly():
         assert prob.moe.status() == 0
         assert_close(got, prob.reference(hidden, ids, wts), f"after give-up, gemv={gemv}")
     pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, GEMV_DEFAULT)
+    prob.close()
+
+
+@pytest.mark.parametrize("case", ["routed", "no valid slot"])
+@pytest.mark.parametrize("num_ctas", [None, 1, 7])
+def test_gemv_writes_every_output_element(case, num_ctas):
+    # an output buffer filled with NaNs beforehand comes back fully written, equal
+    # to the rounding of the accumulator, with tokens that have no valid slot (and
+    # a batch with none at all) as zeros
+    E, K, N, k, M = 8, 512, 256, 4, 5
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl)
+    ids = ids.copy()
+    if case == "routed":
+        ids[2, :] = E + 1  # token 2: no valid slot
+    else:
+        ids[:] = -1
+    out = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    prob.moe.forward(dev(bits16(hidden)), dev(ids), dev(wts), out=out)
+    torch.cuda.synchronize()
+    got = bf16_tensor_to_f64(out)
+    assert np.all(np.isfinite(got))
+    acc = prob.moe.accumulator(M).cpu().numpy()
+    np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16),
+                                  inputs.f32_to_bf16_bits(acc.astype(np.float32)))
+    ref = prob.reference(hidden, np.where((ids < 0) | (ids >= E), -1, ids), wts)
+    if case == "routed":
+        assert np.all(got[2] == 0)
+        assert_close(got, ref, "every element written")
+    else:
+        assert np.all(got == 0)
     prob.close()
