@@ -272,11 +272,22 @@ const char* moe_w4a16_last_error(void);
  *                            offset applied through the group's exact value sum,
  *                            one fp32 rounding per group. The tensor-core kernels
  *                            round the activations to fp16 instead; the two agree
- *                            to about 2^-12 of the output's magnitude. */
+ *                            to about 2^-12 of the output's magnitude.
+ *   MOE_W4A16_OPT_GEMV_ONE_LAUNCH
+ *                            1 = with at most 32 routed slots on the CUDA cores and
+ *                            a grid of at most one CTA per SM, both products run in
+ *                            one cooperative launch (the down product's weights
+ *                            stream right after the gate/up product's; its
+ *                            activation rows are taken over from the gate/up
+ *                            epilogues of the whole grid through counters);
+ *                            0 (default) = two launches, measured faster on GB300
+ *                            (the cooperative launch cannot start while the
+ *                            routing kernel runs). Same arithmetic. */
 enum { MOE_W4A16_OPT_NUM_CTAS = 1, MOE_W4A16_OPT_PROFILE = 2, MOE_W4A16_OPT_PDL = 3,
        MOE_W4A16_OPT_STEP_COST_GATEUP = 4, MOE_W4A16_OPT_STEP_COST_DOWN = 5,
        MOE_W4A16_OPT_WAIT_LIMIT_US = 6, MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES = 7,
-       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8, MOE_W4A16_OPT_GEMV_SMALL_BATCH = 9 };
+       MOE_W4A16_OPT_FUSED_SMALL_BATCH = 8, MOE_W4A16_OPT_GEMV_SMALL_BATCH = 9,
+       MOE_W4A16_OPT_GEMV_ONE_LAUNCH = 10 };
 int moe_w4a16_set_option(moe_w4a16_t h, int option, int value);
 
 /* Milliseconds of each kernel of the last profiled forward, in launch order

@@ -21,7 +21,7 @@ __all__ = [
     "moe_w4a16_align_debug", "moe_w4a16_unpack_debug", "moe_w4a16_read_intermediate",
     "moe_w4a16_schedule_debug", "moe_w4a16_read_accumulator", "moe_w4a16_route", "moe_w4a16_forward_logits", "moe_w4a16_forward_noalloc", "NOALLOC_WORKSPACE_BYTES", "MoEW4A16",
     "OPT_NUM_CTAS", "OPT_PROFILE", "OPT_PDL", "OPT_STEP_COST_GATEUP", "OPT_STEP_COST_DOWN",
-    "OPT_WAIT_LIMIT_US", "OPT_TEST_WAIT_NEVER_COMPLETES", "OPT_FUSED_SMALL_BATCH", "OPT_GEMV_SMALL_BATCH", "STATUS_BAD_EXPERT_ID", "STATUS_TIMEOUT", "STATUS_H_SATURATED",
+    "OPT_WAIT_LIMIT_US", "OPT_TEST_WAIT_NEVER_COMPLETES", "OPT_FUSED_SMALL_BATCH", "OPT_GEMV_SMALL_BATCH", "OPT_GEMV_ONE_LAUNCH", "STATUS_BAD_EXPERT_ID", "STATUS_TIMEOUT", "STATUS_H_SATURATED",
     "STATUS_BAD_SCHEDULE",
 ]
 
@@ -36,6 +36,7 @@ OPT_STEP_COST_GATEUP, OPT_STEP_COST_DOWN, OPT_WAIT_LIMIT_US = 4, 5, 6
 OPT_TEST_WAIT_NEVER_COMPLETES = 7
 OPT_FUSED_SMALL_BATCH = 8
 OPT_GEMV_SMALL_BATCH = 9
+OPT_GEMV_ONE_LAUNCH = 10
 NOALLOC_WORKSPACE_BYTES = 48 << 20
 
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p

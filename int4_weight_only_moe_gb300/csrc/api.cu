@@ -23,6 +23,7 @@ struct moe_w4a16_ctx {
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
   bool fused_small;            // MOE_W4A16_OPT_FUSED_SMALL_BATCH
   int gemv_small;              // MOE_W4A16_OPT_GEMV_SMALL_BATCH (0, 1: <= 128 slots, 2: one token, 3: <= 256 slots)
+  bool gemv_one_launch;        // MOE_W4A16_OPT_GEMV_ONE_LAUNCH
   int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
   uint8_t* w2p;
@@ -190,6 +191,7 @@ int moe_w4a16_create(int E, int K, int N, int topk, int group_size, moe_w4a16_t*
   h->pdl = true;
   h->fused_small = false;
   h->gemv_small = 1;
+  h->gemv_one_launch = false;
   h->step_cost[0] = kDefaultStepCostGateUp;
   h->step_cost[1] = kDefaultStepCostDown;
   cudaError_t e = cudaGetDevice(&h->device);
@@ -374,6 +376,9 @@ int moe_w4a16_set_option(moe_w4a16_t h, int option, int value) {
       if (value < 0 || value > 3) return fail(MOE_W4A16_INVALID_ARG, "GEMV option must be 0, 1, 2 or 3");
       h->gemv_small = value;
       return MOE_W4A16_OK;
+    case MOE_W4A16_OPT_GEMV_ONE_LAUNCH:
+      h->gemv_one_launch = value != 0;
+      return MOE_W4A16_OK;
     case MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES:
       h->test_never_wait = value != 0;
       return MOE_W4A16_OK;
@@ -512,6 +517,10 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
                            : h->gemv_small == 2 ? M == 1
                            : h->gemv_small == 3 ? MK <= kGemvMaxSlots : false;
   const bool gemv = !fused && gemv_wanted && MK * static_cast<long long>(2 * h->N / kBM) * (h->K / 128) < (1LL << 31);
+  // ... and for at most 32 routed slots both of them in one cooperative launch (at
+  // most one CTA per SM; the intermediate's step rows are handed over between CTAs
+  // through counters in the ticket area, which the routing kernel zeroes)
+  const bool gemv_one = gemv && MK <= 32 && h->gemv_one_launch && h->num_ctas <= h->num_sms;
   uint8_t* xv1 = ws + L.xv1;
   uint8_t* xv2 = ws + L.xv2;
   GemvTile* gv_tiles = reinterpret_cast<GemvTile*>(ws + L.gv_tiles);
@@ -593,9 +602,9 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   g1.E = h->E;
   g1.dbg = hdr + 8;
   g1.sched = (sched && h->step_cost[0] > 0) ? sched : nullptr;
-  if (gemv)
-    MOE_CUDA_TRY(launch_gemv_gateup(g1, h->num_ctas, s, pdl));
-  else if (!fused)
+  if (gemv) {
+    if (!gemv_one) MOE_CUDA_TRY(launch_gemv_gateup(g1, h->num_ctas, s, pdl));
+  } else if (!fused)
     MOE_CUDA_TRY(launch_gemm_gateup(g1, h->num_ctas, s, pdl));
   if (prof) MOE_CUDA_TRY(cudaEventRecord(h->ev[3], s));
 
@@ -659,6 +668,18 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
     P.topk = h->topk;
     g2.prep = P;
     MOE_CUDA_TRY(launch_gemm_fused(g1, g2, h->num_ctas, s, false));
+  } else if (gemv_one) {
+    // the counters after the split-unit tickets and the row-tile words:
+    // [kSmallTiles][N/128], one per tile and down step
+    g1.h_ready = g2.h_ready = tickets + kMaxCtas + h->K / kBM;
+    cudaError_t e = launch_gemv_both(g1, g2, h->num_ctas, s, pdl);
+    if (e != cudaSuccess && pdl) {
+      // (should the driver refuse a cooperative launch with programmatic
+      // dependence: launch it after the routing kernel instead)
+      (void)cudaGetLastError();
+      e = launch_gemv_both(g1, g2, h->num_ctas, s, false);
+    }
+    MOE_CUDA_TRY(e);
   } else if (gemv) {
     MOE_CUDA_TRY(launch_gemv_down(g2, h->num_ctas, s, pdl));
   } else {

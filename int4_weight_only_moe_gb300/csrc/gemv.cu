@@ -1,24 +1,22 @@
-// The two expert products of a small batch (at most 32 routed slots) on the CUDA
-// cores: with one to four tokens per expert each product is a matrix-vector
-// product, bound by the packed weight stream, so the weights are dequantised and
+// The two expert products of a small batch (by default at most 128 routed slots)
+// on the CUDA cores: with one to four tokens per expert each product is a
+// matrix-vector product, bound by the packed weight stream, so the weights are
 // multiplied in registers instead of being written to tensor memory for an MMA
 // whose 16-column token tile would be mostly padding.
 //
 //   gate/up:  [g; u] = W1[e] . x_t, epilogue h = SiLU(g) * u -> fp16 intermediate
-//             (blocked layout) and the per-group sums of h the down product needs
+//             (blocked layout) and h as step rows of the down product
 //   down:     y = W2[e] . h_r, epilogue acc[t] += topk_weight * y (fp32 red.add)
 //
-// Arithmetic. A packed word holds eight 4-bit codes u of consecutive reduction
-// elements; one three-input logic op (after a shift for three of the four pairs)
-// turns a pair into the fp16 pair 16 + u, exactly. The products (16 + u) * x are
-// exact in fp32 (5 x 11 significant bits) and summed over the scale group of 32
-// elements in fp32 with mixed-precision fma (f16 operands, f32 addend). The
-// group's contribution is then
-//     sum_k (u_k - 8) s x_k  =  s * (sum_k (16 + u_k) x_k  -  24 * X),
-// with X = sum_k x_k over the group (written alongside the operand rows by the
-// kernel that produces them: the routing + gather kernel for the hidden states,
-// the gate/up epilogue for h). The subtraction cancels about 5 of fp32's 24
-// bits, far below the fp16 rounding of the operands and the bf16 output.
+// Arithmetic. The activations of every scale group of 32 reduction elements are
+// 16-bit block fixed point, v = round(x * 2^e) with the group's exponent e
+// chosen so that its largest |v| lies in [2^13, 2^14), written with the group's
+// exact value sum V by the kernel that produces them (the routing + gather
+// kernel for the hidden states, the gate/up epilogue for h). A packed word holds
+// eight 4-bit codes u; a rotate and a mask turn four of them into bytes, and
+// dp2a multiplies two bytes with two 16-bit values and adds, exactly, in int32.
+// Per group and weight row the result is s * 2^-e * (sum u v - 8 V): the bracket
+// is an exact integer below 2^23, so a group costs one fp32 rounding.
 //
 // Per CTA (one per SM), 24 warps, the same work on every SM sub-partition (warp
 // w runs on sub-partition w % 4):
@@ -45,9 +43,9 @@
 //                CTA order by the last contributor), applies SiLU*up or the
 //                weighted scatter-add
 //
-// Work split: the same stream-K split as the tensor-core kernel (units (tile,
-// 128-row weight tile) of K/128 steps laid end to end, an equal contiguous share
-// per CTA). Every wait is bounded; a wait that gives up raises the CTA's abort
+// Work split: stream-K as in the tensor-core kernel (units (tile, 128-row weight
+// tile) of K/128 steps laid end to end, a contiguous share per CTA, equal in
+// steps, or in cost where the tiles' row counts differ). Every wait is bounded; a wait that gives up raises the CTA's abort
 // flag and records MOE_W4A16_STATUS_TIMEOUT, and every role falls through to the
 // teardown, which lets the copies in flight land.
 #include <cuda_bf16.h>
@@ -64,13 +62,13 @@ namespace moe {
 // stamps of one multiply warp and of the weight producer; read back with
 // moe_gemv_trace_read(). Compiled out otherwise.
 #ifdef MOE_GEMM_TRACE
-__device__ unsigned long long g_gv_cta[2][256][16];
-__device__ unsigned long long g_gv_steps[2][8][1024];
+__device__ unsigned long long g_gv_cta[3][256][16];
+__device__ unsigned long long g_gv_steps[3][8][1024];
 extern "C" int moe_gemv_trace_read(unsigned long long* cta, unsigned long long* steps, int reset) {
   int e = static_cast<int>(cudaMemcpyFromSymbol(cta, g_gv_cta, sizeof(g_gv_cta)));
   if (e == 0) e = static_cast<int>(cudaMemcpyFromSymbol(steps, g_gv_steps, sizeof(g_gv_steps)));
   if (reset) {
-    static unsigned long long z[2 * 8 * 1024];
+    static unsigned long long z[3 * 8 * 1024];
     cudaMemcpyToSymbol(g_gv_cta, z, sizeof(g_gv_cta));
     cudaMemcpyToSymbol(g_gv_steps, z, sizeof(g_gv_steps));
   }
@@ -276,9 +274,20 @@ struct GvSched {
   }
 };
 
-// kMode 1: gate/up + SwiGLU; 2: down + weighted scatter-add.
+// kMode 1: gate/up + SwiGLU; 2: down + weighted scatter-add (b unused: = a);
+// 3: both products of a batch of at most 32 routed slots in one launch, a = the
+// gate/up product's arguments, b = the down product's. In one launch every role
+// runs the gate/up share and then the down share of its CTA as one sequence of
+// steps (the rings run on across the boundary), so the down product's weight
+// stream follows the gate/up one without a gap; the down product's activation
+// rows are the intermediate that the gate/up epilogues of the whole grid write,
+// so the fourth copy producer takes them (and leaves the weight copies to the
+// other three): it waits per (tile, step) for the two gate/up epilogues that
+// write each step row (counters raised with a fence and an atomic add). All CTAs
+// are resident together (cooperative launch).
 template <int kMode>
-__global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a, const GemmArgs b) {
+  constexpr int kNph = kMode == 3 ? 2 : 1;  // products in this launch
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -288,6 +297,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
   volatile int* last_flag = reinterpret_cast<volatile int*>(gbase + kGsMisc + 4);
   int* ntiles_sm = reinterpret_cast<int*>(gbase + kGsMisc + 8);
   volatile int* epi_ok = reinterpret_cast<volatile int*>(gbase + kGsMisc + 16);  // [2][4]
+  // (one launch) multiply warps through the gate/up steps
+  volatile int* phase_a_done = reinterpret_cast<volatile int*>(gbase + kGsMisc + 56);
   GvTile* tiles = reinterpret_cast<GvTile*>(gbase + kGsTiles);
   float* red = reinterpret_cast<float*>(gbase + kGsRed);
   int* bounds = reinterpret_cast<int*>(gbase + kGsBounds);
@@ -358,6 +369,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     mbar_init(bar(kGbNever), 1);
     *abort_flag = 0;
     *last_flag = 0;
+    *phase_a_done = 0;
     fence_mbar_init();
     GV_STAMP(10);
   }
@@ -419,9 +431,16 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
   // CTAs that share a unit, then cost nothing
   const int sc_tiles = weighted ? ntiles : 1;
   const long long sc_unit = weighted ? static_cast<long long>(a.R) * a.KBn : static_cast<long long>(ntiles) * a.R * a.KBn;
+  int* shares_b = reinterpret_cast<int*>(gbase + kGsMisc + 48);  // [2] the down share (one launch)
   {
     const GvSched s0{cum, sc_tiles, G, sc_unit};
     for (int c = threadIdx.x; c <= G; c += blockDim.x) bounds[c] = static_cast<int>(s0.start(c));
+    if (kMode == 3 && warp == kGvWarpEpi0) {
+      // (an epilogue warp, idle here: this CTA's share of the down product)
+      const GvSched s1{cum, sc_tiles, G,
+                       weighted ? static_cast<long long>(b.R) * b.KBn : static_cast<long long>(ntiles) * b.R * b.KBn};
+      if (lane < 2) shares_b[lane] = static_cast<int>(s1.start(static_cast<int>(blockIdx.x) + lane));
+    }
   }
   __syncthreads();
   const long long my_begin = bounds[blockIdx.x], my_end = bounds[blockIdx.x + 1];
@@ -434,8 +453,22 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     }
     return lo;
   };
-  const long long n_it = my_end - my_begin;
+  // this CTA's sequence: the gate/up (or the one) product's n1 steps, then in one
+  // launch the down product's n_it - n1
+  const long long n1 = my_end - my_begin;
+  const long long b2 = kMode == 3 ? shares_b[0] : 0, e2 = kMode == 3 ? shares_b[1] : 0;
+  const long long n_it = n1 + (e2 - b2);
   const GvSeq seq(my_begin, my_end, a.KBn);
+  const GvSeq seq2(b2, e2, kMode == 3 ? b.KBn : a.KBn);
+  // step `it` of the sequence -> product ph, unit, k-block, end of its run in the unit
+  // (a run never crosses from one product to the other)
+  auto step_at = [&](long long it, int& ph, long long& u, int& kb, int& kbe) {
+    ph = (kMode == 3 && it >= n1) ? 1 : 0;
+    if (ph)
+      seq2.at(it - n1, u, kb, kbe);
+    else
+      seq.at(it, u, kb, kbe);
+  };
   // Tiles in shared memory: all of a small batch's; for the align kernel's list
   // the window of this CTA's share (tiles beyond it, only when a CTA spans more
   // than kGvTileCache tiles, are read from global memory).
@@ -464,34 +497,101 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     const uint64_t w_policy = l2_policy_evict_first();  // read once: keep L2 for the operands
     for (long long it = it0; it < it1;) {
       long long u;
-      int kb, kbe;
-      seq.at(it, u, kb, kbe);
+      int ph, kb, kbe;
+      step_at(it, ph, u, kb, kbe);
       const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
-      const int e = tile_at(u / a.R)->e;
-      const int rt = static_cast<int>(u % a.R);
-      const long long woff = ((static_cast<long long>(e) * a.R + rt) * a.KBn + kb) * kGvStepBytes;
-      if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kGvStepBytes <= a.wpack_bytes && e >= 0 &&
-                        e < a.E && run >= 1,
+      const int R = ph ? b.R : a.R, KBn = ph ? b.KBn : a.KBn;
+      const int e = tile_at(u / R)->e;
+      const int rt = static_cast<int>(u % R);
+      const long long woff = ((static_cast<long long>(e) * R + rt) * KBn + kb) * kGvStepBytes;
+      if (MOE_CHECK(woff >= 0 && woff + static_cast<long long>(run) * kGvStepBytes <= (ph ? b.wpack_bytes : a.wpack_bytes) &&
+                        e >= 0 && e < a.E && run >= 1,
                     a.status, a.dbg, 41, woff, run))
-        bulk_g2s_hint(sW + s * kGvChunkBytes + static_cast<uint32_t>(it - it0) * kGvStepBytes, a.wpack + woff,
-                      static_cast<uint32_t>(run) * kGvStepBytes, bar(kGbWFull + s), w_policy);
+        bulk_g2s_hint(sW + s * kGvChunkBytes + static_cast<uint32_t>(it - it0) * kGvStepBytes,
+                      (ph ? b.wpack : a.wpack) + woff, static_cast<uint32_t>(run) * kGvStepBytes, bar(kGbWFull + s),
+                      w_policy);
       it += run;
     }
   };
+
+  // Activation chunks: 8 steps each, every token row of their tiles. In one
+  // launch the down product's steps start a fresh chunk (pad skipped positions):
+  // a chunk holding both products' steps would make the last gate/up steps of
+  // the CTA wait for intermediate rows that they themselves help to finish.
+  const long long nbA = (n1 + kGvBSteps - 1) / kGvBSteps;  // chunks of the first product's steps
+  const long long pad = (kMode == 3 && n_it > n1) ? nbA * kGvBSteps - n1 : 0;
+  auto b_chunk = [&](long long nb, long long& it0, long long& it1) {
+    it0 = nb < nbA ? nb * kGvBSteps : nb * kGvBSteps - pad;
+    const long long lim = nb < nbA ? n1 : n_it;
+    it1 = it0 + kGvBSteps < lim ? it0 + kGvBSteps : lim;
+  };
+  // Copy activation chunk nb into its ring slot, once the slot is free.
+  auto issue_b = [&](long long nb) {
+    const int s = static_cast<int>(nb % kGvNB);
+    long long it0, it1;
+    b_chunk(nb, it0, it1);
+    // the chunk's pieces (one per unit it touches): their bytes, then the copies
+    uint32_t bytes = 0;
+    for (long long it = it0; it < it1;) {
+      long long u;
+      int ph, kb, kbe;
+      step_at(it, ph, u, kb, kbe);
+      const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
+      bytes += static_cast<uint32_t>(tile_at(u / (ph ? b.R : a.R))->n * run * kXvStepBytes);
+      it += run;
+    }
+    blast[s] = static_cast<int>(nb);
+    mbar_arrive_expect_tx(bar(kGbBFull + s), bytes);
+    for (long long it = it0; it < it1;) {
+      long long u;
+      int ph, kb, kbe;
+      step_at(it, ph, u, kb, kbe);
+      const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
+      const GvTile& tl = *tile_at(u / (ph ? b.R : a.R));
+      const int KBn = ph ? b.KBn : a.KBn;
+      for (int t = 0; t < tl.n; ++t) {
+        // (step rows are indexed by the routed slot)
+        const long long xoff = (static_cast<long long>(tl.slot[t]) * KBn + kb) * kXvStepBytes;
+        if (MOE_CHECK(xoff >= 0 && xoff + static_cast<long long>(run) * kXvStepBytes <= (ph ? b.xv_bytes : a.xv_bytes) &&
+                          tl.n <= kGvRows,
+                      a.status, a.dbg, 42, xoff, run))
+          bulk_g2s(sB + static_cast<uint32_t>(s) * kGvBStage + t * kGvBRow + static_cast<uint32_t>(it - it0) * kXvStepBytes,
+                   (ph ? b.xv_in : a.xv_in) + xoff, static_cast<uint32_t>(run) * kXvStepBytes, bar(kGbBFull + s));
+      }
+      it += run;
+    }
+    // a gate/up chunk cut short by the padding: its missing steps' reader
+    // arrivals (4 a step), so that the slot's next use finds it released
+    if (kMode == 3 && pad > 0 && nb == nbA - 1)
+      mbar_arrive_cnt(bar(kGbBEmpty + s), static_cast<uint32_t>(4 * (kGvBSteps - (it1 - it0))));
+  };
+  const long long n_bchunks = (n_it + pad + kGvBSteps - 1) / kGvBSteps;
+  // (in one launch the down product's chunks are the fourth producer's)
+  const long long nb_copier = kMode == 3 ? nbA : n_bchunks;
 
   if (warp >= kGvWarpP0 && warp < kGvWarpEpi0) {
     // ------------------------------------------------ copy producers
     if (lane == 0) {
       const int q = warp - kGvWarpP0;  // (= this warp's sub-partition)
+      // Chunks go round kP producers. A producer issues an activation chunk only
+      // once its weight copies have reached the chunk's steps, and a weight copy
+      // waits for its slot's reader 10 chunks back: so it is never two uses of a
+      // slot ahead of the readers, and a parity wait on the slot's release means
+      // the latest use. In one launch the fourth producer issues no weight copies
+      // and takes the down product's activation chunks, which wait for other
+      // CTAs: it starts only once every multiply warp is through the gate/up
+      // steps (then each slot's barrier is at a known phase, and from there on
+      // only this producer refills the slots).
+      constexpr int kP = kMode == 3 ? 3 : 4;
+      const bool copier = kMode == 3 && q == 3;
       // activation rows: the preceding kernel's output
       bool b_ready = false;
-      const long long n_bchunks = (n_it + kGvBSteps - 1) / kGvBSteps;
-      long long nb = q, nw = q;  // next activation chunk, next weight chunk of this producer
-      while (nw < kGvNWS) nw += 4;  // (the multiply warps copy the ring's first chunks)
-      while (nb < n_bchunks || nw < n_chunks) {
+      long long nb = copier ? n_bchunks : q, nw = copier ? n_chunks : q;  // next activation / weight chunk
+      while (nw < kGvNWS) nw += kP;  // (the multiply warps copy the ring's first chunks)
+      while (nb < nb_copier || nw < n_chunks) {
         // the copy feeding the earlier step first: a wait then only depends on
         // steps whose copies were issued before it
-        if (nb < n_bchunks && (nw >= n_chunks || nb * kGvBSteps <= nw * kGvChunk)) {
+        if (nb < nb_copier && (nw >= n_chunks || nb * kGvBSteps <= nw * kGvChunk)) {
           if (!b_ready) {
             if (!a.ids_after_pdl) pdl_wait();
             if (q == 0) GV_STAMP(2);
@@ -501,46 +601,51 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
           if (!mbar_wait(bar(kGbBEmpty + s), static_cast<uint32_t>((nb / kGvNB) & 1) ^ 1u, abort_flag, status,
                          kStatusTimeout, wait_ns))
             break;
-          const long long it0 = nb * kGvBSteps;
-          const long long it1 = it0 + kGvBSteps < n_it ? it0 + kGvBSteps : n_it;
-          // the chunk's pieces (one per unit it touches): their bytes, then the copies
-          uint32_t bytes = 0;
-          for (long long it = it0; it < it1;) {
-            long long u;
-            int kb, kbe;
-            seq.at(it, u, kb, kbe);
-            const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
-            bytes += static_cast<uint32_t>(tile_at(u / a.R)->n * run * kXvStepBytes);
-            it += run;
-          }
-          blast[s] = static_cast<int>(nb);
-          mbar_arrive_expect_tx(bar(kGbBFull + s), bytes);
-          for (long long it = it0; it < it1;) {
-            long long u;
-            int kb, kbe;
-            seq.at(it, u, kb, kbe);
-            const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
-            const GvTile& tl = *tile_at(u / a.R);
-            for (int t = 0; t < tl.n; ++t) {
-              // (step rows are indexed by the routed slot)
-              const long long xoff = (static_cast<long long>(tl.slot[t]) * a.KBn + kb) * kXvStepBytes;
-              if (MOE_CHECK(xoff >= 0 && xoff + static_cast<long long>(run) * kXvStepBytes <= a.xv_bytes &&
-                                tl.n <= kGvRows,
-                            a.status, a.dbg, 42, xoff, run))
-                bulk_g2s(sB + static_cast<uint32_t>(s) * kGvBStage + t * kGvBRow +
-                             static_cast<uint32_t>(it - it0) * kXvStepBytes,
-                         a.xv_in + xoff, static_cast<uint32_t>(run) * kXvStepBytes, bar(kGbBFull + s));
-            }
-            it += run;
-          }
-          nb += 4;
+          issue_b(nb);
+          nb += kP;
         } else {
           const int s = static_cast<int>(nw % kGvNWS);
           if (!mbar_wait(bar(kGbWEmpty + s), static_cast<uint32_t>((nw / kGvNWS) & 1) ^ 1u, abort_flag, status,
                          kStatusTimeout, wait_ns))
             break;
           issue_w(nw);
-          nw += 4;
+          nw += kP;
+        }
+      }
+      if (copier && *abort_flag == 0 && nb_copier < n_bchunks) {
+        pdl_wait();  // (the zeroed counters)
+        // every multiply warp through the gate/up steps (bounded like every wait)
+        const long long t0 = clock64();
+        while (*phase_a_done < kGvWarpP0 && *abort_flag == 0) {
+          if (((clock64() - t0) >> 10) > static_cast<long long>(wait_ns)) {
+            *abort_flag = 1;
+            atomicOr(status, kStatusTimeout);
+          }
+          __nanosleep(128);
+        }
+        for (long long nc = nb_copier; nc < n_bchunks && *abort_flag == 0; ++nc) {
+          // the chunk's down steps: wait until both gate/up epilogues of every one
+          // of their step rows have stored it (per tile and step: a counter)
+          bool ok = true;
+          long long it0c, it1;
+          b_chunk(nc, it0c, it1);
+          for (long long it = it0c; ok && it < it1;) {
+            long long u;
+            int ph, kb, kbe;
+            step_at(it, ph, u, kb, kbe);
+            const int run = static_cast<int>(it1 - it < kbe - kb ? it1 - it : kbe - kb);
+            const long long ti = u / b.R;
+            if (ph == 1 &&
+                MOE_CHECK(ti >= 0 && ti < kSmallTiles && kb + run <= b.KBn, a.status, a.dbg, 47, ti, kb))
+              ok = wait_counters(b.h_ready + ti * b.KBn + kb, run, 2, abort_flag, status, wait_ns);
+            it += run;
+          }
+          if (nc == nb_copier) GV_STAMP(12);
+          const int s = static_cast<int>(nc % kGvNB);
+          if (!ok || (nc >= kGvNB && !mbar_wait(bar(kGbBEmpty + s), static_cast<uint32_t>((nc / kGvNB) & 1) ^ 1u,
+                                                 abort_flag, status, kStatusTimeout, wait_ns)))
+            break;
+          issue_b(nc);
         }
       }
     }
@@ -552,20 +657,24 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     const int quad = warp & 3;
     const int phase = warp >> 2;
     const int r = quad * 32 + lane;
-    SegIter si(my_begin, my_end, a.KBn);
     long long u;
     int kb0, kb1;
     uint32_t it_base = 0, ru = 0;
     bool ok = true;
+#pragma unroll 1
+    for (int ph = 0; ph < kNph; ++ph) {
+    const int R = ph ? b.R : a.R;
+    SegIter si(ph ? b2 : my_begin, ph ? e2 : my_end, ph ? b.KBn : a.KBn);
     while (ok && si.next(u, kb0, kb1)) {
       const uint32_t len = static_cast<uint32_t>(kb1 - kb0);
-      const int T = tile_at(u / a.R)->n;
+      const int T = tile_at(u / R)->n;
       float acc[kGvRows] = {0.f, 0.f, 0.f, 0.f};
       for (uint32_t it = it_base + ((static_cast<uint32_t>(phase) - it_base) & 3u); it < it_base + len;
            it += kGvPhases) {
         const uint32_t c = it >> 1;
         const uint32_t ws = c % kGvNWS, wpar = (c / kGvNWS) & 1u;
-        const uint32_t cb = it / kGvBSteps;
+        const uint32_t vb = it + ((kMode == 3 && it >= n1) ? static_cast<uint32_t>(pad) : 0u);  // (padded)
+        const uint32_t cb = vb / kGvBSteps;
         const uint32_t sb = cb % kGvNB, bpar = (cb / kGvNB) & 1u;
         bool w_ok = mbar_wait(bar(kGbWFull + ws), wpar, abort_flag, status, kStatusTimeout, wait_ns);
         if (warp == 0 && lane == 0) {
@@ -582,7 +691,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
           break;
         }
         const uint8_t* wstep = gbase + kGsW + ws * kGvChunkBytes + (it & 1u) * kGvStepBytes;
-        const uint8_t* xst = gbase + kGsB + sb * kGvBStage + (it % kGvBSteps) * kXvStepBytes;
+        const uint8_t* xst = gbase + kGsB + sb * kGvBStage + (vb % kGvBSteps) * kXvStepBytes;
         if (T == 1) {
           gv_step<1, 0>(wstep, xst, r, acc);
         } else {
@@ -615,6 +724,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
       if (lane == 0) mbar_arrive(bar(kGbRedFull + rs));
       ++ru;
     }
+    // (one launch: this warp has released every gate/up activation chunk)
+    if (kMode == 3 && ph == 0 && ok && lane == 0) atomicAdd(const_cast<int*>(phase_a_done), 1);
+    }
   } else {
     // ------------------------------------------------ epilogue
     pdl_wait();  // exponents, zeroed accumulator and tickets, routing weights
@@ -623,15 +735,20 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
     if (a.test_never_wait) mbar_wait(bar(kGbNever), 0, abort_flag, a.status, kStatusTimeout, wait_ns);
     const int tid = threadIdx.x - kGvWarpEpi0 * 32;  // = the weight row this thread sums
     const int ew = tid >> 5;
-    SegIter si(my_begin, my_end, a.KBn);
+    const GemmArgs& D = kMode == 3 ? b : a;  // the down product's arguments
     long long u;
     int kb0, kb1;
     uint32_t ru = 0;
-    bool sat = false;
+    bool sat = false, ok = true;
+#pragma unroll 1
+    for (int ph = 0; ph < kNph && ok; ++ph) {
+    const bool down = kMode == 2 || ph == 1;
+    const int R = ph ? b.R : a.R;
+    SegIter si(ph ? b2 : my_begin, ph ? e2 : my_end, ph ? b.KBn : a.KBn);
     while (si.next(u, kb0, kb1)) {
-      const GvTile& tl = *tile_at(u / a.R);
+      const GvTile& tl = *tile_at(u / R);
       const int T = tl.n;
-      const int rt = static_cast<int>(u % a.R);
+      const int rt = static_cast<int>(u % R);
       const uint32_t rs = ru & 1u, rpar = (ru >> 1) & 1u;
       const bool w_ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbRedFull + rs), rpar, abort_flag, status,
                                                           kStatusTimeout, wait_ns));
@@ -639,7 +756,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
       named_bar_sync(kGvEpiBar, kGvEpiThreads);
       const bool all_ok = epi_ok[(ru & 1u) * 4 + 0] && epi_ok[(ru & 1u) * 4 + 1] &&
                           epi_ok[(ru & 1u) * 4 + 2] && epi_ok[(ru & 1u) * 4 + 3];
-      if (!all_ok) break;
+      if (!all_ok) {
+        ok = false;
+        break;
+      }
       // the unit's sums over this CTA's steps: the four phases in order
       float v[kGvRows];
 #pragma unroll
@@ -654,16 +774,16 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
       ++ru;
       if (tid == 0) GV_STAMP(6);
 
-      if (kMode == 2) {
+      if (down) {
 #pragma unroll
         for (int t = 0; t < kGvRows; ++t) {
           if (t >= T) break;
           const int slot = tl.slot[t];
-          int e = a.rowexp[tl.p0 + t];
+          int e = D.rowexp[tl.p0 + t];
           e = e < -kMaxRowExp ? -kMaxRowExp : (e > kMaxRowExp ? kMaxRowExp : e);
-          const float wt = a.topk_weights[slot] * exp2_int(2 * e);
-          const long long ai = static_cast<long long>(slot / a.topk) * a.Kout + static_cast<long long>(rt) * kBM + tid;
-          if (MOE_CHECK(ai >= 0 && ai < a.acc_elems, a.status, a.dbg, 43, ai, slot)) atomicAdd(a.acc + ai, wt * v[t]);
+          const float wt = D.topk_weights[slot] * exp2_int(2 * e);
+          const long long ai = static_cast<long long>(slot / D.topk) * D.Kout + static_cast<long long>(rt) * kBM + tid;
+          if (MOE_CHECK(ai >= 0 && ai < D.acc_elems, a.status, a.dbg, 43, ai, slot)) atomicAdd(D.acc + ai, wt * v[t]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kGbRedEmpty + rs));
@@ -747,10 +867,15 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
             if (lane == 0) reinterpret_cast<int32_t*>(xs + 256)[gi] = xv_header(sum, eg);
           }
         }
+        if (kMode == 3) __threadfence();  // (the step rows are read by other CTAs' copiers)
         named_bar_sync(kGvEpiBar, kGvEpiThreads);  // every thread is done with the staged sums
+        // one launch: the second of the two row tiles of the down step rt / 2 makes
+        // its rows ready
+        if (kMode == 3 && tid == 0) atomicAdd(b.h_ready + (u / R) * b.KBn + (rt >> 1), 1);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kGbRedEmpty + rs));
+    }
     }
     if (__any_sync(0xffffffffu, sat) && lane == 0) atomicOr(status, kStatusHSaturated);
   }
@@ -772,9 +897,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a) {
 
 }  // namespace
 
-static cudaError_t launch_gemv(void (*kernel)(GemmArgs), const GemmArgs& a, int num_ctas, cudaStream_t stream,
-                               bool pdl) {
-  return launch_k(kernel, dim3(static_cast<unsigned>(num_ctas)), dim3(kGvThreads), kGsAlloc, stream, pdl, a);
+static cudaError_t launch_gemv(void (*kernel)(GemmArgs, GemmArgs), const GemmArgs& a, int num_ctas,
+                               cudaStream_t stream, bool pdl) {
+  return launch_k(kernel, dim3(static_cast<unsigned>(num_ctas)), dim3(kGvThreads), kGsAlloc, stream, pdl, a, a);
 }
 cudaError_t launch_gemv_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
   return launch_gemv(gemv_kernel<1>, a, num_ctas, stream, pdl);
@@ -782,10 +907,15 @@ cudaError_t launch_gemv_gateup(const GemmArgs& a, int num_ctas, cudaStream_t str
 cudaError_t launch_gemv_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl) {
   return launch_gemv(gemv_kernel<2>, a, num_ctas, stream, pdl);
 }
+cudaError_t launch_gemv_both(const GemmArgs& a1, const GemmArgs& a2, int num_ctas, cudaStream_t stream, bool pdl) {
+  return launch_k_coop(gemv_kernel<3>, dim3(static_cast<unsigned>(num_ctas)), dim3(kGvThreads), kGsAlloc, stream,
+                       pdl, a1, a2);
+}
 cudaError_t gemv_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGsAlloc);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGsAlloc);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGsAlloc);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGsAlloc);
+  return e;
 }
 
 }  // namespace moe

@@ -185,6 +185,8 @@ cudaError_t gemm_set_attributes();
 // (small_ids set; xv_in / xv_out set): tiles of at most 4 token rows per expert.
 cudaError_t launch_gemv_gateup(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemv_down(const GemmArgs& a, int num_ctas, cudaStream_t stream, bool pdl);
+// both CUDA-core products of a batch of at most 32 routed slots in one cooperative launch
+cudaError_t launch_gemv_both(const GemmArgs& a1, const GemmArgs& a2, int num_ctas, cudaStream_t stream, bool pdl);
 cudaError_t gemv_set_attributes();
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,

@@ -5,6 +5,7 @@
 #pragma once
 #include <cstdint>
 
+#include "layout.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -18,6 +19,29 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - c0 > 800000000ll) return;
   }
+}
+
+// Bounded wait until the n counters at p (raised by other CTAs of the grid with
+// a fence then an atomic add) all reach `target`; then this thread's later bulk
+// copies see the data written before those releases. Gives up like mbar_wait.
+__device__ __noinline__ bool wait_counters(const int32_t* p, int n, int target, volatile int* abort_flag,
+                                           int* status, uint32_t limit_kcycles) {
+  const long long c0 = clock64();
+  for (;;) {
+    int below = 0;
+    for (int k = 0; k < n; ++k) below += ld_relaxed_gpu(p + k) < target ? 1 : 0;
+    if (below == 0) break;
+    if (*abort_flag) return false;
+    if (((clock64() - c0) >> 10) > static_cast<long long>(limit_kcycles)) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(256);
+  }
+  __threadfence();             // acquire: pairs with the writers' fence before their add
+  fence_proxy_async_global();  // and orders the bulk copies (async proxy) after it
+  return true;
 }
 
 struct Sched {

@@ -32,8 +32,9 @@ def _built():
     __graft_entry__.build()
 
 
-def run_path(prob, hidden, ids, wts, gemv):
+def run_path(prob, hidden, ids, wts, gemv, one_launch=0):
     pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, gemv)
+    pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_ONE_LAUNCH, one_launch)
     try:
         got = prob.run(hidden, ids, wts)
         status = prob.moe.status()
@@ -43,6 +44,7 @@ def run_path(prob, hidden, ids, wts, gemv):
         bits = inputs.f32_to_bf16_bits(got.astype(np.float32))  # (exact: got holds bf16 values)
     finally:
         pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, GEMV_DEFAULT)
+        pkg.moe_w4a16_set_option(prob.moe.handle, pkg.OPT_GEMV_ONE_LAUNCH, 0)
     return got, status, acc, inter, bits
 
 
@@ -157,14 +159,16 @@ def test_gemv_intermediate_matches_oracle():
 
 
 def test_both_small_batch_paths_give_up_cleanly():
-    # the give-up hook on each small-batch path in turn; the next call is clean
+    # the give-up hook on each small-batch path in turn (CUDA cores in one launch,
+    # in two, tensor cores); the next call is clean
     E, K, N, k, M = 8, 512, 256, 4, 2
     prob = Problem(E, K, N, k)
     wl = inputs.Workload("mid", E, K, N, k, M, "normal")
     hidden, ids, wts = workload_inputs(wl)
     h = prob.moe.handle
-    for gemv in (1, 0):
+    for gemv, one in ((1, 1), (1, 0), (0, 1)):
         pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, gemv)
+        pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_ONE_LAUNCH, one)
         pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 1000)
         pkg.moe_w4a16_set_option(h, pkg.OPT_TEST_WAIT_NEVER_COMPLETES, 1)
         prob.run(hidden, ids, wts)
@@ -173,8 +177,34 @@ def test_both_small_batch_paths_give_up_cleanly():
         pkg.moe_w4a16_set_option(h, pkg.OPT_WAIT_LIMIT_US, 0)
         got = prob.run(hidden, ids, wts)
         assert prob.moe.status() == 0
-        assert_close(got, prob.reference(hidden, ids, wts), f"after give-up, gemv={gemv}")
+        assert_close(got, prob.reference(hidden, ids, wts), f"after give-up, gemv={gemv} one launch={one}")
     pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_SMALL_BATCH, GEMV_DEFAULT)
+    pkg.moe_w4a16_set_option(h, pkg.OPT_GEMV_ONE_LAUNCH, 0)
+    prob.close()
+
+
+@pytest.mark.parametrize("num_ctas", [None, 1, 3, 7, 64])
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+def test_gemv_one_launch_matches_two_launches(M, num_ctas):
+    # both products in one cooperative launch (at most 32 slots): the same
+    # arithmetic as the two launches, so the intermediate is identical bit for bit
+    # (the split units' sums run in CTA order either way); the output differs
+    # only by the order of the fp32 atomic adds, and both match the oracle.
+    # 1 CTA: every step row of the intermediate comes from the CTA itself; 7 and
+    # 64 CTAs cut the products' units at different places
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k, num_ctas=num_ctas)
+    wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+    hidden, ids, wts = workload_inputs(wl, step=M + 7)
+    ref = prob.reference(hidden, ids, wts)
+    o_out, o_st, o_acc, o_h, o_bits = run_path(prob, hidden, ids, wts, gemv=1, one_launch=1)
+    t_out, t_st, t_acc, t_h, _ = run_path(prob, hidden, ids, wts, gemv=1, one_launch=0)
+    assert o_st == 0 and t_st == 0
+    np.testing.assert_array_equal(o_h, t_h)
+    assert_close(o_out, ref, f"one launch M={M} ctas={num_ctas}")
+    check_accumulator(o_acc, o_bits, ref, f"one launch M={M} ctas={num_ctas}")
+    scale = float(np.abs(t_acc).max()) or 1.0
+    np.testing.assert_allclose(o_acc, t_acc, rtol=2.0 ** -16, atol=2.0 ** -18 * scale)
     prob.close()
 
 
