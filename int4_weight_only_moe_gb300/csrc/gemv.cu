@@ -181,9 +181,11 @@ __device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int 
     for (int t = 0; t < T; ++t) part[t] = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      // codes of elements 2, 4, 3, 5 and 0, 7, 1, 6 as bytes (layout.cuh)
-      const uint32_t c0 = __funnelshift_r(w4[j], w4[j], 2) & 0x0F0F0F0Fu;
-      const uint32_t c1 = __funnelshift_r(w4[j], w4[j], 6) & 0x0F0F0F0Fu;
+      // codes of elements 2, 4, 3, 5 and 0, 7, 1, 6 as bytes (layout.cuh), each
+      // times 4: the codes sit at bits 2..5 of every byte, directly or after a
+      // rotation by 4, so one mask takes them (the factor 4 goes into the scale)
+      const uint32_t c0 = w4[j] & 0x3C3C3C3Cu;
+      const uint32_t c1 = __funnelshift_r(w4[j], w4[j], 4) & 0x3C3C3C3Cu;
 #pragma unroll
       for (int t = 0; t < T; ++t) {
         const uint4 xv = *reinterpret_cast<const uint4*>(x + (T0 + t) * kGvBRow + gi * 64 + j * 16);
@@ -197,9 +199,11 @@ __device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int 
     for (int t = 0; t < T; ++t) {
       const int hdr = *reinterpret_cast<const int*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
       const int e = static_cast<int8_t>(hdr & 0xFF);
-      // sum (u - 8) v: exact in int32 and in fp32 (|.| < 2^23)
-      const float dot = static_cast<float>(part[t] - 8 * (hdr >> 8));
-      acc[T0 + t] = fmaf(s * __int_as_float((127 - e) << 23), dot, acc[T0 + t]);
+      // 4 sum (u - 8) v: exact in int32, and in fp32 (a multiple of 4 below 2^25);
+      // times s 2^(-e-2), an exact power-of-two scaling of s, so the product is
+      // s 2^-e sum (u - 8) v and the fma rounds once
+      const float dot = static_cast<float>(part[t] - 32 * (hdr >> 8));
+      acc[T0 + t] = fmaf(s * __int_as_float((125 - e) << 23), dot, acc[T0 + t]);
     }
   }
 }

@@ -53,9 +53,10 @@ constexpr int kMaxExperts = 1024;
 //   bytes [64 g, 64 g + 64):  the group's four words of 8 elements, 16 bytes each,
 //                             element i of a word in 16-bit slot kXvSlot[i]
 //   bytes [256 + 4 g, +4):    (sum of the group's 32 values) << 8 | (e_g & 0xFF)
-// The slot order pairs the values with the packed codes for dp2a: rotating a
-// packed word right by 2 (by 6) and masking every fourth nibble gives the codes
-// of elements 2, 4, 3, 5 (0, 7, 1, 6) as bytes, which meet slots 0..3 (4..7).
+// The slot order pairs the values with the packed codes for dp2a: masking bits
+// 2..5 of every byte of a packed word (of the word rotated right by 4) gives the
+// codes of elements 2, 4, 3, 5 (0, 7, 1, 6), times 4, as bytes, which meet
+// slots 0..3 (4..7).
 constexpr int kXvStepBytes = 272;
 __host__ __device__ constexpr int xv_slot(int i) {
   return i == 0 ? 4 : i == 1 ? 6 : i == 2 ? 0 : i == 3 ? 2 : i == 4 ? 1 : i == 5 ? 3 : i == 6 ? 7 : 5;

@@ -349,6 +349,32 @@ def test_forward_host_zero_copy_and_staged_paths():
     prob.close()
 
 
+def test_forward_host_output_complete_on_return():
+    # a host-buffer call returns with the output in the caller's buffer: filled
+    # with NaNs before every call, it must hold the whole result as soon as the
+    # call returns, call after call, pinned and pageable
+    E, K, N, k = 16, 512, 256, 4
+    prob = Problem(E, K, N, k)
+    for step in range(12):
+        M = 1 + step % 3
+        pinned = step % 4 != 3
+        wl = inputs.Workload("mid", E, K, N, k, M, "normal")
+        hidden, ids, wts = workload_inputs(wl, step=step + 20)
+        bufs = [torch.from_numpy(bits16(hidden).copy()), torch.from_numpy(ids.copy()), torch.from_numpy(wts.copy()),
+                torch.full((M, K), 0x7FC0, dtype=torch.int16)]
+        if pinned:
+            bufs = [t.pin_memory() for t in bufs]
+        prob.moe.forward_host(*bufs)
+        host_bits = bufs[3].numpy().copy()  # read right after the return, before any other call
+        assert prob.moe.status() == 0
+        dev_out = prob.run(hidden, ids, wts)
+        host_out = host_bits.view(np.uint16).astype(np.uint32) << 16
+        host_out = host_out.view(np.float32).astype(np.float64)
+        assert np.all(np.isfinite(host_out)), f"step {step}: output not complete on return"
+        assert_within_one_ulp(host_out, dev_out)
+    prob.close()
+
+
 @pytest.mark.parametrize("M", [1, 37])
 def test_forward_replays_from_a_cuda_graph(M):
     # the forward allocates nothing and makes no host-synchronising call, so it can
