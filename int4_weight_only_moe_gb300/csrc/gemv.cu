@@ -162,12 +162,12 @@ __device__ __forceinline__ int dp2a_hi(uint32_t x, uint32_t codes, int acc) {
 // of the tile: per scale group, the exact integer sum of code x value over its 32
 // elements (dp2a), minus 8 times the group's value sum, times the weight scale
 // and the group's 2^-e. w: the step's packed weights; x: the step's row 0 in the
-// activation stage (row t at + t * kGvBRow). At most two rows per call (more do
-// not fit the 80 registers a thread of this CTA has; three and four rows take two
-// calls); the groups are unrolled for a single row only, for the same reason.
+// activation stage (row t at + t * kGvBRow). A group's codes are unpacked once
+// for all the tile's rows; the groups are unrolled for a single row only (more
+// would not fit the 80 registers a thread of this CTA has).
 template <int T, int T0>
 __device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int r, float (&acc)[kGvRows]) {
-  static_assert(T >= 1 && T <= 2 && T0 + T <= kGvRows, "rows per call");
+  static_assert(T >= 1 && T <= 4 && T0 + T <= kGvRows, "rows per call");
 #pragma unroll(T == 1 ? 4 : 1)
   for (int gi = 0; gi < 4; ++gi) {
     // group gi: half gi % 2 of the step's k-block gi / 2
@@ -699,9 +699,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a, c
         if (T == 1) {
           gv_step<1, 0>(wstep, xst, r, acc);
         } else {
-          gv_step<2, 0>(wstep, xst, r, acc);
-          if (T == 3) gv_step<1, 2>(wstep, xst, r, acc);
-          if (T == 4) gv_step<2, 2>(wstep, xst, r, acc);
+          if (T == 2) gv_step<2, 0>(wstep, xst, r, acc);
+          else if (T == 3) gv_step<3, 0>(wstep, xst, r, acc);
+          else gv_step<4, 0>(wstep, xst, r, acc);
         }
         __syncwarp();  // every lane has read the step's shared memory
         if (lane == 0) {
