@@ -345,7 +345,7 @@ def run_ours(args):
     # weights and scales, the activation rows read, the intermediate written (and,
     # fused, read back) and the output accumulator.
     fused = False  # (the fused small-batch launch is off by default)
-    gemv = wl.M * wl.topk <= 128  # (by default such a batch runs its products on the CUDA cores)
+    gemv = wl.M * wl.topk <= 256  # (by default such a batch runs its products on the CUDA cores)
     if fused:
         dom_name = "gemm_fused (gate/up + down, one cooperative launch)"
         dom_bytes = (active * (w1b + w2b) + wl.M * wl.K * 2 + 2 * wl.M * wl.topk * wl.N * 2
@@ -397,8 +397,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int32+f32" if wl.M * wl.topk <= 128 else "f16",
-        "dtype_detail": "INT4 weights: at most 128 routed slots (decode) exact int32 dot products of the codes "
+        "dtype": "int32+f32" if wl.M * wl.topk <= 256 else "f16",
+        "dtype_detail": "INT4 weights: at most 256 routed slots (decode) exact int32 dot products of the codes "
                         "with 16-bit block-fixed-point activations (CUDA cores, dp2a), one f32 rounding per "
                         "group of 32; larger batches f16 tensor-core operands, f32 accumulate; bf16 in/out",
         "data": "synthetic (seeded random INT4 weights for all 384 experts, N(0,1) bf16 hidden, "

@@ -259,11 +259,10 @@ const char* moe_w4a16_last_error(void);
  *   MOE_W4A16_OPT_GEMV_SMALL_BATCH
  *                            where a forward (the fused launch off) computes its two
  *                            expert products on the CUDA cores instead of the
- *                            tensor cores: 1 (default) = batches of M * topk <= 128
- *                            routed slots; 2 = single tokens (M == 1) only; 3 =
- *                            batches of up to 256 routed slots (on GB300 slower
- *                            than the tensor cores at 256 with top-8 of 384
- *                            experts); 0 = never. The
+ *                            tensor cores: 1 (default) and 3 = batches of
+ *                            M * topk <= 256 routed slots (on GB300 faster than
+ *                            the tensor cores there with top-8 of 384 experts);
+ *                            2 = single tokens (M == 1) only; 0 = never. The
  *                            CUDA-core kernels compute matrix-vector products over
  *                            tiles of at most 4 token rows per expert: activations
  *                            as 16-bit block fixed point per scale group of 32

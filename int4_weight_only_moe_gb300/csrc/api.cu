@@ -22,7 +22,7 @@ struct moe_w4a16_ctx {
   unsigned long long wait_us;  // GEMM pipeline wait limit (0: the kernels' default)
   bool test_never_wait;        // test hook (MOE_W4A16_OPT_TEST_WAIT_NEVER_COMPLETES)
   bool fused_small;            // MOE_W4A16_OPT_FUSED_SMALL_BATCH
-  int gemv_small;              // MOE_W4A16_OPT_GEMV_SMALL_BATCH (0, 1: <= 128 slots, 2: one token, 3: <= 256 slots)
+  int gemv_small;              // MOE_W4A16_OPT_GEMV_SMALL_BATCH (0, 1 and 3: <= 256 slots, 2: one token)
   bool gemv_one_launch;        // MOE_W4A16_OPT_GEMV_ONE_LAUNCH
   int32_t* dflag;              // device words: pack's scale check [0], g_idx check [1]
   uint8_t* w1p;
@@ -509,9 +509,8 @@ int forward_impl(moe_w4a16_t h, const uint16_t* hidden, const float* logits, con
   const bool fused = h->fused_small && MK <= 32 && !logits && h->num_ctas <= h->num_sms &&
                      (static_cast<long long>(2 * h->N / kBM) * (h->K / (2 * kBK))) % 4 == 0;
   // Otherwise both products as CUDA-core matrix-vector products (tiles of at most
-  // 4 token rows per expert): by default for batches of at most 128 routed slots
-  // (measured faster there than the tensor-core kernels; slower at 256, which the
-  // option's value 3 still allows), else on the tensor cores.
+  // 4 token rows per expert): by default for batches of at most 256 routed slots
+  // (measured faster there than the tensor-core kernels), else on the tensor cores.
   // (their split tables hold step indices as int: at most MK tiles x 2N/128 row tiles x K/128 steps)
   const bool gemv_wanted = h->gemv_small == 1 ? MK <= kGemvDefaultSlots
                            : h->gemv_small == 2 ? M == 1

@@ -1,4 +1,4 @@
-// The two expert products of a small batch (by default at most 128 routed slots)
+// The two expert products of a small batch (by default at most 256 routed slots)
 // on the CUDA cores: with one to four tokens per expert each product is a
 // matrix-vector product, bound by the packed weight stream, so the weights are
 // multiplied in registers instead of being written to tensor memory for an MMA
@@ -243,11 +243,11 @@ struct GvSeq {
   }
 };
 
-// Relative cost of one step of a tile with T token rows (T = 1..4): the multiply
-// warps' time per step, measured at full size -- one row is bound by the weight
-// stream, two and more rows by the arithmetic (the rows after the first are
-// neither unrolled nor free).
-__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 8 : T == 2 ? 18 : T == 3 ? 26 : 37; }
+// Relative cost of one step of a tile with T token rows (T = 1..4): the time per
+// step, measured at full size on 64 experts with T rows each (1.31, 1.66, 2.04
+// times the one-row step for T = 2, 3, 4) -- one row is bound by the weight
+// stream, more by the arithmetic.
+__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 16 : T == 2 ? 21 : T == 3 ? 27 : 33; }
 
 // The stream-K split weighted by tile cost: every unit of tile i costs
 // gv_step_cost(rows of tile i) per step, and CTA c starts at the first step at or

@@ -98,7 +98,7 @@ struct TokenTile {
 // flat slot of each.
 constexpr int kGemvRows = 4;
 constexpr int kGemvMaxSlots = 256;      // routed slots up to which a forward may use them
-constexpr int kGemvDefaultSlots = 128;  // ... and by default (measured faster up to there)
+constexpr int kGemvDefaultSlots = 256;  // ... and by default (measured faster than the tensor cores there)
 struct GemvTile {
   int e, p0, n, pad;
   int slot[kGemvRows];

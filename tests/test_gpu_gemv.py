@@ -21,7 +21,7 @@ from tests.gpu_helpers import (Problem, assert_close, bf16_tensor_to_f64, bits16
                                workload_inputs)
 
 pytestmark = pytest.mark.gpu
-GEMV_DEFAULT = 1  # the CUDA-core path for batches of at most 128 routed slots
+GEMV_DEFAULT = 1  # the CUDA-core path for batches of at most 256 routed slots
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -80,8 +80,8 @@ def test_gemv_matches_oracle_and_tensor_cores(M, num_ctas):
 
 
 def test_gemv_option_values():
-    # 1 (default): batches of <= 128 slots; 2: single-token batches only; 3: up to
-    # 256 slots; 0: never; anything else is rejected
+    # 1 (default) and 3: batches of up to 256 slots; 2: single-token batches only;
+    # 0: never; anything else is rejected
     prob = Problem(8, 256, 128, 2)
     h = prob.moe.handle
     for v in (0, 1, 2, 3):
