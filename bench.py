@@ -589,6 +589,9 @@ def run_profile_case(args):
     data = gb.step_inputs(wl, args.warmup + args.steps)
     out = torch.empty((wl.M, gb.K), dtype=torch.bfloat16, device="cuda")
     gb.moe.ensure_workspace(wl.M)
+    if args.tensor_cores:  # the tensor-core kernels for every batch size
+        import int4_weight_only_moe_gb300 as pkg
+        pkg.moe_w4a16_set_option(gb.moe.handle, pkg.OPT_GEMV_SMALL_BATCH, 0)
     for h, ids, w in data:
         gb.flush()
         gb.moe.forward(h, ids, w, out=out)
@@ -612,6 +615,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--experts", type=int, default=None,
                     help="resident experts in --profile-case (default: the workload's E)")
+    ap.add_argument("--tensor-cores", action="store_true",
+                    help="--profile-case: run the products on the tensor cores whatever the batch size")
     args = ap.parse_args(argv)
     if args.profile_case:
         return run_profile_case(args)

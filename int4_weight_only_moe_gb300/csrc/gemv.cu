@@ -243,11 +243,13 @@ struct GvSeq {
   }
 };
 
-// Relative cost of one step of a tile with T token rows (T = 1..4): the time per
-// step, measured at full size on 64 experts with T rows each (1.31, 1.66, 2.04
-// times the one-row step for T = 2, 3, 4) -- one row is bound by the weight
-// stream, more by the arithmetic.
-__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 16 : T == 2 ? 21 : T == 3 ? 27 : 33; }
+// Relative cost of one step of a tile with T token rows (T = 1..4). One row is
+// bound by the weight stream, more by the arithmetic. Measured at full size on 64
+// experts with T rows each, a step costs 1.31, 1.66, 2.04 times the one-row step
+// for T = 2, 3, 4. In a batch that mixes them the one-row shares stream faster
+// than when all shares are one-row, and the best split (measured at M = 9 to 32)
+// charges 1.44, 1.88, 2.31.
+__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 16 : T == 2 ? 23 : T == 3 ? 30 : 37; }
 
 // The stream-K split weighted by tile cost: every unit of tile i costs
 // gv_step_cost(rows of tile i) per step, and CTA c starts at the first step at or
