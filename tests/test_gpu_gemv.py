@@ -1,11 +1,14 @@
-"""The small-batch CUDA-core path (at most 32 routed slots: tiles of at most 4
-token rows per expert, both products as matrix-vector products) against the
-oracle and against the tensor-core kernels on the same inputs, through the C-ABI.
+"""The small-batch CUDA-core path (by default up to 256 routed slots: tiles of at
+most 4 token rows per expert, both products as matrix-vector products) against
+the oracle and against the tensor-core kernels on the same inputs, through the
+C-ABI.
 
 Covered: every grid size from one CTA (every unit in one CTA's sequence) to more
 CTAs than steps; experts with 1..16 rows (several 4-row tiles of one expert);
-skipped ids; a batch with no valid slot; the give-up path of both paths; and the
-intermediate activations. The two paths compute the same products from
+batches up to 32 slots (routed inside the kernels) and above (the align kernel's
+tile list); skipped ids; a batch with no valid slot; the give-up path of every
+small-batch path; both products in one launch against two; every output element
+written; and the intermediate activations. The two paths compute the same products from
 differently rounded activations (the tensor cores read them as fp16, the CUDA
 cores as 16-bit block fixed point per scale group), so the intermediate may
 differ by about one fp16 unit and the output accumulators by about 2^-12 of
@@ -94,7 +97,7 @@ def test_gemv_option_values():
 @pytest.mark.parametrize("num_ctas", [None, 1, 5, 256])
 @pytest.mark.parametrize("M", [9, 37, 64])
 def test_gemv_align_tile_list(M, num_ctas):
-    # more than 32 routed slots (up to 256 with option 3): the align kernel writes
+    # more than 32 routed slots (up to 256): the align kernel writes
     # the tile list and the CUDA-core kernels read it (1 CTA: every tile through
     # the global-memory fallback of the kernel's tile window)
     E, K, N, k = 16, 512, 256, 4
