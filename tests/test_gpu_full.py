@@ -98,6 +98,24 @@ def test_full_size_parity(full_problem, name):
     np.testing.assert_array_equal(bits.view(np.uint16), inputs.f32_to_bf16_bits(acc.astype(np.float32)))
 
 
+def test_full_size_zipf_small_batch_cuda_cores(full_problem):
+    # 32 Zipf-routed tokens (256 routed slots) run on the CUDA cores by default:
+    # the hottest experts take several 4-row tiles, and tiles of 1..4 rows mix
+    # under the cost-weighted split; every row against the oracle
+    wl = inputs.Workload("small32_zipf", 384, 7168, 2048, 8, 32, "zipf")
+    hidden, ids, wts = workload_inputs(wl)
+    counts = np.bincount(ids.reshape(-1), minlength=wl.E)
+    assert counts.max() > 4 and np.any((counts > 1) & (counts < 4))  # several tiles; mixed tile sizes
+    got, bits, acc = run_with_accumulator(full_problem, hidden, ids, wts)
+    assert full_problem.moe.status() == 0
+    toks = np.arange(wl.M)
+    ref = oracle_pool.oracle_rows(wl, toks)
+    record("small32 Zipf (CUDA cores, multi-tile experts)", toks, got, ref, acc)
+    assert_close(got, ref, "small32 Zipf")
+    check_accumulator(acc, bits, ref, "small32 Zipf")
+    np.testing.assert_array_equal(bits.view(np.uint16), inputs.f32_to_bf16_bits(acc.astype(np.float32)))
+
+
 def test_decode_intermediate_full_size(full_problem):
     # SiLU(gate) * up of the 8 routed rows of a decode step, element by element
     wl = inputs.WORKLOADS["decode"]
