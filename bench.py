@@ -353,11 +353,11 @@ def run_ours(args):
         dom_ms = kmean[2] + kmean[3]
     elif gemv:
         # the CUDA-core gate/up kernel: weights and scales, the activation step rows
-        # (272 bytes per row and step: 128 16-bit values and 4 group headers) read,
+        # (288 bytes per row and step: 128 16-bit values and 4 group headers) read,
         # h written twice (step rows for the down kernel, blocked fp16 for read-back)
         dom_name = "gemv_gateup (CUDA cores)"
-        dom_bytes = (active * w1b + wl.M * wl.topk * (wl.K // 128) * 272
-                     + wl.M * wl.topk * (wl.N * 2 + (wl.N // 128) * 272))
+        dom_bytes = (active * w1b + wl.M * wl.topk * (wl.K // 128) * 288
+                     + wl.M * wl.topk * (wl.N * 2 + (wl.N // 128) * 288))
         dom_ms = kmean[2]
     else:
         dom_name = "gemm_gateup"

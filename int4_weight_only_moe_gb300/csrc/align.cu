@@ -407,7 +407,7 @@ __device__ void gather_row(const GatherArgs& g, int p, int sid, int* red, int ex
           *reinterpret_cast<uint4*>(xv_step + (ch & 15) * 16) =
               make_uint4(q[0] | (static_cast<uint32_t>(q[1]) << 16), q[2] | (static_cast<uint32_t>(q[3]) << 16),
                          q[4] | (static_cast<uint32_t>(q[5]) << 16), q[6] | (static_cast<uint32_t>(q[7]) << 16));
-          if ((ch & 3) == 0) reinterpret_cast<int32_t*>(xv_step + 256)[(ch >> 2) & 3] = xv_header(sum, eg);
+          if ((ch & 3) == 0) xv_header(xv_step, (ch >> 2) & 3, sum, eg);
         }
       } else if (in_row) {
         const uint4 o = make_uint4(bf16x2_to_f16x2_scaled(x.x, f), bf16x2_to_f16x2_scaled(x.y, f),

@@ -105,7 +105,7 @@ constexpr int kGvNWS = 10;                                // weight ring (chunks
 constexpr int kGvBSteps = 8;                              // steps per activation chunk
 constexpr int kGvNB = 3;                                  // activation ring (chunks)
 constexpr int kGvBRow = kGvBSteps * kXvStepBytes;         // one token row of a chunk
-constexpr int kGvBStage = kGvRows * kGvBRow;              // [row][step][272 B]
+constexpr int kGvBStage = kGvRows * kGvBRow;              // [row][step][288 B]
 // barriers
 constexpr int kGbWFull = 0;                      // weight chunk landed (bulk-copy bytes)
 constexpr int kGbWEmpty = kGbWFull + kGvNWS;     // weight chunk read (4 warps x 2 steps)
@@ -120,7 +120,7 @@ using GvTile = GemvTile;  // (layout.cuh)
 static_assert(sizeof(GvTile) == 32, "tile table entry size");
 constexpr int kGvTileCache = kSmallTiles;  // tiles kept in shared memory (a batch's all, up to 32 slots)
 
-// shared memory map (offsets from a 1024-aligned base)
+// shared memory map (offsets from a 128-aligned base)
 constexpr int kGsBar = 0;
 constexpr int kGsMisc = kGsBar + ((kGvNumBars * 8 + 63) / 64) * 64;
 // the last chunk / step copied into each ring slot (for the teardown's drain)
@@ -130,10 +130,10 @@ constexpr int kGsCum = kGsLast + (((kGvNWS + kGvNB) * 4 + 63) / 64) * 64;  // in
 constexpr int kGsTiles = kGsCum + (((kGemvMaxSlots + 1) * 4 + 63) / 64) * 64;
 constexpr int kGsRed = kGsTiles + kSmallTiles * static_cast<int>(sizeof(GvTile));  // [2][phase][t][128] f32
 constexpr int kGsBounds = kGsRed + 2 * kGvPhases * kGvRows * kBM * 4;  // int [kMaxCtas + 1]: shares
-constexpr int kGsW = ((kGsBounds + (kMaxCtas + 1) * 4 + 1023) / 1024) * 1024;
+constexpr int kGsW = ((kGsBounds + (kMaxCtas + 1) * 4 + 127) / 128) * 128;
 constexpr int kGsB = kGsW + kGvNWS * kGvChunkBytes;
 constexpr int kGsEnd = kGsB + kGvNB * kGvBStage;
-constexpr int kGsAlloc = kGsEnd + 1024;  // (the base is aligned to 1024 inside)
+constexpr int kGsAlloc = kGsEnd + 128;  // (the base is aligned to 128 inside)
 static_assert(kGsAlloc <= 227 * 1024, "shared memory budget");
 static_assert(kGvStepBytes % 16 == 0 && kGvBStage % 16 == 0 && kGsB % 16 == 0, "16-byte alignment");
 // Parity safety: a multiply warp sees every second weight chunk (its steps are 4
@@ -197,13 +197,13 @@ __device__ __forceinline__ void gv_step(const uint8_t* w, const uint8_t* x, int 
     }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-      const int hdr = *reinterpret_cast<const int*>(x + (T0 + t) * kGvBRow + 256 + gi * 4);
-      const int e = static_cast<int8_t>(hdr & 0xFF);
+      // the group's header: 2^-(e+2) and 32 times its value sum V
+      const int2 hdr = *reinterpret_cast<const int2*>(x + (T0 + t) * kGvBRow + 256 + gi * 8);
       // 4 sum (u - 8) v: exact in int32, and in fp32 (a multiple of 4 below 2^25);
       // times s 2^(-e-2), an exact power-of-two scaling of s, so the product is
       // s 2^-e sum (u - 8) v and the fma rounds once
-      const float dot = static_cast<float>(part[t] - 32 * (hdr >> 8));
-      acc[T0 + t] = fmaf(s * __int_as_float((125 - e) << 23), dot, acc[T0 + t]);
+      const float dot = static_cast<float>(part[t] - hdr.y);
+      acc[T0 + t] = fmaf(s * __int_as_float(hdr.x), dot, acc[T0 + t]);
     }
   }
 }
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a, c
   constexpr int kNph = kMode == 3 ? 2 : 1;  // products in this launch
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t base = (raw + 127u) & ~127u;  // (bulk copies need 16-byte alignment)
   uint8_t* gbase = smem_raw + (base - raw);
   auto bar = [&](int i) -> uint32_t { return base + kGsBar + static_cast<uint32_t>(i) * 8u; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kGsMisc);
@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a, c
           if (xs_ok) {
             *reinterpret_cast<int16_t*>(xs + gi * 64 + ((f & 31) >> 3) * 16 + xv_slot(f & 7) * 2) =
                 static_cast<int16_t>(v16);
-            if (lane == 0) reinterpret_cast<int32_t*>(xs + 256)[gi] = xv_header(sum, eg);
+            if (lane == 0) xv_header(xs, gi, sum, eg);
           }
         }
         if (kMode == 3) __threadfence();  // (the step rows are read by other CTAs' copiers)

@@ -45,19 +45,21 @@ constexpr int kMaxExperts = 1024;
 
 // Activation rows of the small-batch CUDA-core products ("step rows"): per padded
 // row p and pipeline step kb (128 reduction elements) of an operand with KBn
-// steps, 272 bytes at (p * KBn + kb) * 272. A row's steps are contiguous, so one
+// steps, 288 bytes at (p * KBn + kb) * 288. A row's steps are contiguous, so one
 // copy brings several steps of a row. Each scale group g (32 elements) of the
 // step is stored as 16-bit block fixed point: v = round(x * 2^e_g) with e_g
 // chosen so that the group's largest |x| times 2^e_g lies in [2^13, 2^14)
 // (xv_group_exp; 0 for an all-zero group):
 //   bytes [64 g, 64 g + 64):  the group's four words of 8 elements, 16 bytes each,
 //                             element i of a word in 16-bit slot kXvSlot[i]
-//   bytes [256 + 4 g, +4):    (sum of the group's 32 values) << 8 | (e_g & 0xFF)
+//   bytes [256 + 8 g, +4):    2^-(e_g + 2) as a float (the factor 4 goes with the
+//                             codes times 4 that the product kernels take)
+//   bytes [260 + 8 g, +4):    32 times the sum of the group's 32 values (int32)
 // The slot order pairs the values with the packed codes for dp2a: masking bits
 // 2..5 of every byte of a packed word (of the word rotated right by 4) gives the
 // codes of elements 2, 4, 3, 5 (0, 7, 1, 6), times 4, as bytes, which meet
 // slots 0..3 (4..7).
-constexpr int kXvStepBytes = 272;
+constexpr int kXvStepBytes = 288;
 __host__ __device__ constexpr int xv_slot(int i) {
   return i == 0 ? 4 : i == 1 ? 6 : i == 2 ? 0 : i == 3 ? 2 : i == 4 ? 1 : i == 5 ? 3 : i == 6 ? 7 : 5;
 }
@@ -74,8 +76,12 @@ __device__ __forceinline__ int xv_group_exp(float m) {
 __device__ __forceinline__ int xv_quantize(float x, int e) {
   return __float2int_rn(x * __int_as_float((127 + e) << 23));
 }
-__device__ __forceinline__ int32_t xv_header(int sum, int e) {
-  return static_cast<int32_t>((static_cast<uint32_t>(sum) << 8) | (static_cast<uint32_t>(e) & 0xFFu));
+// Write group g's header into the step row at `row`.
+__device__ __forceinline__ void xv_header(uint8_t* row, int g, int sum, int e) {
+  int2 h;
+  h.x = (125 - e) << 23;  // 2^-(e + 2): |e| <= kXvMaxExp, a normal float
+  h.y = 32 * sum;         // |sum| < 2^19
+  *reinterpret_cast<int2*>(row + 256 + 8 * g) = h;
 }
 #endif
 
