@@ -247,9 +247,9 @@ struct GvSeq {
 // bound by the weight stream, more by the arithmetic. Measured at full size on 64
 // experts with T rows each, a step costs 1.31, 1.66, 2.04 times the one-row step
 // for T = 2, 3, 4. In a batch that mixes them the one-row shares stream faster
-// than when all shares are one-row, and the best split (measured at M = 9 to 32)
-// charges 1.44, 1.88, 2.31.
-__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 16 : T == 2 ? 23 : T == 3 ? 30 : 37; }
+// than when all shares are one-row, and the best split (measured at M = 6 to 32)
+// charges 1.38, 1.75, 2.19.
+__host__ __device__ constexpr int gv_step_cost(int T) { return T <= 1 ? 16 : T == 2 ? 22 : T == 3 ? 28 : 35; }
 
 // The stream-K split weighted by tile cost: every unit of tile i costs
 // gv_step_cost(rows of tile i) per step, and CTA c starts at the first step at or
