@@ -887,18 +887,18 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(const GemmArgs a, c
   }
 
   // ------------------------------------------------ teardown
-  // Every copy issued is waited for by its readers unless a wait gave up: let the
-  // latest copy into every slot land before shared memory is released.
+  // Every copy issued is waited for by its readers unless a wait gave up. Then
+  // thread 0 lets the latest copy into every slot land before it exits (the
+  // CTA's shared memory lives until its last thread has exited).
   __syncwarp();
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && *abort_flag != 0) {
     for (int i = 0; i < kGvNWS; ++i)
       if (wlast[i] >= 0) mbar_wait_drain(bar(kGbWFull + i), static_cast<uint32_t>((wlast[i] / kGvNWS) & 1));
     for (int i = 0; i < kGvNB; ++i)
       if (blast[i] >= 0) mbar_wait_drain(bar(kGbBFull + i), static_cast<uint32_t>((blast[i] / kGvNB) & 1));
-    GV_STAMP(7);
   }
-  __syncthreads();
+  if (threadIdx.x == 0) GV_STAMP(7);
 }
 
 }  // namespace
